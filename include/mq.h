@@ -1,0 +1,217 @@
+/*
+ * mq.h - C ABI of the GB300 (sm_103a) W4A4 + block-sparse 4-bit residual linear.
+ *
+ * The method: MosaicQuant, "Inlier-Outlier Disaggregation for Unified 4-Bit
+ * LLM Quantization" (technical summary page).  The weight matrix W^ is
+ * split into a dense 4-bit base Q(W^) and a sparse 4-bit residual R
+ * (Metodologia 1); the residual budget is spent on 64x128 blocks chosen by a
+ * Hessian-guided Delta-score, top-K (Metodologia 2); the ZipperEngine computes
+ * the residual inside the dense 4-bit GEMM and reduce-adds the two partial
+ * products (Metodologia 3).  The linear computed is
+ *
+ *     Y = Q(X) (Q(W^) + R^)^T,   R^ = 4-bit residual on the selected blocks.
+ *
+ * Formats (the pages fix none of them; these are this library's):
+ *   - INT4 codes are symmetric, in [-7, 7]; two per byte, element 2j in the low
+ *     nibble and 2j+1 in the high nibble, as 4-bit two's complement.
+ *   - one fp16 scale per 128 inputs ("group"): per token for activations, per
+ *     output row for base weights, per block row for residual blocks;
+ *     scale = fp16_RNE(amax / 7) saturated to 65504, code = clamp(RNE(v/scale), -7, 7).
+ *   - residual blocks are 64 output rows x 128 inputs (one group);
+ *     Delta_b = sum_{k in block} h_k * sum_{n in block} R[n,k]^2 with
+ *     h_k = mean over calibration rows of x_k^2; the top floor(budget * #blocks)
+ *     blocks by Delta (ties: lower block index b = (n/64) * (K/128) + k/128) get
+ *     a residual.
+ *
+ * Conventions for every entry point:
+ *   - All pointers are DEVICE pointers unless stated.  The caller owns every
+ *     buffer; the library never allocates, frees or synchronizes (except
+ *     mq_check_device_error, which synchronizes the given stream).
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream).
+ *   - Sizes: K % 128 == 0 and N % 128 == 0 (so N % 64 == 0 for residual
+ *     blocks); M >= 1; K <= 2^20, N <= 2^20, M <= 2^20.
+ *   - Errors are returned, never raised: MQ_ERR_INVALID_ARG for bad sizes or
+ *     NULL pointers, MQ_ERR_ALIGNMENT for misaligned buffers,
+ *     MQ_ERR_UNSUPPORTED_DEVICE when the current device is not compute
+ *     capability 10.3, MQ_ERR_CUDA when a launch fails (detail in
+ *     mq_last_error()).  Nothing is launched when an error is returned.
+ *   - Device-side waits are bounded; a wait that runs out sets a device error
+ *     word and the kernel returns early.  mq_check_device_error() reports it
+ *     as MQ_ERR_TIMEOUT.
+ */
+#ifndef MQ_H_
+#define MQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* mq_stream_t; /* same as cudaStream_t */
+
+typedef enum {
+  MQ_OK = 0,
+  MQ_ERR_INVALID_ARG = 1,
+  MQ_ERR_ALIGNMENT = 2,
+  MQ_ERR_UNSUPPORTED_DEVICE = 3,
+  MQ_ERR_CUDA = 4,
+  MQ_ERR_TIMEOUT = 5,
+  MQ_ERR_WORKSPACE = 6
+} mq_status;
+
+typedef enum { MQ_F16 = 0, MQ_BF16 = 1, MQ_F32 = 2 } mq_dtype;
+
+/* ------------------------------------------------------------------------ */
+/* Online: activation quantizer (ZipperEngine's "quantization" stage,       */
+/* Metodologia 3).                                                          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Quantize X per token and per 128-input group.
+ *   x    [M, ldx] MQ_F16 or MQ_BF16 (xt), row-major, row stride ldx >= K
+ *        elements; x and ldx*2 bytes 8-byte aligned.  Values must be finite.
+ *   xq   [M, K/2] packed codes (row-major, dense), 16-byte aligned.
+ *   xs   [M, K/128] fp16 scale bits (row-major, dense), 2-byte aligned.
+ * Bit-exact against the definition above: amax, amax/7 and v/scale are formed
+ * in IEEE fp32 and each rounds to the same value the exact rational would.
+ */
+mq_status mq_quantize_act(const void* x, mq_dtype xt, int64_t M, int64_t K, int64_t ldx,
+                          uint8_t* xq, uint16_t* xs, mq_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Offline: Delta-score block selection (Metodologia 2) and packing          */
+/* (Metodologia 1).                                                          */
+/* ------------------------------------------------------------------------ */
+
+/* floor(budget * (N/64) * (K/128) + 1e-9) clamped to [0, #blocks]; 0 for
+ * budget <= 0 or invalid sizes.  Host-only, no device work. */
+int64_t mq_num_selected(int64_t N, int64_t K, double budget);
+
+/* Bytes of device workspace mq_select_blocks needs for (N, K). */
+size_t mq_select_workspace_bytes(int64_t N, int64_t K);
+
+/*
+ * Select the residual blocks of W^ by Delta-score and write them as CSR over
+ * 64-row block rows.
+ *   w        [N, K] fp16 bits, row-major (the weight matrix W^).
+ *   xcal     [C, K] calibration activations, MQ_F16 or MQ_BF16 (xct), C >= 1.
+ *   budget   fraction of blocks in [0, 1].
+ *   row_ptr  [N/64 + 1] int32: entries of block row br are
+ *            col_idx[row_ptr[br] .. row_ptr[br+1]).
+ *   col_idx  [mq_num_selected(N, K, budget)] int32 group index g, ascending
+ *            within a row (may be NULL when that count is 0).
+ *   h_out    optional [K] float64: the diagonal Hessian h_k.
+ *   delta_out optional [(N/64)*(K/128)] float64: Delta_b, b = br*(K/128) + g.
+ *   ws       workspace of at least mq_select_workspace_bytes(N, K) bytes,
+ *            256-byte aligned (else MQ_ERR_WORKSPACE).
+ * h and Delta are formed in float64 in a fixed order (ascending c, then
+ * ascending rows, then ascending k) without fused multiply-add, so both are
+ * reproducible bit for bit.
+ */
+mq_status mq_select_blocks(const uint16_t* w, int64_t N, int64_t K, const void* xcal,
+                           mq_dtype xct, int64_t C, double budget, int32_t* row_ptr,
+                           int32_t* col_idx, double* h_out, double* delta_out, void* ws,
+                           size_t ws_bytes, mq_stream_t stream);
+
+/*
+ * Pack W^ into the dense 4-bit base and the 4-bit residual of the blocks
+ * listed by (row_ptr, col_idx).
+ *   w     [N, K] fp16 bits, row-major.
+ *   nnzb  number of listed blocks (== row_ptr[N/64]); the host cannot read
+ *         device row_ptr, so the caller passes it.
+ *   wq    base codes, tiled (N*K/2 bytes, 16-byte aligned):
+ *           unit (t, g) for output rows 128t..128t+127 and group g is 8192
+ *           contiguous bytes at ((t*(K/128) + g) * 8192); inside a unit,
+ *           byte  j*2048 + r*16 + b  holds the codes of row 128t + r and
+ *           inputs 128g + 32j + 2b (low nibble) and +1 (high nibble),
+ *           j in [0,4), r in [0,128), b in [0,16).
+ *   wsc   base scales, tiled fp16: scale of (row 128t + r, group g) at
+ *           (t*(K/128) + g)*128 + r   (N*K/128 entries, 16-byte aligned).
+ *   rq    residual codes, [nnzb] blocks of 4096 bytes in CSR order; inside
+ *           block i, byte j*1024 + r*16 + b holds row 64*br + r, inputs
+ *           128g + 32j + 2b (low) and +1 (high), r in [0,64)  (16-byte aligned).
+ *   rsc   residual scales, fp16 [nnzb][64] in CSR order (16-byte aligned).
+ * rq and rsc may be NULL when nnzb == 0.
+ */
+mq_status mq_pack_weights(const uint16_t* w, int64_t N, int64_t K, const int32_t* row_ptr,
+                          const int32_t* col_idx, int64_t nnzb, uint8_t* wq, uint16_t* wsc,
+                          uint8_t* rq, uint16_t* rsc, mq_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Online: the fused dense + sparse-residual GEMM (ZipperEngine,             */
+/* Metodologia 3).                                                           */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of device workspace mq_w4a4_residual_gemm needs for (M, N, K). */
+size_t mq_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/* Zero a GEMM workspace before its first use (and after an MQ_ERR_TIMEOUT);
+ * the GEMM leaves it zeroed again on every normal exit. */
+mq_status mq_gemm_workspace_init(void* ws, size_t ws_bytes, mq_stream_t stream);
+
+/*
+ *   Y[m, n] = sum_g xs[m,g] * ( wsc[n,g] * Dw[m,n,g] + rsc[n,g] * Dr[m,n,g] )
+ * with the integer group dots Dw = sum_{k in g} xq[m,k] * wq[n,k] and, for the
+ * listed blocks, Dr = sum_{k in g} xq[m,k] * rq[n,k]; both are exact.  One
+ * kernel streams each weight unit once, reads each activation tile once per
+ * output tile, adds the residual product of a block in the same pass, and
+ * reduce-adds both partial products in fp32 in ascending-g order (split-K
+ * partials are summed in a fixed order, so the result is deterministic).
+ *   xq, xs   from mq_quantize_act (M tokens).
+ *   wq, wsc, row_ptr, col_idx, nnzb, rq, rsc   from mq_select_blocks /
+ *            mq_pack_weights (nnzb == 0: residual pointers may be NULL).
+ *   y        [M, N] row-major, MQ_BF16 (round to nearest even) or MQ_F32.
+ *   ws       at least mq_gemm_workspace_bytes(M, N, K) bytes, 256-byte
+ *            aligned, zeroed once by mq_gemm_workspace_init; one workspace
+ *            must not be used by two GEMMs in flight at the same time.
+ */
+mq_status mq_w4a4_residual_gemm(const uint8_t* xq, const uint16_t* xs, int64_t M,
+                                const uint8_t* wq, const uint16_t* wsc, int64_t N, int64_t K,
+                                const int32_t* row_ptr, const int32_t* col_idx, int64_t nnzb,
+                                const uint8_t* rq, const uint16_t* rsc, void* y, mq_dtype yt,
+                                void* ws, size_t ws_bytes, mq_stream_t stream);
+
+/*
+ * Test hook: the same kernel, but instead of the fp32 reduce-add it writes the
+ * raw integer group dots it computed on the tensor cores:
+ *   dw [M, N, K/128] int32 : Dw[m, n, g]
+ *   dr [M, nnzb, 64] int32 : Dr of CSR entry i, block row r  (NULL if nnzb == 0)
+ * Same argument rules as mq_w4a4_residual_gemm otherwise.
+ */
+mq_status mq_debug_group_dots(const uint8_t* xq, const uint16_t* xs, int64_t M, const uint8_t* wq,
+                              const uint16_t* wsc, int64_t N, int64_t K, const int32_t* row_ptr,
+                              const int32_t* col_idx, int64_t nnzb, const uint8_t* rq,
+                              const uint16_t* rsc, int32_t* dw, int32_t* dr, void* ws,
+                              size_t ws_bytes, mq_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Status                                                                    */
+/* ------------------------------------------------------------------------ */
+
+/* Synchronize `stream`, read and clear the device error word of the current
+ * device: MQ_ERR_TIMEOUT if a bounded device-side wait ran out since the last
+ * check, MQ_ERR_CUDA if the stream reports an error, else MQ_OK. */
+mq_status mq_check_device_error(mq_stream_t stream);
+
+/* Limit, in nanoseconds, of every device-side wait launched afterwards
+ * (default 1e9; values outside [1e3, 6e10] are clamped). */
+void mq_set_wait_timeout_ns(uint64_t ns);
+
+/* Test hook for failure detection: launch one CTA whose bounded wait is on an
+ * mbarrier that nothing ever arrives on; it gives up after the configured
+ * limit, sets the device error word and exits.  Follow with
+ * mq_check_device_error, which then returns MQ_ERR_TIMEOUT. */
+mq_status mq_debug_wait_timeout(mq_stream_t stream);
+
+const char* mq_status_string(mq_status s);
+/* Thread-local detail of the last error returned on this host thread. */
+const char* mq_last_error(void);
+/* Library version string. */
+const char* mq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MQ_H_ */

@@ -1,0 +1,85 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every symbol include/mq.h declares, sizes its workspaces, counts selected
+blocks like the oracle, and rejects bad arguments before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle as O
+from dense_sparse_int4_gb300 import build as B
+from dense_sparse_int4_gb300 import mq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    B.build()
+    return mq.lib()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "mq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(mq.EXPORTS)
+
+
+def test_version_and_status_strings(L):
+    assert "sm_103a" in mq.version()
+    for s in range(7):
+        assert L.mq_status_string(s)
+
+
+def test_num_selected_matches_oracle(L, golden_dir):
+    for line in open(os.path.join(golden_dir, "num_selected.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        N, K, b, want = line.split()
+        assert L.mq_num_selected(int(N), int(K), float(b)) == int(want)
+        assert O.num_selected(int(N), int(K), float(b)) == int(want)
+
+
+def test_workspace_sizes(L):
+    assert L.mq_select_workspace_bytes(4096, 4096) >= 2048 * 8 + 4096 * 8 + 2048
+    # decode shapes split K -> partials + counters; huge M needs no split
+    assert L.mq_gemm_workspace_bytes(32, 4096, 4096) > 0
+    assert L.mq_gemm_workspace_bytes(2048, 14336, 4096) == 0
+    assert L.mq_gemm_workspace_bytes(4, 100, 4096) == 0  # invalid N
+
+
+def test_argument_validation_before_device(L):
+    P = ctypes.c_void_p
+    bad = P(0)
+    assert L.mq_quantize_act(bad, 0, 4, 512, 512, bad, bad, None) == mq.MQ_ERR_INVALID_ARG
+    fake = P(4096)  # never dereferenced: validation fails first
+    assert L.mq_quantize_act(fake, 0, 4, 500, 512, fake, fake, None) == mq.MQ_ERR_INVALID_ARG  # K % 128
+    assert L.mq_quantize_act(P(4098), 0, 4, 512, 512, fake, fake, None) == mq.MQ_ERR_ALIGNMENT
+    assert L.mq_quantize_act(fake, 7, 4, 512, 512, fake, fake, None) == mq.MQ_ERR_INVALID_ARG  # dtype
+    # gemm: N not a multiple of 128; misaligned xq; workspace too small
+    args = [fake, fake, 4, fake, fake, 192, 512, fake, fake, 0, None, None, fake, 1, None, 0, None]
+    assert L.mq_w4a4_residual_gemm(*args) == mq.MQ_ERR_INVALID_ARG
+    args[5] = 512
+    args[0] = P(4097)
+    assert L.mq_w4a4_residual_gemm(*args) == mq.MQ_ERR_ALIGNMENT
+    args[0] = fake
+    args[2] = 32
+    args[6] = 4096
+    args[5] = 4096
+    assert L.mq_w4a4_residual_gemm(*args) == mq.MQ_ERR_WORKSPACE
+    # residual count without residual pointers
+    args = [fake, fake, 4, fake, fake, 512, 512, fake, fake, 3, None, None, fake, 1, None, 0, None]
+    assert L.mq_w4a4_residual_gemm(*args) == mq.MQ_ERR_INVALID_ARG
+    # select: budget outside [0, 1]
+    assert L.mq_select_blocks(fake, 512, 512, fake, 0, 256, 1.5, fake, fake, None, None, fake, 1 << 20,
+                              None) == mq.MQ_ERR_INVALID_ARG
+    assert b"budget" in L.mq_last_error()

@@ -1,0 +1,287 @@
+"""GPU parity: the CUDA path (through the C ABI) against the oracle.
+
+Integer stages (quantized activations, packed weights, block lists, group
+dots) must match bit for bit; the fp32 epilogue within 1e-5 of the sum of
+absolute terms; bf16 outputs within 1 ulp.  Small cases are compared whole;
+the full-size workloads are compared on sampled outputs the oracle computes
+one by one."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from dense_sparse_int4_gb300 import mq, synth
+from tests.gpu_helpers import (check_bf16, check_close, dev_act, dev_half, host_u16, logical_rq, logical_wq,
+                               logical_wsc, logical_xs, oracle_prep_for_csr, packed_from_csr)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    yield
+    mq.check_device_error()
+
+
+# ----------------------------------------------------------------------------
+# activation quantizer
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,K,dtype", [(4, 512, "f16"), (37, 384, "f16"), (1, 128, "bf16"), (300, 1024, "bf16"),
+                                       (2048, 4096, "bf16"), (32, 14336, "f16")])
+def test_quantize_act_bit_exact(M, K, dtype):
+    x = synth.activations(M, K, seed=M + K, count=synth.n_outliers(K), dtype=dtype)
+    if M > 2:  # edge rows: all zeros, fp16-subnormal scale, huge values
+        x[0] = 0
+        sub = np.float32(2.0 ** -20)
+        x[1] = synth.to_bits(np.full(K, sub, np.float32) * np.sign(np.random.default_rng(0).standard_normal(K)).astype(np.float32), dtype)
+        if dtype == "bf16":
+            x[2, ::7] = synth.to_bits(np.array([1e6], np.float32), "bf16")[0]
+    xt = dev_act(x, dtype == "bf16")
+    xq, xs = mq.quantize_act(xt)
+    torch.cuda.synchronize()
+    q, s = O.quantize_act(x, dtype == "bf16")
+    assert np.array_equal(xq.cpu().numpy(), O.pack_nibbles(q))
+    assert np.array_equal(logical_xs(xs, M), s)
+    assert not host_u16(xs)[:, M:].any()  # padding entries zeroed
+
+
+def test_quantize_act_row_stride():
+    M, K, ld = 5, 256, 384
+    x = synth.activations(M, ld, seed=3, count=4)
+    xt = dev_half(x)[:, :K]
+    xq, xs = mq.quantize_act(xt)
+    q, s = O.quantize_act(np.ascontiguousarray(x[:, :K]), False)
+    assert np.array_equal(xq.cpu().numpy(), O.pack_nibbles(q))
+    assert np.array_equal(logical_xs(xs, M), s)
+
+
+# ----------------------------------------------------------------------------
+# offline: selection and packing
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("N,K,budget,conc", [(512, 512, 0.10, False), (512, 512, 0.0, False), (512, 512, 1.0, False),
+                                             (1024, 4096, 0.10, True), (4096, 4096, 0.10, False),
+                                             (1024, 5120, 0.20, True)])
+def test_select_blocks_bit_exact(N, K, budget, conc):
+    w = synth.weights(N, K, seed=N ^ K)
+    if conc:
+        w = synth.inject_concentrated(w, seed=1)
+    xcal = synth.calibration(K, seed=N ^ K, count=synth.n_outliers(K))
+    rp, ci, h, d = mq.select_blocks(dev_half(w), dev_half(xcal), budget, want_h=True, want_delta=True)
+    p = O.prepare(w, xcal, False, budget)
+    assert np.array_equal(h.cpu().numpy(), p.h)  # bitwise: fixed order, no FMA on either side
+    assert np.array_equal(d.cpu().numpy(), p.delta)
+    assert np.array_equal(rp.cpu().numpy(), p.row_ptr)
+    assert np.array_equal(ci.cpu().numpy(), p.col_idx)
+
+
+def test_select_blocks_bf16_calibration():
+    N, K = 512, 1024
+    w = synth.weights(N, K, seed=5)
+    xcal = synth.calibration(K, seed=5, count=4, dtype="bf16")
+    rp, ci, h, d = mq.select_blocks(dev_half(w), dev_act(xcal, True), 0.1, want_h=True, want_delta=True)
+    p = O.prepare(w, xcal, True, 0.1)
+    assert np.array_equal(h.cpu().numpy(), p.h) and np.array_equal(d.cpu().numpy(), p.delta)
+    assert np.array_equal(ci.cpu().numpy(), p.col_idx)
+
+
+@pytest.mark.parametrize("N,K,budget", [(512, 512, 0.10), (1024, 4096, 0.25), (256, 384, 1.0), (4096, 1024, 0.0)])
+def test_pack_weights_bit_exact(N, K, budget):
+    w = synth.inject_concentrated(synth.weights(N, K, seed=7), seed=7, frac=0.05)
+    xcal = synth.calibration(K, seed=7, count=4)
+    pl = mq.prepare_linear(dev_half(w), dev_half(xcal), budget)
+    p = O.prepare(w, xcal, False, budget)
+    assert np.array_equal(logical_wq(pl.wq, N, K), O.pack_nibbles(p.qw))
+    assert np.array_equal(logical_wsc(pl.wsc, N, K), p.sw)
+    assert pl.nnzb == p.ksel
+    assert np.array_equal(logical_rq(pl.rq, pl.nnzb), p.qr)
+    assert np.array_equal(host_u16(pl.rsc)[: pl.nnzb], p.sr)
+
+
+# ----------------------------------------------------------------------------
+# the fused GEMM
+# ----------------------------------------------------------------------------
+
+def _case(M, N, K, budget, seed, x_dtype="f16", conc=False):
+    x = synth.activations(M, K, seed=seed, count=synth.n_outliers(K), dtype=x_dtype)
+    w = synth.weights(N, K, seed=seed)
+    if conc:
+        w = synth.inject_concentrated(w, seed=seed)
+    xcal = synth.calibration(K, seed=seed, count=synth.n_outliers(K), dtype=x_dtype)
+    return x, w, xcal
+
+
+@pytest.mark.parametrize("M,N,K,budget", [(4, 512, 512, 0.10), (17, 256, 512, 0.5), (33, 384, 768, 1.0),
+                                          (64, 128, 256, 0.25), (100, 256, 1024, 0.3), (1, 128, 128, 1.0)])
+def test_group_dots_bit_exact(M, N, K, budget):
+    x, w, xcal = _case(M, N, K, budget, seed=11)
+    pl = mq.prepare_linear(dev_half(w), dev_half(xcal), budget)
+    xq, xs = mq.quantize_act(dev_half(x))
+    dw, dr = mq.debug_group_dots(xq, xs, M, pl)
+    mq.check_device_error()
+    qx, sx = O.quantize_act(x, False)
+    p = O.prepare(w, xcal, False, budget)
+    assert np.array_equal(dw.cpu().numpy(), O.group_dots(qx, p.qw))
+    if p.ksel:
+        assert np.array_equal(dr.cpu().numpy(), O.residual_dots(qx, p.qr, p.col_idx))
+
+
+def test_group_dots_extremes():
+    """Adversarial codes: every product +49, every product -49, alternating
+    cancellation; sums reach +-6272 per group, exactly."""
+    M, N, K = 32, 128, 256
+    x = np.full((M, K), 7.0, np.float32)
+    w = np.full((N, K), 7.0 * 0.01, np.float32)
+    w[64:, :] *= -1.0
+    x[16:, 1::2] *= -1.0
+    xb, wb = synth.f32_to_f16_bits(x), synth.f32_to_f16_bits(w)
+    xcal = synth.calibration(K, seed=1, count=4)
+    pl = mq.prepare_linear(dev_half(wb), dev_half(xcal), 1.0)
+    xq, xs = mq.quantize_act(dev_half(xb))
+    dw, _ = mq.debug_group_dots(xq, xs, M, pl)
+    qx, _ = O.quantize_act(xb, False)
+    p = O.prepare(wb, xcal, False, 1.0)
+    ref = O.group_dots(qx, p.qw)
+    assert ref.max() == 6272 and ref.min() == -6272 and (ref == 0).any()
+    assert np.array_equal(dw.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("M,N,K,budget,x_dtype", [
+    (4, 512, 512, 0.10, "f16"),      # the 512x512 single linear, top-3 of 32 blocks
+    (1, 256, 512, 0.20, "f16"), (8, 1024, 2048, 0.10, "f16"), (16, 512, 1024, 0.0, "f16"),
+    (17, 384, 640, 0.30, "bf16"), (32, 1024, 4096, 0.10, "f16"), (33, 256, 512, 1.0, "f16"),
+    (64, 512, 1024, 0.10, "bf16"), (65, 256, 768, 0.10, "f16"), (128, 256, 512, 0.10, "f16"),
+    (200, 384, 1280, 0.15, "bf16"),
+])
+def test_gemm_matches_oracle(M, N, K, budget, x_dtype):
+    x, w, xcal = _case(M, N, K, budget, seed=M * 7 + N, x_dtype=x_dtype)
+    isb = x_dtype == "bf16"
+    pl = mq.prepare_linear(dev_half(w), dev_act(xcal, isb), budget)
+    xq, xs = mq.quantize_act(dev_act(x, isb))
+    y32 = mq.gemm(xq, xs, M, pl, out_dtype=torch.float32)
+    y16 = mq.gemm(xq, xs, M, pl, out_dtype=torch.bfloat16)
+    mq.check_device_error()
+    qx, sx = O.quantize_act(x, isb)
+    p = O.prepare(w, xcal, isb, budget)
+    y, a = O.linear(qx, sx, p)
+    check_close(y32.cpu().numpy(), y, a)
+    check_bf16(host_u16(y16), y, a)
+    # deterministic: a second call gives the same bits
+    y32b = mq.gemm(xq, xs, M, pl, out_dtype=torch.float32)
+    assert torch.equal(y32, y32b)
+
+
+def test_gemm_concentrated_block_row():
+    """Every residual block in one block row; no residual anywhere else."""
+    M, N, K = 32, 512, 2048
+    x, w, _ = _case(M, N, K, 0.0, seed=3)
+    G = K // 128
+    rp = np.zeros(N // 64 + 1, np.int32)
+    rp[3:] = G  # block row 2 holds all G blocks
+    ci = np.arange(G, dtype=np.int32)
+    pl = packed_from_csr(dev_half(w), rp, ci)
+    xq, xs = mq.quantize_act(dev_half(x))
+    y32 = mq.gemm(xq, xs, M, pl, out_dtype=torch.float32)
+    p = oracle_prep_for_csr(w, rp, ci)
+    qx, sx = O.quantize_act(x, False)
+    y, a = O.linear(qx, sx, p)
+    check_close(y32.cpu().numpy(), y, a)
+
+
+def test_gemm_both_halves_and_empty_rows():
+    """Blocks in both 64-row halves of a tile at the same group, single halves,
+    and tiles with no residual at all."""
+    M, N, K = 20, 512, 1024
+    x, w, _ = _case(M, N, K, 0.0, seed=9)
+    G = K // 128
+    rows = {0: [0, 3, 7], 1: [3, 5], 2: [], 3: [1], 4: [], 5: [], 6: [0, 7], 7: [0, 1, 2, 3, 4, 5, 6, 7]}
+    rp = np.zeros(N // 64 + 1, np.int32)
+    ci = []
+    for br in range(N // 64):
+        ci += rows[br]
+        rp[br + 1] = len(ci)
+    ci = np.array(ci, np.int32)
+    pl = packed_from_csr(dev_half(w), rp, ci)
+    xq, xs = mq.quantize_act(dev_half(x))
+    y32 = mq.gemm(xq, xs, M, pl, out_dtype=torch.float32)
+    dw, dr = mq.debug_group_dots(xq, xs, M, pl)
+    p = oracle_prep_for_csr(w, rp, ci)
+    qx, sx = O.quantize_act(x, False)
+    y, a = O.linear(qx, sx, p)
+    check_close(y32.cpu().numpy(), y, a)
+    assert np.array_equal(dr.cpu().numpy(), O.residual_dots(qx, p.qr, ci))
+
+
+# ----------------------------------------------------------------------------
+# full-size workloads, sampled outputs
+# ----------------------------------------------------------------------------
+
+def _sampled_parity(M, lin, budget, x_dtype, seed, conc=False, nsamp=384):
+    N, K = lin.N, lin.K
+    x, w, xcal = _case(M, N, K, budget, seed=seed, x_dtype=x_dtype, conc=conc)
+    isb = x_dtype == "bf16"
+    pl = mq.prepare_linear(dev_half(w), dev_act(xcal, isb), budget)
+    xq, xs = mq.quantize_act(dev_act(x, isb))
+    y16 = mq.gemm(xq, xs, M, pl, out_dtype=torch.bfloat16)
+    y32 = mq.gemm(xq, xs, M, pl, out_dtype=torch.float32)
+    mq.check_device_error()
+    qx, sx = O.quantize_act(x, isb)
+    assert np.array_equal(xq.cpu().numpy(), O.pack_nibbles(qx))
+    p = O.prepare(w, xcal, isb, budget)
+    assert np.array_equal(pl.row_ptr.cpu().numpy(), p.row_ptr) and np.array_equal(pl.col_idx[: pl.nnzb].cpu().numpy(), p.col_idx)
+    rng = np.random.default_rng(seed)
+    ms = rng.integers(0, M, nsamp)
+    ns = rng.integers(0, N, nsamp)
+    # plus every row of one selected block row and the last tile's rows
+    if p.ksel:
+        br = int(O.csr_block_rows(p.row_ptr)[0])
+        ns = np.concatenate([ns, np.arange(br * 64, br * 64 + 64), np.arange(N - 16, N)])
+        ms = np.concatenate([ms, np.full(64, M - 1), np.zeros(16, np.int64)])
+    y, a = O.linear_entries(qx, sx, p, ms, ns)
+    check_close(y32.cpu().numpy()[ms, ns], y, a)
+    check_bf16(host_u16(y16)[ms, ns], y, a)
+
+
+@pytest.mark.parametrize("lin", synth.LLAMA3_8B, ids=lambda l: l.name)
+@pytest.mark.parametrize("M", [4, 32])
+def test_llama3_decode_linears_sampled(lin, M):
+    _sampled_parity(M, lin, 0.10, "f16", seed=sum(map(ord, lin.name)) + M)
+
+
+def test_prefill_2048_sampled():
+    _sampled_parity(2048, synth.Linear("gate", 4096, 14336), 0.10, "bf16", seed=2)
+
+
+@pytest.mark.parametrize("M,lin,budget", [(512, synth.QWEN3_32B[6], 0.20), (4, synth.QWEN3_32B[4], 0.05),
+                                          (32, synth.QWEN3_32B[3], 0.10)], ids=["down-512", "gate-4", "o-32"])
+def test_qwen3_sampled_concentrated(M, lin, budget):
+    _sampled_parity(M, lin, budget, "f16", seed=5, conc=True, nsamp=256)
+
+
+# ----------------------------------------------------------------------------
+# failure detection: a bounded device wait that runs out
+# ----------------------------------------------------------------------------
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    mq.set_wait_timeout_ns(2_000_000)  # 2 ms
+    try:
+        mq.debug_wait_timeout()
+        with pytest.raises(mq.MQError) as ei:
+            mq.check_device_error()
+        assert ei.value.status == mq.MQ_ERR_TIMEOUT
+    finally:
+        mq.set_wait_timeout_ns(1_000_000_000)
+    mq.check_device_error()  # cleared
+    x, w, xcal = _case(4, 256, 512, 0.1, seed=1)
+    pl = mq.prepare_linear(dev_half(w), dev_half(xcal), 0.1)
+    y = mq.linear(dev_half(x), pl, out_dtype=torch.float32)
+    mq.check_device_error()
+    qx, sx = O.quantize_act(x, False)
+    yo, a = O.linear(qx, sx, O.prepare(w, xcal, False, 0.1))
+    check_close(y.cpu().numpy(), yo, a)
