@@ -5,94 +5,113 @@
 //
 //   Y[m,n] = sum_g sx[m,g] * ( sw[n,g] * Dw[m,n,g] + sr[n,g] * Dr[m,n,g] )
 //
-// sm_103a design (one CTA = 128 weight rows x TN tokens x a K range):
-//   * INT4 codes run on the 5th-generation tensor cores as E4M3 bytes holding
-//     the same integers exactly (|q| <= 8 is exact in E4M3); products are at
-//     most 49 and a group sum at most 6272 < 2^24, so the fp32 accumulator of
-//     tcgen05.mma kind::f8f6f4 holds every group dot exactly.  (The
-//     integer tensor-core kind is not available on sm_103a.)
-//   * swap-AB: weight rows are the MMA M dimension (128), tokens the N
-//     dimension (TN), so decode batches of 4..32 tokens fill one MMA.
-//   * warp 0 (producer): 1-D bulk copies of the contiguous 8 KiB weight unit,
-//     its 256 B of scales, the residual blocks of this tile and group, a 2-D
-//     TMA box of packed activations (rows past M read as zeros) and the
-//     activation scales, into a 4-deep shared-memory ring.
-//   * warps 2-5 (converters, one per TMEM lane quarter): unpack weight codes
-//     to E4M3 in registers and store them straight into tensor memory (the
-//     MMA's A operand lives in TMEM: no shared-memory round trip), and unpack
-//     the activations into a 128B-swizzled K-major shared-memory B tile.
-//   * warp 1 (MMA issuer): 4 MMAs of K=32 per group into a double-buffered
-//     TMEM accumulator, plus 4 more into a residual accumulator when the
-//     group has a residual block in this tile (tiles and groups without one
-//     issue nothing extra); tcgen05.commit releases the stages.
-//   * warps 6-9 (drain): per group, tcgen05.ld the integer-valued dots and
-//     reduce-add sx * (sw * Dw + sr * Dr) into fp32 registers (the scales
-//     change every 128 inputs, so the accumulator is drained every group).
-//   * split-K: CTAs of one output tile write fp32 partials to the workspace;
-//     the last to arrive (atomic counter) sums them in split order and stores
-//     Y, then resets the counter.  No floating-point atomics: deterministic.
+// sm_103a design.
+//   * Numbers: INT4 codes run on the 5th-generation tensor cores as E4M3 bytes
+//     holding the same integers exactly (|q| <= 8 is exact in E4M3); products
+//     are at most 49 and a group sum at most 6272, so the fp32 accumulator of
+//     tcgen05.mma kind::f8f6f4 holds every group dot exactly.  (The integer
+//     tensor-core kind is not available on sm_103a.)
+//   * Shape: swap-AB.  128 weight rows are the MMA M dimension, TN tokens the
+//     N dimension, so decode batches of 4..32 tokens fill one MMA.  A "unit"
+//     is one 128-row weight tile x UG consecutive 128-input groups (UG = 2
+//     for decode tiles: 16 KiB of codes in one bulk copy).
+//   * Data movement: every operand is laid out so that a unit needs few, large
+//     bulk copies (the bulk-copy engine's cost grows with the number of copies
+//     as much as with bytes): the unit's weight codes and their scales are
+//     contiguous, and so are the group-major packed activations and scales of
+//     its groups.
+//   * Schedule: persistent stream-K.  One CTA per SM takes an equal,
+//     contiguous range of units (tile-major); tiles cut by a range boundary
+//     are finished through the workspace by whichever CTA arrives last, which
+//     sums the pieces in CTA order (deterministic; no floating-point atomics).
+//   * Pipeline per CTA:
+//       warp 0  producer: bulk copies into a ring of shared-memory stages.
+//               The first stages' weights are requested before anything else
+//               (before the block list is read and before waiting on the
+//               preceding kernel: programmatic dependent launch), so weight
+//               streaming overlaps the kernel's start and its predecessor's end.
+//       warp 1  reads the block list of the CTA's tiles into a residual map,
+//               then issues the MMAs: 4 of K=32 per item into a ring of TMEM
+//               accumulators.  An item is one group's base product or, only
+//               where the block list has a block, its residual product, which
+//               reuses the group's activation tile (residual-free groups issue
+//               nothing extra).
+//       converter groups of 4 warps (one per TMEM lane quarter), working on
+//               alternating units: INT4 -> E4M3 in registers; weights go
+//               straight into tensor memory (the MMA's A operand lives in
+//               TMEM: no shared-memory round trip), activations into a
+//               128B-swizzled K-major shared-memory tile.
+//       4 drain warps: per item, tcgen05.ld the integer-valued dots and
+//               reduce-add sx * (sw * Dw) or sx * (sr * Dr) into fp32 registers
+//               (the scales change every 128 inputs); at tile ends, store Y
+//               or a stream-K piece.
 // Every mbarrier wait is bounded (see mbar_wait).
 #include "mq_internal.cuh"
 
 #include <cuda_bf16.h>
 
-#include <mutex>
+#include <algorithm>
 
 namespace mq {
 
-constexpr int kThreads = 320;  // 10 warps
-constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpConv0 = 2, kWarpDrain0 = 6;
-constexpr int kMaxGroupsPerCta = 256;
+constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpConv0 = 2;
+constexpr int kMaxUnitsPerCta = 1024;  // size of the CTA's residual map (in groups: 2 per unit max)
+constexpr int kPlanCtas = 152;         // persistent CTAs (one per GB300 SM)
+constexpr int kMinUnitsPerCta = 4;
 
-template <int TN>
+template <int TN, int UG>
 struct Cfg {
-  // ring depth: enough weight bytes in flight per SM to cover HBM latency
-  static constexpr int kStages = TN <= 32 ? 8 : (TN <= 64 ? 5 : 4);
-  static constexpr int kB = TN * 128;      // E4M3 activations, SW128 K-major (1024-aligned)
-  static constexpr int kA = 8192;          // packed base unit
-  static constexpr int kR = 2 * 4096;      // packed residual blocks (top, bottom halves)
-  static constexpr int kXQ = TN * 64;      // packed activations (TMA box)
-  static constexpr int kWS = 256;          // base scales, 128 x fp16
-  static constexpr int kRS = 256;          // residual scales, 2 x 64 x fp16
-  static constexpr int kSX = TN * 2;       // activation scales, TN x fp16
+  static constexpr int kStages = (TN <= 32) ? (UG == 2 ? 4 : 8) : (TN <= 64 ? 3 : 4);  // shared-memory ring
+  // Converter groups (4 warps each, one per TMEM lane quarter) work on
+  // alternating units, so several units are unpacked at once.
+  static constexpr int kGroups = TN <= 16 ? 4 : (TN <= 32 ? 3 : (TN <= 64 ? 2 : 1));
+  static constexpr int kSlotsPerGroup = kGroups >= 3 ? 2 : 8 / kGroups;
+  static constexpr int kASlots = kGroups * kSlotsPerGroup;  // TMEM A ring (32 cols each), split per group
+  static constexpr int kWarpDrain0 = kWarpConv0 + 4 * kGroups;
+  static constexpr int kThreads = 32 * (kWarpDrain0 + 4);
+  static constexpr int kDSlots = TN <= 16 ? 8 : (TN <= 32 ? 6 : (TN <= 64 ? 4 : 2));  // TMEM accumulators
+  // stage layout: per group u of the unit
+  static constexpr int kB = TN * 128;  // E4M3 activations, SW128 K-major (1024-aligned), per group
+  static constexpr int kXQ = TN * 64;  // packed activations, per group (stride kXQ, or Mp*64 when merged)
   static constexpr int oB = 0;
-  static constexpr int oA = oB + kB;
-  static constexpr int oR = oA + kA;
-  static constexpr int oXQ = oR + kR;
-  static constexpr int oWS = oXQ + kXQ;
-  static constexpr int oRS = oWS + kWS;
-  static constexpr int oSX = oRS + kRS;
-  static constexpr int oEnd = oSX + ((kSX + 15) / 16) * 16;
+  static constexpr int oA = oB + UG * kB;        // packed weight codes, UG x 8192
+  static constexpr int oR = oA + UG * 8192;      // packed residual blocks, UG x (rows 0-63, rows 64-127)
+  static constexpr int oXQ = oR + UG * 2 * 4096;
+  static constexpr int oWS = oXQ + UG * kXQ;     // weight scales, UG x 128 fp16
+  static constexpr int oRS = oWS + UG * 256;     // residual scales, UG x 2 x 64 fp16
+  static constexpr int oSX = oRS + UG * 256;     // activation scales, UG x TN fp16
+  static constexpr int oEnd = oSX + ((UG * TN * 2 + 15) / 16) * 16;
   static constexpr int kStageBytes = (oEnd + 1023) / 1024 * 1024;
-  // TMEM columns: A ring 2 x (32 base + 32 residual), D_w x 2, D_r x 1
   static constexpr int tA = 0;
-  static constexpr int tDw = 128;
-  static constexpr int tDr = 128 + 2 * TN;
-  static constexpr int kTmemNeed = 128 + 3 * TN;
+  static constexpr int tD = kASlots * 32;
+  static constexpr int kTmemNeed = tD + kDSlots * TN;
   static constexpr int kTmemCols = kTmemNeed <= 256 ? 256 : 512;
   static_assert(kTmemNeed <= 512, "TMEM budget");
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align slack*/;
-  static_assert(kSmemBytes + 4096 <= 227 * 1024, "shared memory budget");
+  static_assert(kSmemBytes + 12 * 1024 <= 227 * 1024, "shared memory budget");
   // instruction descriptor: D f32, A/B E4M3, both K-major, N = TN, M = 128
-  static constexpr uint32_t kIdesc = (1u << 4) | (static_cast<uint32_t>(TN >> 3) << 17) |
-                                     (static_cast<uint32_t>(128 >> 4) << 24);
+  static constexpr uint32_t kIdesc =
+      (1u << 4) | (static_cast<uint32_t>(TN >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
 };
 
 struct GemmParams {
+  const uint8_t* xq;   // [G][Mp][64]
+  const uint16_t* xs;  // [G][Mp]
   const uint8_t* wq;
   const uint16_t* wsc;
-  const uint16_t* xs;  // [G][Mp]
   const int32_t* row_ptr;
   const int32_t* col_idx;
   const uint8_t* rq;
   const uint16_t* rsc;
   void* y;
   int y_f32;
-  int32_t* dots_w;  // debug
-  int32_t* dots_r;  // debug
-  float* partials;
-  int32_t* counters;
-  int M, Mp, N, K, G, splits, nnzb;
+  int32_t* dots_w;    // debug
+  int32_t* dots_r;    // debug
+  float* partials;    // [ctas][2 slots][128 rows][TN]
+  int32_t* counters;  // [tiles]
+  int M, Mp, N, K, G, tiles_n, tiles_m, nnzb;
+  int64_t units;  // tiles * G / UG
+  int ctas;
   uint64_t timeout_ns;
   uint32_t* err;
 };
@@ -100,351 +119,482 @@ struct GemmParams {
 // Shared-memory matrix descriptor: 128B-swizzled K-major tile, 8-row atoms of
 // 1024 B (stride byte offset), descriptor version 1, start address >> 4.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | (static_cast<uint64_t>(1024 >> 4) << 32) |
-         (1ull << 46) | (2ull << 61);
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (1ull << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-struct __align__(8) StageInfo {
-  int32_t flags;    // bit 0: residual block for rows 0-63, bit 1: rows 64-127
-  int32_t blk[2];   // CSR entry of each half
-  int32_t pad;
-};
-
-template <int kStages>
+template <int kStages, int kASlots, int kDSlots, int UG>
 struct __align__(8) Ctl {
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t conv_full[2];
-  uint64_t a_empty[2];
-  uint64_t d_full[2];
-  uint64_t d_empty[2];
-  uint64_t dr_full;
-  uint64_t dr_empty;
-  StageInfo info[kStages];
+  uint64_t conv_full[kASlots];
+  uint64_t a_empty[kASlots];
+  uint64_t d_full[kDSlots];
+  uint64_t d_empty[kDSlots];
+  uint64_t drain_bar;  // bounded barrier of the 128 drain threads
+  uint64_t red_bar;    // bulk loads of stream-K pieces
+  uint64_t map_ready;  // residual map of the CTA's units is built
+  int32_t blk[kStages][UG][2];  // CSR entry of each group's top / bottom residual block, or -1
+  int64_t deferred[2];          // tiles this CTA completed last (at most its first and last)
   uint32_t tmem_base;
   int abort_flag;
-  int is_last;
-  int nres_total;  // drain-wide epilogue decision
+  int ndeferred;
 };
 
-template <int TN, bool kDebug>
-__global__ void __launch_bounds__(kThreads, 1)
-    w4a4_residual_gemm_kernel(const __grid_constant__ CUtensorMap xq_map, const GemmParams p) {
-  using C = Cfg<TN>;
-  constexpr int kStages = C::kStages;
+// first unit of CTA c, and the CTA that owns unit u (balanced contiguous ranges)
+__device__ __forceinline__ int64_t cta_first_unit(int64_t c, int64_t U, int64_t P) { return c * U / P; }
+__device__ __forceinline__ int64_t cta_of_unit(int64_t u, int64_t U, int64_t P) { return ((u + 1) * P - 1) / U; }
+
+template <int TN, int UG, bool kDebug>
+__global__ void __launch_bounds__(Cfg<TN, UG>::kThreads, 1) w4a4_residual_gemm_kernel(const GemmParams p) {
+  using C = Cfg<TN, UG>;
+  constexpr int NS = C::kStages, ND = C::kDSlots;
+  constexpr int NG = C::kGroups, SPG = C::kSlotsPerGroup, kWarpDrain0 = C::kWarpDrain0;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ Ctl<kStages> ctl;
-  __shared__ int32_t res_flag_s[2][kMaxGroupsPerCta];  // per local group: CSR entry of top / bottom block or -1
+  __shared__ Ctl<NS, C::kASlots, ND, UG> ctl;
+  __shared__ int32_t res_map[2][kMaxUnitsPerCta];  // per local group: CSR entry of top / bottom block or -1
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x;           // weight tile
-  const int split = blockIdx.y;       // K split
-  const int mt = blockIdx.z;          // token tile
-  const int m0 = mt * TN;
-  const int g_begin = static_cast<int>((static_cast<int64_t>(split) * p.G) / p.splits);
-  const int g_end = static_cast<int>((static_cast<int64_t>(split + 1) * p.G) / p.splits);
-  const int ngroups = g_end - g_begin;
+  const int64_t U = p.units, P = p.ctas, c = blockIdx.x;
+  const int64_t u0 = cta_first_unit(c, U, P), u1 = cta_first_unit(c + 1, U, P);
+  const int nunits = static_cast<int>(u1 - u0);
+  const int G = p.G, GU = p.G / UG;  // groups, units per tile
   volatile int* abort_flag = &ctl.abort_flag;
+  const uint64_t tmo = p.timeout_ns;
+  // Activations of a decode tile (one token tile, m0 = 0) are contiguous over
+  // the unit's groups: one copy, group stride Mp rows; else one copy per group.
+  const bool merged = (p.tiles_m == 1) && (p.Mp <= TN);
+  const int xq_stride = merged ? p.Mp * 64 : C::kXQ;  // bytes between groups in the stage
+  const int sx_stride = merged ? p.Mp : TN;           // fp16 entries between groups in the stage
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&ctl.full[s], 1);
-      mbar_init(&ctl.empty[s], 1 + 128);
+      mbar_init(&ctl.empty[s], 1 + 128);  // MMA commit + the drain threads (they read the scales)
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::kASlots; ++i) {
       mbar_init(&ctl.conv_full[i], 128);
       mbar_init(&ctl.a_empty[i], 1);
+    }
+    for (int i = 0; i < ND; ++i) {
       mbar_init(&ctl.d_full[i], 1);
       mbar_init(&ctl.d_empty[i], 128);
     }
-    mbar_init(&ctl.dr_full, 1);
-    mbar_init(&ctl.dr_empty, 128);
+    mbar_init(&ctl.drain_bar, 128);
+    mbar_init(&ctl.red_bar, 1);
+    mbar_init(&ctl.map_ready, 32);
     ctl.abort_flag = 0;
-    ctl.is_last = 0;
+    ctl.ndeferred = 0;
     fence_mbar_init();
   }
+  // The next kernel may launch now: before its own dependency wait it only
+  // streams read-only weights, and everything else it touches waits for this
+  // grid to complete.
+  pdl_trigger();
   if (warp == kWarpMma) tmem_alloc(&ctl.tmem_base, C::kTmemCols);
-  if (warp == kWarpProducer) {
-    // Residual blocks of this tile's two block rows inside [g_begin, g_end):
-    // the CSR rows are ascending in g, so a scan of each row suffices.
-    for (int i = lane; i < ngroups; i += 32) {
-      res_flag_s[0][i] = -1;
-      res_flag_s[1][i] = -1;
-    }
-    __syncwarp();
-    for (int half = 0; half < 2; ++half) {
-      const int br = 2 * t + half;
-      // entries are clamped to [0, nnzb) so a malformed list cannot index out of bounds
-      const int e0 = p.nnzb ? max(0, min(p.nnzb, p.row_ptr[br])) : 0;
-      const int e1 = p.nnzb ? max(e0, min(p.nnzb, p.row_ptr[br + 1])) : 0;
-      for (int e = e0 + lane; e < e1; e += 32) {
-        const int g = p.col_idx[e];
-        if (g >= g_begin && g < g_end) res_flag_s[half][g - g_begin] = e;
-      }
-    }
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
-  const uint64_t tmo = p.timeout_ns;
+
+  // unit -> tile (weight-tile major: consecutive tiles share a weight tile) -> (t, mt); first group g0
+  auto unit_tile = [&](int64_t u) { return u / GU; };
+  auto unit_g0 = [&](int64_t u) { return static_cast<int>(u % GU) * UG; };
+  auto tile_t = [&](int64_t tile) { return static_cast<int>(tile / p.tiles_m); };
+  auto tile_mt = [&](int64_t tile) { return static_cast<int>(tile % p.tiles_m); };
 
   if (warp == kWarpProducer) {
+    // --- 1. weights (codes + scales) of the first stages, lane i arming stage i
+    const int pre = min(NS, nunits);
+    if (lane < pre) {
+      const int64_t u = u0 + lane;
+      const int64_t wunit = static_cast<int64_t>(tile_t(unit_tile(u))) * G + unit_g0(u);
+      uint8_t* sb = smem + lane * C::kStageBytes;
+      mbar_expect_tx(&ctl.full[lane], UG * (8192 + 256));
+      bulk_g2s(sb + C::oA, p.wq + wunit * 8192, UG * 8192, &ctl.full[lane]);
+      bulk_g2s(sb + C::oWS, p.wsc + wunit * 128, UG * 256, &ctl.full[lane]);
+    }
+    __syncwarp();
+    // --- 2. activations are the preceding kernel's output; the residual map
+    // comes from the MMA warp
+    pdl_wait();
+    volatile int never0 = 0;
+    mbar_wait(&ctl.map_ready, 0, &never0, tmo, p.err);
     if (lane == 0) {
-      int it = 0;
-      for (; it < ngroups; ++it) {
-        const int st = it % kStages;
-        const uint32_t ph = (it / kStages) & 1;
-        if (!mbar_wait(&ctl.empty[st], ph ^ 1, abort_flag, tmo, p.err)) break;
-        const int g = g_begin + it;
-        const int e_top = res_flag_s[0][it], e_bot = res_flag_s[1][it];
-        StageInfo& si = ctl.info[st];
-        si.flags = (e_top >= 0 ? 1 : 0) | (e_bot >= 0 ? 2 : 0);
-        si.blk[0] = e_top;
-        si.blk[1] = e_bot;
+      int i = 0;
+      for (; i < nunits; ++i) {
+        const int st = i % NS;
+        const int64_t u = u0 + i;
+        const int64_t tile = unit_tile(u);
+        const int g0 = unit_g0(u);
+        const int m0 = tile_mt(tile) * TN;
+        const int64_t wunit = static_cast<int64_t>(tile_t(tile)) * G + g0;
         uint8_t* sb = smem + st * C::kStageBytes;
-        const int sx_rows = min(TN, p.Mp - m0);
-        uint32_t bytes = C::kA + C::kWS + C::kXQ + sx_rows * 2;
-        if (e_top >= 0) bytes += 4096 + 128;
-        if (e_bot >= 0) bytes += 4096 + 128;
+        if (i >= pre) {
+          if (!mbar_wait(&ctl.empty[st], ((i / NS) & 1) ^ 1, abort_flag, tmo, p.err)) break;
+          mbar_expect_tx(&ctl.full[st], UG * (8192 + 256));
+          bulk_g2s(sb + C::oA, p.wq + wunit * 8192, UG * 8192, &ctl.full[st]);
+          bulk_g2s(sb + C::oWS, p.wsc + wunit * 128, UG * 256, &ctl.full[st]);
+        }
+        const int rows = min(TN, p.Mp - m0);  // token rows present (multiple of 8)
+        uint32_t bytes = UG * rows * (64 + 2);
+        int e[UG][2];
+#pragma unroll
+        for (int q = 0; q < UG; ++q) {
+          e[q][0] = res_map[0][i * UG + q];
+          e[q][1] = res_map[1][i * UG + q];
+          ctl.blk[st][q][0] = e[q][0];
+          ctl.blk[st][q][1] = e[q][1];
+          bytes += (e[q][0] >= 0 ? 4096 + 128 : 0) + (e[q][1] >= 0 ? 4096 + 128 : 0);
+        }
         mbar_arrive_expect_tx(&ctl.full[st], bytes);
-        const int64_t unit = static_cast<int64_t>(t) * p.G + g;
-        bulk_g2s(sb + C::oA, p.wq + unit * 8192, 8192, &ctl.full[st]);
-        bulk_g2s(sb + C::oWS, p.wsc + unit * 128, 256, &ctl.full[st]);
-        tma_2d_g2s(sb + C::oXQ, &xq_map, g * 64, m0, &ctl.full[st]);
-        bulk_g2s(sb + C::oSX, p.xs + static_cast<int64_t>(g) * p.Mp + m0, sx_rows * 2, &ctl.full[st]);
-        if (e_top >= 0) {
-          bulk_g2s(sb + C::oR, p.rq + static_cast<int64_t>(e_top) * 4096, 4096, &ctl.full[st]);
-          bulk_g2s(sb + C::oRS, p.rsc + static_cast<int64_t>(e_top) * 64, 128, &ctl.full[st]);
+        if (merged) {
+          bulk_g2s(sb + C::oXQ, p.xq + static_cast<int64_t>(g0) * p.Mp * 64, UG * p.Mp * 64, &ctl.full[st]);
+          bulk_g2s(sb + C::oSX, p.xs + static_cast<int64_t>(g0) * p.Mp, UG * p.Mp * 2, &ctl.full[st]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < UG; ++q) {
+            const int64_t row0 = static_cast<int64_t>(g0 + q) * p.Mp + m0;
+            bulk_g2s(sb + C::oXQ + q * C::kXQ, p.xq + row0 * 64, rows * 64, &ctl.full[st]);
+            bulk_g2s(sb + C::oSX + q * TN * 2, p.xs + row0, rows * 2, &ctl.full[st]);
+          }
         }
-        if (e_bot >= 0) {
-          bulk_g2s(sb + C::oR + 4096, p.rq + static_cast<int64_t>(e_bot) * 4096, 4096, &ctl.full[st]);
-          bulk_g2s(sb + C::oRS + 128, p.rsc + static_cast<int64_t>(e_bot) * 64, 128, &ctl.full[st]);
-        }
+#pragma unroll
+        for (int q = 0; q < UG; ++q)
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            if (e[q][h] >= 0) {
+              bulk_g2s(sb + C::oR + (q * 2 + h) * 4096, p.rq + static_cast<int64_t>(e[q][h]) * 4096, 4096,
+                       &ctl.full[st]);
+              bulk_g2s(sb + C::oRS + (q * 2 + h) * 128, p.rsc + static_cast<int64_t>(e[q][h]) * 64, 128,
+                       &ctl.full[st]);
+            }
       }
-      // Before the CTA may exit, every copy issued must have landed (the
-      // last kStages stages; earlier ones were consumed).  Bounded as well.
+      // Before the CTA may exit, every copy issued must have landed: the last
+      // NS stages (earlier ones were consumed).  A stage whose weights were
+      // requested but whose arrival never came (loop left early) gets it now.
       volatile int never = 0;
-      for (int j = max(0, it - kStages); j < it; ++j)
-        mbar_wait(&ctl.full[j % kStages], (j / kStages) & 1, &never, tmo, p.err);
+      for (int j = i; j < pre; ++j) mbar_arrive(&ctl.full[j]);
+      const int issued = max(i, pre);
+      for (int j = max(0, issued - NS); j < issued; ++j)
+        mbar_wait(&ctl.full[j % NS], (j / NS) & 1, &never, tmo, p.err);
     }
   } else if (warp == kWarpMma) {
-    if (lane == 0) {
-      int nres = 0;
-      int issued = 0;
-      for (int it = 0; it < ngroups; ++it) {
-        const int st = it % kStages;
-        const int a = it & 1, d = it & 1;
-        const uint32_t aph = (it >> 1) & 1;
-        if (!mbar_wait(&ctl.conv_full[a], aph, abort_flag, tmo, p.err)) break;
-        if (!mbar_wait(&ctl.d_empty[d], aph ^ 1, abort_flag, tmo, p.err)) break;
-        const bool has_res = ctl.info[st].flags != 0;
-        if (has_res && !mbar_wait(&ctl.dr_empty, (nres & 1) ^ 1, abort_flag, tmo, p.err)) break;
-        tc_fence_after();
-        const uint32_t b_addr = smem_u32(smem + st * C::kStageBytes + C::oB);
-        const uint32_t a_col = tmem + C::tA + a * 64;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          tc_mma_ts(tmem + C::tDw + d * TN, a_col + 8 * j, sw128_desc(b_addr + 32 * j), C::kIdesc, j > 0);
-        if (has_res) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            tc_mma_ts(tmem + C::tDr, a_col + 32 + 8 * j, sw128_desc(b_addr + 32 * j), C::kIdesc, j > 0);
+    // residual map of this CTA's groups, from the block-list rows of its tiles
+    const int ngroups = nunits * UG;
+    for (int i = lane; i < ngroups; i += 32) {
+      res_map[0][i] = -1;
+      res_map[1][i] = -1;
+    }
+    __syncwarp();
+    if (p.nnzb > 0) {
+      const int64_t gbase = u0 * UG;  // CTA-local group index = (tile*G + g) - gbase
+      for (int64_t tile = unit_tile(u0); tile <= unit_tile(u1 - 1); ++tile) {
+        const int t = tile_t(tile);
+        for (int half = 0; half < 2; ++half) {
+          const int br = 2 * t + half;
+          // entries are clamped to [0, nnzb) so a malformed list cannot index out of bounds
+          const int e0 = max(0, min(p.nnzb, p.row_ptr[br]));
+          const int e1 = max(e0, min(p.nnzb, p.row_ptr[br + 1]));
+          for (int e = e0 + lane; e < e1; e += 32) {
+            const int g = p.col_idx[e];
+            const int64_t lg = tile * G + g - gbase;
+            if (g >= 0 && g < G && lg >= 0 && lg < ngroups) res_map[half][lg] = e;
+          }
         }
-        tc_commit(&ctl.empty[st]);
-        tc_commit(&ctl.a_empty[a]);
-        tc_commit(&ctl.d_full[d]);
-        if (has_res) {
-          tc_commit(&ctl.dr_full);
-          ++nres;
-        }
-        issued = it + 1;
       }
-      // Let the last MMAs finish before TMEM can be released.
-      if (issued > 0) {
-        const int it = issued - 1;
+    }
+    mbar_arrive(&ctl.map_ready);
+    if (lane == 0) {
+      int item = 0;   // global item order (accumulator ring)
+      int gitem[NG];  // per converter group item counters (A rings)
+#pragma unroll
+      for (int gg = 0; gg < NG; ++gg) gitem[gg] = 0;
+      bool ok = true;
+      for (int i = 0; i < nunits && ok; ++i) {
+        const int st = i % NS;
+        const int grp = i % NG;
+        const uint32_t b_base = smem_u32(smem + st * C::kStageBytes + C::oB);
+        for (int q = 0; q < UG && ok; ++q) {
+          int nitems = 1;
+          for (int k = 0; k < nitems; ++k, ++item) {
+            int li = 0;
+#pragma unroll
+            for (int gg = 0; gg < NG; ++gg)
+              if (gg == grp) li = gitem[gg]++;
+            const int a = grp * SPG + li % SPG, d = item % ND;
+            if (!mbar_wait(&ctl.conv_full[a], (li / SPG) & 1, abort_flag, tmo, p.err)) { ok = false; break; }
+            if (k == 0) nitems = 1 + ((ctl.blk[st][q][0] >= 0) || (ctl.blk[st][q][1] >= 0));
+            if (!mbar_wait(&ctl.d_empty[d], ((item / ND) & 1) ^ 1, abort_flag, tmo, p.err)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t a_col = tmem + C::tA + a * 32;
+            const uint32_t d_col = tmem + C::tD + d * TN;
+            const uint32_t b_addr = b_base + q * C::kB;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              tc_mma_ts(d_col, a_col + 8 * j, sw128_desc(b_addr + 32 * j), C::kIdesc, j > 0);
+            tc_commit(&ctl.a_empty[a]);
+            tc_commit(&ctl.d_full[d]);
+          }
+        }
+        if (ok) tc_commit(&ctl.empty[st]);
+      }
+      // Let the issued MMAs finish before TMEM can be released.
+      if (item > 0) {
         volatile int never = 0;
-        mbar_wait(&ctl.d_full[it & 1], (it >> 1) & 1, &never, tmo, p.err);
+        const int last = item - 1;
+        mbar_wait(&ctl.d_full[last % ND], (last / ND) & 1, &never, tmo, p.err);
       }
     }
   } else if (warp < kWarpDrain0) {
     // ---------------- converters ----------------
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;      // weight row of this thread (TMEM lane)
-    const int ctid = (warp - kWarpConv0) * 32 + lane;
+    const int r = quarter * 32 + lane;  // weight row of this thread (TMEM lane)
+    const int grp = (warp - kWarpConv0) >> 2;
+    const int ctid = (((warp - kWarpConv0) & 3) << 5) + lane;  // 0..127 within the group
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    for (int it = 0; it < ngroups; ++it) {
-      const int st = it % kStages;
-      const uint32_t ph = (it / kStages) & 1;
-      const int a = it & 1;
-      const uint32_t aph = (it >> 1) & 1;
-      if (!mbar_wait(&ctl.full[st], ph, abort_flag, tmo, p.err)) break;
-      if (!mbar_wait(&ctl.a_empty[a], aph ^ 1, abort_flag, tmo, p.err)) break;
-      tc_fence_after();
+    const int half = r >> 6;
+    int item = 0;  // this group's items
+    bool ok = true;
+    for (int i = grp; i < nunits && ok; i += NG) {
+      const int st = i % NS;
+      if (!mbar_wait(&ctl.full[st], (i / NS) & 1, abort_flag, tmo, p.err)) break;
       uint8_t* sb = smem + st * C::kStageBytes;
-      const uint32_t a_col = tmem + lane_base + C::tA + a * 64;
-      // weights: K-step j of row r is the 16 bytes at j*2048 + r*16
+      for (int q = 0; q < UG; ++q) {
+        const int e_top = ctl.blk[st][q][0], e_bot = ctl.blk[st][q][1];
+        {  // base item: weights of row r, K-step j = the 16 bytes at j*2048 + r*16
+          const int a = grp * SPG + item % SPG;
+          if (!mbar_wait(&ctl.a_empty[a], ((item / SPG) & 1) ^ 1, abort_flag, tmo, p.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_col = tmem + lane_base + C::tA + a * 32;
+          const uint8_t* wsrc = sb + C::oA + q * 8192 + r * 16;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint4 pk = *reinterpret_cast<const uint4*>(sb + C::oA + j * 2048 + r * 16);
-        uint32_t e[8];
-        int4x8_to_e4m3(pk.x, e[0], e[1]);
-        int4x8_to_e4m3(pk.y, e[2], e[3]);
-        int4x8_to_e4m3(pk.z, e[4], e[5]);
-        int4x8_to_e4m3(pk.w, e[6], e[7]);
-        tmem_st8(a_col + 8 * j, e);
-      }
-      const int flags = ctl.info[st].flags;
-      const int half = r >> 6;
-      if (flags != 0) {  // whole warp takes this branch together (tcgen05.st is warp-wide)
-        const bool mine = (flags >> half) & 1;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t e[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-          if (mine) {
-            const uint4 pk = *reinterpret_cast<const uint4*>(sb + C::oR + half * 4096 + j * 1024 + (r & 63) * 16);
-            int4x8_to_e4m3(pk.x, e[0], e[1]);
-            int4x8_to_e4m3(pk.y, e[2], e[3]);
-            int4x8_to_e4m3(pk.z, e[4], e[5]);
-            int4x8_to_e4m3(pk.w, e[6], e[7]);
+          for (int j = 0; j < 4; ++j) {
+            const uint4 pk = *reinterpret_cast<const uint4*>(wsrc + j * 2048);
+            uint32_t ev[8];
+            int4x8_to_e4m3(pk.x, ev[0], ev[1]);
+            int4x8_to_e4m3(pk.y, ev[2], ev[3]);
+            int4x8_to_e4m3(pk.z, ev[4], ev[5]);
+            int4x8_to_e4m3(pk.w, ev[6], ev[7]);
+            tmem_st8(a_col + 8 * j, ev);
           }
-          tmem_st8(a_col + 32 + 8 * j, e);
+          // activations: row m, K-step j -> two 16-byte chunks 2j, 2j+1 of the
+          // 128-byte swizzled row (chunk c of row m sits at chunk c ^ (m & 7))
+          const uint8_t* xsrc = sb + C::oXQ + q * xq_stride;
+          uint8_t* btile = sb + C::oB + q * C::kB;
+          for (int idx = ctid; idx < TN * 4; idx += 128) {
+            const int m = idx >> 2, j = idx & 3;
+            const uint4 pk = *reinterpret_cast<const uint4*>(xsrc + m * 64 + j * 16);
+            uint4 lo, hi;
+            int4x8_to_e4m3(pk.x, lo.x, lo.y);
+            int4x8_to_e4m3(pk.y, lo.z, lo.w);
+            int4x8_to_e4m3(pk.z, hi.x, hi.y);
+            int4x8_to_e4m3(pk.w, hi.z, hi.w);
+            uint8_t* row = btile + (m >> 3) * 1024 + (m & 7) * 128;
+            *reinterpret_cast<uint4*>(row + (((2 * j) ^ (m & 7)) * 16)) = lo;
+            *reinterpret_cast<uint4*>(row + (((2 * j + 1) ^ (m & 7)) * 16)) = hi;
+          }
+          tc_wait_st();
+          fence_proxy_async_smem();
+          tc_fence_before();
+          mbar_arrive(&ctl.conv_full[a]);
+          ++item;
+        }
+        if (e_top >= 0 || e_bot >= 0) {  // residual item (same activation tile)
+          const int a = grp * SPG + item % SPG;
+          if (!mbar_wait(&ctl.a_empty[a], ((item / SPG) & 1) ^ 1, abort_flag, tmo, p.err)) { ok = false; break; }
+          tc_fence_after();
+          if ((half == 0 ? e_top : e_bot) >= 0) {  // warp-uniform: a warp's 32 rows sit in one half
+            const uint32_t a_col = tmem + lane_base + C::tA + a * 32;
+            const uint8_t* rsrc = sb + C::oR + (q * 2 + half) * 4096 + (r & 63) * 16;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint4 pk = *reinterpret_cast<const uint4*>(rsrc + j * 1024);
+              uint32_t ev[8];
+              int4x8_to_e4m3(pk.x, ev[0], ev[1]);
+              int4x8_to_e4m3(pk.y, ev[2], ev[3]);
+              int4x8_to_e4m3(pk.z, ev[4], ev[5]);
+              int4x8_to_e4m3(pk.w, ev[6], ev[7]);
+              tmem_st8(a_col + 8 * j, ev);
+            }
+            tc_wait_st();
+          }
+          tc_fence_before();
+          mbar_arrive(&ctl.conv_full[a]);
+          ++item;
         }
       }
-      // activations: row m, K-step j -> two 16-byte chunks 2j, 2j+1 of the
-      // 128-byte swizzled row (chunk c of row m sits at chunk c ^ (m & 7))
-      for (int idx = ctid; idx < TN * 4; idx += 128) {
-        const int m = idx >> 2, j = idx & 3;
-        const uint4 pk = *reinterpret_cast<const uint4*>(sb + C::oXQ + m * 64 + j * 16);
-        uint4 lo, hi;
-        int4x8_to_e4m3(pk.x, lo.x, lo.y);
-        int4x8_to_e4m3(pk.y, lo.z, lo.w);
-        int4x8_to_e4m3(pk.z, hi.x, hi.y);
-        int4x8_to_e4m3(pk.w, hi.z, hi.w);
-        uint8_t* row = sb + C::oB + (m >> 3) * 1024 + (m & 7) * 128;
-        *reinterpret_cast<uint4*>(row + (((2 * j) ^ (m & 7)) * 16)) = lo;
-        *reinterpret_cast<uint4*>(row + (((2 * j + 1) ^ (m & 7)) * 16)) = hi;
-      }
-      tc_wait_st();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&ctl.conv_full[a]);
     }
   } else {
-    // ---------------- drain ----------------
+    // ---------------- drain + epilogue ----------------
+    pdl_wait();  // the workspace and Y may still be in use by the preceding kernel
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const int dtid = (warp - kWarpDrain0) * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const int n = t * kTileN + r;
+    const int half = r >> 6;
     float acc[TN];
 #pragma unroll
     for (int i = 0; i < TN; ++i) acc[i] = 0.0f;
-    int nres = 0;
+    int item = 0;
+    int nbar = 0;  // phases of drain_bar used so far
     bool ok = true;
-    for (int it = 0; it < ngroups && ok; ++it) {
-      const int st = it % kStages;
-      const uint32_t ph = (it / kStages) & 1;
-      const int d = it & 1;
-      const uint32_t dph = (it >> 1) & 1;
-      if (!mbar_wait(&ctl.full[st], ph, abort_flag, tmo, p.err)) { ok = false; break; }
-      if (!mbar_wait(&ctl.d_full[d], dph, abort_flag, tmo, p.err)) { ok = false; break; }
+    // bounded barrier of the 128 drain threads (an mbarrier, so a broken pipeline cannot hang it)
+    auto drain_sync = [&]() -> bool {
+      mbar_arrive(&ctl.drain_bar);
+      const bool passed = mbar_wait(&ctl.drain_bar, nbar & 1, abort_flag, tmo, p.err);
+      ++nbar;
+      return passed;
+    };
+    for (int i = 0; i < nunits && ok; ++i) {
+      const int st = i % NS;
+      const int64_t u = u0 + i;
+      if (!mbar_wait(&ctl.full[st], (i / NS) & 1, abort_flag, tmo, p.err)) { ok = false; break; }
       const uint8_t* sb = smem + st * C::kStageBytes;
-      const StageInfo si = ctl.info[st];
-      const bool any_res = si.flags != 0;
-      const int half = r >> 6;
-      const bool mine = (si.flags >> half) & 1;
-      if (any_res && !mbar_wait(&ctl.dr_full, nres & 1, abort_flag, tmo, p.err)) { ok = false; break; }
-      tc_fence_after();
-      const float sw = __half2float(__ushort_as_half(reinterpret_cast<const uint16_t*>(sb + C::oWS)[r]));
-      const float sr = mine ? __half2float(__ushort_as_half(reinterpret_cast<const uint16_t*>(sb + C::oRS)[r])) : 0.0f;
-      const uint16_t* sxs = reinterpret_cast<const uint16_t*>(sb + C::oSX);
-      const int g = g_begin + it;
+      const int64_t tile = unit_tile(u);
+      const int g0 = unit_g0(u);
+      const int n = tile_t(tile) * kTileN + r;
+      const int m0 = tile_mt(tile) * TN;
+      for (int q = 0; q < UG && ok; ++q) {
+        const int e_top = ctl.blk[st][q][0], e_bot = ctl.blk[st][q][1];
+        const int nitems = 1 + (e_top >= 0 || e_bot >= 0);
+        const int e_mine = half == 0 ? e_top : e_bot;
+        const uint16_t* sxs = reinterpret_cast<const uint16_t*>(sb + C::oSX) + q * sx_stride;
+        for (int k = 0; k < nitems; ++k, ++item) {
+          const int d = item % ND;
+          if (!mbar_wait(&ctl.d_full[d], (item / ND) & 1, abort_flag, tmo, p.err)) { ok = false; break; }
+          tc_fence_after();
+          const bool use = (k == 0) || (e_mine >= 0);
+          const float s =
+              (k == 0) ? __half2float(__ushort_as_half(reinterpret_cast<const uint16_t*>(sb + C::oWS)[q * 128 + r]))
+              : use    ? __half2float(__ushort_as_half(reinterpret_cast<const uint16_t*>(sb + C::oRS)[q * 128 + r]))
+                       : 0.0f;
 #pragma unroll
-      for (int c = 0; c < TN / 16; ++c) {
-        uint32_t dw[16], dr[16];
-        tmem_ld16(tmem + lane_base + C::tDw + d * TN + 16 * c, dw);
-        if (any_res) tmem_ld16(tmem + lane_base + C::tDr + 16 * c, dr);
-        tc_wait_ld();
-        if (kDebug) {
+          for (int cc = 0; cc < TN / 16; ++cc) {
+            uint32_t dv[16];
+            tmem_ld16(tmem + lane_base + C::tD + d * TN + 16 * cc, dv);
+            tc_wait_ld();
+            if (kDebug) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int m = m0 + 16 * c + i;
-            if (m < p.M) {
-              p.dots_w[(static_cast<int64_t>(m) * p.N + n) * p.G + g] = static_cast<int32_t>(__uint_as_float(dw[i]));
-              if (mine)
-                p.dots_r[(static_cast<int64_t>(m) * p.nnzb + si.blk[half]) * 64 + (r & 63)] =
-                    static_cast<int32_t>(__uint_as_float(dr[i]));
+              for (int i2 = 0; i2 < 16; ++i2) {
+                const int m = m0 + 16 * cc + i2;
+                if (m < p.M && use) {
+                  const int32_t v = static_cast<int32_t>(__uint_as_float(dv[i2]));
+                  if (k == 0)
+                    p.dots_w[(static_cast<int64_t>(m) * p.N + n) * G + g0 + q] = v;
+                  else
+                    p.dots_r[(static_cast<int64_t>(m) * p.nnzb + e_mine) * 64 + (r & 63)] = v;
+                }
+              }
+            } else if (use) {
+#pragma unroll
+              for (int i2 = 0; i2 < 16; ++i2) {
+                const int mi = 16 * cc + i2;
+                const float sx = (m0 + mi < p.Mp) ? __half2float(__ushort_as_half(sxs[mi])) : 0.0f;
+                acc[mi] = fmaf(sx, s * __uint_as_float(dv[i2]), acc[mi]);
+              }
             }
           }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int mi = 16 * c + i;
-            const float sx = (m0 + mi < p.Mp) ? __half2float(__ushort_as_half(sxs[mi])) : 0.0f;
-            float tsum = sw * __uint_as_float(dw[i]);
-            if (mine) tsum = fmaf(sr, __uint_as_float(dr[i]), tsum);
-            acc[mi] = fmaf(sx, tsum, acc[mi]);
-          }
+          tc_fence_before();
+          mbar_arrive(&ctl.d_empty[d]);
         }
       }
-      tc_fence_before();
-      mbar_arrive(&ctl.d_empty[d]);
-      if (any_res) {
-        mbar_arrive(&ctl.dr_empty);
-        ++nres;
-      }
-      mbar_arrive(&ctl.empty[st]);
-    }
-    // ---------------- epilogue ----------------
-    // All 128 drain threads agree on whether to run it (a thread that gave up
-    // must not leave the others waiting at a named barrier).
-    if (!ok) *abort_flag = 1;
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    if (dtid == 0) ctl.nres_total = (*abort_flag) ? 0 : 1;
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    const bool run_epilogue = ctl.nres_total != 0;
-    if (!kDebug && run_epilogue) {
-      const int mvalid = min(TN, p.M - m0);
-      const int tiles_n = p.N / kTileN;
-      const int tile_id = mt * tiles_n + t;
-      auto store = [&](int mi, float v) {
-        const int64_t off = static_cast<int64_t>(m0 + mi) * p.N + n;
-        if (p.y_f32)
-          static_cast<float*>(p.y)[off] = v;
-        else
-          static_cast<__nv_bfloat16*>(p.y)[off] = __float2bfloat16_rn(v);
-      };
-      if (p.splits == 1) {
-#pragma unroll
-        for (int mi = 0; mi < TN; ++mi)
-          if (mi < mvalid) store(mi, acc[mi]);
-      } else {
-        float* part = p.partials + (static_cast<int64_t>(tile_id) * p.splits) * (TN * kTileN);
-        float* mine_part = part + static_cast<int64_t>(split) * (TN * kTileN);
-#pragma unroll
-        for (int mi = 0; mi < TN; ++mi) mine_part[mi * kTileN + r] = acc[mi];
-        __threadfence();
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (dtid == 0) {
-          const int old = atomicAdd(&p.counters[tile_id], 1);
-          ctl.is_last = (old == p.splits - 1) ? 1 : 0;
-        }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (ctl.is_last) {
-          __threadfence();
+      if (!ok) break;
+      mbar_arrive(&ctl.empty[st]);  // scales read: the stage may be refilled
+      // ---- tile end: store Y, or hand a stream-K piece to the workspace ----
+      const bool tile_end = (g0 + UG == G) || (i == nunits - 1);
+      if (!kDebug && tile_end) {
+        const int mvalid = min(TN, p.M - m0);
+        const int64_t tu0 = tile * GU, tu1 = tu0 + GU;  // the tile's units
+        if (tu0 >= u0 && tu1 <= u1) {  // whole tile in this CTA
 #pragma unroll
           for (int mi = 0; mi < TN; ++mi) {
             if (mi < mvalid) {
-              float sum = 0.0f;
-              for (int s = 0; s < p.splits; ++s)
-                sum += (s == split) ? acc[mi] : __ldcg(part + static_cast<int64_t>(s) * (TN * kTileN) + mi * kTileN + r);
-              store(mi, sum);
+              const int64_t off = static_cast<int64_t>(m0 + mi) * p.N + n;
+              if (p.y_f32)
+                static_cast<float*>(p.y)[off] = acc[mi];
+              else
+                static_cast<__nv_bfloat16*>(p.y)[off] = __float2bfloat16_rn(acc[mi]);
             }
           }
-          if (dtid == 0) p.counters[tile_id] = 0;
+        } else {
+          // A stream-K piece: write it (thread-contiguous rows), count it in;
+          // the CTA that brings the count to the number of pieces finishes
+          // the tile after its own range is done (deferred: no stall here).
+          const int slot = (tile == unit_tile(u0)) ? 0 : 1;
+          float4* mypart = reinterpret_cast<float4*>(p.partials + ((c * 2 + slot) * kTileN + r) * TN);
+#pragma unroll
+          for (int q4 = 0; q4 < TN / 4; ++q4)
+            mypart[q4] = make_float4(acc[4 * q4], acc[4 * q4 + 1], acc[4 * q4 + 2], acc[4 * q4 + 3]);
+          __threadfence();
+          if (!drain_sync()) { ok = false; break; }
+          if (dtid == 0) {
+            const int64_t cf = cta_of_unit(tu0, U, P), cl = cta_of_unit(tu1 - 1, U, P);
+            const int old = atomicAdd(&p.counters[tile], 1);
+            if (old == static_cast<int>(cl - cf)) ctl.deferred[ctl.ndeferred++] = tile;
+          }
         }
+#pragma unroll
+        for (int mi = 0; mi < TN; ++mi) acc[mi] = 0.0f;
+      }
+    }
+    // ---- finish the tiles this CTA completed last: bulk-copy every piece
+    // into the (now idle) stage memory, sum in CTA order, store Y ----
+    if (!kDebug && ok && drain_sync()) {
+      const int nd = ctl.ndeferred;
+      constexpr uint32_t kPieceBytes = TN * kTileN * 4;
+      const int per_round = (NS * C::kStageBytes) / kPieceBytes;
+      int nred = 0;  // phases of red_bar used
+      for (int di = 0; di < nd && ok; ++di) {
+        const int64_t tile = ctl.deferred[di];
+        const int64_t tu0 = tile * GU, tu1 = tu0 + GU;
+        const int64_t cf = cta_of_unit(tu0, U, P), cl = cta_of_unit(tu1 - 1, U, P);
+        const int m0 = tile_mt(tile) * TN;
+        const int n = tile_t(tile) * kTileN + r;
+        const int mvalid = min(TN, p.M - m0);
+#pragma unroll
+        for (int mi = 0; mi < TN; ++mi) acc[mi] = 0.0f;
+        for (int64_t cb = cf; cb <= cl && ok; cb += per_round) {
+          const int npieces = static_cast<int>(min(static_cast<int64_t>(per_round), cl - cb + 1));
+          if (dtid == 0) {
+            __threadfence();
+            fence_proxy_async_global();  // other CTAs' generic writes -> this bulk (async) read
+            mbar_arrive_expect_tx(&ctl.red_bar, npieces * kPieceBytes);
+            for (int k = 0; k < npieces; ++k) {
+              const int64_t c2 = cb + k;
+              const int slot2 = (tile == unit_tile(cta_first_unit(c2, U, P))) ? 0 : 1;
+              bulk_g2s(smem + k * kPieceBytes, p.partials + (c2 * 2 + slot2) * (kTileN * TN), kPieceBytes,
+                       &ctl.red_bar);
+            }
+          }
+          if (!mbar_wait(&ctl.red_bar, nred & 1, abort_flag, tmo, p.err)) { ok = false; break; }
+          ++nred;
+          for (int k = 0; k < npieces; ++k) {
+            const float4* piece = reinterpret_cast<const float4*>(smem + k * kPieceBytes) + r * (TN / 4);
+#pragma unroll
+            for (int q4 = 0; q4 < TN / 4; ++q4) {
+              const float4 v = piece[q4];
+              acc[4 * q4] += v.x;
+              acc[4 * q4 + 1] += v.y;
+              acc[4 * q4 + 2] += v.z;
+              acc[4 * q4 + 3] += v.w;
+            }
+          }
+          if (!drain_sync()) { ok = false; break; }  // smem free for the next round
+        }
+        if (!ok) break;
+#pragma unroll
+        for (int mi = 0; mi < TN; ++mi) {
+          if (mi < mvalid) {
+            const int64_t off = static_cast<int64_t>(m0 + mi) * p.N + n;
+            if (p.y_f32)
+              static_cast<float*>(p.y)[off] = acc[mi];
+            else
+              static_cast<__nv_bfloat16*>(p.y)[off] = __float2bfloat16_rn(acc[mi]);
+          }
+        }
+        if (dtid == 0) p.counters[tile] = 0;  // ready for the next launch
       }
     }
   }
@@ -459,28 +609,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // host side
 // ---------------------------------------------------------------------------
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  });
-  return fn;
-}
-
 struct Plan {
-  int tn;
-  int tiles_m;
-  int splits;
+  int tn, ug;
+  int tiles_m, tiles_n, G;
+  int64_t units;
+  int ctas;
   size_t ws_partials;  // bytes
   size_t ws_counters;  // bytes
 };
@@ -494,77 +627,72 @@ static int pick_tn(int64_t M) {
 
 static size_t a256(size_t b) { return (b + 255) / 256 * 256; }
 
-static Plan make_plan(int64_t M, int64_t N, int64_t K, int nsm) {
+// The plan depends only on (M, N, K): the workspace size must not depend on the device.
+static Plan make_plan(int64_t M, int64_t N, int64_t K) {
   Plan pl;
   pl.tn = pick_tn(M);
   pl.tiles_m = static_cast<int>((M + pl.tn - 1) / pl.tn);
-  const int64_t G = K / kGroup;
-  const int64_t base = (N / kTileN) * pl.tiles_m;
-  const int64_t target = 2LL * nsm;
-  int64_t s = (target + base - 1) / base;  // enough CTAs to cover the GPU twice
-  const int64_t max_s = G >= 8 ? G / 4 : 1;  // keep >= 4 groups per split
-  if (s > max_s) s = max_s;
-  const int64_t min_s = (G + kMaxGroupsPerCta - 1) / kMaxGroupsPerCta;  // CTA-local residual map size
-  if (s < min_s) s = min_s;
-  if (s < 1) s = 1;
-  pl.splits = static_cast<int>(s);
-  if (pl.splits > 1) {
-    pl.ws_partials = a256(static_cast<size_t>(base) * pl.splits * pl.tn * kTileN * sizeof(float));
-    pl.ws_counters = a256(static_cast<size_t>(base) * sizeof(int32_t));
-  } else {
-    pl.ws_partials = 0;
-    pl.ws_counters = 0;
-  }
+  pl.tiles_n = static_cast<int>(N / kTileN);
+  pl.G = static_cast<int>(K / kGroup);
+  pl.ug = (pl.tn <= 64 && pl.G % 2 == 0) ? 2 : 1;
+  pl.units = static_cast<int64_t>(pl.tiles_m) * pl.tiles_n * (pl.G / pl.ug);
+  // at least kMinUnitsPerCta units per CTA bounds the pieces a tile is cut into
+  int64_t ctas = std::min<int64_t>(kPlanCtas, std::max<int64_t>(1, pl.units / kMinUnitsPerCta));
+  const int64_t min_ctas = (pl.units * pl.ug + kMaxUnitsPerCta - 1) / kMaxUnitsPerCta;
+  if (ctas < min_ctas) ctas = min_ctas;
+  pl.ctas = static_cast<int>(ctas);
+  pl.ws_partials = a256(static_cast<size_t>(pl.ctas) * 2 * pl.tn * kTileN * sizeof(float));
+  pl.ws_counters = a256(static_cast<size_t>(pl.tiles_m) * pl.tiles_n * sizeof(int32_t));
   return pl;
 }
 
-// The workspace size must not depend on the device, so the plan for sizing
-// uses the largest SM count the library targets (152 on GB300).
-constexpr int kPlanSms = 152;
-
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  const Plan pl = make_plan(M, N, K, kPlanSms);
+  const Plan pl = make_plan(M, N, K);
   return pl.ws_partials + pl.ws_counters;
 }
 
-template <int TN, bool kDebug>
-static mq_status launch_tn(const CUtensorMap& map, const GemmParams& gp, const Plan& pl, cudaStream_t stream) {
-  using C = Cfg<TN>;
-  auto kern = w4a4_residual_gemm_kernel<TN, kDebug>;
+template <int TN, int UG, bool kDebug>
+static mq_status launch_cfg(const GemmParams& gp, const Plan& pl, cudaStream_t stream) {
+  using C = Cfg<TN, UG>;
+  auto kern = w4a4_residual_gemm_kernel<TN, UG, kDebug>;
   static bool attr_set = false;  // per template instance
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
       return launch_status("gemm: smem attribute");
     attr_set = true;
   }
-  dim3 grid(gp.N / kTileN, pl.splits, pl.tiles_m);
-  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(map, gp);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(pl.ctas), 1, 1);
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, gp) != cudaSuccess) return launch_status("gemm launch");
   return launch_status("gemm");
+}
+
+template <int TN, bool kDebug>
+static mq_status launch_tn(const GemmParams& gp, const Plan& pl, cudaStream_t stream) {
+  return pl.ug == 2 ? launch_cfg<TN, (TN <= 64 ? 2 : 1), kDebug>(gp, pl, stream) : launch_cfg<TN, 1, kDebug>(gp, pl, stream);
 }
 
 mq_status gemm_launch(const uint8_t* xq, const uint16_t* xs, int64_t M, const uint8_t* wq, const uint16_t* wsc,
                       int64_t N, int64_t K, const int32_t* row_ptr, const int32_t* col_idx, int64_t nnzb,
                       const uint8_t* rq, const uint16_t* rsc, void* y, mq_dtype yt, int32_t* dots_w,
                       int32_t* dots_r, void* ws, size_t ws_bytes, cudaStream_t stream) {
-  const Plan pl = make_plan(M, N, K, kPlanSms);
-  if (ws_bytes < pl.ws_partials + pl.ws_counters || (pl.ws_partials && ws == nullptr))
+  const Plan pl = make_plan(M, N, K);
+  if (ws_bytes < pl.ws_partials + pl.ws_counters || ws == nullptr)
     return set_error(MQ_ERR_WORKSPACE, "gemm: workspace of %zu bytes needed, %zu given",
                      pl.ws_partials + pl.ws_counters, ws_bytes);
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return set_error(MQ_ERR_CUDA, "gemm: cuTensorMapEncodeTiled unavailable");
-  CUtensorMap map;
-  const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(M)};
-  const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(K / 2)};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(pl.tn)};
-  const cuuint32_t estride[2] = {1, 1};
-  CUresult cr = enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(xq), gdim, gstride, box, estride,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (cr != CUDA_SUCCESS) return set_error(MQ_ERR_CUDA, "gemm: tensor map encode failed (%d)", static_cast<int>(cr));
   GemmParams gp;
+  gp.xq = xq;
+  gp.xs = xs;
   gp.wq = wq;
   gp.wsc = wsc;
-  gp.xs = xs;
   gp.row_ptr = row_ptr;
   gp.col_idx = col_idx;
   gp.rq = rq;
@@ -573,24 +701,27 @@ mq_status gemm_launch(const uint8_t* xq, const uint16_t* xs, int64_t M, const ui
   gp.y_f32 = yt == MQ_F32;
   gp.dots_w = dots_w;
   gp.dots_r = dots_r;
-  gp.partials = pl.ws_partials ? static_cast<float*>(ws) : nullptr;
-  gp.counters = pl.ws_partials ? reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + pl.ws_partials) : nullptr;
+  gp.partials = static_cast<float*>(ws);
+  gp.counters = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + pl.ws_partials);
   gp.M = static_cast<int>(M);
   gp.Mp = static_cast<int>((M + 7) / 8 * 8);
   gp.N = static_cast<int>(N);
   gp.K = static_cast<int>(K);
-  gp.G = static_cast<int>(K / kGroup);
-  gp.splits = pl.splits;
+  gp.G = pl.G;
+  gp.tiles_n = pl.tiles_n;
+  gp.tiles_m = pl.tiles_m;
   gp.nnzb = static_cast<int>(nnzb);
+  gp.units = pl.units;
+  gp.ctas = pl.ctas;
   gp.timeout_ns = wait_timeout_ns();
   gp.err = device_error_word();
   if (!gp.err) return set_error(MQ_ERR_CUDA, "gemm: device error word unavailable");
   const bool dbg = dots_w != nullptr;
   switch (pl.tn) {
-    case 16: return dbg ? launch_tn<16, true>(map, gp, pl, stream) : launch_tn<16, false>(map, gp, pl, stream);
-    case 32: return dbg ? launch_tn<32, true>(map, gp, pl, stream) : launch_tn<32, false>(map, gp, pl, stream);
-    case 64: return dbg ? launch_tn<64, true>(map, gp, pl, stream) : launch_tn<64, false>(map, gp, pl, stream);
-    default: return dbg ? launch_tn<128, true>(map, gp, pl, stream) : launch_tn<128, false>(map, gp, pl, stream);
+    case 16: return dbg ? launch_tn<16, true>(gp, pl, stream) : launch_tn<16, false>(gp, pl, stream);
+    case 32: return dbg ? launch_tn<32, true>(gp, pl, stream) : launch_tn<32, false>(gp, pl, stream);
+    case 64: return dbg ? launch_tn<64, true>(gp, pl, stream) : launch_tn<64, false>(gp, pl, stream);
+    default: return dbg ? launch_tn<128, true>(gp, pl, stream) : launch_tn<128, false>(gp, pl, stream);
   }
 }
 

@@ -48,19 +48,27 @@ __device__ __forceinline__ void load4(const uint16_t* p, float (&v)[4]) {
   }
 }
 
-// xs layout: [K/128][Mp], Mp = round_up(M, 8); the kernel also zeroes the
-// padding entries m in [M, Mp).
+// Output layouts (group-major, so the GEMM fetches one group's activation
+// tile with a single bulk copy): xq [K/128][Mp][64] bytes, xs [K/128][Mp]
+// fp16, Mp = round_up(M, 8); the padding tokens m in [M, Mp) get zero codes
+// and zero scales.
 template <bool kBf16>
 __global__ void __launch_bounds__(256) quantize_act_kernel(const uint16_t* __restrict__ x, int64_t M,
                                                            int64_t K, int64_t ldx, int64_t Mp,
                                                            uint8_t* __restrict__ xq,
                                                            uint16_t* __restrict__ xs) {
+  // The next kernel (typically the GEMM, which starts by streaming weights)
+  // may launch at once; x may be the preceding kernel's output, so wait for it.
+  pdl_trigger();
+  pdl_wait();
   const int64_t G = K / kGroup;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= Mp * G) return;
   const int64_t m = warp / G, g = warp % G;
-  if (m >= M) {  // padding row of the scale table
+  uint16_t* qdst = reinterpret_cast<uint16_t*>(xq + (g * Mp + m) * (kGroup / 2)) + lane;
+  if (m >= M) {  // padding token
+    *qdst = 0;
     if (lane == 0) xs[g * Mp + m] = 0;
     return;
   }
@@ -74,8 +82,7 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const uint16_t* __res
   uint32_t packed = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) packed |= (static_cast<uint32_t>(code_of(v[i], s)) & 0xFu) << (4 * i);
-  *reinterpret_cast<uint16_t*>(xq + m * (K / 2) + g * (kGroup / 2) + 2 * lane) =
-      static_cast<uint16_t>(packed);
+  *qdst = static_cast<uint16_t>(packed);
   if (lane == 0) xs[g * Mp + m] = sb;
 }
 
@@ -85,12 +92,19 @@ mq_status quantize_act_launch(const void* x, mq_dtype xt, int64_t M, int64_t K, 
   const int64_t warps = Mp * (K / kGroup);
   const int64_t blocks = (warps * 32 + 255) / 256;
   if (blocks > 0x7FFFFFFF) return set_error(MQ_ERR_INVALID_ARG, "quantize_act: problem too large");
-  if (xt == MQ_BF16)
-    quantize_act_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        static_cast<const uint16_t*>(x), M, K, ldx, Mp, xq, xs);
-  else
-    quantize_act_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        static_cast<const uint16_t*>(x), M, K, ldx, Mp, xq, xs);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const uint16_t* xp = static_cast<const uint16_t*>(x);
+  const cudaError_t e = (xt == MQ_BF16) ? cudaLaunchKernelEx(&cfg, quantize_act_kernel<true>, xp, M, K, ldx, Mp, xq, xs)
+                                        : cudaLaunchKernelEx(&cfg, quantize_act_kernel<false>, xp, M, K, ldx, Mp, xq, xs);
+  if (e != cudaSuccess) return launch_status("quantize_act launch");
   return launch_status("quantize_act");
 }
 

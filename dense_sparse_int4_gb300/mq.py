@@ -102,12 +102,12 @@ def padded_tokens(M: int) -> int:
 # ---------------------------------------------------------------------------
 
 def quantize_act(x: torch.Tensor, xq: torch.Tensor | None = None, xs: torch.Tensor | None = None, stream=None):
-    """x [M, K] fp16/bf16 (row stride x.stride(0)) -> xq [M, K/2] uint8, xs [K/128, Mp] fp16."""
+    """x [M, K] fp16/bf16 (row stride x.stride(0)) -> xq [K/128, Mp, 64] uint8, xs [K/128, Mp] fp16."""
     M, K = x.shape
     if x.stride(1) != 1:
         raise ValueError("x must have unit stride along K")
     if xq is None:
-        xq = torch.empty((M, K // 2), dtype=torch.uint8, device=x.device)
+        xq = torch.empty((K // 128, padded_tokens(M), 64), dtype=torch.uint8, device=x.device)
     if xs is None:
         xs = torch.empty((K // 128, padded_tokens(M)), dtype=torch.float16, device=x.device)
     _check(lib().mq_quantize_act(_ptr(x), _dtype_code(x.dtype), M, K, x.stride(0), _ptr(xq), _ptr(xs),
@@ -235,7 +235,7 @@ def debug_group_dots(xq, xs, M: int, pl: PackedLinear, stream=None):
                                      _ptr(pl.rq) if nz else None, _ptr(pl.rsc) if nz else None, _ptr(dw),
                                      _ptr(dr) if nz else None, _ptr(ws), wsb, _stream(stream)),
            "mq_debug_group_dots")
-    return dw, dr[: pl.nnzb]
+    return dw, dr[:, : pl.nnzb]
 
 
 def linear(x: torch.Tensor, pl: PackedLinear, out_dtype=torch.bfloat16, stream=None) -> torch.Tensor:

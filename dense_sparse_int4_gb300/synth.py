@@ -31,7 +31,9 @@ def _rng(seed: int, stream: int, sub: int = 0) -> np.random.Generator:
 
 
 def f32_to_f16_bits(a: np.ndarray) -> np.ndarray:
-    return np.ascontiguousarray(a, np.float32).astype(np.float16).view(np.uint16)
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.float16)
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
 
 
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:

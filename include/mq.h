@@ -72,8 +72,14 @@ typedef enum { MQ_F16 = 0, MQ_BF16 = 1, MQ_F32 = 2 } mq_dtype;
  * Quantize X per token and per 128-input group.
  *   x    [M, ldx] MQ_F16 or MQ_BF16 (xt), row-major, row stride ldx >= K
  *        elements; x and ldx*2 bytes 8-byte aligned.  Values must be finite.
- *   xq   [M, K/2] packed codes (row-major, dense), 16-byte aligned.
- *   xs   [M, K/128] fp16 scale bits (row-major, dense), 2-byte aligned.
+ *   Mp   = round_up(M, 8) (padding tokens m in [M, Mp) get zero codes and scales).
+ *   xq   [K/128][Mp][64] bytes, group-major: byte (g*Mp + m)*64 + j holds the
+ *        codes of token m, inputs 128g + 2j (low nibble) and 128g + 2j + 1
+ *        (high nibble).  K*Mp/2 bytes, 16-byte aligned.
+ *   xs   [K/128][Mp] fp16 scale bits: entry g*Mp + m is the scale of token m in
+ *        group g.  16-byte aligned.
+ *   (Group-major so the GEMM fetches a group's activation tile, codes and
+ *   scales, with one bulk copy each.)
  * Bit-exact against the definition above: amax, amax/7 and v/scale are formed
  * in IEEE fp32 and each rounds to the same value the exact rational would.
  */

@@ -46,6 +46,17 @@ def logical_rq(rq: torch.Tensor, nnzb: int) -> np.ndarray:
     return O.unpack_nibbles(a)
 
 
+def logical_xq(xq: torch.Tensor, M: int) -> np.ndarray:
+    """[K/128][Mp][64] bytes -> packed [M, K/2] (token-major)."""
+    a = xq.cpu().numpy()
+    G, Mp, _ = a.shape
+    return a.transpose(1, 0, 2).reshape(Mp, G * 64)[:M].copy()
+
+
+def xq_padding(xq: torch.Tensor, M: int) -> np.ndarray:
+    return xq.cpu().numpy()[:, M:, :]
+
+
 def logical_xs(xs: torch.Tensor, M: int) -> np.ndarray:
     """[K/128][Mp] -> [M, K/128]."""
     return host_u16(xs)[:, :M].T.copy()

@@ -12,7 +12,8 @@ import torch
 import oracle as O
 from dense_sparse_int4_gb300 import mq, synth
 from tests.gpu_helpers import (check_bf16, check_close, dev_act, dev_half, host_u16, logical_rq, logical_wq,
-                               logical_wsc, logical_xs, oracle_prep_for_csr, packed_from_csr)
+                               logical_wsc, logical_xq, logical_xs, oracle_prep_for_csr, packed_from_csr,
+                               xq_padding)
 
 pytestmark = pytest.mark.gpu
 
@@ -46,9 +47,9 @@ def test_quantize_act_bit_exact(M, K, dtype):
     xq, xs = mq.quantize_act(xt)
     torch.cuda.synchronize()
     q, s = O.quantize_act(x, dtype == "bf16")
-    assert np.array_equal(xq.cpu().numpy(), O.pack_nibbles(q))
+    assert np.array_equal(logical_xq(xq, M), O.pack_nibbles(q))
     assert np.array_equal(logical_xs(xs, M), s)
-    assert not host_u16(xs)[:, M:].any()  # padding entries zeroed
+    assert not host_u16(xs)[:, M:].any() and not xq_padding(xq, M).any()  # padding tokens zeroed
 
 
 def test_quantize_act_row_stride():
@@ -57,7 +58,7 @@ def test_quantize_act_row_stride():
     xt = dev_half(x)[:, :K]
     xq, xs = mq.quantize_act(xt)
     q, s = O.quantize_act(np.ascontiguousarray(x[:, :K]), False)
-    assert np.array_equal(xq.cpu().numpy(), O.pack_nibbles(q))
+    assert np.array_equal(logical_xq(xq, M), O.pack_nibbles(q))
     assert np.array_equal(logical_xs(xs, M), s)
 
 
@@ -232,7 +233,7 @@ def _sampled_parity(M, lin, budget, x_dtype, seed, conc=False, nsamp=384):
     y32 = mq.gemm(xq, xs, M, pl, out_dtype=torch.float32)
     mq.check_device_error()
     qx, sx = O.quantize_act(x, isb)
-    assert np.array_equal(xq.cpu().numpy(), O.pack_nibbles(qx))
+    assert np.array_equal(logical_xq(xq, M), O.pack_nibbles(qx))
     p = O.prepare(w, xcal, isb, budget)
     assert np.array_equal(pl.row_ptr.cpu().numpy(), p.row_ptr) and np.array_equal(pl.col_idx[: pl.nnzb].cpu().numpy(), p.col_idx)
     rng = np.random.default_rng(seed)
