@@ -1,0 +1,71 @@
+// mq_w4a4_residual_gemm_noalloc: the fused GEMM for callers that cannot
+// allocate device memory (a runtime whose allocator is owned by someone else,
+// a process that must not call cudaMalloc while a graph or a latency-critical
+// loop is live, an embedder that passes in only its own input and output
+// buffers).  Instead of a caller-provided workspace, it uses the fixed scratch
+// array below.
+//
+// The array is a file-scope __device__ variable: every GPU that loads this
+// library holds kNoAllocScratchBytes of it until the process exits.  Host
+// code cannot use the array's name as a device address, so on the first call
+// on each device, with that device current, the entry point resolves the
+// address with cudaGetSymbolAddress (checking the result) and caches it.
+#include <mutex>
+
+#include "mq_internal.cuh"
+
+namespace mq {
+
+// 8 MiB: the GEMM needs two fp32 pieces of a 128-row x TN-token tile per
+// persistent CTA plus one counter per tile, which is at most ~5 MB for decode
+// batches of up to 32 tokens at any N and K.
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+static void* g_noalloc_ptr[kNoAllocMaxDevices];
+static std::mutex g_noalloc_mu;
+
+static mq_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return launch_status("noalloc: cudaGetDevice");
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return set_error(MQ_ERR_UNSUPPORTED_DEVICE, "noalloc: device index %d", dev);
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr)
+      return set_error(MQ_ERR_CUDA, "noalloc: scratch address on device %d: %s", dev, cudaGetErrorString(e));
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return MQ_OK;
+}
+
+}  // namespace mq
+
+extern "C" mq_status mq_w4a4_residual_gemm_noalloc(const uint8_t* xq, const uint16_t* xs, int64_t M,
+                                                   const uint8_t* wq, const uint16_t* wsc, int64_t N, int64_t K,
+                                                   const int32_t* row_ptr, const int32_t* col_idx, int64_t nnzb,
+                                                   const uint8_t* rq, const uint16_t* rsc, void* y, mq_dtype yt,
+                                                   mq_stream_t stream) {
+  using namespace mq;
+  const size_t need = mq_gemm_workspace_bytes(M, N, K);
+  if (need == 0)
+    return set_error(MQ_ERR_INVALID_ARG, "noalloc gemm: bad sizes M=%lld N=%lld K=%lld", (long long)M, (long long)N,
+                     (long long)K);
+  if (need > kNoAllocScratchBytes)
+    return set_error(MQ_ERR_WORKSPACE,
+                     "noalloc gemm: M=%lld N=%lld K=%lld needs %zu bytes of scratch, more than the fixed %zu "
+                     "(supported: up to 32 tokens)",
+                     (long long)M, (long long)N, (long long)K, need, kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  if (mq_status s = noalloc_scratch(&scratch); s != MQ_OK) return s;
+  // The array keeps the previous call's contents: the tile counters must
+  // start at zero, so the used range is cleared on the stream first.
+  if (cudaMemsetAsync(scratch, 0, need, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return launch_status("noalloc gemm: clearing scratch");
+  return mq_w4a4_residual_gemm(xq, xs, M, wq, wsc, N, K, row_ptr, col_idx, nnzb, rq, rsc, y, yt, scratch, need,
+                               stream);
+}

@@ -22,6 +22,7 @@ MQ_F16, MQ_BF16, MQ_F32 = 0, 1, 2
 EXPORTS = (
     "mq_quantize_act", "mq_num_selected", "mq_select_workspace_bytes", "mq_select_blocks",
     "mq_pack_weights", "mq_gemm_workspace_bytes", "mq_gemm_workspace_init", "mq_w4a4_residual_gemm",
+    "mq_w4a4_residual_gemm_noalloc",
     "mq_debug_group_dots", "mq_check_device_error", "mq_set_wait_timeout_ns", "mq_debug_wait_timeout",
     "mq_status_string", "mq_last_error", "mq_version",
 )

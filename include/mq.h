@@ -180,6 +180,30 @@ mq_status mq_w4a4_residual_gemm(const uint8_t* xq, const uint16_t* xs, int64_t M
                                 void* ws, size_t ws_bytes, mq_stream_t stream);
 
 /*
+ * The fused GEMM without a caller-provided workspace, for callers that cannot
+ * allocate device memory (their allocator belongs to another runtime, or they
+ * may not call cudaMalloc while a captured graph or a latency-critical loop is
+ * live) and can only hand over their own inputs and outputs.  This entry point
+ * has no counterpart in the paper; it is a deployment convenience.
+ *   Arguments and results as mq_w4a4_residual_gemm, without ws / ws_bytes.
+ *   Scratch: one fixed 8 MiB array in the library's device memory (held on
+ *     every GPU that loads the library until the process exits).  That covers
+ *     up to 32 tokens at any N and K; larger problems return MQ_ERR_WORKSPACE.
+ *   The first call on a device resolves the array's device address (with that
+ *     device current); make that first call before any stream capture.
+ *   The array is shared by every call and keeps the last call's contents; each
+ *     call clears the part it uses on `stream` before the kernel.  Calls that
+ *     overlap on the GPU (two streams, or two devices' threads racing on one
+ *     device) race on the array: serialize them.
+ *   Allocates nothing (no cudaMalloc / cudaFree, no allocating library call).
+ */
+mq_status mq_w4a4_residual_gemm_noalloc(const uint8_t* xq, const uint16_t* xs, int64_t M,
+                                        const uint8_t* wq, const uint16_t* wsc, int64_t N, int64_t K,
+                                        const int32_t* row_ptr, const int32_t* col_idx, int64_t nnzb,
+                                        const uint8_t* rq, const uint16_t* rsc, void* y, mq_dtype yt,
+                                        mq_stream_t stream);
+
+/*
  * Test hook: the same kernel, but instead of the fp32 reduce-add it writes the
  * raw integer group dots it computed on the tensor cores:
  *   dw [M, N, K/128] int32 : Dw[m, n, g]
