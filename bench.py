@@ -239,7 +239,7 @@ class Step:
         self.lins, self.xs_dev = lins, xs_dev
         self.copies = copies
         if budget0:  # same base weights, no residual: the budget-0 kernel
-            self.copies = [{k: mq.PackedLinear(v.N, v.K, 0, v.wq, v.wsc, v.row_ptr, v.col_idx, v.rq, v.rsc)
+            self.copies = [{k: mq.PackedLinear(v.N, v.K, 0, v.wpk, v.row_ptr, v.col_idx, v.rpk)
                             for k, v in c.items()} for c in copies]
         self.q = {}
         for M in MS:

@@ -17,13 +17,11 @@ mq_status select_blocks_launch(const uint16_t* w, int64_t N, int64_t K, const vo
                                int64_t C, int64_t ksel, int32_t* row_ptr, int32_t* col_idx, double* h_out,
                                double* delta_out, void* ws, cudaStream_t stream);
 mq_status pack_weights_launch(const uint16_t* w, int64_t N, int64_t K, const int32_t* row_ptr,
-                              const int32_t* col_idx, int64_t nnzb, uint8_t* wq, uint16_t* wsc, uint8_t* rq,
-                              uint16_t* rsc, cudaStream_t stream);
+                              const int32_t* col_idx, int64_t nnzb, uint8_t* wpk, uint8_t* rpk, cudaStream_t stream);
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
-mq_status gemm_launch(const uint8_t* xq, const uint16_t* xs, int64_t M, const uint8_t* wq, const uint16_t* wsc,
-                      int64_t N, int64_t K, const int32_t* row_ptr, const int32_t* col_idx, int64_t nnzb,
-                      const uint8_t* rq, const uint16_t* rsc, void* y, mq_dtype yt, int32_t* dots_w,
-                      int32_t* dots_r, void* ws, size_t ws_bytes, cudaStream_t stream);
+mq_status gemm_launch(const uint8_t* xq, const uint16_t* xs, int64_t M, const uint8_t* wpk, int64_t N, int64_t K,
+                      const int32_t* row_ptr, const int32_t* col_idx, int64_t nnzb, const uint8_t* rpk, void* y,
+                      mq_dtype yt, int32_t* dots_w, int32_t* dots_r, void* ws, size_t ws_bytes, cudaStream_t stream);
 mq_status wait_timeout_probe_launch(cudaStream_t stream);
 mq_status error_word_address(uint32_t** out);
 
@@ -179,19 +177,18 @@ mq_status mq_select_blocks(const uint16_t* w, int64_t N, int64_t K, const void* 
 }
 
 mq_status mq_pack_weights(const uint16_t* w, int64_t N, int64_t K, const int32_t* row_ptr, const int32_t* col_idx,
-                          int64_t nnzb, uint8_t* wq, uint16_t* wsc, uint8_t* rq, uint16_t* rsc, mq_stream_t stream) {
-  MQ_CHECK(w && wq && wsc, MQ_ERR_INVALID_ARG, "pack_weights: NULL pointer");
+                          int64_t nnzb, uint8_t* wpk, uint8_t* rpk, mq_stream_t stream) {
+  MQ_CHECK(w && wpk, MQ_ERR_INVALID_ARG, "pack_weights: NULL pointer");
   MQ_CHECK(sizes_ok(1, N, K), MQ_ERR_INVALID_ARG, "pack_weights: bad sizes N=%lld K=%lld", (long long)N,
            (long long)K);
   MQ_CHECK(nnzb >= 0 && nnzb <= (N / kBlockRows) * (K / kGroup), MQ_ERR_INVALID_ARG, "pack_weights: bad nnzb %lld",
            (long long)nnzb);
-  MQ_CHECK(nnzb == 0 || (row_ptr && col_idx && rq && rsc), MQ_ERR_INVALID_ARG,
+  MQ_CHECK(nnzb == 0 || (row_ptr && col_idx && rpk), MQ_ERR_INVALID_ARG,
            "pack_weights: residual pointers are NULL but nnzb = %lld", (long long)nnzb);
-  MQ_CHECK(aligned(w, 8) && aligned(wq, 16) && aligned(wsc, 16) && aligned(rq, 16) && aligned(rsc, 16),
-           MQ_ERR_ALIGNMENT, "pack_weights: w must be 8-byte aligned, outputs 16-byte aligned");
+  MQ_CHECK(aligned(w, 8) && aligned(wpk, 16) && aligned(rpk, 16), MQ_ERR_ALIGNMENT,
+           "pack_weights: w must be 8-byte aligned, outputs 16-byte aligned");
   if (mq_status s = check_device(); s != MQ_OK) return s;
-  return pack_weights_launch(w, N, K, row_ptr, col_idx, nnzb, wq, wsc, rq, rsc,
-                             reinterpret_cast<cudaStream_t>(stream));
+  return pack_weights_launch(w, N, K, row_ptr, col_idx, nnzb, wpk, rpk, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t mq_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
@@ -207,46 +204,46 @@ mq_status mq_gemm_workspace_init(void* ws, size_t ws_bytes, mq_stream_t stream) 
   return MQ_OK;
 }
 
-static mq_status gemm_common(const uint8_t* xq, const uint16_t* xs, int64_t M, const uint8_t* wq, const uint16_t* wsc,
-                             int64_t N, int64_t K, const int32_t* row_ptr, const int32_t* col_idx, int64_t nnzb,
-                             const uint8_t* rq, const uint16_t* rsc, void* ws, size_t ws_bytes) {
-  MQ_CHECK(xq && xs && wq && wsc, MQ_ERR_INVALID_ARG, "gemm: NULL pointer");
+static mq_status gemm_common(const uint8_t* xq, const uint16_t* xs, int64_t M, const uint8_t* wpk, int64_t N,
+                             int64_t K, const int32_t* row_ptr, const int32_t* col_idx, int64_t nnzb,
+                             const uint8_t* rpk, void* ws, size_t ws_bytes) {
+  MQ_CHECK(xq && xs && wpk, MQ_ERR_INVALID_ARG, "gemm: NULL pointer");
   MQ_CHECK(sizes_ok(M, N, K), MQ_ERR_INVALID_ARG, "gemm: bad sizes M=%lld N=%lld K=%lld", (long long)M,
            (long long)N, (long long)K);
   MQ_CHECK(nnzb >= 0 && nnzb <= (N / kBlockRows) * (K / kGroup), MQ_ERR_INVALID_ARG, "gemm: bad nnzb %lld",
            (long long)nnzb);
-  MQ_CHECK(nnzb == 0 || (row_ptr && col_idx && rq && rsc), MQ_ERR_INVALID_ARG,
+  MQ_CHECK(nnzb == 0 || (row_ptr && col_idx && rpk), MQ_ERR_INVALID_ARG,
            "gemm: residual pointers are NULL but nnzb = %lld", (long long)nnzb);
-  MQ_CHECK(aligned(xq, 16) && aligned(xs, 16) && aligned(wq, 16) && aligned(wsc, 16) && aligned(rq, 16) &&
-               aligned(rsc, 16) && aligned(row_ptr, 4) && aligned(col_idx, 4),
-           MQ_ERR_ALIGNMENT, "gemm: xq, xs, wq, wsc, rq, rsc must be 16-byte aligned");
+  MQ_CHECK(aligned(xq, 16) && aligned(xs, 16) && aligned(wpk, 16) && aligned(rpk, 16) && aligned(row_ptr, 4) &&
+               aligned(col_idx, 4),
+           MQ_ERR_ALIGNMENT, "gemm: xq, xs, wpk, rpk must be 16-byte aligned");
   const size_t need = gemm_workspace_bytes(M, N, K);
   MQ_CHECK(ws_bytes >= need && (need == 0 || (ws && aligned(ws, 256))), MQ_ERR_WORKSPACE,
            "gemm: workspace of %zu bytes (256-aligned) needed, %zu given", need, ws_bytes);
   return check_device();
 }
 
-mq_status mq_w4a4_residual_gemm(const uint8_t* xq, const uint16_t* xs, int64_t M, const uint8_t* wq,
-                                const uint16_t* wsc, int64_t N, int64_t K, const int32_t* row_ptr,
-                                const int32_t* col_idx, int64_t nnzb, const uint8_t* rq, const uint16_t* rsc, void* y,
-                                mq_dtype yt, void* ws, size_t ws_bytes, mq_stream_t stream) {
+mq_status mq_w4a4_residual_gemm(const uint8_t* xq, const uint16_t* xs, int64_t M, const uint8_t* wpk, int64_t N,
+                                int64_t K, const int32_t* row_ptr, const int32_t* col_idx, int64_t nnzb,
+                                const uint8_t* rpk, void* y, mq_dtype yt, void* ws, size_t ws_bytes,
+                                mq_stream_t stream) {
   MQ_CHECK(y, MQ_ERR_INVALID_ARG, "gemm: y is NULL");
   MQ_CHECK(yt == MQ_BF16 || yt == MQ_F32, MQ_ERR_INVALID_ARG, "gemm: y must be bf16 or fp32");
   MQ_CHECK(aligned(y, yt == MQ_F32 ? 4 : 2), MQ_ERR_ALIGNMENT, "gemm: y misaligned");
-  if (mq_status s = gemm_common(xq, xs, M, wq, wsc, N, K, row_ptr, col_idx, nnzb, rq, rsc, ws, ws_bytes); s != MQ_OK)
+  if (mq_status s = gemm_common(xq, xs, M, wpk, N, K, row_ptr, col_idx, nnzb, rpk, ws, ws_bytes); s != MQ_OK)
     return s;
-  return gemm_launch(xq, xs, M, wq, wsc, N, K, row_ptr, col_idx, nnzb, rq, rsc, y, yt, nullptr, nullptr, ws, ws_bytes,
+  return gemm_launch(xq, xs, M, wpk, N, K, row_ptr, col_idx, nnzb, rpk, y, yt, nullptr, nullptr, ws, ws_bytes,
                      reinterpret_cast<cudaStream_t>(stream));
 }
 
-mq_status mq_debug_group_dots(const uint8_t* xq, const uint16_t* xs, int64_t M, const uint8_t* wq,
-                              const uint16_t* wsc, int64_t N, int64_t K, const int32_t* row_ptr,
-                              const int32_t* col_idx, int64_t nnzb, const uint8_t* rq, const uint16_t* rsc,
-                              int32_t* dw, int32_t* dr, void* ws, size_t ws_bytes, mq_stream_t stream) {
+mq_status mq_debug_group_dots(const uint8_t* xq, const uint16_t* xs, int64_t M, const uint8_t* wpk, int64_t N,
+                              int64_t K, const int32_t* row_ptr, const int32_t* col_idx, int64_t nnzb,
+                              const uint8_t* rpk, int32_t* dw, int32_t* dr, void* ws, size_t ws_bytes,
+                              mq_stream_t stream) {
   MQ_CHECK(dw && (nnzb == 0 || dr), MQ_ERR_INVALID_ARG, "debug_group_dots: NULL output");
-  if (mq_status s = gemm_common(xq, xs, M, wq, wsc, N, K, row_ptr, col_idx, nnzb, rq, rsc, ws, ws_bytes); s != MQ_OK)
+  if (mq_status s = gemm_common(xq, xs, M, wpk, N, K, row_ptr, col_idx, nnzb, rpk, ws, ws_bytes); s != MQ_OK)
     return s;
-  return gemm_launch(xq, xs, M, wq, wsc, N, K, row_ptr, col_idx, nnzb, rq, rsc, nullptr, MQ_F32, dw, dr, ws, ws_bytes,
+  return gemm_launch(xq, xs, M, wpk, N, K, row_ptr, col_idx, nnzb, rpk, nullptr, MQ_F32, dw, dr, ws, ws_bytes,
                      reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -89,8 +89,8 @@ struct Cfg {
   static constexpr int kB = TN * 128;  // E4M3 activations, SW128 K-major (1024-aligned)
   static constexpr int kXQ = TN * 64;  // packed activations (group stride kXQ, or Mp*64 when merged)
   static constexpr int oB = 0;
-  static constexpr int oA = oB + UG * kB;     // packed weight codes, UG x 8192
-  static constexpr int oXQ = oA + UG * 8192;
+  static constexpr int oA = oB + UG * kB;     // UG packed weight records (codes, then scales)
+  static constexpr int oXQ = oA + UG * kWRecBytes;
   static constexpr int oEnd = oXQ + UG * kXQ;
   static constexpr int kStageBytes = (oEnd + 1023) / 1024 * 1024;
   static constexpr int kRingBytes = kStages * kStageBytes;
@@ -115,12 +115,10 @@ struct Cfg {
 struct GemmParams {
   const uint8_t* xq;   // [G][Mp][64]
   const uint16_t* xs;  // [G][Mp]
-  const uint8_t* wq;
-  const uint16_t* wsc;
+  const uint8_t* wpk;  // base records
   const int32_t* row_ptr;
   const int32_t* col_idx;
-  const uint8_t* rq;
-  const uint16_t* rsc;
+  const uint8_t* rpk;  // residual records
   void* y;
   int y_f32;
   int32_t* dots_w;    // debug
@@ -285,10 +283,13 @@ __global__ void __launch_bounds__(Cfg<TN, UG>::kThreads, 1) w4a4_residual_gemm_k
       const int64_t u = u0 + lane;
       const int64_t wunit = static_cast<int64_t>(tile_t(unit_tile(u))) * G + unit_g0(u);
       uint8_t* sb = smem + lane * C::kStageBytes;
-      mbar_expect_tx(&ctl.full[lane], UG * 8192);
-      bulk_g2s(sb + C::oA, p.wq + wunit * 8192, UG * 8192, &ctl.full[lane]);
+      mbar_expect_tx(&ctl.full[lane], UG * kWRecBytes);
+      bulk_g2s(sb + C::oA, p.wpk + wunit * kWRecBytes, UG * kWRecBytes, &ctl.full[lane]);
       mbar_expect_tx(&ctl.sc_full[lane], UG * 256);
-      bulk_g2s(scring + lane * C::kScBytes + C::sWS, p.wsc + wunit * 128, UG * 256, &ctl.sc_full[lane]);
+#pragma unroll
+      for (int q = 0; q < UG; ++q)
+        bulk_g2s(scring + lane * C::kScBytes + C::sWS + q * 256, p.wpk + (wunit + q) * kWRecBytes + kWRecScales, 256,
+                 &ctl.sc_full[lane]);
     }
     __syncwarp();
     // --- 2. activations are the preceding kernel's output; the residual map
@@ -332,14 +333,16 @@ __global__ void __launch_bounds__(Cfg<TN, UG>::kThreads, 1) w4a4_residual_gemm_k
           ctl.blk[st][q][1] = ctl.sblk[sc][q][1] = e[q][1];
         }
         // weights of prefetched stages were already counted
-        mbar_arrive_expect_tx(&ctl.full[st], (i >= pre ? UG * 8192 : 0) + UG * rows * 64);
+        mbar_arrive_expect_tx(&ctl.full[st], (i >= pre ? UG * kWRecBytes : 0) + UG * rows * 64);
         mbar_arrive_expect_tx(&ctl.sc_full[sc], (i >= pre ? UG * 256 : 0) + UG * rows * 2 + rs_bytes);
         if (i < 12) MQ_TRACE(8 + i);
       }
       __syncwarp();
       if (i >= pre) {
-        if (lane == 1) bulk_g2s(sb + C::oA, p.wq + wunit * 8192, UG * 8192, &ctl.full[st]);
-        if (lane == 2) bulk_g2s(scb + C::sWS, p.wsc + wunit * 128, UG * 256, &ctl.sc_full[sc]);
+        if (lane == 1) bulk_g2s(sb + C::oA, p.wpk + wunit * kWRecBytes, UG * kWRecBytes, &ctl.full[st]);
+        if (lane >= 24 && lane < 24 + UG)
+          bulk_g2s(scb + C::sWS + (lane - 24) * 256, p.wpk + (wunit + lane - 24) * kWRecBytes + kWRecScales, 256,
+                   &ctl.sc_full[sc]);
       }
       if (merged) {
         if (lane == 3)
@@ -359,7 +362,7 @@ __global__ void __launch_bounds__(Cfg<TN, UG>::kThreads, 1) w4a4_residual_gemm_k
       if (lane >= 8 && lane < 8 + 2 * UG) {
         const int q = (lane - 8) >> 1, h = (lane - 8) & 1;
         if (e[q][h] >= 0)
-          bulk_g2s(scb + C::sRS + (q * 2 + h) * 128, p.rsc + static_cast<int64_t>(e[q][h]) * 64, 128,
+          bulk_g2s(scb + C::sRS + (q * 2 + h) * 128, p.rpk + static_cast<int64_t>(e[q][h]) * kRRecBytes + kRRecScales, 128,
                    &ctl.sc_full[sc]);
       }
       if (lane >= 16 && lane < 16 + 2 * UG) {
@@ -369,7 +372,7 @@ __global__ void __launch_bounds__(Cfg<TN, UG>::kThreads, 1) w4a4_residual_gemm_k
           const int rs = ri % NR;
           if (mbar_wait(&ctl.r_empty[rs], ((ri / NR) & 1) ^ 1, abort_flag, tmo, p.err)) {
             mbar_arrive_expect_tx(&ctl.r_full[rs], 4096);
-            bulk_g2s(rring + rs * 4096, p.rq + static_cast<int64_t>(e[q][h]) * 4096, 4096, &ctl.r_full[rs]);
+            bulk_g2s(rring + rs * 4096, p.rpk + static_cast<int64_t>(e[q][h]) * kRRecBytes, 4096, &ctl.r_full[rs]);
           } else {
             rok = 0;
           }
@@ -488,7 +491,7 @@ __global__ void __launch_bounds__(Cfg<TN, UG>::kThreads, 1) w4a4_residual_gemm_k
         const int a = grp * SPG + item % SPG;
         if (!mbar_wait(&ctl.a_empty[a], ((item / SPG) & 1) ^ 1, abort_flag, tmo, p.err)) break;
         tc_fence_after();
-        codes_to_tmem(sb + C::oA + q * 8192 + r * 16, 2048, tmem + lane_base + C::tA + a * 32);
+        codes_to_tmem(sb + C::oA + q * kWRecBytes + r * 16, 2048, tmem + lane_base + C::tA + a * 32);
         // activations: row m, K-step j -> two 16-byte chunks 2j, 2j+1 of the
         // 128-byte swizzled row (chunk c of row m sits at chunk c ^ (m & 7))
         const uint8_t* xsrc = sb + C::oXQ + q * xq_stride;
@@ -803,10 +806,19 @@ static mq_status launch_tn(const GemmParams& gp, const Plan& pl, cudaStream_t st
   return pl.ug == 2 ? launch_cfg<TN, (TN <= 64 ? 2 : 1), kDebug>(gp, pl, stream) : launch_cfg<TN, 1, kDebug>(gp, pl, stream);
 }
 
-mq_status gemm_launch(const uint8_t* xq, const uint16_t* xs, int64_t M, const uint8_t* wq, const uint16_t* wsc,
-                      int64_t N, int64_t K, const int32_t* row_ptr, const int32_t* col_idx, int64_t nnzb,
-                      const uint8_t* rq, const uint16_t* rsc, void* y, mq_dtype yt, int32_t* dots_w,
-                      int32_t* dots_r, void* ws, size_t ws_bytes, cudaStream_t stream) {
+mq_status gemm_decode_launch(bool* handled, const uint8_t* xq, const uint16_t* xs, int64_t M, const uint8_t* wpk,
+                             int64_t N, int64_t K, const int32_t* row_ptr, const int32_t* col_idx, int64_t nnzb,
+                             const uint8_t* rpk, void* y, mq_dtype yt, int32_t* dots_w, int32_t* dots_r,
+                             cudaStream_t stream);
+
+mq_status gemm_launch(const uint8_t* xq, const uint16_t* xs, int64_t M, const uint8_t* wpk, int64_t N, int64_t K,
+                      const int32_t* row_ptr, const int32_t* col_idx, int64_t nnzb, const uint8_t* rpk, void* y,
+                      mq_dtype yt, int32_t* dots_w, int32_t* dots_r, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  // Decode batches: the cluster split-K kernel (gemm_decode.cu), when it covers the shape.
+  bool handled = false;
+  const mq_status ds = gemm_decode_launch(&handled, xq, xs, M, wpk, N, K, row_ptr, col_idx, nnzb, rpk, y, yt, dots_w,
+                                          dots_r, stream);
+  if (handled || ds != MQ_OK) return ds;
   const Plan pl = make_plan(M, N, K);
   if (ws_bytes < pl.ws_partials + pl.ws_counters || ws == nullptr)
     return set_error(MQ_ERR_WORKSPACE, "gemm: workspace of %zu bytes needed, %zu given",
@@ -814,12 +826,10 @@ mq_status gemm_launch(const uint8_t* xq, const uint16_t* xs, int64_t M, const ui
   GemmParams gp;
   gp.xq = xq;
   gp.xs = xs;
-  gp.wq = wq;
-  gp.wsc = wsc;
+  gp.wpk = wpk;
   gp.row_ptr = row_ptr;
   gp.col_idx = col_idx;
-  gp.rq = rq;
-  gp.rsc = rsc;
+  gp.rpk = rpk;
   gp.y = y;
   gp.y_f32 = yt == MQ_F32;
   gp.dots_w = dots_w;

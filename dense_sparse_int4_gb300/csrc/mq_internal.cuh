@@ -15,6 +15,10 @@ namespace mq {
 constexpr int kGroup = 128;   // inputs per scale group
 constexpr int kBlockRows = 64;  // output rows per residual block
 constexpr int kTileN = 128;   // weight rows per GEMM tile (tensor-core M)
+// packed records (mq_pack_weights): codes, then fp16 scales
+constexpr int kWRecBytes = MQ_WREC_BYTES, kWRecScales = 8192;
+constexpr int kRRecBytes = MQ_RREC_BYTES, kRRecScales = 4096;
+static_assert(kWRecBytes == kWRecScales + 2 * kTileN && kRRecBytes == kRRecScales + 2 * kBlockRows, "records");
 
 // device error word bits
 constexpr uint32_t kDevErrTimeout = 1u;

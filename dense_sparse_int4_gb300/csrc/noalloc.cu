@@ -46,10 +46,9 @@ static mq_status noalloc_scratch(void** out) {
 }  // namespace mq
 
 extern "C" mq_status mq_w4a4_residual_gemm_noalloc(const uint8_t* xq, const uint16_t* xs, int64_t M,
-                                                   const uint8_t* wq, const uint16_t* wsc, int64_t N, int64_t K,
+                                                   const uint8_t* wpk, int64_t N, int64_t K,
                                                    const int32_t* row_ptr, const int32_t* col_idx, int64_t nnzb,
-                                                   const uint8_t* rq, const uint16_t* rsc, void* y, mq_dtype yt,
-                                                   mq_stream_t stream) {
+                                                   const uint8_t* rpk, void* y, mq_dtype yt, mq_stream_t stream) {
   using namespace mq;
   const size_t need = mq_gemm_workspace_bytes(M, N, K);
   if (need == 0)
@@ -66,6 +65,5 @@ extern "C" mq_status mq_w4a4_residual_gemm_noalloc(const uint8_t* xq, const uint
   // start at zero, so the used range is cleared on the stream first.
   if (cudaMemsetAsync(scratch, 0, need, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return launch_status("noalloc gemm: clearing scratch");
-  return mq_w4a4_residual_gemm(xq, xs, M, wq, wsc, N, K, row_ptr, col_idx, nnzb, rq, rsc, y, yt, scratch, need,
-                               stream);
+  return mq_w4a4_residual_gemm(xq, xs, M, wpk, N, K, row_ptr, col_idx, nnzb, rpk, y, yt, scratch, need, stream);
 }

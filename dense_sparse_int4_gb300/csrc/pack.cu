@@ -1,7 +1,8 @@
 // Offline packing of W^ = Q(W^) + R (MosaicQuant summary, Metodologia 1):
 // the dense 4-bit base (per output row, per 128-input group) and the 4-bit
-// residual of the selected 64x128 blocks (one scale per block row), written in
-// the tiled layouts the fused GEMM streams (see mq_pack_weights in mq.h).
+// residual of the selected 64x128 blocks (one scale per block row), written as
+// the records the fused GEMM streams (codes and their scales side by side, so
+// one bulk copy brings both; see mq_pack_weights in mq.h).
 //
 // Exactness: the base follows the same fp32 argument as the activation
 // quantizer.  The residual R = w - s*q is exactly representable in fp32 (it
@@ -57,7 +58,7 @@ __device__ __forceinline__ RowGroup quant_row_group(const uint16_t* __restrict__
 
 // One warp per (row n, group g).
 __global__ void __launch_bounds__(256) pack_base_kernel(const uint16_t* __restrict__ w, int64_t N, int64_t K,
-                                                        uint8_t* __restrict__ wq, uint16_t* __restrict__ wsc) {
+                                                        uint8_t* __restrict__ wpk) {
   const int64_t G = K / kGroup;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -65,17 +66,17 @@ __global__ void __launch_bounds__(256) pack_base_kernel(const uint16_t* __restri
   const int64_t n = warp / G, g = warp % G;
   const RowGroup rg = quant_row_group(w, K, n, g, lane);
   const int64_t t = n / kTileN, r = n % kTileN;
-  uint8_t* unit = wq + (t * G + g) * 8192;
+  uint8_t* rec = wpk + (t * G + g) * kWRecBytes;
   // inputs 4l..4l+3 sit in K-step j = l/8, bytes 2*(l%8), 2*(l%8)+1 of the row's 16-byte chunk
-  *reinterpret_cast<uint16_t*>(unit + (lane / 8) * 2048 + r * 16 + (lane % 8) * 2) = pack4(rg.q);
-  if (lane == 0) wsc[(t * G + g) * kTileN + r] = rg.sbits;
+  *reinterpret_cast<uint16_t*>(rec + (lane / 8) * 2048 + r * 16 + (lane % 8) * 2) = pack4(rg.q);
+  if (lane == 0) *reinterpret_cast<uint16_t*>(rec + kWRecScales + 2 * r) = rg.sbits;
 }
 
 // One warp per (CSR entry i, block row r).
 __global__ void __launch_bounds__(256) pack_residual_kernel(const uint16_t* __restrict__ w, int64_t N, int64_t K,
                                                             const int32_t* __restrict__ row_ptr,
                                                             const int32_t* __restrict__ col_idx, int64_t nnzb,
-                                                            uint8_t* __restrict__ rq, uint16_t* __restrict__ rsc) {
+                                                            uint8_t* __restrict__ rpk) {
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= nnzb * kBlockRows) return;
@@ -99,21 +100,21 @@ __global__ void __launch_bounds__(256) pack_residual_kernel(const uint16_t* __re
   float q[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) q[k] = pk_code(res[k], s);
-  uint8_t* blk = rq + i * 4096;
-  *reinterpret_cast<uint16_t*>(blk + (lane / 8) * 1024 + r * 16 + (lane % 8) * 2) = pack4(q);
-  if (lane == 0) rsc[i * kBlockRows + r] = sb;
+  uint8_t* rec = rpk + i * kRRecBytes;
+  *reinterpret_cast<uint16_t*>(rec + (lane / 8) * 1024 + r * 16 + (lane % 8) * 2) = pack4(q);
+  if (lane == 0) *reinterpret_cast<uint16_t*>(rec + kRRecScales + 2 * r) = sb;
 }
 
 mq_status pack_weights_launch(const uint16_t* w, int64_t N, int64_t K, const int32_t* row_ptr,
-                              const int32_t* col_idx, int64_t nnzb, uint8_t* wq, uint16_t* wsc,
-                              uint8_t* rq, uint16_t* rsc, cudaStream_t stream) {
+                              const int32_t* col_idx, int64_t nnzb, uint8_t* wpk, uint8_t* rpk,
+                              cudaStream_t stream) {
   const int64_t warps = N * (K / kGroup);
-  pack_base_kernel<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, stream>>>(w, N, K, wq, wsc);
+  pack_base_kernel<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, stream>>>(w, N, K, wpk);
   if (mq_status s = launch_status("pack: base"); s != MQ_OK) return s;
   if (nnzb > 0) {
     const int64_t rw = nnzb * kBlockRows;
     pack_residual_kernel<<<static_cast<unsigned>((rw * 32 + 255) / 256), 256, 0, stream>>>(
-        w, N, K, row_ptr, col_idx, nnzb, rq, rsc);
+        w, N, K, row_ptr, col_idx, nnzb, rpk);
     if (mq_status s = launch_status("pack: residual"); s != MQ_OK) return s;
   }
   return MQ_OK;

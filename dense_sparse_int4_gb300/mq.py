@@ -18,6 +18,8 @@ LIB_PATH = os.path.join(_PKG, "_build", "libmq.so")
 
 MQ_OK, MQ_ERR_INVALID_ARG, MQ_ERR_ALIGNMENT, MQ_ERR_UNSUPPORTED_DEVICE, MQ_ERR_CUDA, MQ_ERR_TIMEOUT, MQ_ERR_WORKSPACE = range(7)
 MQ_F16, MQ_BF16, MQ_F32 = 0, 1, 2
+WREC_BYTES, WREC_SCALES = 8448, 8192  # base record: 128x128 codes, then 128 fp16 scales
+RREC_BYTES, RREC_SCALES = 4224, 4096  # residual record: 64x128 codes, then 64 fp16 scales
 
 EXPORTS = (
     "mq_quantize_act", "mq_num_selected", "mq_select_workspace_bytes", "mq_select_blocks",
@@ -50,11 +52,12 @@ def lib() -> ctypes.CDLL:
             "mq_num_selected": (i64, [i64, i64, dbl]),
             "mq_select_workspace_bytes": (sz, [i64, i64]),
             "mq_select_blocks": (i32, [P, i64, i64, P, i32, i64, dbl, P, P, P, P, P, sz, P]),
-            "mq_pack_weights": (i32, [P, i64, i64, P, P, i64, P, P, P, P, P]),
+            "mq_pack_weights": (i32, [P, i64, i64, P, P, i64, P, P, P]),
             "mq_gemm_workspace_bytes": (sz, [i64, i64, i64]),
             "mq_gemm_workspace_init": (i32, [P, sz, P]),
-            "mq_w4a4_residual_gemm": (i32, [P, P, i64, P, P, i64, i64, P, P, i64, P, P, P, i32, P, sz, P]),
-            "mq_debug_group_dots": (i32, [P, P, i64, P, P, i64, i64, P, P, i64, P, P, P, P, P, sz, P]),
+            "mq_w4a4_residual_gemm": (i32, [P, P, i64, P, i64, i64, P, P, i64, P, P, i32, P, sz, P]),
+            "mq_w4a4_residual_gemm_noalloc": (i32, [P, P, i64, P, i64, i64, P, P, i64, P, P, i32, P]),
+            "mq_debug_group_dots": (i32, [P, P, i64, P, i64, i64, P, P, i64, P, P, P, P, sz, P]),
             "mq_check_device_error": (i32, [P]),
             "mq_set_wait_timeout_ns": (None, [u64]),
             "mq_debug_wait_timeout": (i32, [P]),
@@ -149,12 +152,10 @@ class PackedLinear:
     N: int
     K: int
     nnzb: int
-    wq: torch.Tensor  # uint8 [N*K/2] tiled
-    wsc: torch.Tensor  # fp16 [N*K/128] tiled
+    wpk: torch.Tensor  # uint8 [(N/128)*(K/128), WREC_BYTES] base records
     row_ptr: torch.Tensor  # int32 [N/64 + 1]
     col_idx: torch.Tensor  # int32 [nnzb]
-    rq: torch.Tensor  # uint8 [nnzb, 4096]
-    rsc: torch.Tensor  # fp16 [nnzb, 64]
+    rpk: torch.Tensor  # uint8 [nnzb, RREC_BYTES] residual records in CSR order
 
     def weight_bytes(self) -> int:
         """Bytes the GEMM must stream per call: base codes + scales + residual + CSR."""
@@ -162,22 +163,20 @@ class PackedLinear:
                 + 4 * (self.N // 64 + 1))
 
     def clone(self) -> "PackedLinear":
-        return PackedLinear(self.N, self.K, self.nnzb, self.wq.clone(), self.wsc.clone(), self.row_ptr.clone(),
-                            self.col_idx.clone(), self.rq.clone(), self.rsc.clone())
+        return PackedLinear(self.N, self.K, self.nnzb, self.wpk.clone(), self.row_ptr.clone(), self.col_idx.clone(),
+                            self.rpk.clone())
 
 
 def pack_weights(w: torch.Tensor, row_ptr: torch.Tensor, col_idx: torch.Tensor, stream=None) -> PackedLinear:
     N, K = w.shape
     dev = w.device
     nnzb = int(col_idx.numel())
-    wq = torch.empty(N * K // 2, dtype=torch.uint8, device=dev)
-    wsc = torch.empty(N * (K // 128), dtype=torch.float16, device=dev)
-    rq = torch.empty((max(nnzb, 1), 4096), dtype=torch.uint8, device=dev)
-    rsc = torch.empty((max(nnzb, 1), 64), dtype=torch.float16, device=dev)
+    wpk = torch.empty(((N // 128) * (K // 128), WREC_BYTES), dtype=torch.uint8, device=dev)
+    rpk = torch.empty((max(nnzb, 1), RREC_BYTES), dtype=torch.uint8, device=dev)
     ci = col_idx if nnzb else torch.zeros(1, dtype=torch.int32, device=dev)
-    _check(lib().mq_pack_weights(_ptr(w), N, K, _ptr(row_ptr), _ptr(ci), nnzb, _ptr(wq), _ptr(wsc), _ptr(rq),
-                                 _ptr(rsc), _stream(stream)), "mq_pack_weights")
-    return PackedLinear(N, K, nnzb, wq, wsc, row_ptr, ci, rq, rsc)
+    _check(lib().mq_pack_weights(_ptr(w), N, K, _ptr(row_ptr), _ptr(ci), nnzb, _ptr(wpk), _ptr(rpk),
+                                 _stream(stream)), "mq_pack_weights")
+    return PackedLinear(N, K, nnzb, wpk, row_ptr, ci, rpk)
 
 
 def prepare_linear(w: torch.Tensor, xcal: torch.Tensor, budget: float, stream=None) -> PackedLinear:
@@ -216,10 +215,9 @@ def gemm(xq: torch.Tensor, xs: torch.Tensor, M: int, pl: PackedLinear, out: torc
     else:
         wsb = ws.numel()
     nz = pl.nnzb > 0
-    _check(lib().mq_w4a4_residual_gemm(_ptr(xq), _ptr(xs), M, _ptr(pl.wq), _ptr(pl.wsc), pl.N, pl.K,
-                                       _ptr(pl.row_ptr), _ptr(pl.col_idx) if nz else None, pl.nnzb,
-                                       _ptr(pl.rq) if nz else None, _ptr(pl.rsc) if nz else None, _ptr(out),
-                                       _dtype_code(out.dtype), _ptr(ws), wsb, _stream(stream)),
+    _check(lib().mq_w4a4_residual_gemm(_ptr(xq), _ptr(xs), M, _ptr(pl.wpk), pl.N, pl.K, _ptr(pl.row_ptr),
+                                       _ptr(pl.col_idx) if nz else None, pl.nnzb, _ptr(pl.rpk) if nz else None,
+                                       _ptr(out), _dtype_code(out.dtype), _ptr(ws), wsb, _stream(stream)),
            "mq_w4a4_residual_gemm")
     return out
 
@@ -231,10 +229,9 @@ def debug_group_dots(xq, xs, M: int, pl: PackedLinear, stream=None):
     dr = torch.empty((M, max(pl.nnzb, 1), 64), dtype=torch.int32, device=dev)
     ws, wsb = gemm_workspace(M, pl.N, pl.K, dev)
     nz = pl.nnzb > 0
-    _check(lib().mq_debug_group_dots(_ptr(xq), _ptr(xs), M, _ptr(pl.wq), _ptr(pl.wsc), pl.N, pl.K,
-                                     _ptr(pl.row_ptr), _ptr(pl.col_idx) if nz else None, pl.nnzb,
-                                     _ptr(pl.rq) if nz else None, _ptr(pl.rsc) if nz else None, _ptr(dw),
-                                     _ptr(dr) if nz else None, _ptr(ws), wsb, _stream(stream)),
+    _check(lib().mq_debug_group_dots(_ptr(xq), _ptr(xs), M, _ptr(pl.wpk), pl.N, pl.K, _ptr(pl.row_ptr),
+                                     _ptr(pl.col_idx) if nz else None, pl.nnzb, _ptr(pl.rpk) if nz else None,
+                                     _ptr(dw), _ptr(dr) if nz else None, _ptr(ws), wsb, _stream(stream)),
            "mq_debug_group_dots")
     return dw, dr[:, : pl.nnzb]
 

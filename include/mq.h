@@ -121,29 +121,38 @@ mq_status mq_select_blocks(const uint16_t* w, int64_t N, int64_t K, const void* 
                            int32_t* col_idx, double* h_out, double* delta_out, void* ws,
                            size_t ws_bytes, mq_stream_t stream);
 
+/* Bytes of one packed base-weight record (128 output rows x 128 inputs:
+ * 8192 bytes of codes, then 128 fp16 scales) and of one packed residual-block
+ * record (64 rows x 128 inputs: 4096 bytes of codes, then 64 fp16 scales). */
+#define MQ_WREC_BYTES 8448
+#define MQ_RREC_BYTES 4224
+
 /*
  * Pack W^ into the dense 4-bit base and the 4-bit residual of the blocks
  * listed by (row_ptr, col_idx).
  *   w     [N, K] fp16 bits, row-major.
  *   nnzb  number of listed blocks (== row_ptr[N/64]); the host cannot read
  *         device row_ptr, so the caller passes it.
- *   wq    base codes, tiled (N*K/2 bytes, 16-byte aligned):
- *           unit (t, g) for output rows 128t..128t+127 and group g is 8192
- *           contiguous bytes at ((t*(K/128) + g) * 8192); inside a unit,
- *           byte  j*2048 + r*16 + b  holds the codes of row 128t + r and
- *           inputs 128g + 32j + 2b (low nibble) and +1 (high nibble),
- *           j in [0,4), r in [0,128), b in [0,16).
- *   wsc   base scales, tiled fp16: scale of (row 128t + r, group g) at
- *           (t*(K/128) + g)*128 + r   (N*K/128 entries, 16-byte aligned).
- *   rq    residual codes, [nnzb] blocks of 4096 bytes in CSR order; inside
- *           block i, byte j*1024 + r*16 + b holds row 64*br + r, inputs
- *           128g + 32j + 2b (low) and +1 (high), r in [0,64)  (16-byte aligned).
- *   rsc   residual scales, fp16 [nnzb][64] in CSR order (16-byte aligned).
- * rq and rsc may be NULL when nnzb == 0.
+ *   wpk   base weights, (N/128)*(K/128) records of MQ_WREC_BYTES, record
+ *           (t, g) at byte (t*(K/128) + g) * MQ_WREC_BYTES, for output rows
+ *           128t..128t+127 and inputs of group g (16-byte aligned).  Inside a
+ *           record:
+ *             byte j*2048 + r*16 + b (j in [0,4), r in [0,128), b in [0,16))
+ *               holds the codes of row 128t + r, inputs 128g + 32j + 2b (low
+ *               nibble) and +1 (high nibble);
+ *             bytes 8192 + 2r, +1: the fp16 scale of row 128t + r, group g.
+ *           Consecutive groups of one row tile are consecutive records, so a
+ *           run of groups, codes and scales, is one contiguous range.
+ *   rpk   residual blocks, nnzb records of MQ_RREC_BYTES in CSR order
+ *           (16-byte aligned).  Inside record i (block row br, group g):
+ *             byte j*1024 + r*16 + b (r in [0,64)): row 64*br + r, inputs
+ *               128g + 32j + 2b (low nibble) and +1 (high nibble);
+ *             bytes 4096 + 2r, +1: the fp16 scale of block row r.
+ * rpk may be NULL when nnzb == 0.
  */
 mq_status mq_pack_weights(const uint16_t* w, int64_t N, int64_t K, const int32_t* row_ptr,
-                          const int32_t* col_idx, int64_t nnzb, uint8_t* wq, uint16_t* wsc,
-                          uint8_t* rq, uint16_t* rsc, mq_stream_t stream);
+                          const int32_t* col_idx, int64_t nnzb, uint8_t* wpk, uint8_t* rpk,
+                          mq_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Online: the fused dense + sparse-residual GEMM (ZipperEngine,             */
@@ -158,26 +167,27 @@ size_t mq_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 mq_status mq_gemm_workspace_init(void* ws, size_t ws_bytes, mq_stream_t stream);
 
 /*
- *   Y[m, n] = sum_g xs[m,g] * ( wsc[n,g] * Dw[m,n,g] + rsc[n,g] * Dr[m,n,g] )
- * with the integer group dots Dw = sum_{k in g} xq[m,k] * wq[n,k] and, for the
- * listed blocks, Dr = sum_{k in g} xq[m,k] * rq[n,k]; both are exact.  One
+ *   Y[m, n] = sum_g sx[m,g] * ( sw[n,g] * Dw[m,n,g] + sr[n,g] * Dr[m,n,g] )
+ * with the activation scales sx (xs), the base and residual scales sw, sr
+ * (from wpk, rpk), the integer group dots Dw = sum_{k in g} qx[m,k] * qw[n,k]
+ * and, for the listed blocks, Dr = sum_{k in g} qx[m,k] * qr[n,k]; the dots
+ * are exact.  One
  * kernel streams each weight unit once, reads each activation tile once per
  * output tile, adds the residual product of a block in the same pass, and
  * reduce-adds both partial products in fp32 in ascending-g order (split-K
  * partials are summed in a fixed order, so the result is deterministic).
  *   xq, xs   from mq_quantize_act (M tokens).
- *   wq, wsc, row_ptr, col_idx, nnzb, rq, rsc   from mq_select_blocks /
- *            mq_pack_weights (nnzb == 0: residual pointers may be NULL).
+ *   wpk, row_ptr, col_idx, nnzb, rpk   from mq_select_blocks /
+ *            mq_pack_weights (nnzb == 0: row_ptr, col_idx and rpk may be NULL).
  *   y        [M, N] row-major, MQ_BF16 (round to nearest even) or MQ_F32.
  *   ws       at least mq_gemm_workspace_bytes(M, N, K) bytes, 256-byte
  *            aligned, zeroed once by mq_gemm_workspace_init; one workspace
  *            must not be used by two GEMMs in flight at the same time.
  */
 mq_status mq_w4a4_residual_gemm(const uint8_t* xq, const uint16_t* xs, int64_t M,
-                                const uint8_t* wq, const uint16_t* wsc, int64_t N, int64_t K,
-                                const int32_t* row_ptr, const int32_t* col_idx, int64_t nnzb,
-                                const uint8_t* rq, const uint16_t* rsc, void* y, mq_dtype yt,
-                                void* ws, size_t ws_bytes, mq_stream_t stream);
+                                const uint8_t* wpk, int64_t N, int64_t K, const int32_t* row_ptr,
+                                const int32_t* col_idx, int64_t nnzb, const uint8_t* rpk, void* y,
+                                mq_dtype yt, void* ws, size_t ws_bytes, mq_stream_t stream);
 
 /*
  * The fused GEMM without a caller-provided workspace, for callers that cannot
@@ -198,10 +208,9 @@ mq_status mq_w4a4_residual_gemm(const uint8_t* xq, const uint16_t* xs, int64_t M
  *   Allocates nothing (no cudaMalloc / cudaFree, no allocating library call).
  */
 mq_status mq_w4a4_residual_gemm_noalloc(const uint8_t* xq, const uint16_t* xs, int64_t M,
-                                        const uint8_t* wq, const uint16_t* wsc, int64_t N, int64_t K,
+                                        const uint8_t* wpk, int64_t N, int64_t K,
                                         const int32_t* row_ptr, const int32_t* col_idx, int64_t nnzb,
-                                        const uint8_t* rq, const uint16_t* rsc, void* y, mq_dtype yt,
-                                        mq_stream_t stream);
+                                        const uint8_t* rpk, void* y, mq_dtype yt, mq_stream_t stream);
 
 /*
  * Test hook: the same kernel, but instead of the fp32 reduce-add it writes the
@@ -210,10 +219,9 @@ mq_status mq_w4a4_residual_gemm_noalloc(const uint8_t* xq, const uint16_t* xs, i
  *   dr [M, nnzb, 64] int32 : Dr of CSR entry i, block row r  (NULL if nnzb == 0)
  * Same argument rules as mq_w4a4_residual_gemm otherwise.
  */
-mq_status mq_debug_group_dots(const uint8_t* xq, const uint16_t* xs, int64_t M, const uint8_t* wq,
-                              const uint16_t* wsc, int64_t N, int64_t K, const int32_t* row_ptr,
-                              const int32_t* col_idx, int64_t nnzb, const uint8_t* rq,
-                              const uint16_t* rsc, int32_t* dw, int32_t* dr, void* ws,
+mq_status mq_debug_group_dots(const uint8_t* xq, const uint16_t* xs, int64_t M, const uint8_t* wpk,
+                              int64_t N, int64_t K, const int32_t* row_ptr, const int32_t* col_idx,
+                              int64_t nnzb, const uint8_t* rpk, int32_t* dw, int32_t* dr, void* ws,
                               size_t ws_bytes, mq_stream_t stream);
 
 /* ------------------------------------------------------------------------ */

@@ -26,24 +26,37 @@ def host_u16(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def logical_wq(wq: torch.Tensor, N: int, K: int) -> np.ndarray:
-    """tiled [N/128][K/128][4][128][16] bytes -> logical packed [N, K/2]."""
+def _records(t: torch.Tensor, n: int, size: int) -> np.ndarray:
+    return t.cpu().numpy().reshape(-1)[: n * size].reshape(n, size)
+
+
+def logical_wq(wpk: torch.Tensor, N: int, K: int) -> np.ndarray:
+    """base records [N/128][K/128] (codes [4][128][16] bytes, then scales) -> logical packed [N, K/2]."""
     T, G = N // 128, K // 128
-    a = wq.cpu().numpy().reshape(T, G, 4, 128, 16)
+    a = _records(wpk, T * G, mq.WREC_BYTES)[:, : mq.WREC_SCALES].reshape(T, G, 4, 128, 16)
     return a.transpose(0, 3, 1, 2, 4).reshape(N, K // 2)
 
 
-def logical_wsc(wsc: torch.Tensor, N: int, K: int) -> np.ndarray:
+def logical_wsc(wpk: torch.Tensor, N: int, K: int) -> np.ndarray:
+    """base records -> scale bits [N, K/128]."""
     T, G = N // 128, K // 128
-    return host_u16(wsc).reshape(T, G, 128).transpose(0, 2, 1).reshape(N, G)
+    a = _records(wpk, T * G, mq.WREC_BYTES)[:, mq.WREC_SCALES:].copy().view(np.uint16).reshape(T, G, 128)
+    return a.transpose(0, 2, 1).reshape(N, G)
 
 
-def logical_rq(rq: torch.Tensor, nnzb: int) -> np.ndarray:
-    """[nnzb][4][64][16] bytes -> codes [nnzb, 64, 128]."""
+def logical_rq(rpk: torch.Tensor, nnzb: int) -> np.ndarray:
+    """residual records (codes [4][64][16] bytes, then scales) -> codes [nnzb, 64, 128]."""
     if nnzb == 0:
         return np.zeros((0, 64, 128), np.int8)
-    a = rq[:nnzb].cpu().numpy().reshape(nnzb, 4, 64, 16).transpose(0, 2, 1, 3).reshape(nnzb, 64, 64)
-    return O.unpack_nibbles(a)
+    a = _records(rpk, nnzb, mq.RREC_BYTES)[:, : mq.RREC_SCALES].reshape(nnzb, 4, 64, 16)
+    return O.unpack_nibbles(a.transpose(0, 2, 1, 3).reshape(nnzb, 64, 64))
+
+
+def logical_rsc(rpk: torch.Tensor, nnzb: int) -> np.ndarray:
+    """residual records -> scale bits [nnzb, 64]."""
+    if nnzb == 0:
+        return np.zeros((0, 64), np.uint16)
+    return _records(rpk, nnzb, mq.RREC_BYTES)[:, mq.RREC_SCALES:].copy().view(np.uint16)
 
 
 def logical_xq(xq: torch.Tensor, M: int) -> np.ndarray:

@@ -67,19 +67,20 @@ def test_argument_validation_before_device(L):
     assert L.mq_quantize_act(fake, 0, 4, 500, 512, fake, fake, None) == mq.MQ_ERR_INVALID_ARG  # K % 128
     assert L.mq_quantize_act(P(4098), 0, 4, 512, 512, fake, fake, None) == mq.MQ_ERR_ALIGNMENT
     assert L.mq_quantize_act(fake, 7, 4, 512, 512, fake, fake, None) == mq.MQ_ERR_INVALID_ARG  # dtype
-    # gemm: N not a multiple of 128; misaligned xq; workspace too small
-    args = [fake, fake, 4, fake, fake, 192, 512, fake, fake, 0, None, None, fake, 1, None, 0, None]
+    # gemm (xq, xs, M, wpk, N, K, row_ptr, col_idx, nnzb, rpk, y, yt, ws, ws_bytes, stream):
+    # N not a multiple of 128; misaligned xq; workspace too small
+    args = [fake, fake, 4, fake, 192, 512, fake, fake, 0, None, fake, 1, None, 0, None]
     assert L.mq_w4a4_residual_gemm(*args) == mq.MQ_ERR_INVALID_ARG
-    args[5] = 512
+    args[4] = 512
     args[0] = P(4097)
     assert L.mq_w4a4_residual_gemm(*args) == mq.MQ_ERR_ALIGNMENT
     args[0] = fake
     args[2] = 32
-    args[6] = 4096
     args[5] = 4096
+    args[4] = 4096
     assert L.mq_w4a4_residual_gemm(*args) == mq.MQ_ERR_WORKSPACE
-    # residual count without residual pointers
-    args = [fake, fake, 4, fake, fake, 512, 512, fake, fake, 3, None, None, fake, 1, None, 0, None]
+    # residual count without residual records
+    args = [fake, fake, 4, fake, 512, 512, fake, fake, 3, None, fake, 1, None, 0, None]
     assert L.mq_w4a4_residual_gemm(*args) == mq.MQ_ERR_INVALID_ARG
     # select: budget outside [0, 1]
     assert L.mq_select_blocks(fake, 512, 512, fake, 0, 256, 1.5, fake, fake, None, None, fake, 1 << 20,

@@ -11,7 +11,7 @@ import torch
 
 import oracle as O
 from dense_sparse_int4_gb300 import mq, synth
-from tests.gpu_helpers import (check_bf16, check_close, dev_act, dev_half, host_u16, logical_rq, logical_wq,
+from tests.gpu_helpers import (check_bf16, check_close, dev_act, dev_half, host_u16, logical_rq, logical_rsc, logical_wq,
                                logical_wsc, logical_xq, logical_xs, oracle_prep_for_csr, packed_from_csr,
                                xq_padding)
 
@@ -98,11 +98,11 @@ def test_pack_weights_bit_exact(N, K, budget):
     xcal = synth.calibration(K, seed=7, count=4)
     pl = mq.prepare_linear(dev_half(w), dev_half(xcal), budget)
     p = O.prepare(w, xcal, False, budget)
-    assert np.array_equal(logical_wq(pl.wq, N, K), O.pack_nibbles(p.qw))
-    assert np.array_equal(logical_wsc(pl.wsc, N, K), p.sw)
+    assert np.array_equal(logical_wq(pl.wpk, N, K), O.pack_nibbles(p.qw))
+    assert np.array_equal(logical_wsc(pl.wpk, N, K), p.sw)
     assert pl.nnzb == p.ksel
-    assert np.array_equal(logical_rq(pl.rq, pl.nnzb), p.qr)
-    assert np.array_equal(host_u16(pl.rsc)[: pl.nnzb], p.sr)
+    assert np.array_equal(logical_rq(pl.rpk, pl.nnzb), p.qr)
+    assert np.array_equal(logical_rsc(pl.rpk, pl.nnzb), p.sr)
 
 
 # ----------------------------------------------------------------------------

@@ -29,7 +29,7 @@ def lib():
     P, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
     fn = L.mq_w4a4_residual_gemm_noalloc
     fn.restype = i32
-    fn.argtypes = [P, P, i64, P, P, i64, i64, P, P, i64, P, P, P, i32, P]
+    fn.argtypes = [P, P, i64, P, i64, i64, P, P, i64, P, P, i32, P]
     return L
 
 
@@ -37,9 +37,9 @@ def _noalloc(L, xq, xs, M, pl, out):
     from dense_sparse_int4_gb300 import mq
     p = lambda t: ctypes.c_void_p(t.data_ptr())
     nz = pl.nnzb > 0
-    return L.mq_w4a4_residual_gemm_noalloc(p(xq), p(xs), M, p(pl.wq), p(pl.wsc), pl.N, pl.K, p(pl.row_ptr),
-                                           p(pl.col_idx) if nz else None, pl.nnzb, p(pl.rq) if nz else None,
-                                           p(pl.rsc) if nz else None, p(out), mq._dtype_code(out.dtype),
+    return L.mq_w4a4_residual_gemm_noalloc(p(xq), p(xs), M, p(pl.wpk), pl.N, pl.K, p(pl.row_ptr),
+                                           p(pl.col_idx) if nz else None, pl.nnzb, p(pl.rpk) if nz else None,
+                                           p(out), mq._dtype_code(out.dtype),
                                            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
