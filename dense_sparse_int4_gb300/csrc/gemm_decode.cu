@@ -4,40 +4,39 @@
 //
 //   Y[m,n] = sum_g sx[m,g] * ( sw[n,g] * Dw[m,n,g] + sr[n,g] * Dr[m,n,g] )
 //
-// in one kernel: the residual product of a selected 64x128 block is issued
-// on the same activation tile right after the dense product of its group, and
-// both are reduce-added into the same fp32 accumulators.
+// in one kernel: the residual product of a selected 64x128 block runs on the
+// same activation tile as the dense product of its group, and both are
+// reduce-added into the same fp32 accumulators.
 //
-// At decode sizes the work is streaming the 4-bit weights, so the design is
-// about keeping the copy engine and the converters busy and the fixed costs
-// of a launch small:
+// At decode sizes the work is streaming the 4-bit weights; the tensor cores
+// have room to spare, but each 128x128 group needs four K=32 MMAs and 16384
+// codes converted to E4M3, and both must keep up with HBM.  The design:
 //   * Split-K over a thread-block cluster of CS CTAs.  A cluster owns whole
 //     128-row weight tiles (one after another, persistently); CTA rank j
-//     handles the same K slice [j*G/CS, (j+1)*G/CS) of every tile it visits.
-//     So a CTA's activations never change: they are loaded and converted to
-//     E4M3 tensor-core tiles once, at the start, and stay in shared memory.
+//     handles the same K slice [j*G/CS, (j+1)*G/CS) of every tile it visits,
+//     so its activations are loaded and converted to E4M3 tensor-core tiles
+//     once, at the start, and stay in shared memory.
 //   * One bulk copy per stage: a stage is two consecutive base-weight records
 //     of one tile (codes and scales side by side, 16.5 KiB); residual blocks
 //     come as one record each into a small ring, only where the block list
-//     has them.
-//   * The block list (CSR by 64-row block row) of every tile the CTA visits
-//     is read once, up front, by the producer warp's lanes in parallel, into
-//     a static map (entry and ring position of each residual block); the
-//     dense products never wait for it.
-//   * Four worker warpgroups take the stages round-robin.  Each converts a
-//     group's INT4 codes to E4M3 in registers straight into its own tensor-
-//     memory A operand, issues the group's four K=32 MMAs itself and drains
-//     the integer-valued dots into its own fp32 accumulators (sx * (s * D)).
-//     A and D are double-buffered, so the next item is converted while the
-//     tensor core works on the current one.  The residual item of a group
-//     reuses the group's activation tile.
+//     has them.  The block list (CSR by 64-row block row) of every tile the
+//     CTA visits is read once, up front, into a static map.
+//   * Four converter warpgroups take the stages round-robin and convert each
+//     group's codes in registers straight into their own double-buffered
+//     tensor-memory A operand.  The weight codes are looked up as q + 8 (a
+//     cheaper 16-entry table); the dot then exceeds the true one by exactly
+//     8 * sum_k qx[m,k], which the drain subtracts (the group sums of the
+//     resident activations are computed once).  All dots stay exact integers.
+//   * One MMA warp serves the four warpgroups in whatever order their items
+//     become ready, issuing each item's four MMAs back to back, so the
+//     converters never wait on MMA issue.  Each warpgroup drains its own
+//     results: acc[m] += sx[m] * (s * D[m]) in fp32.
 //   * At the end of a tile the four warpgroup partials are added in a fixed
-//     order into a shared-memory buffer laid out by owner rank; each CTA then
-//     pushes the rows owned by rank k into rank k's shared memory with one
-//     bulk copy (distributed shared memory, counted on the owner's barrier),
-//     and each rank sums its 128/CS rows over the CS partials in rank order
-//     and stores Y.  No global workspace, no atomics: the result is
-//     deterministic.
+//     order into a row-major shared-memory buffer; each CTA then pushes the
+//     rows owned by rank k into rank k's shared memory with one bulk copy
+//     (distributed shared memory, counted on the owner's barrier), and each
+//     rank sums its 128/CS rows over the CS partials in rank order and stores
+//     Y.  No global workspace, no atomics: the result is deterministic.
 // Every wait is bounded (mbar_wait): a wait that runs out records the error,
 // raises the CTA's abort flag, and every role winds down.
 #include "mq_internal.cuh"
@@ -48,23 +47,29 @@
 #include <mutex>
 
 // Timeline probes for profiling builds (compiled out unless MQ_DEC_TRACE is
-// defined, in which case the build supplies mq_dec_trace_stamp).
+// defined, in which case the build supplies the two functions).
 #ifdef MQ_DEC_TRACE
 __device__ void mq_dec_trace_stamp(int slot);
+__device__ void mq_dec_trace_prof(int w, const long long* acc, int n);
 #define MQ_DTRACE(slot) mq_dec_trace_stamp(slot)
+#define MQ_PT() (pt_ = clock64())
+#define MQ_PA(k) (prof_[k] += clock64() - pt_)
 #else
 #define MQ_DTRACE(slot) ((void)0)
+#define MQ_PT() ((void)0)
+#define MQ_PA(k) ((void)0)
 #endif
 
 namespace mq {
 namespace {
 
-constexpr int kWG = 4;                  // worker warpgroups (warps 0..15)
+constexpr int kWG = 4;                  // converter warpgroups (warps 0..15)
 constexpr int kWorkers = 32 * 16;
-constexpr int kWarpProducer = 16;
-constexpr int kWarpEpi0 = 17;           // epilogue warps 17, 18
+constexpr int kWarpMma = 16;
+constexpr int kWarpProducer = 17;
+constexpr int kWarpEpi0 = 18;           // epilogue warps 18, 19
 constexpr int kEpiThreads = 64;
-constexpr int kThreads = 32 * kWarpEpi0 + kEpiThreads;  // 608
+constexpr int kThreads = 32 * kWarpEpi0 + kEpiThreads;  // 640
 constexpr int kUG = 2;                  // groups per stage
 constexpr int kStageBytes = kUG * kWRecBytes;
 constexpr int kMaxStages = 16;
@@ -84,7 +89,7 @@ struct DecParams {
   const int32_t* col_idx;
   const uint8_t* rpk;
   void* y;
-  int y_f32, y_vec;     // fp32 output; y 16-byte aligned (vector stores)
+  int y_f32;
   int32_t* dots_w;      // test hook: raw group dots instead of Y
   int32_t* dots_r;
   int M, Mp, N, G, nnzb, tiles;
@@ -96,18 +101,19 @@ struct DecParams {
 
 struct __align__(8) DecCtl {
   uint64_t full[kMaxStages];     // producer arrival + record bytes
-  uint64_t empty[kMaxStages];    // the warpgroup that read the stage
+  uint64_t empty[kMaxStages];    // the 4 warps of the warpgroup that converted the stage
   uint64_t r_full[kRSlots];
   uint64_t r_empty[kRSlots];
-  uint64_t mma_bar[kWG][2];      // tcgen05.commit of a warpgroup's MMAs, per D buffer
-  uint64_t wg_bar[kWG];          // bounded 128-thread barrier of a warpgroup
-  uint64_t work_bar;             // bounded barrier of the 512 workers
-  uint64_t epi_bar;              // bounded barrier of the epilogue threads
+  uint64_t a_ready[kWG][2];      // A buffer b of warpgroup w holds a converted item (4 warp arrivals)
+  uint64_t d_ready[kWG][2];      // its MMAs are complete (tcgen05.commit)
+  uint64_t work_bar;             // activation tiles converted (16 warp arrivals)
+  uint64_t epi_bar;              // bounded barrier of the 2 epilogue warps
   uint64_t map_ready;            // residual map and ring positions are built
   uint64_t chain[kWG];           // warpgroup w may add its partial of the tile (w >= 1)
   uint64_t rb_done;              // the CTA's partial of the tile is complete
   uint64_t rx_full;              // every rank's rows for this CTA have landed (bytes)
   uint64_t rx_free;              // every owner has consumed this CTA's last push
+  int32_t item_gl[kWG][2];       // slice group of the item in A buffer b (-1: warpgroup finished)
   int32_t map[kMaxVisits][kMaxSlice][2];   // CSR entry of the slice's residual blocks per tile, or -1
   int32_t rpos[kMaxVisits][kMaxSlice][2];  // position of that block in the residual-ring order
   int32_t sc_off[kMaxVisits + 1], sc_a0[kMaxVisits], sc_a1[kMaxVisits];
@@ -126,8 +132,10 @@ __device__ __forceinline__ uint32_t cluster_index() {
   asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
   return r;
 }
-__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+// Every thread of every CTA of the cluster, together.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
 __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
@@ -145,6 +153,16 @@ __device__ __forceinline__ void bulk_s2peer(uint32_t dst_cluster, const void* sr
           dst_cluster),
       "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
       : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
 }
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
@@ -199,26 +217,60 @@ __device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
   return r;
 }
 
-// 64 bytes of one row's codes (4 K-steps of 16 bytes at src + j*jstride) -> E4M3 in this thread's TMEM lane.
-__device__ __forceinline__ void row_codes_to_tmem(const uint8_t* src, int jstride, uint32_t a_col) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint4 pk = *reinterpret_cast<const uint4*>(src + j * jstride);
-    uint32_t ev[8];
-    int4x8_to_e4m3(pk.x, ev[0], ev[1]);
-    int4x8_to_e4m3(pk.y, ev[2], ev[3]);
-    int4x8_to_e4m3(pk.z, ev[4], ev[5]);
-    int4x8_to_e4m3(pk.w, ev[6], ev[7]);
-    tmem_st8(a_col + 8 * j, ev);
-  }
+// Eight INT4 codes q (two's complement nibbles, element i in bits 4i..4i+3)
+// -> eight E4M3 bytes holding q + 8 exactly.  The nibble u = q + 8 is p ^ 8;
+// two 8-entry prmt tables cover u in [0, 8) and [8, 16): a selector nibble
+// with its top bit set makes prmt emit the sign of the table byte, 0 here
+// (all entries are positive), so each table contributes only its own half
+// and an OR merges them.  9 operations per 8 codes.
+__device__ __forceinline__ void uint4x8_to_e4m3(uint32_t p, uint32_t& lo, uint32_t& hi) {
+  constexpr uint32_t kLoA = 0x44403800u, kLoB = 0x4E4C4A48u;  // 0, 1, 2, 3 | 4, 5, 6, 7
+  constexpr uint32_t kHiA = 0x53525150u, kHiB = 0x57565554u;  // 8, 9, 10, 11 | 12, 13, 14, 15
+  const uint32_t u = p ^ 0x88888888u;
+  lo = prmt(kLoA, kLoB, u) | prmt(kHiA, kHiB, p);
+  hi = prmt(kLoA, kLoB, u >> 16) | prmt(kHiA, kHiB, p >> 16);
 }
 
-// One MMA item of a worker warpgroup: a group's dense product (kind 0) or its
+// Store 32 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+// 64 bytes of one row's weight codes (4 K-steps of 16 bytes at src + j*jstride)
+// -> E4M3 (q + 8) in this thread's TMEM lane, 32 columns in one store.
+__device__ __forceinline__ void row_codes_to_tmem(const uint8_t* src, int jstride, uint32_t a_col) {
+  uint4 pk[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) pk[j] = *reinterpret_cast<const uint4*>(src + j * jstride);
+  uint32_t ev[32];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint4x8_to_e4m3(pk[j].x, ev[8 * j + 0], ev[8 * j + 1]);
+    uint4x8_to_e4m3(pk[j].y, ev[8 * j + 2], ev[8 * j + 3]);
+    uint4x8_to_e4m3(pk[j].z, ev[8 * j + 4], ev[8 * j + 5]);
+    uint4x8_to_e4m3(pk[j].w, ev[8 * j + 6], ev[8 * j + 7]);
+  }
+  tmem_st32(a_col, ev);
+}
+
+// Sum of the eight signed codes of a word of packed activations.
+__device__ __forceinline__ int nibble_sum8(uint32_t p) {
+  const uint32_t u = p ^ 0x88888888u;  // q + 8 in [1, 15]
+  const uint32_t b = (u & 0x0F0F0F0Fu) + ((u >> 4) & 0x0F0F0F0Fu);
+  return static_cast<int>((b * 0x01010101u) >> 24) - 64;
+}
+
+// One item of a converter warpgroup: a group's dense product (kind 0) or its
 // residual product (kind 1).
 struct Item {
   int i, q, kind;  // stage, group within the stage, kind
-  int e;           // kind 1: CSR entry of this thread's half's block, or -1
-  float s;         // this row's scale (weight or residual)
 };
 
 template <int TN, bool kDebug>
@@ -228,8 +280,9 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* btiles = smem;                                  // [ns][TN rows][128 B] E4M3, 128B-swizzled K-major
   float* sxs = reinterpret_cast<float*>(smem + p.oSX);     // [ns][TN] activation scales
-  float* rb = reinterpret_cast<float*>(smem + p.oRB);      // [CS owners][TN][R] the CTA's partial of a tile
-  float* rx = reinterpret_cast<float*>(smem + p.oRX);      // [CS sources][TN][R] the rows this CTA owns
+  float* sums = sxs + kMaxSlice * TN;                      // [ns][TN] 8 * (sum of the group's activation codes)
+  float* rb = reinterpret_cast<float*>(smem + p.oRB);      // [128 rows][TN] the CTA's partial of a tile
+  float* rx = reinterpret_cast<float*>(smem + p.oRX);      // [CS sources][R rows][TN] the rows this CTA owns
   uint8_t* rring = smem + p.oR;                            // [kRSlots] residual records
   uint8_t* stages = smem + p.oStage;                       // [nstages] x two base records
   if (threadIdx.x == 0) MQ_DTRACE(0);
@@ -254,22 +307,23 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&ctl.full[s], 1);
-      mbar_init(&ctl.empty[s], 1);
+      mbar_init(&ctl.empty[s], 4);
     }
     for (int s = 0; s < kRSlots; ++s) {
       mbar_init(&ctl.r_full[s], 1);
-      mbar_init(&ctl.r_empty[s], 1);
+      mbar_init(&ctl.r_empty[s], 4);
     }
     for (int w = 0; w < kWG; ++w) {
-      mbar_init(&ctl.mma_bar[w][0], 1);
-      mbar_init(&ctl.mma_bar[w][1], 1);
-      mbar_init(&ctl.wg_bar[w], 128);
-      mbar_init(&ctl.chain[w], 128);
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&ctl.a_ready[w][b], 4);
+        mbar_init(&ctl.d_ready[w][b], 1);
+      }
+      mbar_init(&ctl.chain[w], 4);
     }
-    mbar_init(&ctl.work_bar, kWorkers);
-    mbar_init(&ctl.epi_bar, kEpiThreads);
+    mbar_init(&ctl.work_bar, 16);
+    mbar_init(&ctl.epi_bar, 2);
     mbar_init(&ctl.map_ready, 1);
-    mbar_init(&ctl.rb_done, 128);
+    mbar_init(&ctl.rb_done, 4);
     mbar_init(&ctl.rx_full, 1);
     mbar_init(&ctl.rx_free, CS);
     ctl.abort_flag = 0;
@@ -278,10 +332,9 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
   // The next kernel may start launching: everything it reads before its own
   // dependency wait is read-only here.
   pdl_trigger();
-  // Cluster barrier: every CTA's barriers are initialised before any peer
+  // Every CTA of the cluster has its barriers initialised before any peer
   // pushes into them (also a barrier of this CTA's threads).
-  cluster_arrive();
-  cluster_wait();
+  cluster_sync_all();
   if (threadIdx.x == 0) MQ_DTRACE(1);
 
   if (warp == kWarpProducer) {
@@ -403,50 +456,103 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
       }
       if (lane == 0 && i < 8) MQ_DTRACE(4 + i);
     }
-  } else if (warp < kWarpProducer) {
-    // ---------------- workers ----------------
-    const int w = warp >> 2, quarter = warp & 3;
-    const int r = quarter * 32 + lane;  // weight row of the tile = TMEM lane = thread of the warpgroup
-    const int half = r >> 6;
-    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+  } else if (warp == kWarpMma) {
+    // ---------------- MMA issue: serve whichever warpgroup has an item ready ----------------
     constexpr uint32_t kIdesc =
         (1u << 4) | (static_cast<uint32_t>(TN >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
+    const bool ok0 = mbar_wait(&ctl.work_bar, 0, abort_flag, tmo, p.err);  // activation tiles and TMEM ready
+    tc_fence_after();
+    if (lane == 0 && ok0) {
+      const uint32_t tmem = ctl.tmem_base;
+      const uint32_t bt = smem_u32(btiles);
+      int n[kWG] = {0, 0, 0, 0};
+      int alive = kWG;
+      uint64_t t_idle = 0;
+      while (alive > 0) {
+        bool progressed = false;
+#pragma unroll
+        for (int w = 0; w < kWG; ++w) {
+          if (n[w] < 0) continue;
+          const int b = n[w] & 1;
+          if (!mbar_test(&ctl.a_ready[w][b], (n[w] >> 1) & 1)) continue;
+          const int gl = ctl.item_gl[w][b];
+          if (gl < 0) {  // the warpgroup has no more items
+            n[w] = -1;
+            --alive;
+            continue;
+          }
+          tc_fence_after();
+          const uint32_t a_col = tmem + w * 128 + 32 * b, d_col = tmem + w * 128 + 64 + TN * b;
+          const uint32_t b_addr = bt + gl * (TN * 128);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) tc_mma_ts(d_col, a_col + 8 * j, sw128_desc(b_addr + 32 * j), kIdesc, j > 0);
+          tc_commit(&ctl.d_ready[w][b]);
+          ++n[w];
+          progressed = true;
+        }
+        if (progressed) {
+          t_idle = 0;
+        } else {
+          if (*abort_flag) break;
+          const uint64_t now = globaltimer();
+          if (t_idle == 0) {
+            t_idle = now;
+          } else if (now - t_idle > tmo) {
+            atomicOr(p.err, kDevErrTimeout);
+            *abort_flag = 1;
+            break;
+          }
+        }
+      }
+    }
+  } else if (warp < kWarpMma) {
+    // ---------------- converters + drain ----------------
+    const int w = warp >> 2, quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // weight row of the tile = TMEM lane
+    const int half = r >> 6;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     bool ok = true;
-    int nsync = 0;
-    auto wg_sync = [&]() -> bool {  // bounded barrier of the warpgroup's 128 threads
-      mbar_arrive(&ctl.wg_bar[w]);
-      const bool passed = mbar_wait(&ctl.wg_bar[w], nsync & 1, abort_flag, tmo, p.err);
-      ++nsync;
-      return passed;
-    };
     if (warp == 0) tmem_alloc(&ctl.tmem_base, kTmemCols);
 
-    // --- this slice's activations, once: packed codes -> E4M3 tiles, scales -> fp32
+    // --- this slice's activations, once: packed codes -> E4M3 tiles, their
+    // group sums, and the scales -> fp32
     pdl_wait();
     {
       const int tid = threadIdx.x;  // 0..511
-      for (int idx = tid; idx < ns * TN * 4; idx += kWorkers) {
-        const int gl = idx / (TN * 4), m = (idx >> 2) % TN, jj = idx & 3;
-        uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-        if (m < p.Mp) {
-          const uint4 pk = ld_global_16(p.xq + (static_cast<int64_t>(gs + gl) * p.Mp + m) * 64 + jj * 16);
-          int4x8_to_e4m3(pk.x, lo.x, lo.y);
-          int4x8_to_e4m3(pk.y, lo.z, lo.w);
-          int4x8_to_e4m3(pk.z, hi.x, hi.y);
-          int4x8_to_e4m3(pk.w, hi.z, hi.w);
-        }
-        // row m of the tile: 128 bytes in its 8-row atom, 16-byte chunk c stored at chunk c ^ (m & 7)
-        uint8_t* row = btiles + gl * (TN * 128) + (m >> 3) * 1024 + (m & 7) * 128;
-        *reinterpret_cast<uint4*>(row + (((2 * jj) ^ (m & 7)) * 16)) = lo;
-        *reinterpret_cast<uint4*>(row + (((2 * jj + 1) ^ (m & 7)) * 16)) = hi;
-      }
       for (int idx = tid; idx < ns * TN; idx += kWorkers) {
         const int gl = idx / TN, m = idx % TN;
-        sxs[idx] = m < p.Mp ? __half2float(__ushort_as_half(p.xs[static_cast<int64_t>(gs + gl) * p.Mp + m])) : 0.0f;
+        uint8_t* row = btiles + gl * (TN * 128) + (m >> 3) * 1024 + (m & 7) * 128;
+        int sum = 0;
+        float sx = 0.0f;
+        if (m < p.Mp) {
+          const uint8_t* src = p.xq + (static_cast<int64_t>(gs + gl) * p.Mp + m) * 64;
+          uint4 pk[4];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) pk[jj] = ld_global_16(src + jj * 16);
+          sx = __half2float(__ushort_as_half(p.xs[static_cast<int64_t>(gs + gl) * p.Mp + m]));
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            uint4 lo, hi;
+            int4x8_to_e4m3(pk[jj].x, lo.x, lo.y);
+            int4x8_to_e4m3(pk[jj].y, lo.z, lo.w);
+            int4x8_to_e4m3(pk[jj].z, hi.x, hi.y);
+            int4x8_to_e4m3(pk[jj].w, hi.z, hi.w);
+            sum += nibble_sum8(pk[jj].x) + nibble_sum8(pk[jj].y) + nibble_sum8(pk[jj].z) + nibble_sum8(pk[jj].w);
+            // 16-byte chunk c of row m is stored at chunk c ^ (m & 7) of its 128-byte row
+            *reinterpret_cast<uint4*>(row + (((2 * jj) ^ (m & 7)) * 16)) = lo;
+            *reinterpret_cast<uint4*>(row + (((2 * jj + 1) ^ (m & 7)) * 16)) = hi;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(row + c * 16) = make_uint4(0, 0, 0, 0);
+        }
+        sxs[gl * TN + m] = sx;
+        sums[gl * TN + m] = 8.0f * static_cast<float>(sum);
       }
       fence_proxy_async_smem();  // generic writes -> the tensor core's reads
       tc_fence_before();
-      mbar_arrive(&ctl.work_bar);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.work_bar);
       ok = mbar_wait(&ctl.work_bar, 0, abort_flag, tmo, p.err);
       tc_fence_after();
       if (threadIdx.x == 0) MQ_DTRACE(12);
@@ -457,83 +563,114 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
     uint64_t acc[TN / 2];
 #pragma unroll
     for (int k = 0; k < TN / 2; ++k) acc[k] = 0;
+#ifdef MQ_DEC_TRACE
+    long long prof_[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0}, pt_ = 0;
+#endif
 
     bool map_seen = false;
-    // Advance the item cursor: the residual item of a group follows its dense
-    // item when the block list has a block there; then the next group, then
-    // this warpgroup's next stage.  Returns 0 (no more items), 1, or -1 (gave up).
+    // Items of this warpgroup: its stages in order; in a stage, the dense
+    // items of its groups, then the residual items of the groups that have a
+    // block.  Returns 1 (next item in `it`), 0 (no more items), -1 (gave up).
     auto advance = [&](Item& it) -> int {
-      if (it.kind == 0) {
-        if (!map_seen) {
-          if (!mbar_wait(&ctl.map_ready, 0, abort_flag, tmo, p.err)) return -1;
-          map_seen = true;
-        }
-        const int v = it.i / spv, gl = (it.i % spv) * kUG + it.q;
-        if (ctl.map[v][gl][0] >= 0 || ctl.map[v][gl][1] >= 0) {
+      const int ng = stage_ng(it.i);
+      if (it.kind == 0 && it.q + 1 < ng) {
+        ++it.q;
+        return 1;
+      }
+      // residual items of this stage, after its dense items
+      if (!map_seen) {
+        if (!mbar_wait(&ctl.map_ready, 0, abort_flag, tmo, p.err)) return -1;
+        map_seen = true;
+      }
+      const int v = it.i / spv, g0l = (it.i % spv) * kUG;
+      for (int q = it.kind == 0 ? 0 : it.q + 1; q < ng; ++q)
+        if (ctl.map[v][g0l + q][0] >= 0 || ctl.map[v][g0l + q][1] >= 0) {
           it.kind = 1;
+          it.q = q;
           return 1;
         }
-      }
       it.kind = 0;
-      if (++it.q < stage_ng(it.i)) return 1;
       it.q = 0;
       it.i += kWG;
       return it.i < total ? 1 : 0;
     };
-    // Wait for the item's inputs and convert its codes into A buffer b.
-    auto prepare = [&](Item& it, int b) -> bool {
+    // Per in-flight item, by buffer: the item, the row's scale and (residual)
+    // the CSR entry of this thread's block (two named slots, so they stay in registers).
+    struct InFlight {
+      Item it;
+      float s;
+      int e;
+    };
+    InFlight fl0 = {{0, 0, 0}, 0.0f, -1}, fl1 = fl0;
+    auto fl_get = [&](int b) -> InFlight { return b ? fl1 : fl0; };
+    // Wait for the item's inputs and convert its codes into A buffer b; then
+    // hand it to the MMA warp and release what this warpgroup has read.
+    auto submit = [&](const Item& it, int b) -> bool {
       const int st = it.i % NS;
       const uint32_t a_col = colA + 32 * b + lane_base;
+      const int v = it.i / spv, gl = (it.i % spv) * kUG + it.q;
+      InFlight f;
+      f.it = it;
       if (it.kind == 0) {
+        MQ_PT();
         if (it.q == 0 && !mbar_wait(&ctl.full[st], (it.i / NS) & 1, abort_flag, tmo, p.err)) return false;
+        MQ_PA(1);
+        MQ_PT();
         const uint8_t* rec = stages + st * kStageBytes + it.q * kWRecBytes;
-        it.s = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(rec + kWRecScales + 2 * r)));
+        f.s = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(rec + kWRecScales + 2 * r)));
+        f.e = -1;
         row_codes_to_tmem(rec + r * 16, 2048, a_col);
-        it.e = -1;
+        MQ_PA(2);
       } else {
-        const int v = it.i / spv, gl = (it.i % spv) * kUG + it.q;
-        it.e = ctl.map[v][gl][half];
-        it.s = 0.0f;
-        if (it.e >= 0) {  // warp-uniform: a warp's 32 rows lie in one half
+        const int e = ctl.map[v][gl][half];
+        f.e = e;
+        f.s = 0.0f;
+        if (e >= 0) {  // warp-uniform: a warp's 32 rows lie in one half
           const int c = ctl.rpos[v][gl][half], slot = c % kRSlots;
+          MQ_PT();
           if (!mbar_wait(&ctl.r_full[slot], (c / kRSlots) & 1, abort_flag, tmo, p.err)) return false;
+          MQ_PA(1);
+          MQ_PT();
           const uint8_t* rec = rring + slot * kRRecBytes;
-          it.s = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(rec + kRRecScales + 2 * (r & 63))));
+          f.s = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(rec + kRRecScales + 2 * (r & 63))));
           row_codes_to_tmem(rec + (r & 63) * 16, 1024, a_col);
+          MQ_PA(2);
         }
       }
-      return true;
-    };
-    // Barrier (the item's A is complete and D buffer b is drained), then one
-    // thread issues the item's MMAs and releases what the warpgroup has read.
-    auto issue = [&](const Item& it, int b) -> bool {
+      if (b)
+        fl1 = f;
+      else
+        fl0 = f;
+      MQ_PT();
       tc_wait_st();
       tc_fence_before();
-      if (!wg_sync()) return false;
-      if (r == 0) {
-        tc_fence_after();
-        const int gl = (it.i % spv) * kUG + it.q;
-        const uint32_t b_addr = smem_u32(btiles + gl * (TN * 128));
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          tc_mma_ts(colD + TN * b, colA + 32 * b + 8 * j, sw128_desc(b_addr + 32 * j), kIdesc, j > 0);
-        tc_commit(&ctl.mma_bar[w][b]);
-        if (it.kind == 0 && it.q == stage_ng(it.i) - 1) mbar_arrive(&ctl.empty[it.i % NS]);  // stage read
-        if (it.kind == 1) {                                                                  // residual records read
-          const int v = it.i / spv, gl2 = (it.i % spv) * kUG + it.q;
+      __syncwarp();
+      if (lane == 0) {
+        if (r == 0) ctl.item_gl[w][b] = gl;
+        // the stage's codes and scales are read once its last dense item is converted
+        if (it.kind == 0 && it.q == stage_ng(it.i) - 1) mbar_arrive(&ctl.empty[st]);
+        if (it.kind == 1) {
 #pragma unroll
           for (int h = 0; h < 2; ++h)
-            if (ctl.map[v][gl2][h] >= 0) mbar_arrive(&ctl.r_empty[ctl.rpos[v][gl2][h] % kRSlots]);
+            if (ctl.map[v][gl][h] >= 0) mbar_arrive(&ctl.r_empty[ctl.rpos[v][gl][h] % kRSlots]);
         }
+        // item_gl is written by warp quarter 0 before its own arrival; the MMA
+        // warp's wait needs all four arrivals, so it sees the value
+        mbar_arrive(&ctl.a_ready[w][b]);
       }
+      MQ_PA(6);
       return true;
     };
-    // acc[m] += sx[m] * (s * D[m]) from D buffer b (or, as a test hook, store the dots)
-    auto drain = [&](const Item& it, int b) {
+    // acc[m] += sx[m] * (s * (D[m] - 8 * sum_m)) from D buffer b (or, as a test hook, store the dots)
+    auto drain = [&](int b) {
+      const InFlight f = fl_get(b);
+      const Item it = f.it;
       const int gl = (it.i % spv) * kUG + it.q;
-      const bool use = it.kind == 0 || it.e >= 0;
+      const int e = f.e;
+      const bool use = it.kind == 0 || e >= 0;
       const float4* sx4 = reinterpret_cast<const float4*>(sxs + gl * TN);
-      const uint64_t s2 = f2pack(it.s, it.s);
+      const float4* su4 = reinterpret_cast<const float4*>(sums + gl * TN);
+      const uint64_t s2 = f2pack(f.s, f.s), m1 = f2pack(-1.0f, -1.0f);
 #pragma unroll
       for (int cc = 0; cc < TN / 16; ++cc) {
         uint32_t dv[16];
@@ -546,32 +683,34 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
             for (int i2 = 0; i2 < 16; ++i2) {
               const int m = 16 * cc + i2;
               if (m < p.M) {
-                const int32_t d = static_cast<int32_t>(__uint_as_float(dv[i2]));
+                const int32_t d =
+                    static_cast<int32_t>(__uint_as_float(dv[i2])) - static_cast<int32_t>(sums[gl * TN + m]);
                 if (it.kind == 0)
                   p.dots_w[(static_cast<int64_t>(m) * p.N + n) * G + gs + gl] = d;
                 else
-                  p.dots_r[(static_cast<int64_t>(m) * p.nnzb + it.e) * 64 + (r & 63)] = d;
+                  p.dots_r[(static_cast<int64_t>(m) * p.nnzb + e) * 64 + (r & 63)] = d;
               }
             }
           }
         } else if (use) {
 #pragma unroll
           for (int j4 = 0; j4 < 4; ++j4) {
-            const float4 sv = sx4[cc * 4 + j4];  // tokens 16cc + 4j4 .. +3
+            const float4 sv = sx4[cc * 4 + j4], cv = su4[cc * 4 + j4];  // tokens 16cc + 4j4 .. +3
             const int jp = cc * 8 + j4 * 2;
-            acc[jp] = f2fma(f2pack(sv.x, sv.y),
-                            f2mul(f2pack(__uint_as_float(dv[4 * j4]), __uint_as_float(dv[4 * j4 + 1])), s2), acc[jp]);
-            acc[jp + 1] =
-                f2fma(f2pack(sv.z, sv.w),
-                      f2mul(f2pack(__uint_as_float(dv[4 * j4 + 2]), __uint_as_float(dv[4 * j4 + 3])), s2), acc[jp + 1]);
+            // the dot of q with x is the dot of q + 8 minus 8 * sum(x): exact integers
+            const uint64_t d0 = f2fma(f2pack(cv.x, cv.y), m1,
+                                      f2pack(__uint_as_float(dv[4 * j4]), __uint_as_float(dv[4 * j4 + 1])));
+            const uint64_t d1 = f2fma(f2pack(cv.z, cv.w), m1,
+                                      f2pack(__uint_as_float(dv[4 * j4 + 2]), __uint_as_float(dv[4 * j4 + 3])));
+            acc[jp] = f2fma(f2pack(sv.x, sv.y), f2mul(d0, s2), acc[jp]);
+            acc[jp + 1] = f2fma(f2pack(sv.z, sv.w), f2mul(d1, s2), acc[jp + 1]);
           }
         }
       }
       tc_fence_before();
     };
-    // End of visit v: add this warpgroup's partial into the CTA's buffer, in
-    // warpgroup order.  Element (m, row) sits at ((row / R) * TN + m) * R + row % R:
-    // the rows each rank owns are one contiguous block.
+    // End of visit v: add this warpgroup's partial into the CTA's row-major
+    // buffer, in warpgroup order.
     auto finish_visit = [&](int v) -> bool {
       bool passed;
       if (w == 0)  // every owner has consumed the previous tile's push out of this buffer
@@ -579,64 +718,97 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
       else
         passed = mbar_wait(&ctl.chain[w], v & 1, abort_flag, tmo, p.err);
       if (!passed) return false;
-      float* rbo = rb + (r / R) * (TN * R) + (r % R);
+      float4* row = reinterpret_cast<float4*>(rb + r * TN);
 #pragma unroll
-      for (int k = 0; k < TN / 2; ++k) {
-        float a0, a1;
-        f2unpack(acc[k], a0, a1);
-        if (w == 0) {
-          rbo[(2 * k) * R] = a0;
-          rbo[(2 * k + 1) * R] = a1;
-        } else {
-          rbo[(2 * k) * R] += a0;
-          rbo[(2 * k + 1) * R] += a1;
+      for (int k = 0; k < TN / 4; ++k) {
+        float4 a;
+        f2unpack(acc[2 * k], a.x, a.y);
+        f2unpack(acc[2 * k + 1], a.z, a.w);
+        if (w != 0) {
+          const float4 o = row[k];
+          a.x = o.x + a.x;
+          a.y = o.y + a.y;
+          a.z = o.z + a.z;
+          a.w = o.w + a.w;
         }
-        acc[k] = 0;
+        row[k] = a;
+        acc[2 * k] = 0;
+        acc[2 * k + 1] = 0;
       }
-      mbar_arrive(w + 1 < kWG ? &ctl.chain[w + 1] : &ctl.rb_done);
+      // the buffer is pushed by bulk copies (the async proxy): order these
+      // generic writes before them
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(w + 1 < kWG ? &ctl.chain[w + 1] : &ctl.rb_done);
       if (r == 0 && v < 2) MQ_DTRACE(29 + w * 2 + v);
       return true;
     };
 
-    // Software pipeline over this warpgroup's items: prepare item k+1 (its A
-    // buffer was freed when item k-1's MMAs were waited for) while item k's
-    // MMAs run; then drain item k and issue item k+1.
-    int cur_v = 0;
-    Item cur;
-    cur.i = w;
-    cur.q = 0;
-    cur.kind = 0;
-    cur.e = -1;
-    cur.s = 0.0f;
-    bool have = ok && cur.i < total;
-    int k = 0;
-    if (have) {
-      ok = prepare(cur, 0) && issue(cur, 0);
-      if (r == 0) MQ_DTRACE(13 + w);
-    }
-    while (ok && have) {
-      Item nxt = cur;
-      const int adv = advance(nxt);
-      if (adv < 0) { ok = false; break; }
-      const bool have_next = adv > 0;
-      if (have_next && !(ok = prepare(nxt, (k + 1) & 1))) break;
-      if (!(ok = mbar_wait(&ctl.mma_bar[w][k & 1], (k >> 1) & 1, abort_flag, tmo, p.err))) break;
+    // Pipeline: up to two items at the MMA warp.  Item k uses buffers k & 1,
+    // so before it is converted, item k-2 (same buffers) is drained; after
+    // each drain, the visits whose items are all drained are finished.
+    int cur_v = 0;  // visits before cur_v are finished
+    int ndrained = 0;
+    Item nxt;
+    nxt.i = w;
+    nxt.q = 0;
+    nxt.kind = 0;
+    bool have = ok && nxt.i < total;
+    int k = 0;  // items submitted
+    // Drain the oldest in-flight item.  The visits before its own are complete
+    // (items come in visit order), so they are finished first: the
+    // accumulators then hold only this visit's items.
+    auto drain_one = [&]() -> bool {
+      const int b = ndrained & 1;
+      MQ_PT();
+      bool passed = true;
+      const int vj = fl_get(b).it.i / spv;
+      while (passed && cur_v < vj) passed = finish_visit(cur_v++);
+      MQ_PA(5);
+      if (!passed) return false;
+      MQ_PT();
+      if (!mbar_wait(&ctl.d_ready[w][b], (ndrained >> 1) & 1, abort_flag, tmo, p.err)) return false;
+      MQ_PA(3);
+      MQ_PT();
       tc_fence_after();
-      drain(cur, k & 1);
-      if (r == 0 && k < 2) MQ_DTRACE(21 + w * 2 + k);
-      const int vn = have_next ? nxt.i / spv : nvis;  // visits before vn are complete for this warpgroup
-      while (ok && cur_v < vn) ok = finish_visit(cur_v++);
-      if (!ok) break;
-      if (have_next && !(ok = issue(nxt, (k + 1) & 1))) break;
-      cur = nxt;
-      have = have_next;
+      drain(b);
+      MQ_PA(4);
+      ++ndrained;
+      return true;
+    };
+    while (ok && have) {
+      if (k >= 2) {  // item k-2 leaves buffers k & 1
+        if (!(ok = drain_one())) break;
+      }
+      if (!(ok = submit(nxt, k & 1))) break;
       ++k;
+      MQ_PT();
+      const int adv = advance(nxt);
+      MQ_PA(0);
+      if (adv < 0) {
+        ok = false;
+        break;
+      }
+      have = adv > 0;
+    }
+    // the last in-flight items
+    while (ok && ndrained < k) ok = drain_one();
+    if (ok) {  // tell the MMA warp this warpgroup is done (buffer k & 1 is free: item k-2 is drained)
+      __syncwarp();
+      if (lane == 0) {
+        if (r == 0) ctl.item_gl[w][k & 1] = -1;
+        mbar_arrive(&ctl.a_ready[w][k & 1]);
+      }
     }
     while (ok && cur_v < nvis) ok = finish_visit(cur_v++);
+#ifdef MQ_DEC_TRACE
+    prof_[8] = k;
+    if (r == 0) mq_dec_trace_prof(w, prof_, 9);
+#endif
   } else {
     // ---------------- epilogue: push partial rows to their owners, sum the owned rows, store Y ----------------
     const int et = threadIdx.x - 32 * kWarpEpi0;  // 0..63
-    const uint32_t chunk = static_cast<uint32_t>(TN * R * 4);  // one owner's rows of one partial
+    const uint32_t chunk = static_cast<uint32_t>(R * TN * 4);  // one owner's rows of one partial
     pdl_wait();  // Y may still be in use by the preceding kernel
     int nsync = 0;
     bool ok = true;
@@ -650,7 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
       if (CS > 1) {
         if (et == 0) {  // one bulk copy per owner: rows [k*R, (k+1)*R) of this CTA's partial
           const uint32_t rx_dst = smem_u32(rx) + rank * chunk, bar = smem_u32(&ctl.rx_full);
-          for (int k = 0; k < CS; ++k) bulk_s2peer(mapa(rx_dst, k), rb + k * (TN * R), chunk, mapa(bar, k));
+          for (int k = 0; k < CS; ++k) bulk_s2peer(mapa(rx_dst, k), rb + k * (R * TN), chunk, mapa(bar, k));
         }
         if (!mbar_wait(&ctl.rx_full, v & 1, abort_flag, tmo, p.err)) { ok = false; break; }
         src = rx;
@@ -661,41 +833,35 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
       }
       if (et == 0 && v < 2) MQ_DTRACE(39 + v);
       if (!kDebug) {
-        const int RQ = R / 4;
-        for (int idx = et; idx < p.M * RQ; idx += kEpiThreads) {
-          const int m = idx / RQ, rq = idx % RQ;
-          const float4* sp = reinterpret_cast<const float4*>(src + m * R + rq * 4);
+        // thread: one owned row, four tokens; sources summed in rank order
+        for (int idx = et; idx < R * (TN / 4); idx += kEpiThreads) {
+          const int row = idx % R, m4 = (idx / R) * 4;
+          if (m4 >= p.M) continue;
+          const float4* sp = reinterpret_cast<const float4*>(src + row * TN + m4);
           float4 s = sp[0];
           for (int j = 1; j < nsrc; ++j) {  // ascending rank = ascending K slice
-            const float4 t = sp[j * (TN * R / 4)];
+            const float4 t = sp[j * (R * TN / 4)];
             s.x += t.x;
             s.y += t.y;
             s.z += t.z;
             s.w += t.w;
           }
-          const int64_t o = static_cast<int64_t>(m) * p.N + tile * kTileN + rank * R + rq * 4;
-          if (p.y_f32) {
-            float* yo = static_cast<float*>(p.y) + o;
-            if (p.y_vec) {
-              *reinterpret_cast<float4*>(yo) = s;
-            } else {
-              yo[0] = s.x; yo[1] = s.y; yo[2] = s.z; yo[3] = s.w;
-            }
-          } else {
-            __nv_bfloat16* yo = static_cast<__nv_bfloat16*>(p.y) + o;
-            const __nv_bfloat162 lo = __floats2bfloat162_rn(s.x, s.y), hi = __floats2bfloat162_rn(s.z, s.w);
-            if (p.y_vec) {
-              uint2 u;
-              u.x = *reinterpret_cast<const uint32_t*>(&lo);
-              u.y = *reinterpret_cast<const uint32_t*>(&hi);
-              *reinterpret_cast<uint2*>(yo) = u;
-            } else {
-              yo[0] = lo.x; yo[1] = lo.y; yo[2] = hi.x; yo[3] = hi.y;
+          const int64_t n = tile * kTileN + rank * R + row;
+          const float vals[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            if (m4 + t < p.M) {
+              const int64_t o = static_cast<int64_t>(m4 + t) * p.N + n;
+              if (p.y_f32)
+                static_cast<float*>(p.y)[o] = vals[t];
+              else
+                static_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(vals[t]);
             }
           }
         }
       }
-      mbar_arrive(&ctl.epi_bar);  // every epilogue thread has read the received rows
+      __syncwarp();
+      if ((et & 31) == 0) mbar_arrive(&ctl.epi_bar);  // both epilogue warps have read the received rows
       if (!mbar_wait(&ctl.epi_bar, nsync & 1, abort_flag, tmo, p.err)) { ok = false; break; }
       ++nsync;
       if (et == 0 && v < 2) MQ_DTRACE(41 + v);
@@ -725,10 +891,9 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
     __syncthreads();
   }
   if (warp == 0) tmem_dealloc(ctl.tmem_base, kTmemCols);
-  // Cluster barrier: every CTA has received all its rows, so every push out of
-  // this CTA's shared memory has been read.
-  cluster_arrive();
-  cluster_wait();
+  // Every CTA has received all its rows, so every push out of this CTA's
+  // shared memory has been read.
+  cluster_sync_all();
   if (threadIdx.x == 0) MQ_DTRACE(45);
 }
 
@@ -799,7 +964,7 @@ static bool decode_plan(int64_t M, int64_t N, int64_t K, DecPlan* out) {
     pl.tn = tn;
     pl.cs = cs;
     pl.oSX = bbytes;
-    pl.oRB = up1024(pl.oSX + ns * tn * 4);
+    pl.oRB = up1024(pl.oSX + 2 * kMaxSlice * tn * 4);  // scales, then group sums
     pl.oRX = pl.oRB + tn * kTileN * 4;
     pl.oR = pl.oRX + (cs > 1 ? tn * kTileN * 4 : 0);
     pl.oStage = up1024(pl.oR + kRSlots * kRRecBytes);
@@ -874,7 +1039,6 @@ mq_status gemm_decode_launch(bool* handled, const uint8_t* xq, const uint16_t* x
   dp.rpk = rpk;
   dp.y = y;
   dp.y_f32 = yt == MQ_F32;
-  dp.y_vec = aligned(y, 16);
   dp.dots_w = dots_w;
   dp.dots_r = dots_r;
   dp.M = static_cast<int>(M);
