@@ -65,11 +65,13 @@ namespace {
 
 constexpr int kWG = 4;                  // converter warpgroups (warps 0..15)
 constexpr int kWorkers = 32 * 16;
-constexpr int kWarpMma = 16;
-constexpr int kWarpProducer = 17;
-constexpr int kWarpEpi0 = 18;           // epilogue warps 18, 19
-constexpr int kEpiThreads = 64;
-constexpr int kThreads = 32 * kWarpEpi0 + kEpiThreads;  // 640
+constexpr int kWarpMma = 16;           // MMA issue (kMmaWarps warps, each serving kWG / kMmaWarps warpgroups)
+constexpr int kMmaWarps = 1;
+constexpr int kWarpProducer = kWarpMma + kMmaWarps;
+constexpr int kWarpEpi0 = kWarpProducer + 1;  // epilogue warps
+// 20 warps: 5 per SM sub-partition, so each thread can have 96 registers
+constexpr int kThreads = 32 * 20;
+constexpr int kEpiThreads = kThreads - 32 * kWarpEpi0;
 constexpr int kUG = 2;                  // groups per stage
 constexpr int kStageBytes = kUG * kWRecBytes;
 constexpr int kMaxStages = 16;
@@ -107,7 +109,7 @@ struct __align__(8) DecCtl {
   uint64_t a_ready[kWG][2];      // A buffer b of warpgroup w holds a converted item (4 warp arrivals)
   uint64_t d_ready[kWG][2];      // its MMAs are complete (tcgen05.commit)
   uint64_t work_bar;             // activation tiles converted (16 warp arrivals)
-  uint64_t epi_bar;              // bounded barrier of the 2 epilogue warps
+  uint64_t epi_bar;              // bounded barrier of the epilogue warps (one arrival each)
   uint64_t map_ready;            // residual map and ring positions are built
   uint64_t chain[kWG];           // warpgroup w may add its partial of the tile (w >= 1)
   uint64_t rb_done;              // the CTA's partial of the tile is complete
@@ -321,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
       mbar_init(&ctl.chain[w], 4);
     }
     mbar_init(&ctl.work_bar, 16);
-    mbar_init(&ctl.epi_bar, 2);
+    mbar_init(&ctl.epi_bar, kEpiThreads / 32);
     mbar_init(&ctl.map_ready, 1);
     mbar_init(&ctl.rb_done, 4);
     mbar_init(&ctl.rx_full, 1);
@@ -456,8 +458,9 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
       }
       if (lane == 0 && i < 8) MQ_DTRACE(4 + i);
     }
-  } else if (warp == kWarpMma) {
-    // ---------------- MMA issue: serve whichever warpgroup has an item ready ----------------
+  } else if (warp >= kWarpMma && warp < kWarpMma + kMmaWarps) {
+    // ---------------- MMA issue: serve whichever of its warpgroups has an item ready ----------------
+    const int w0 = (warp - kWarpMma) * (kWG / kMmaWarps);
     constexpr uint32_t kIdesc =
         (1u << 4) | (static_cast<uint32_t>(TN >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
     const bool ok0 = mbar_wait(&ctl.work_bar, 0, abort_flag, tmo, p.err);  // activation tiles and TMEM ready
@@ -465,29 +468,35 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
     if (lane == 0 && ok0) {
       const uint32_t tmem = ctl.tmem_base;
       const uint32_t bt = smem_u32(btiles);
-      int n[kWG] = {0, 0, 0, 0};
-      int alive = kWG;
+      int n[kWG / kMmaWarps] = {};
+      int alive = kWG / kMmaWarps;
       uint64_t t_idle = 0;
+#ifdef MQ_DEC_TRACE
+      long long prof_[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0}, pt_ = 0, tl_ = clock64();
+#endif
       while (alive > 0) {
         bool progressed = false;
 #pragma unroll
-        for (int w = 0; w < kWG; ++w) {
-          if (n[w] < 0) continue;
-          const int b = n[w] & 1;
-          if (!mbar_test(&ctl.a_ready[w][b], (n[w] >> 1) & 1)) continue;
+        for (int x = 0; x < kWG / kMmaWarps; ++x) {
+          const int w = w0 + x;
+          if (n[x] < 0) continue;
+          const int b = n[x] & 1;
+          if (!mbar_test(&ctl.a_ready[w][b], (n[x] >> 1) & 1)) continue;
           const int gl = ctl.item_gl[w][b];
           if (gl < 0) {  // the warpgroup has no more items
-            n[w] = -1;
+            n[x] = -1;
             --alive;
             continue;
           }
+          MQ_PT();
           tc_fence_after();
           const uint32_t a_col = tmem + w * 128 + 32 * b, d_col = tmem + w * 128 + 64 + TN * b;
           const uint32_t b_addr = bt + gl * (TN * 128);
 #pragma unroll
           for (int j = 0; j < 4; ++j) tc_mma_ts(d_col, a_col + 8 * j, sw128_desc(b_addr + 32 * j), kIdesc, j > 0);
           tc_commit(&ctl.d_ready[w][b]);
-          ++n[w];
+          MQ_PA(0);
+          ++n[x];
           progressed = true;
         }
         if (progressed) {
@@ -504,6 +513,10 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
           }
         }
       }
+#ifdef MQ_DEC_TRACE
+      prof_[1] = clock64() - tl_;  // the whole issue loop
+      if (w0 == 0) mq_dec_trace_prof(4, prof_, 9);
+#endif
     }
   } else if (warp < kWarpMma) {
     // ---------------- converters + drain ----------------
@@ -603,13 +616,12 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
     };
     InFlight fl0 = {{0, 0, 0}, 0.0f, -1}, fl1 = fl0;
     auto fl_get = [&](int b) -> InFlight { return b ? fl1 : fl0; };
-    // Wait for the item's inputs and convert its codes into A buffer b; then
-    // hand it to the MMA warp and release what this warpgroup has read.
-    auto submit = [&](const Item& it, int b) -> bool {
+    // Wait for the item's inputs and convert its codes into A buffer b (the
+    // tensor-memory stores are issued, not awaited).
+    auto convert = [&](const Item& it, int b, InFlight& f) -> bool {
       const int st = it.i % NS;
       const uint32_t a_col = colA + 32 * b + lane_base;
       const int v = it.i / spv, gl = (it.i % spv) * kUG + it.q;
-      InFlight f;
       f.it = it;
       if (it.kind == 0) {
         MQ_PT();
@@ -637,10 +649,13 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
           MQ_PA(2);
         }
       }
-      if (b)
-        fl1 = f;
-      else
-        fl0 = f;
+      return true;
+    };
+    // Hand the converted item in A buffer b to the MMA warp and release what
+    // this warpgroup has read.
+    auto handoff = [&](const Item& it, int b) {
+      const int st = it.i % NS;
+      const int v = it.i / spv, gl = (it.i % spv) * kUG + it.q;
       MQ_PT();
       tc_wait_st();
       tc_fence_before();
@@ -659,7 +674,6 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
         mbar_arrive(&ctl.a_ready[w][b]);
       }
       MQ_PA(6);
-      return true;
     };
     // acc[m] += sx[m] * (s * (D[m] - 8 * sum_m)) from D buffer b (or, as a test hook, store the dots)
     auto drain = [&](int b) {
@@ -744,9 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
       return true;
     };
 
-    // Pipeline: up to two items at the MMA warp.  Item k uses buffers k & 1,
-    // so before it is converted, item k-2 (same buffers) is drained; after
-    // each drain, the visits whose items are all drained are finished.
+    // Pipeline: up to two items at the MMA warp; item k uses buffers k & 1.
     int cur_v = 0;  // visits before cur_v are finished
     int ndrained = 0;
     Item nxt;
@@ -755,10 +767,10 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
     nxt.kind = 0;
     bool have = ok && nxt.i < total;
     int k = 0;  // items submitted
-    // Drain the oldest in-flight item.  The visits before its own are complete
-    // (items come in visit order), so they are finished first: the
-    // accumulators then hold only this visit's items.
-    auto drain_one = [&]() -> bool {
+    // Before the oldest in-flight item is drained: the visits before its own
+    // are complete (items come in visit order), so they are finished first
+    // (the accumulators then hold only this visit's items); then its MMAs.
+    auto ready_to_drain = [&]() -> bool {
       const int b = ndrained & 1;
       MQ_PT();
       bool passed = true;
@@ -767,20 +779,31 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
       MQ_PA(5);
       if (!passed) return false;
       MQ_PT();
-      if (!mbar_wait(&ctl.d_ready[w][b], (ndrained >> 1) & 1, abort_flag, tmo, p.err)) return false;
+      passed = mbar_wait(&ctl.d_ready[w][b], (ndrained >> 1) & 1, abort_flag, tmo, p.err);
       MQ_PA(3);
-      MQ_PT();
       tc_fence_after();
-      drain(b);
+      return passed;
+    };
+    auto drain_oldest = [&]() {
+      MQ_PT();
+      drain(ndrained & 1);
       MQ_PA(4);
       ++ndrained;
-      return true;
     };
     while (ok && have) {
-      if (k >= 2) {  // item k-2 leaves buffers k & 1
-        if (!(ok = drain_one())) break;
-      }
-      if (!(ok = submit(nxt, k & 1))) break;
+      const int b = k & 1;
+      // Item k-2 used buffers b: once its MMAs are done, A[b] is free; item k
+      // is converted into it, and item k-2 is drained from D[b] while the
+      // tensor-memory stores of the conversion complete.
+      if (k >= 2 && !(ok = ready_to_drain())) break;
+      InFlight f;
+      if (!(ok = convert(nxt, b, f))) break;
+      if (k >= 2) drain_oldest();
+      if (b)
+        fl1 = f;
+      else
+        fl0 = f;
+      handoff(nxt, b);
       ++k;
       MQ_PT();
       const int adv = advance(nxt);
@@ -792,7 +815,10 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
       have = adv > 0;
     }
     // the last in-flight items
-    while (ok && ndrained < k) ok = drain_one();
+    while (ok && ndrained < k) {
+      if (!(ok = ready_to_drain())) break;
+      drain_oldest();
+    }
     if (ok) {  // tell the MMA warp this warpgroup is done (buffer k & 1 is free: item k-2 is drained)
       __syncwarp();
       if (lane == 0) {
@@ -807,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
 #endif
   } else {
     // ---------------- epilogue: push partial rows to their owners, sum the owned rows, store Y ----------------
-    const int et = threadIdx.x - 32 * kWarpEpi0;  // 0..63
+    const int et = threadIdx.x - 32 * kWarpEpi0;  // 0 .. kEpiThreads-1
     const uint32_t chunk = static_cast<uint32_t>(R * TN * 4);  // one owner's rows of one partial
     pdl_wait();  // Y may still be in use by the preceding kernel
     int nsync = 0;
@@ -861,7 +887,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
         }
       }
       __syncwarp();
-      if ((et & 31) == 0) mbar_arrive(&ctl.epi_bar);  // both epilogue warps have read the received rows
+      if ((et & 31) == 0) mbar_arrive(&ctl.epi_bar);  // every epilogue warp has read the received rows
       if (!mbar_wait(&ctl.epi_bar, nsync & 1, abort_flag, tmo, p.err)) { ok = false; break; }
       ++nsync;
       if (et == 0 && v < 2) MQ_DTRACE(41 + v);
