@@ -22,6 +22,7 @@ size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 mq_status gemm_launch(const uint8_t* xq, const uint16_t* xs, int64_t M, const uint8_t* wpk, int64_t N, int64_t K,
                       const int32_t* row_ptr, const int32_t* col_idx, int64_t nnzb, const uint8_t* rpk, void* y,
                       mq_dtype yt, int32_t* dots_w, int32_t* dots_r, void* ws, size_t ws_bytes, cudaStream_t stream);
+mq_status gemm_plan_info(int64_t M, int64_t N, int64_t K, int32_t* info);
 mq_status wait_timeout_probe_launch(cudaStream_t stream);
 mq_status error_word_address(uint32_t** out);
 
@@ -245,6 +246,14 @@ mq_status mq_debug_group_dots(const uint8_t* xq, const uint16_t* xs, int64_t M, 
     return s;
   return gemm_launch(xq, xs, M, wpk, N, K, row_ptr, col_idx, nnzb, rpk, nullptr, MQ_F32, dw, dr, ws, ws_bytes,
                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+mq_status mq_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t* info) {
+  MQ_CHECK(info, MQ_ERR_INVALID_ARG, "gemm_plan: info is NULL");
+  MQ_CHECK(sizes_ok(M, N, K), MQ_ERR_INVALID_ARG, "gemm_plan: bad sizes M=%lld N=%lld K=%lld", (long long)M,
+           (long long)N, (long long)K);
+  if (mq_status s = check_device(); s != MQ_OK) return s;
+  return gemm_plan_info(M, N, K, info);
 }
 
 mq_status mq_check_device_error(mq_stream_t stream) {

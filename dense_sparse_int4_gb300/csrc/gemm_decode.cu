@@ -5,33 +5,45 @@
 //   Y[m,n] = sum_g sx[m,g] * ( sw[n,g] * Dw[m,n,g] + sr[n,g] * Dr[m,n,g] )
 //
 // in one kernel: the residual product of a selected 64x128 block runs on the
-// same activation tile as the dense product of its group, and both are
+// same activation fragments as the dense product of its group, and both are
 // reduce-added into the same fp32 accumulators.
 //
-// At decode sizes the work is streaming the 4-bit weights; the tensor cores
-// have room to spare, but each 128x128 group needs four K=32 MMAs and 16384
-// codes converted to E4M3, and both must keep up with HBM.  The design:
+// At decode sizes the work is streaming the 4-bit weights.  Every 128-input
+// group has its own scales, so its integer dot must be finished, scaled and
+// added before the next group's; the warp-level FP8 MMA (mma.sync m16n8k32
+// e4m3, fp32 accumulators in registers) runs on sm_103a far faster than
+// decode needs and keeps that per-group step inside one warp, with no
+// hand-offs between roles.  So each MMA warp works alone:
+//   * it owns 32 rows of the tile and every third group of the CTA's list;
+//     per group it loads its rows' packed codes (one 32-bit word per row,
+//     K-step and thread), unpacks them in registers, runs the MMAs against
+//     the resident activation fragments, and scales the exact dots into its
+//     fp32 accumulators;
+//   * unpacking is a mask: a byte 0x00..0x0F read as E4M3 is exactly
+//     b * 2^-9 (subnormals below 8, the lowest normal binade from 8), so the
+//     nibble u = q + 8 (q XOR 8) moved into a byte is u * 2^-9 with no table
+//     (4 operations per 8 codes).  The dot is then 2^-9 * (D + 8 * sum_k
+//     qx[m,k]); the scaling step subtracts the activation term (the group
+//     sums of the resident activations are computed once) and folds 2^9 into
+//     the activation scale.  Every partial sum is a multiple of 2^-9 below 2^14
+//     in magnitude, so the fp32 accumulation is exact;
+//   * K is permuted inside each 32-wide MMA step: the thread that holds MMA
+//     columns 4t..4t+3 gets the even codes 8t, 8t+2, .., 8t+6 of the step and
+//     the one holding 16+4t..16+4t+3 the odd ones, which is the order the
+//     mask leaves them in.  A and B use the same permutation, so the dot is
+//     unchanged.
+// Around the warps:
 //   * Split-K over a thread-block cluster of CS CTAs.  A cluster owns whole
 //     128-row weight tiles (one after another, persistently); CTA rank j
 //     handles the same K slice [j*G/CS, (j+1)*G/CS) of every tile it visits,
-//     so its activations are loaded and converted to E4M3 tensor-core tiles
-//     once, at the start, and stay in shared memory.
-//   * One bulk copy per stage: a stage is two consecutive base-weight records
-//     of one tile (codes and scales side by side, 16.5 KiB); residual blocks
-//     come as one record each into a small ring, only where the block list
-//     has them.  The block list (CSR by 64-row block row) of every tile the
-//     CTA visits is read once, up front, into a static map.
-//   * Four converter warpgroups take the stages round-robin and convert each
-//     group's codes in registers straight into their own double-buffered
-//     tensor-memory A operand.  The weight codes are looked up as q + 8 (a
-//     cheaper 16-entry table); the dot then exceeds the true one by exactly
-//     8 * sum_k qx[m,k], which the drain subtracts (the group sums of the
-//     resident activations are computed once).  All dots stay exact integers.
-//   * One MMA warp serves the four warpgroups in whatever order their items
-//     become ready, issuing each item's four MMAs back to back, so the
-//     converters never wait on MMA issue.  Each warpgroup drains its own
-//     results: acc[m] += sx[m] * (s * D[m]) in fp32.
-//   * At the end of a tile the four warpgroup partials are added in a fixed
+//     so its activations are converted to E4M3 fragments once, at the start,
+//     and stay in shared memory.
+//   * A producer warp streams the base-weight records (codes and scales side
+//     by side, 8.25 KiB, one bulk copy each) into a ring of stages, and the
+//     residual block records the CSR block list has in this slice into a
+//     small ring.  The block lists of every tile the CTA visits are read once,
+//     up front, into a static map.
+//   * At the end of a tile the three warp sets' partials are added in a fixed
 //     order into a row-major shared-memory buffer; each CTA then pushes the
 //     rows owned by rank k into rank k's shared memory with one bulk copy
 //     (distributed shared memory, counted on the owner's barrier), and each
@@ -63,24 +75,20 @@ __device__ void mq_dec_trace_prof(int w, const long long* acc, int n);
 namespace mq {
 namespace {
 
-constexpr int kWG = 4;                  // converter warpgroups (warps 0..15)
-constexpr int kWorkers = 32 * 16;
-constexpr int kWarpMma = 16;           // MMA issue (kMmaWarps warps, each serving kWG / kMmaWarps warpgroups)
-constexpr int kMmaWarps = 1;
-constexpr int kWarpProducer = kWarpMma + kMmaWarps;
-constexpr int kWarpEpi0 = kWarpProducer + 1;  // epilogue warps
-// 20 warps: 5 per SM sub-partition, so each thread can have 96 registers
-constexpr int kThreads = 32 * 20;
-constexpr int kEpiThreads = kThreads - 32 * kWarpEpi0;
-constexpr int kUG = 2;                  // groups per stage
-constexpr int kStageBytes = kUG * kWRecBytes;
-constexpr int kMaxStages = 16;
-constexpr int kRSlots = 6;              // residual-record ring
-constexpr int kMaxVisits = 16;          // tiles visited per CTA
-constexpr int kMaxSlice = 32;           // groups in a CTA's K slice
-constexpr int kMaxBBytes = 64 * 1024;   // resident activation tiles
+constexpr int kSlots = 3;                 // warp sets; set q takes groups q, q+3, q+6, .. of the CTA's list
+constexpr int kMmaWarps = 4 * kSlots;     // warp w: rows 32*(w%4) .. +31 of set w/4
+constexpr int kWarpProducer = kMmaWarps;      // 12: activations, then the base-weight stages
+constexpr int kWarpResidual = kMmaWarps + 1;  // 13: block list, then the residual records
+constexpr int kWarpEpi0 = kMmaWarps + 2;      // epilogue warps 14, 15
+constexpr int kEpiThreads = 64;
+constexpr int kThreads = 32 * kWarpEpi0 + kEpiThreads;  // 512: 4 warps per sub-partition
+constexpr int kStageBytes = kWRecBytes;   // one group's base record per stage
+constexpr int kMaxStages = 24;
+constexpr int kRSlots = 6;                // residual-record ring
+constexpr int kMaxVisits = 16;            // tiles visited per CTA
+constexpr int kMaxSlice = 32;             // groups in a CTA's K slice
+constexpr int kMaxBBytes = 112 * 1024;    // resident activation fragments
 constexpr int kSmemLimit = 227 * 1024;
-constexpr int kTmemCols = 512;          // per warpgroup 128: A0, A1 (32 each), D0, D1 (TN each)
 constexpr int kMaxCS = 8;
 
 struct DecParams {
@@ -96,32 +104,33 @@ struct DecParams {
   int32_t* dots_r;
   int M, Mp, N, G, nnzb, tiles;
   int cs, nclusters, nstages;
-  uint32_t oSX, oRB, oRX, oR, oStage;  // shared-memory offsets; the activation tiles are at 0
+  uint32_t oSX, oRB, oRX, oR, oStage;  // shared-memory offsets; the activation fragments are at 0
   uint64_t timeout_ns;
   uint32_t* err;
 };
 
 struct __align__(8) DecCtl {
   uint64_t full[kMaxStages];     // producer arrival + record bytes
-  uint64_t empty[kMaxStages];    // the 4 warps of the warpgroup that converted the stage
+  uint64_t empty[kMaxStages];    // the 4 warps of the consuming set are done with the stage
   uint64_t r_full[kRSlots];
-  uint64_t r_empty[kRSlots];
-  uint64_t a_ready[kWG][2];      // A buffer b of warpgroup w holds a converted item (4 warp arrivals)
-  uint64_t d_ready[kWG][2];      // its MMAs are complete (tcgen05.commit)
-  uint64_t work_bar;             // activation tiles converted (16 warp arrivals)
-  uint64_t epi_bar;              // bounded barrier of the epilogue warps (one arrival each)
+  uint64_t r_empty[kRSlots];     // the 2 warps that used the residual record
+  uint64_t x_full;               // the slice's packed activations and scales have landed (bytes)
+  uint64_t work_bar;             // activation fragments converted (one arrival per MMA warp)
+  uint64_t epi_bar;              // bounded barrier of the 2 epilogue warps
   uint64_t map_ready;            // residual map and ring positions are built
-  uint64_t chain[kWG];           // warpgroup w may add its partial of the tile (w >= 1)
-  uint64_t rb_done;              // the CTA's partial of the tile is complete
+  uint64_t chain[kSlots - 1];    // set q has added its partial of the tile
+  uint64_t rb_done;              // the last set has added its partial: the CTA's partial is complete
   uint64_t rx_full;              // every rank's rows for this CTA have landed (bytes)
   uint64_t rx_free;              // every owner has consumed this CTA's last push
-  int32_t item_gl[kWG][2];       // slice group of the item in A buffer b (-1: warpgroup finished)
+  uint64_t exit_bar;             // every warp of the CTA is done with its role
   int32_t map[kMaxVisits][kMaxSlice][2];   // CSR entry of the slice's residual blocks per tile, or -1
   int32_t rpos[kMaxVisits][kMaxSlice][2];  // position of that block in the residual-ring order
   int32_t sc_off[kMaxVisits + 1], sc_a0[kMaxVisits], sc_a1[kMaxVisits];
-  uint32_t tmem_base;
   int abort_flag;
 };
+// Static shared memory of the kernel: the control block, padded as the
+// dynamic array that follows it is aligned.
+constexpr int kCtlBytes = (static_cast<int>(sizeof(DecCtl)) + 127) / 128 * 128;
 
 // --- cluster / misc PTX -------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -156,16 +165,6 @@ __device__ __forceinline__ void bulk_s2peer(uint32_t dst_cluster, const void* sr
       "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
       : "memory");
 }
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -191,15 +190,66 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
     }
   }
 }
+// Bounded wait for the roles that wait long (producers for free slots, the
+// epilogue for a finished tile): each try_wait may stay suspended up to
+// `hint_ns` (it returns as soon as the phase completes), so the waiting warp
+// takes few issue slots from the MMA warps.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_long(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                               uint64_t timeout_ns, uint32_t* err_word) {
+  constexpr uint32_t kHintNs = 20000;
+  if (mbar_try_wait_hint(bar, parity, kHintNs)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    __nanosleep(200);  // back off: a waiting warp issues nothing while asleep
+    if (mbar_try_wait_hint(bar, parity, kHintNs)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > timeout_ns) {
+      atomicOr(err_word, kDevErrTimeout);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
-__device__ __forceinline__ uint4 ld_global_16(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
-
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (1ull << 16) |
-         (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+// 16-byte shared-memory load by shared-window address.
+__device__ __forceinline__ float4 lds_f4(uint32_t saddr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(saddr)
+               : "memory");
+  return v;
 }
+
+// D(16x8, fp32) += A(16x32, E4M3, row-major) * B(32x8, E4M3, column-major):
+// the warp-level FP8 MMA.
+__device__ __forceinline__ void mma_e4m3(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// The same with a zero accumulator in (the first K-step of a group).
+__device__ __forceinline__ void mma_e4m3_zc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%10, %10, %10, %10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+// Packed fp32 pairs (one instruction for two lanes' worth of fp32 math).
 __device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
   uint64_t r;
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
@@ -219,47 +269,13 @@ __device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
   return r;
 }
 
-// Eight INT4 codes q (two's complement nibbles, element i in bits 4i..4i+3)
-// -> eight E4M3 bytes holding q + 8 exactly.  The nibble u = q + 8 is p ^ 8;
-// two 8-entry prmt tables cover u in [0, 8) and [8, 16): a selector nibble
-// with its top bit set makes prmt emit the sign of the table byte, 0 here
-// (all entries are positive), so each table contributes only its own half
-// and an OR merges them.  9 operations per 8 codes.
-__device__ __forceinline__ void uint4x8_to_e4m3(uint32_t p, uint32_t& lo, uint32_t& hi) {
-  constexpr uint32_t kLoA = 0x44403800u, kLoB = 0x4E4C4A48u;  // 0, 1, 2, 3 | 4, 5, 6, 7
-  constexpr uint32_t kHiA = 0x53525150u, kHiB = 0x57565554u;  // 8, 9, 10, 11 | 12, 13, 14, 15
+// Eight weight codes q (two's complement nibbles, element i in bits 4i..4i+3)
+// -> two words of four E4M3 bytes holding (q + 8) * 2^-9 exactly: the even
+// elements 0, 2, 4, 6 in `ev`, the odd ones in `od`.
+__device__ __forceinline__ void unpack_u4(uint32_t p, uint32_t& ev, uint32_t& od) {
   const uint32_t u = p ^ 0x88888888u;
-  lo = prmt(kLoA, kLoB, u) | prmt(kHiA, kHiB, p);
-  hi = prmt(kLoA, kLoB, u >> 16) | prmt(kHiA, kHiB, p >> 16);
-}
-
-// Store 32 consecutive 32-bit columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
-      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
-      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
-      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-      : "memory");
-}
-
-// 64 bytes of one row's weight codes (4 K-steps of 16 bytes at src + j*jstride)
-// -> E4M3 (q + 8) in this thread's TMEM lane, 32 columns in one store.
-__device__ __forceinline__ void row_codes_to_tmem(const uint8_t* src, int jstride, uint32_t a_col) {
-  uint4 pk[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) pk[j] = *reinterpret_cast<const uint4*>(src + j * jstride);
-  uint32_t ev[32];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint4x8_to_e4m3(pk[j].x, ev[8 * j + 0], ev[8 * j + 1]);
-    uint4x8_to_e4m3(pk[j].y, ev[8 * j + 2], ev[8 * j + 3]);
-    uint4x8_to_e4m3(pk[j].z, ev[8 * j + 4], ev[8 * j + 5]);
-    uint4x8_to_e4m3(pk[j].w, ev[8 * j + 6], ev[8 * j + 7]);
-  }
-  tmem_st32(a_col, ev);
+  ev = u & 0x0F0F0F0Fu;
+  od = (u >> 4) & 0x0F0F0F0Fu;
 }
 
 // Sum of the eight signed codes of a word of packed activations.
@@ -269,24 +285,26 @@ __device__ __forceinline__ int nibble_sum8(uint32_t p) {
   return static_cast<int>((b * 0x01010101u) >> 24) - 64;
 }
 
-// One item of a converter warpgroup: a group's dense product (kind 0) or its
-// residual product (kind 1).
-struct Item {
-  int i, q, kind;  // stage, group within the stage, kind
-};
-
 template <int TN, bool kDebug>
-__global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParams p) {
+__global__ void __maxnreg__(128) w4a4_decode_kernel(const DecParams p) {
+  constexpr int NB = TN / 8;                 // 8-token blocks of one MMA
+  constexpr int kGroupFrag = 4 * NB * 256;   // activation fragment bytes of one group
+  constexpr int kChains = NB == 1 ? 2 : 1;   // accumulator sets per MMA tile, for independent MMAs
   extern __shared__ uint8_t smem_raw[];
   __shared__ DecCtl ctl;
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* btiles = smem;                                  // [ns][TN rows][128 B] E4M3, 128B-swizzled K-major
-  float* sxs = reinterpret_cast<float*>(smem + p.oSX);     // [ns][TN] activation scales
-  float* sums = sxs + kMaxSlice * TN;                      // [ns][TN] 8 * (sum of the group's activation codes)
+  // 1024-aligned by offsetting the shared array itself (keeps accesses in the shared window)
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  // Activation fragments: [ns][4 K-steps][NB][32 lanes] x 8 bytes (E4M3); lane
+  // (g, t) of block nb holds token 8nb + g: the even codes 8t, 8t+2, .., 8t+6
+  // of the K-step, then the odd ones.
+  uint8_t* bfrag = smem;
+  // [ns][TN/2] x {sx[2i], sx[2i+1], c[2i], c[2i+1]}: activation scales and the
+  // offset term c = 2^-9 * 8 * (sum of the group's activation codes)
+  float4* sxc = reinterpret_cast<float4*>(smem + p.oSX);
   float* rb = reinterpret_cast<float*>(smem + p.oRB);      // [128 rows][TN] the CTA's partial of a tile
   float* rx = reinterpret_cast<float*>(smem + p.oRX);      // [CS sources][R rows][TN] the rows this CTA owns
   uint8_t* rring = smem + p.oR;                            // [kRSlots] residual records
-  uint8_t* stages = smem + p.oStage;                       // [nstages] x two base records
+  uint8_t* stages = smem + p.oStage;                       // [nstages] base records
   if (threadIdx.x == 0) MQ_DTRACE(0);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -295,16 +313,12 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
   const int rank = static_cast<int>(cluster_rank());
   const int cid = static_cast<int>(cluster_index());
   const int gs = rank * G / CS, ge = (rank + 1) * G / CS, ns = ge - gs;  // this CTA's K slice
-  const int spv = (ns + kUG - 1) / kUG;                                   // stages per visited tile
   const int nvis = (p.tiles - cid + p.nclusters - 1) / p.nclusters;       // tiles cid, cid + nclusters, ...
-  const int total = nvis * spv;
+  const int total = nvis * ns;                                            // stage i: group i % ns of visit i / ns
   volatile int* abort_flag = &ctl.abort_flag;
   const uint64_t tmo = p.timeout_ns;
   auto tile_of = [&](int v) { return static_cast<int64_t>(cid) + static_cast<int64_t>(v) * p.nclusters; };
-  auto stage_ng = [&](int i) { return min(kUG, ns - (i % spv) * kUG); };
-  auto stage_rec = [&](int i) {  // first record of stage i
-    return p.wpk + (tile_of(i / spv) * G + gs + (i % spv) * kUG) * kWRecBytes;
-  };
+  auto stage_rec = [&](int i) { return p.wpk + (tile_of(i / ns) * G + gs + i % ns) * kWRecBytes; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -313,21 +327,17 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
     }
     for (int s = 0; s < kRSlots; ++s) {
       mbar_init(&ctl.r_full[s], 1);
-      mbar_init(&ctl.r_empty[s], 4);
+      mbar_init(&ctl.r_empty[s], 2);
     }
-    for (int w = 0; w < kWG; ++w) {
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(&ctl.a_ready[w][b], 4);
-        mbar_init(&ctl.d_ready[w][b], 1);
-      }
-      mbar_init(&ctl.chain[w], 4);
-    }
-    mbar_init(&ctl.work_bar, 16);
+    mbar_init(&ctl.x_full, 1);
+    mbar_init(&ctl.work_bar, kMmaWarps);
     mbar_init(&ctl.epi_bar, kEpiThreads / 32);
     mbar_init(&ctl.map_ready, 1);
+    for (int s = 0; s + 1 < kSlots; ++s) mbar_init(&ctl.chain[s], 4);
     mbar_init(&ctl.rb_done, 4);
     mbar_init(&ctl.rx_full, 1);
     mbar_init(&ctl.rx_free, CS);
+    mbar_init(&ctl.exit_bar, kThreads / 32);
     ctl.abort_flag = 0;
     fence_mbar_init();
   }
@@ -340,17 +350,50 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
   if (threadIdx.x == 0) MQ_DTRACE(1);
 
   if (warp == kWarpProducer) {
-    // ---------------- producer: block list, then stages in order ----------------
+    // ---------------- producer: activations, then the base-weight stages in order ----------------
     const int pre = min(NS, total);
-    if (lane < pre) prefetch_l2(stage_rec(lane), stage_ng(lane) * kWRecBytes);  // no dependency: L2 only
-    // Everything below may read buffers the preceding kernel wrote (weights
-    // packed just before, the block list): wait for it.
+    if (lane < pre) prefetch_l2(stage_rec(lane), kWRecBytes);  // no dependency: L2 only
+    // Everything below may read buffers the preceding kernel wrote (the
+    // activations just quantized, weights just packed): wait for it.
     pdl_wait();
     if (lane == 0) MQ_DTRACE(2);
-    if (lane < pre) {  // the first stages: weights in flight before the block list is read
-      mbar_arrive_expect_tx(&ctl.full[lane], stage_ng(lane) * kWRecBytes);
-      bulk_g2s(stages + lane * kStageBytes, stage_rec(lane), stage_ng(lane) * kWRecBytes, &ctl.full[lane]);
+    {  // the slice's packed activations (group gl into the upper half of its
+       // fragment block) and scales (into the reduction buffer, unused until
+       // the first tile ends), ahead of every weight copy
+      const uint32_t xbytes = static_cast<uint32_t>(p.Mp) * 64;
+      if (lane == 0) mbar_arrive_expect_tx(&ctl.x_full, ns * xbytes + ns * p.Mp * 2);
+      __syncwarp();
+      for (int gl = lane; gl < ns; gl += 32)
+        bulk_g2s(bfrag + gl * kGroupFrag + TN * 64, p.xq + static_cast<int64_t>(gs + gl) * xbytes, xbytes,
+                 &ctl.x_full);
+      if (lane == 0)
+        bulk_g2s(rb, p.xs + static_cast<int64_t>(gs) * p.Mp, static_cast<uint32_t>(ns * p.Mp * 2), &ctl.x_full);
     }
+    if (lane < pre) {  // the first stages, all at once
+      mbar_arrive_expect_tx(&ctl.full[lane], kWRecBytes);
+      bulk_g2s(stages + lane * kStageBytes, stage_rec(lane), kWRecBytes, &ctl.full[lane]);
+    }
+    // then each stage once its slot is free; (v, gl) = visit and group of
+    // stage i, st its slot, ph the parity of the slot's previous use
+    int v = pre / ns, gl = pre - (pre / ns) * ns, st = 0, ph = 0;
+    for (int i = pre; i < total; ++i) {
+      int ok = 1;
+      if (lane == 0) {
+        ok = mbar_wait_long(&ctl.empty[st], ph, abort_flag, tmo, p.err);
+        if (ok) {
+          mbar_arrive_expect_tx(&ctl.full[st], kWRecBytes);
+          bulk_g2s(stages + st * kStageBytes, p.wpk + (tile_of(v) * G + gs + gl) * kWRecBytes, kWRecBytes,
+                   &ctl.full[st]);
+        }
+      }
+      if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
+      if (lane == 0 && i < pre + 8) MQ_DTRACE(4 + i - pre);
+      if (++gl == ns) gl = 0, ++v;
+      if (++st == NS) st = 0, ph ^= 1;
+    }
+  } else if (warp == kWarpResidual) {
+    // ---------------- residual producer: block list, then the residual records in order ----------------
+    pdl_wait();  // the block list may have been written by the preceding kernel
     // Block list of every visited tile, restricted to this slice: lane v reads
     // the row pointers of tile v's two block rows, then all lanes read the
     // entries of all tiles at once.
@@ -427,16 +470,14 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
       mbar_arrive(&ctl.map_ready);
       MQ_DTRACE(3);
     }
-    for (int i = 0; i < total; ++i) {
-      const int st = i % NS;
-      const int v = i / spv, g0l = (i % spv) * kUG, ng = stage_ng(i);
-      // lanes 0..3: the residual records of the stage's groups, into the ring
+    for (int i = 0, v = 0, gl = 0; i < total; ++i, gl = gl + 1 == ns ? 0 : gl + 1, v += gl == 0) {
+      // lanes 0, 1: the residual records of stage i's two halves (group gl of visit v), into the ring
       int rok = 1;
-      if (lane < kUG * 2 && (lane >> 1) < ng) {
-        const int e = ctl.map[v][g0l + (lane >> 1)][lane & 1];
+      if (lane < 2) {
+        const int e = ctl.map[v][gl][lane];
         if (e >= 0) {
-          const int c = ctl.rpos[v][g0l + (lane >> 1)][lane & 1], slot = c % kRSlots;
-          if (c >= kRSlots) rok = mbar_wait(&ctl.r_empty[slot], ((c / kRSlots) & 1) ^ 1, abort_flag, tmo, p.err);
+          const int c = ctl.rpos[v][gl][lane], slot = c % kRSlots;
+          if (c >= kRSlots) rok = mbar_wait_long(&ctl.r_empty[slot], ((c / kRSlots) & 1) ^ 1, abort_flag, tmo, p.err);
           if (rok) {
             mbar_arrive_expect_tx(&ctl.r_full[slot], kRRecBytes);
             bulk_g2s(rring + slot * kRRecBytes, p.rpk + static_cast<int64_t>(e) * kRRecBytes, kRRecBytes,
@@ -445,395 +486,246 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
         }
       }
       if (!__all_sync(0xFFFFFFFFu, rok)) break;
-      if (i >= pre) {  // the base records of stage i, once its slot is free
-        int ok = 1;
-        if (lane == 0) {
-          ok = mbar_wait(&ctl.empty[st], ((i / NS) & 1) ^ 1, abort_flag, tmo, p.err);
-          if (ok) {
-            mbar_arrive_expect_tx(&ctl.full[st], ng * kWRecBytes);
-            bulk_g2s(stages + st * kStageBytes, stage_rec(i), ng * kWRecBytes, &ctl.full[st]);
-          }
-        }
-        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
-      }
-      if (lane == 0 && i < 8) MQ_DTRACE(4 + i);
     }
-  } else if (warp >= kWarpMma && warp < kWarpMma + kMmaWarps) {
-    // ---------------- MMA issue: serve whichever of its warpgroups has an item ready ----------------
-    const int w0 = (warp - kWarpMma) * (kWG / kMmaWarps);
-    constexpr uint32_t kIdesc =
-        (1u << 4) | (static_cast<uint32_t>(TN >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
-    const bool ok0 = mbar_wait(&ctl.work_bar, 0, abort_flag, tmo, p.err);  // activation tiles and TMEM ready
-    tc_fence_after();
-    if (lane == 0 && ok0) {
-      const uint32_t tmem = ctl.tmem_base;
-      const uint32_t bt = smem_u32(btiles);
-      int n[kWG / kMmaWarps] = {};
-      int alive = kWG / kMmaWarps;
-      uint64_t t_idle = 0;
-#ifdef MQ_DEC_TRACE
-      long long prof_[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0}, pt_ = 0, tl_ = clock64();
-#endif
-      while (alive > 0) {
-        bool progressed = false;
-#pragma unroll
-        for (int x = 0; x < kWG / kMmaWarps; ++x) {
-          const int w = w0 + x;
-          if (n[x] < 0) continue;
-          const int b = n[x] & 1;
-          if (!mbar_test(&ctl.a_ready[w][b], (n[x] >> 1) & 1)) continue;
-          const int gl = ctl.item_gl[w][b];
-          if (gl < 0) {  // the warpgroup has no more items
-            n[x] = -1;
-            --alive;
-            continue;
-          }
-          MQ_PT();
-          tc_fence_after();
-          const uint32_t a_col = tmem + w * 128 + 32 * b, d_col = tmem + w * 128 + 64 + TN * b;
-          const uint32_t b_addr = bt + gl * (TN * 128);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) tc_mma_ts(d_col, a_col + 8 * j, sw128_desc(b_addr + 32 * j), kIdesc, j > 0);
-          tc_commit(&ctl.d_ready[w][b]);
-          MQ_PA(0);
-          ++n[x];
-          progressed = true;
-        }
-        if (progressed) {
-          t_idle = 0;
-        } else {
-          if (*abort_flag) break;
-          const uint64_t now = globaltimer();
-          if (t_idle == 0) {
-            t_idle = now;
-          } else if (now - t_idle > tmo) {
-            atomicOr(p.err, kDevErrTimeout);
-            *abort_flag = 1;
-            break;
-          }
-        }
-      }
-#ifdef MQ_DEC_TRACE
-      prof_[1] = clock64() - tl_;  // the whole issue loop
-      if (w0 == 0) mq_dec_trace_prof(4, prof_, 9);
-#endif
-    }
-  } else if (warp < kWarpMma) {
-    // ---------------- converters + drain ----------------
-    const int w = warp >> 2, quarter = warp & 3;
-    const int r = quarter * 32 + lane;  // weight row of the tile = TMEM lane
-    const int half = r >> 6;
-    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+  } else if (warp < kMmaWarps) {
+    // ---------------- MMA warps ----------------
+    const int gq = lane >> 2, tq = lane & 3;   // MMA fragment coordinates: row / token group, thread in group
+    const int q = warp >> 2;                   // warp set: stages q, q + kSlots, ...
+    const int rb0 = 32 * (warp & 3);           // first tile row of this warp
+    const int half = rb0 >> 6;                 // residual block (64 rows) of its rows
     bool ok = true;
-    if (warp == 0) tmem_alloc(&ctl.tmem_base, kTmemCols);
 
-    // --- this slice's activations, once: packed codes -> E4M3 tiles, their
-    // group sums, and the scales -> fp32
+    // --- this slice's activations, once: packed codes -> E4M3 fragments,
+    // their group sums, and the scales -> fp32.  Warp w converts groups w,
+    // w + kMmaWarps, ..; each group's packed codes sit in the upper half of
+    // its own fragment block, so the warp reads all of them before writing.
     pdl_wait();
-    {
-      const int tid = threadIdx.x;  // 0..511
-      for (int idx = tid; idx < ns * TN; idx += kWorkers) {
-        const int gl = idx / TN, m = idx % TN;
-        uint8_t* row = btiles + gl * (TN * 128) + (m >> 3) * 1024 + (m & 7) * 128;
-        int sum = 0;
-        float sx = 0.0f;
-        if (m < p.Mp) {
-          const uint8_t* src = p.xq + (static_cast<int64_t>(gs + gl) * p.Mp + m) * 64;
-          uint4 pk[4];
+    if (!(ok = mbar_wait_long(&ctl.x_full, 0, abort_flag, tmo, p.err))) {
+      // fall through to the arrival below; the abort flag is up
+    } else {
+      const uint16_t* xs_raw = reinterpret_cast<const uint16_t*>(rb);  // [ns][Mp]
+      float* sxcf = reinterpret_cast<float*>(sxc);
+      for (int gl = warp; gl < ns; gl += kMmaWarps) {
+        uint8_t* blk = bfrag + gl * kGroupFrag;
+        const uint8_t* raw = blk + TN * 64;  // [Mp][64]
+        uint32_t wv[NB][4];
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) pk[jj] = ld_global_16(src + jj * 16);
-          sx = __half2float(__ushort_as_half(p.xs[static_cast<int64_t>(gs + gl) * p.Mp + m]));
+        for (int nb = 0; nb < NB; ++nb) {
+          const int m = 8 * nb + gq;
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            uint4 lo, hi;
-            int4x8_to_e4m3(pk[jj].x, lo.x, lo.y);
-            int4x8_to_e4m3(pk[jj].y, lo.z, lo.w);
-            int4x8_to_e4m3(pk[jj].z, hi.x, hi.y);
-            int4x8_to_e4m3(pk[jj].w, hi.z, hi.w);
-            sum += nibble_sum8(pk[jj].x) + nibble_sum8(pk[jj].y) + nibble_sum8(pk[jj].z) + nibble_sum8(pk[jj].w);
-            // 16-byte chunk c of row m is stored at chunk c ^ (m & 7) of its 128-byte row
-            *reinterpret_cast<uint4*>(row + (((2 * jj) ^ (m & 7)) * 16)) = lo;
-            *reinterpret_cast<uint4*>(row + (((2 * jj + 1) ^ (m & 7)) * 16)) = hi;
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(row + c * 16) = make_uint4(0, 0, 0, 0);
+          for (int j = 0; j < 4; ++j)
+            wv[nb][j] = m < p.Mp ? *reinterpret_cast<const uint32_t*>(raw + m * 64 + j * 16 + tq * 4) : 0u;
         }
-        sxs[gl * TN + m] = sx;
-        sums[gl * TN + m] = 8.0f * static_cast<float>(sum);
-      }
-      fence_proxy_async_smem();  // generic writes -> the tensor core's reads
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.work_bar);
-      ok = mbar_wait(&ctl.work_bar, 0, abort_flag, tmo, p.err);
-      tc_fence_after();
-      if (threadIdx.x == 0) MQ_DTRACE(12);
-    }
-    const uint32_t tmem = ctl.tmem_base;
-    const uint32_t colA = tmem + w * 128, colD = tmem + w * 128 + 64;  // buffer b: +32b, +TN*b
-
-    uint64_t acc[TN / 2];
+        __syncwarp();
 #pragma unroll
-    for (int k = 0; k < TN / 2; ++k) acc[k] = 0;
+        for (int nb = 0; nb < NB; ++nb) {
+          int sum = 0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t lo, hi;  // codes 0..3, 4..7 of the word
+            int4x8_to_e4m3(wv[nb][j], lo, hi);
+            *reinterpret_cast<uint2*>(blk + ((j * NB + nb) * 32 + lane) * 8) =
+                make_uint2(prmt(lo, hi, 0x6420u), prmt(lo, hi, 0x7531u));  // even | odd codes
+            sum += nibble_sum8(wv[nb][j]);
+          }
+          sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);  // the token's four quarters of each K-step
+          sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+          const int m = 8 * nb + gq;
+          if (tq == 0) {
+            float* dst = sxcf + (gl * (TN / 2) + m / 2) * 4 + (m & 1);
+            dst[0] = m < p.Mp ? 512.0f * __half2float(__ushort_as_half(xs_raw[gl * p.Mp + m])) : 0.0f;  // 2^9 sx
+            dst[2] = static_cast<float>(sum) * (1.0f / 64.0f);  // 8 * sum * 2^-9, exact
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl.work_bar);
+    ok = mbar_wait_long(&ctl.work_bar, 0, abort_flag, tmo, p.err) && ok;
+    if (threadIdx.x == 0) MQ_DTRACE(12);
+
+    // accumulators of row tile mt (rows rb0 + 16mt + gq, +8) and token block
+    // nb, as fp32 pairs: [0] = row +0, tokens 8nb+2tq, +1; [1] = row +8, same tokens
+    uint64_t acc[2][NB][2];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) acc[mt][nb][0] = acc[mt][nb][1] = 0ull;
 #ifdef MQ_DEC_TRACE
     long long prof_[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0}, pt_ = 0;
 #endif
 
-    bool map_seen = false;
-    // Items of this warpgroup: its stages in order; in a stage, the dense
-    // items of its groups, then the residual items of the groups that have a
-    // block.  Returns 1 (next item in `it`), 0 (no more items), -1 (gave up).
-    auto advance = [&](Item& it) -> int {
-      const int ng = stage_ng(it.i);
-      if (it.kind == 0 && it.q + 1 < ng) {
-        ++it.q;
-        return 1;
-      }
-      // residual items of this stage, after its dense items
-      if (!map_seen) {
-        if (!mbar_wait(&ctl.map_ready, 0, abort_flag, tmo, p.err)) return -1;
-        map_seen = true;
-      }
-      const int v = it.i / spv, g0l = (it.i % spv) * kUG;
-      for (int q = it.kind == 0 ? 0 : it.q + 1; q < ng; ++q)
-        if (ctl.map[v][g0l + q][0] >= 0 || ctl.map[v][g0l + q][1] >= 0) {
-          it.kind = 1;
-          it.q = q;
-          return 1;
+    // One group's product for this warp's 32 rows, scaled into the
+    // accumulators: dense (base record, K-steps 2048 bytes apart, first row
+    // rb0) or residual (residual record, 1024 apart, first row rb0 - 64*half).
+    // sc: the record's fp16 scales; e: the block's CSR entry (residual) or -1.
+    auto group_product = [&](const uint8_t* codes, int jstride, int row0, const uint16_t* sc, int gl,
+                             int64_t tile, int e) {
+      float d[kChains][2][NB][4];
+      const uint8_t* bg = bfrag + gl * kGroupFrag + lane * 8;
+      const uint8_t* wr = codes + (row0 + gq) * 16 + tq * 4;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t a[2][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(wr + j * jstride + mt * 256);        // row +0
+          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(wr + j * jstride + mt * 256 + 128);  // row +8
+          unpack_u4(w0, a[mt][0], a[mt][2]);
+          unpack_u4(w1, a[mt][1], a[mt][3]);
         }
-      it.kind = 0;
-      it.q = 0;
-      it.i += kWG;
-      return it.i < total ? 1 : 0;
-    };
-    // Per in-flight item, by buffer: the item, the row's scale and (residual)
-    // the CSR entry of this thread's block (two named slots, so they stay in registers).
-    struct InFlight {
-      Item it;
-      float s;
-      int e;
-    };
-    InFlight fl0 = {{0, 0, 0}, 0.0f, -1}, fl1 = fl0;
-    auto fl_get = [&](int b) -> InFlight { return b ? fl1 : fl0; };
-    // Wait for the item's inputs and convert its codes into A buffer b (the
-    // tensor-memory stores are issued, not awaited).
-    auto convert = [&](const Item& it, int b, InFlight& f) -> bool {
-      const int st = it.i % NS;
-      const uint32_t a_col = colA + 32 * b + lane_base;
-      const int v = it.i / spv, gl = (it.i % spv) * kUG + it.q;
-      f.it = it;
-      if (it.kind == 0) {
-        MQ_PT();
-        if (it.q == 0 && !mbar_wait(&ctl.full[st], (it.i / NS) & 1, abort_flag, tmo, p.err)) return false;
-        MQ_PA(1);
-        MQ_PT();
-        const uint8_t* rec = stages + st * kStageBytes + it.q * kWRecBytes;
-        f.s = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(rec + kWRecScales + 2 * r)));
-        f.e = -1;
-        row_codes_to_tmem(rec + r * 16, 2048, a_col);
-        MQ_PA(2);
-      } else {
-        const int e = ctl.map[v][gl][half];
-        f.e = e;
-        f.s = 0.0f;
-        if (e >= 0) {  // warp-uniform: a warp's 32 rows lie in one half
-          const int c = ctl.rpos[v][gl][half], slot = c % kRSlots;
-          MQ_PT();
-          if (!mbar_wait(&ctl.r_full[slot], (c / kRSlots) & 1, abort_flag, tmo, p.err)) return false;
-          MQ_PA(1);
-          MQ_PT();
-          const uint8_t* rec = rring + slot * kRRecBytes;
-          f.s = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(rec + kRRecScales + 2 * (r & 63))));
-          row_codes_to_tmem(rec + (r & 63) * 16, 1024, a_col);
-          MQ_PA(2);
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          const uint2 b = *reinterpret_cast<const uint2*>(bg + (j * NB + nb) * 256);
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            if (j < kChains)
+              mma_e4m3_zc(d[j % kChains][mt][nb], a[mt], b.x, b.y);
+            else
+              mma_e4m3(d[j % kChains][mt][nb], a[mt], b.x, b.y);
+          }
         }
       }
-      return true;
-    };
-    // Hand the converted item in A buffer b to the MMA warp and release what
-    // this warpgroup has read.
-    auto handoff = [&](const Item& it, int b) {
-      const int st = it.i % NS;
-      const int v = it.i / spv, gl = (it.i % spv) * kUG + it.q;
-      MQ_PT();
-      tc_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (r == 0) ctl.item_gl[w][b] = gl;
-        // the stage's codes and scales are read once its last dense item is converted
-        if (it.kind == 0 && it.q == stage_ng(it.i) - 1) mbar_arrive(&ctl.empty[st]);
-        if (it.kind == 1) {
+      if (kChains > 1) {
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
-            if (ctl.map[v][gl][h] >= 0) mbar_arrive(&ctl.r_empty[ctl.rpos[v][gl][h] % kRSlots]);
-        }
-        // item_gl is written by warp quarter 0 before its own arrival; the MMA
-        // warp's wait needs all four arrivals, so it sees the value
-        mbar_arrive(&ctl.a_ready[w][b]);
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) d[0][mt][nb][r] += d[kChains - 1][mt][nb][r];
       }
-      MQ_PA(6);
-    };
-    // acc[m] += sx[m] * (s * (D[m] - 8 * sum_m)) from D buffer b (or, as a test hook, store the dots)
-    auto drain = [&](int b) {
-      const InFlight f = fl_get(b);
-      const Item it = f.it;
-      const int gl = (it.i % spv) * kUG + it.q;
-      const int e = f.e;
-      const bool use = it.kind == 0 || e >= 0;
-      const float4* sx4 = reinterpret_cast<const float4*>(sxs + gl * TN);
-      const float4* su4 = reinterpret_cast<const float4*>(sums + gl * TN);
-      const uint64_t s2 = f2pack(f.s, f.s), m1 = f2pack(-1.0f, -1.0f);
+      uint64_t s2[2][2];  // the rows' scales, paired
 #pragma unroll
-      for (int cc = 0; cc < TN / 16; ++cc) {
-        uint32_t dv[16];
-        tmem_ld16(colD + TN * b + 16 * cc + lane_base, dv);
-        tc_wait_ld();
-        if (kDebug) {
-          if (use) {
-            const int64_t n = tile_of(it.i / spv) * kTileN + r;
+      for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-            for (int i2 = 0; i2 < 16; ++i2) {
-              const int m = 16 * cc + i2;
-              if (m < p.M) {
-                const int32_t d =
-                    static_cast<int32_t>(__uint_as_float(dv[i2])) - static_cast<int32_t>(sums[gl * TN + m]);
-                if (it.kind == 0)
-                  p.dots_w[(static_cast<int64_t>(m) * p.N + n) * G + gs + gl] = d;
-                else
-                  p.dots_r[(static_cast<int64_t>(m) * p.nnzb + e) * 64 + (r & 63)] = d;
+        for (int h = 0; h < 2; ++h) {
+          const float sv = __half2float(__ushort_as_half(sc[row0 + 16 * mt + 8 * h + gq]));
+          s2[mt][h] = f2pack(sv, sv);
+        }
+      const float4* sg = sxc + gl * (TN / 2) + tq;
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        const float4 f = sg[4 * nb];  // tokens t0 = 8nb + 2tq, t0 + 1: 2^9 sx, 2^9 sx, c, c
+        const uint64_t sx2 = f2pack(f.x, f.y), c2 = f2pack(f.z, f.w), m1 = f2pack(-1.0f, -1.0f);
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          // 2^-9 times the dot of q with x: the measured dot minus the offset term, exact
+          if (kDebug) {
+            const float e00 = d[0][mt][nb][0] - f.z, e01 = d[0][mt][nb][1] - f.w;
+            const float e10 = d[0][mt][nb][2] - f.z, e11 = d[0][mt][nb][3] - f.w;
+            const float ev[2][2] = {{e00, e01}, {e10, e11}};
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int c = 0; c < 2; ++c) {
+                const int m = 8 * nb + 2 * tq + c, r = rb0 + 16 * mt + 8 * h + gq;
+                if (m < p.M) {
+                  const int32_t dv = static_cast<int32_t>(ev[h][c] * 512.0f);
+                  if (e < 0)
+                    p.dots_w[(static_cast<int64_t>(m) * p.N + tile * kTileN + r) * G + gs + gl] = dv;
+                  else
+                    p.dots_r[(static_cast<int64_t>(m) * p.nnzb + e) * 64 + (r & 63)] = dv;
+                }
               }
-            }
-          }
-        } else if (use) {
-#pragma unroll
-          for (int j4 = 0; j4 < 4; ++j4) {
-            const float4 sv = sx4[cc * 4 + j4], cv = su4[cc * 4 + j4];  // tokens 16cc + 4j4 .. +3
-            const int jp = cc * 8 + j4 * 2;
-            // the dot of q with x is the dot of q + 8 minus 8 * sum(x): exact integers
-            const uint64_t d0 = f2fma(f2pack(cv.x, cv.y), m1,
-                                      f2pack(__uint_as_float(dv[4 * j4]), __uint_as_float(dv[4 * j4 + 1])));
-            const uint64_t d1 = f2fma(f2pack(cv.z, cv.w), m1,
-                                      f2pack(__uint_as_float(dv[4 * j4 + 2]), __uint_as_float(dv[4 * j4 + 3])));
-            acc[jp] = f2fma(f2pack(sv.x, sv.y), f2mul(d0, s2), acc[jp]);
-            acc[jp + 1] = f2fma(f2pack(sv.z, sv.w), f2mul(d1, s2), acc[jp + 1]);
+          } else {
+            const uint64_t e0 = f2fma(c2, m1, f2pack(d[0][mt][nb][0], d[0][mt][nb][1]));  // row +0
+            const uint64_t e1 = f2fma(c2, m1, f2pack(d[0][mt][nb][2], d[0][mt][nb][3]));  // row +8
+            acc[mt][nb][0] = f2fma(sx2, f2mul(s2[mt][0], e0), acc[mt][nb][0]);
+            acc[mt][nb][1] = f2fma(sx2, f2mul(s2[mt][1], e1), acc[mt][nb][1]);
           }
         }
       }
-      tc_fence_before();
     };
-    // End of visit v: add this warpgroup's partial into the CTA's row-major
-    // buffer, in warpgroup order.
+    // End of visit v: add this warp's partial into the CTA's row-major
+    // buffer, set 0 first, then set 1, then set 2 (each over all 128 rows).
     auto finish_visit = [&](int v) -> bool {
       bool passed;
-      if (w == 0)  // every owner has consumed the previous tile's push out of this buffer
+      if (q == 0)  // every owner has consumed the previous tile's push out of this buffer
         passed = v == 0 || mbar_wait_cluster(&ctl.rx_free, (v - 1) & 1, abort_flag, tmo, p.err);
       else
-        passed = mbar_wait(&ctl.chain[w], v & 1, abort_flag, tmo, p.err);
+        passed = mbar_wait_long(&ctl.chain[q - 1], v & 1, abort_flag, tmo, p.err);
       if (!passed) return false;
-      float4* row = reinterpret_cast<float4*>(rb + r * TN);
 #pragma unroll
-      for (int k = 0; k < TN / 4; ++k) {
-        float4 a;
-        f2unpack(acc[2 * k], a.x, a.y);
-        f2unpack(acc[2 * k + 1], a.z, a.w);
-        if (w != 0) {
-          const float4 o = row[k];
-          a.x = o.x + a.x;
-          a.y = o.y + a.y;
-          a.z = o.z + a.z;
-          a.w = o.w + a.w;
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          float2* r0 = reinterpret_cast<float2*>(rb + (rb0 + 16 * mt + gq) * TN + 8 * nb + 2 * tq);
+          float2* r1 = r0 + 4 * TN;  // row + 8
+          float2 v0, v1;
+          f2unpack(acc[mt][nb][0], v0.x, v0.y);
+          f2unpack(acc[mt][nb][1], v1.x, v1.y);
+          if (q != 0) {
+            const float2 o0 = *r0, o1 = *r1;
+            v0 = make_float2(o0.x + v0.x, o0.y + v0.y);
+            v1 = make_float2(o1.x + v1.x, o1.y + v1.y);
+          }
+          *r0 = v0;
+          *r1 = v1;
+          acc[mt][nb][0] = acc[mt][nb][1] = 0ull;
         }
-        row[k] = a;
-        acc[2 * k] = 0;
-        acc[2 * k + 1] = 0;
-      }
       // the buffer is pushed by bulk copies (the async proxy): order these
       // generic writes before them
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(w + 1 < kWG ? &ctl.chain[w + 1] : &ctl.rb_done);
-      if (r == 0 && v < 2) MQ_DTRACE(29 + w * 2 + v);
+      if (lane == 0) mbar_arrive(q + 1 < kSlots ? &ctl.chain[q] : &ctl.rb_done);
+      if (lane == 0 && v == 0) MQ_DTRACE(13 + warp);
       return true;
     };
 
-    // Pipeline: up to two items at the MMA warp; item k uses buffers k & 1.
-    int cur_v = 0;  // visits before cur_v are finished
-    int ndrained = 0;
-    Item nxt;
-    nxt.i = w;
-    nxt.q = 0;
-    nxt.kind = 0;
-    bool have = ok && nxt.i < total;
-    int k = 0;  // items submitted
-    // Before the oldest in-flight item is drained: the visits before its own
-    // are complete (items come in visit order), so they are finished first
-    // (the accumulators then hold only this visit's items); then its MMAs.
-    auto ready_to_drain = [&]() -> bool {
-      const int b = ndrained & 1;
+    bool map_seen = false;
+    int cur_v = 0;
+    // stage i = q, q + kSlots, ..: group gl of visit v, in slot st whose fill parity is ph
+    int v = q / ns, gl = q - (q / ns) * ns, st = q, ph = 0;
+    for (int i = q; ok && i < total; i += kSlots) {
       MQ_PT();
-      bool passed = true;
-      const int vj = fl_get(b).it.i / spv;
-      while (passed && cur_v < vj) passed = finish_visit(cur_v++);
+      while (ok && cur_v < v) ok = finish_visit(cur_v++);
       MQ_PA(5);
-      if (!passed) return false;
+      if (!ok) break;
       MQ_PT();
-      passed = mbar_wait(&ctl.d_ready[w][b], (ndrained >> 1) & 1, abort_flag, tmo, p.err);
-      MQ_PA(3);
-      tc_fence_after();
-      return passed;
-    };
-    auto drain_oldest = [&]() {
+      if (!(ok = mbar_wait(&ctl.full[st], ph, abort_flag, tmo, p.err))) break;
+      MQ_PA(1);
+      const int64_t tile = tile_of(v);
+      const uint8_t* rec = stages + st * kStageBytes;
       MQ_PT();
-      drain(ndrained & 1);
-      MQ_PA(4);
-      ++ndrained;
-    };
-    while (ok && have) {
-      const int b = k & 1;
-      // Item k-2 used buffers b: once its MMAs are done, A[b] is free; item k
-      // is converted into it, and item k-2 is drained from D[b] while the
-      // tensor-memory stores of the conversion complete.
-      if (k >= 2 && !(ok = ready_to_drain())) break;
-      InFlight f;
-      if (!(ok = convert(nxt, b, f))) break;
-      if (k >= 2) drain_oldest();
-      if (b)
-        fl1 = f;
-      else
-        fl0 = f;
-      handoff(nxt, b);
-      ++k;
-      MQ_PT();
-      const int adv = advance(nxt);
-      MQ_PA(0);
-      if (adv < 0) {
-        ok = false;
-        break;
+      group_product(rec, 2048, rb0, reinterpret_cast<const uint16_t*>(rec + kWRecScales), gl, tile, -1);
+      MQ_PA(2);
+      // the residual block of this warp's rows, if the block list has one here
+      if (!map_seen) {
+        MQ_PT();
+        if (!(ok = mbar_wait(&ctl.map_ready, 0, abort_flag, tmo, p.err))) break;
+        MQ_PA(0);
+        map_seen = true;
       }
-      have = adv > 0;
-    }
-    // the last in-flight items
-    while (ok && ndrained < k) {
-      if (!(ok = ready_to_drain())) break;
-      drain_oldest();
-    }
-    if (ok) {  // tell the MMA warp this warpgroup is done (buffer k & 1 is free: item k-2 is drained)
+      const int e = ctl.map[v][gl][half];
+      if (e >= 0) {
+        const int c = ctl.rpos[v][gl][half], slot = c % kRSlots;
+        MQ_PT();
+        if (!(ok = mbar_wait(&ctl.r_full[slot], (c / kRSlots) & 1, abort_flag, tmo, p.err))) break;
+        MQ_PA(3);
+        MQ_PT();
+        const uint8_t* rrec = rring + slot * kRRecBytes;
+        group_product(rrec, 1024, rb0 - 64 * half, reinterpret_cast<const uint16_t*>(rrec + kRRecScales), gl, tile,
+                      e);
+        MQ_PA(4);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.r_empty[slot]);  // the 2 warps of this half release it
+      }
       __syncwarp();
-      if (lane == 0) {
-        if (r == 0) ctl.item_gl[w][k & 1] = -1;
-        mbar_arrive(&ctl.a_ready[w][k & 1]);
-      }
+      if (lane == 0) mbar_arrive(&ctl.empty[st]);  // the set's 4 warps release the stage
+      for (gl += kSlots; gl >= ns; gl -= ns) ++v;
+      if ((st += kSlots) >= NS) st -= NS, ph ^= 1;
     }
     while (ok && cur_v < nvis) ok = finish_visit(cur_v++);
 #ifdef MQ_DEC_TRACE
-    prof_[8] = k;
-    if (r == 0) mq_dec_trace_prof(w, prof_, 9);
+    prof_[8] = (total - q + kSlots - 1) / kSlots;
+    if (lane == 0 && warp < 4) mq_dec_trace_prof(warp, prof_, 9);
 #endif
   } else {
     // ---------------- epilogue: push partial rows to their owners, sum the owned rows, store Y ----------------
     const int et = threadIdx.x - 32 * kWarpEpi0;  // 0 .. kEpiThreads-1
+#ifdef MQ_DEC_TRACE
+    long long prof_[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0}, pt_ = 0;
+#endif
     const uint32_t chunk = static_cast<uint32_t>(R * TN * 4);  // one owner's rows of one partial
     pdl_wait();  // Y may still be in use by the preceding kernel
     int nsync = 0;
@@ -841,8 +733,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
     for (int v = 0; ok && v < nvis; ++v) {
       const int64_t tile = tile_of(v);
       if (et == 0 && CS > 1) mbar_arrive_expect_tx(&ctl.rx_full, CS * chunk);
-      if (!mbar_wait(&ctl.rb_done, v & 1, abort_flag, tmo, p.err)) { ok = false; break; }
-      if (et == 0 && v < 2) MQ_DTRACE(37 + v);
+      if (!mbar_wait_long(&ctl.rb_done, v & 1, abort_flag, tmo, p.err)) { ok = false; break; }
+      if (et == 0 && v < 2) MQ_DTRACE(45 + v);
       const float* src;
       int nsrc;
       if (CS > 1) {
@@ -850,47 +742,73 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
           const uint32_t rx_dst = smem_u32(rx) + rank * chunk, bar = smem_u32(&ctl.rx_full);
           for (int k = 0; k < CS; ++k) bulk_s2peer(mapa(rx_dst, k), rb + k * (R * TN), chunk, mapa(bar, k));
         }
-        if (!mbar_wait(&ctl.rx_full, v & 1, abort_flag, tmo, p.err)) { ok = false; break; }
+        if (!mbar_wait_long(&ctl.rx_full, v & 1, abort_flag, tmo, p.err)) { ok = false; break; }
         src = rx;
         nsrc = CS;
       } else {
         src = rb;
         nsrc = 1;
       }
-      if (et == 0 && v < 2) MQ_DTRACE(39 + v);
+      if (et == 0 && v < 2) MQ_DTRACE(47 + v);
       if (!kDebug) {
-        // thread: one owned row, four tokens; sources summed in rank order
-        for (int idx = et; idx < R * (TN / 4); idx += kEpiThreads) {
-          const int row = idx % R, m4 = (idx / R) * 4;
-          if (m4 >= p.M) continue;
-          const float4* sp = reinterpret_cast<const float4*>(src + row * TN + m4);
-          float4 s = sp[0];
-          for (int j = 1; j < nsrc; ++j) {  // ascending rank = ascending K slice
-            const float4 t = sp[j * (R * TN / 4)];
-            s.x += t.x;
-            s.y += t.y;
-            s.z += t.z;
-            s.w += t.w;
-          }
-          const int64_t n = tile * kTileN + rank * R + row;
-          const float vals[4] = {s.x, s.y, s.z, s.w};
+        // thread: one owned row, four tokens; sources summed in rank order.
+        // Four items' loads go ahead of their stores.
+        const uint32_t src_s = smem_u32(src);
+        const int rsh = __ffs(R) - 1;  // R = 128 / CS is a power of two
+        constexpr int kU = 4;
+        for (int base = et; base < R * (TN / 4); base += kU * kEpiThreads) {
+          MQ_PT();
+          float4 acc4[kU];
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            if (m4 + t < p.M) {
-              const int64_t o = static_cast<int64_t>(m4 + t) * p.N + n;
-              if (p.y_f32)
-                static_cast<float*>(p.y)[o] = vals[t];
-              else
-                static_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(vals[t]);
+          for (int u = 0; u < kU; ++u) {
+            const int idx = base + u * kEpiThreads;
+            const int row = idx & (R - 1), m4 = (idx >> rsh) * 4;
+            if (idx < R * (TN / 4) && m4 < p.M) {
+              const uint32_t a = src_s + static_cast<uint32_t>(row * TN + m4) * 4;
+              float4 sv = lds_f4(a);
+              for (int j = 1; j < nsrc; ++j) {  // ascending rank = ascending K slice
+                const float4 t = lds_f4(a + static_cast<uint32_t>(j * R * TN) * 4);
+                sv.x += t.x;
+                sv.y += t.y;
+                sv.z += t.z;
+                sv.w += t.w;
+              }
+              acc4[u] = sv;
             }
           }
+          MQ_PA(base == et ? 0 : 2);
+          MQ_PT();
+#pragma unroll
+          for (int u = 0; u < kU; ++u) {
+            const int idx = base + u * kEpiThreads;
+            const int row = idx & (R - 1), m4 = (idx >> rsh) * 4;
+            if (idx < R * (TN / 4) && m4 < p.M) {
+              const int64_t n = tile * kTileN + rank * R + row;
+              const float vals[4] = {acc4[u].x, acc4[u].y, acc4[u].z, acc4[u].w};
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                if (m4 + t < p.M) {
+                  const int64_t o = static_cast<int64_t>(m4 + t) * p.N + n;
+                  if (p.y_f32)
+                    static_cast<float*>(p.y)[o] = vals[t];
+                  else
+                    static_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(vals[t]);
+                }
+              }
+            }
+          }
+          MQ_PA(base == et ? 1 : 3);
         }
       }
+      if (et == 0 && v < 2) MQ_DTRACE(53 + v);
       __syncwarp();
       if ((et & 31) == 0) mbar_arrive(&ctl.epi_bar);  // every epilogue warp has read the received rows
-      if (!mbar_wait(&ctl.epi_bar, nsync & 1, abort_flag, tmo, p.err)) { ok = false; break; }
+      if (!mbar_wait_long(&ctl.epi_bar, nsync & 1, abort_flag, tmo, p.err)) { ok = false; break; }
       ++nsync;
-      if (et == 0 && v < 2) MQ_DTRACE(41 + v);
+      if (et == 0 && v < 2) MQ_DTRACE(49 + v);
+#ifdef MQ_DEC_TRACE
+      if (et == 0 && v == 0) mq_dec_trace_prof(5, prof_, 9);
+#endif
       // Tell every source its push has been consumed (it may reuse its buffer
       // and push again); not after the last tile: nobody waits for that.
       if (et == 0 && v + 1 < nvis) {
@@ -902,13 +820,16 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
     }
   }
 
-  tc_fence_before();
+  // Every role is done: warps that finish early wait suspended on a barrier
+  // rather than in a hardware barrier, then all threads meet.
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&ctl.exit_bar);
+  mbar_wait_long(&ctl.exit_bar, 0, abort_flag, tmo, p.err);
   __syncthreads();
-  tc_fence_after();
-  if (threadIdx.x == 0) MQ_DTRACE(44);
+  if (threadIdx.x == 0) MQ_DTRACE(51);
   if (*abort_flag) {
-    // A wait gave up: copies or MMAs may still be landing in this CTA's shared
-    // or tensor memory.  They finish within microseconds; give them 200 us.
+    // A wait gave up: bulk copies may still be landing in this CTA's shared
+    // memory.  They finish within microseconds; give them 200 us.
     if (threadIdx.x == 0) {
       const uint64_t t0 = globaltimer();
       while (globaltimer() - t0 < 200000ull) {
@@ -916,11 +837,10 @@ __global__ void __launch_bounds__(kThreads, 1) w4a4_decode_kernel(const DecParam
     }
     __syncthreads();
   }
-  if (warp == 0) tmem_dealloc(ctl.tmem_base, kTmemCols);
   // Every CTA has received all its rows, so every push out of this CTA's
   // shared memory has been read.
   cluster_sync_all();
-  if (threadIdx.x == 0) MQ_DTRACE(45);
+  if (threadIdx.x == 0) MQ_DTRACE(52);
 }
 
 // ---------------------------------------------------------------------------
@@ -946,7 +866,7 @@ static int max_clusters(int cs) {
   std::lock_guard<std::mutex> lk(mu);
   if (cache[dev][cs] != 0) return cache[dev][cs];
   const void* kern = kernel_ptr<32, false>();
-  const int smem = kSmemLimit - static_cast<int>(sizeof(DecCtl));
+  const int smem = kSmemLimit - kCtlBytes;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
     cudaGetLastError();
     return 0;
@@ -974,10 +894,10 @@ static int max_clusters(int cs) {
 static uint32_t up1024(uint32_t b) { return (b + 1023u) / 1024u * 1024u; }
 
 // Pick the cluster size: the makespan of a CTA is (visits x slice) groups
-// plus a per-visit reduction; the slice's activation tiles must fit.
+// plus a per-visit reduction; the slice's activation fragments must fit.
 static bool decode_plan(int64_t M, int64_t N, int64_t K, DecPlan* out) {
   if (M > 32) return false;
-  const int tn = M <= 16 ? 16 : 32;
+  const int tn = M <= 8 ? 8 : M <= 16 ? 16 : 32;
   const int G = static_cast<int>(K / kGroup), tiles = static_cast<int>(N / kTileN);
   double best = 1e30;
   bool found = false;
@@ -990,13 +910,13 @@ static bool decode_plan(int64_t M, int64_t N, int64_t K, DecPlan* out) {
     pl.tn = tn;
     pl.cs = cs;
     pl.oSX = bbytes;
-    pl.oRB = up1024(pl.oSX + 2 * kMaxSlice * tn * 4);  // scales, then group sums
+    pl.oRB = up1024(pl.oSX + kMaxSlice * tn * 8);  // scales and offset terms
     pl.oRX = pl.oRB + tn * kTileN * 4;
     pl.oR = pl.oRX + (cs > 1 ? tn * kTileN * 4 : 0);
     pl.oStage = up1024(pl.oR + kRSlots * kRRecBytes);
-    const int avail = kSmemLimit - static_cast<int>(sizeof(DecCtl)) - 1024 - static_cast<int>(pl.oStage);
+    const int avail = kSmemLimit - kCtlBytes - 1024 - static_cast<int>(pl.oStage);
     pl.nstages = std::min(kMaxStages, avail / kStageBytes);
-    if (pl.nstages < 3) continue;
+    if (pl.nstages < 2 * kSlots) continue;
     pl.smem = pl.oStage + pl.nstages * kStageBytes + 1024;
     const int ncl = max_clusters(cs);
     if (ncl <= 0) continue;
@@ -1020,7 +940,7 @@ static mq_status launch_decode(const DecParams& dp, const DecPlan& pl, cudaStrea
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return launch_status("decode gemm: device");
   if (!smem_set[dev]) {
-    const int want = kSmemLimit - static_cast<int>(sizeof(DecCtl));
+    const int want = kSmemLimit - kCtlBytes;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, want) != cudaSuccess)
       return launch_status("decode gemm: smem attribute");
     smem_set[dev] = true;
@@ -1045,6 +965,21 @@ static mq_status launch_decode(const DecParams& dp, const DecPlan& pl, cudaStrea
 }
 
 }  // namespace
+
+// The kernel choice for (M, N, K) on the current device: {1, tokens per
+// tile, cluster size, clusters, stages} for the decode kernel, else zeros.
+mq_status gemm_plan_info(int64_t M, int64_t N, int64_t K, int32_t* info) {
+  DecPlan pl;
+  for (int i = 0; i < 5; ++i) info[i] = 0;
+  if (decode_plan(M, N, K, &pl)) {
+    info[0] = 1;
+    info[1] = pl.tn;
+    info[2] = pl.cs;
+    info[3] = pl.nclusters;
+    info[4] = pl.nstages;
+  }
+  return MQ_OK;
+}
 
 // Runs the decode kernel when it covers (M, N, K) on this device; *handled
 // tells the caller whether it did (else the general kernel runs).
@@ -1085,6 +1020,7 @@ mq_status gemm_decode_launch(bool* handled, const uint8_t* xq, const uint16_t* x
   dp.err = device_error_word();
   if (!dp.err) return set_error(MQ_ERR_CUDA, "decode gemm: device error word unavailable");
   const bool dbg = dots_w != nullptr;
+  if (pl.tn == 8) return dbg ? launch_decode<8, true>(dp, pl, stream) : launch_decode<8, false>(dp, pl, stream);
   if (pl.tn == 16) return dbg ? launch_decode<16, true>(dp, pl, stream) : launch_decode<16, false>(dp, pl, stream);
   return dbg ? launch_decode<32, true>(dp, pl, stream) : launch_decode<32, false>(dp, pl, stream);
 }

@@ -24,7 +24,7 @@ RREC_BYTES, RREC_SCALES = 4224, 4096  # residual record: 64x128 codes, then 64 f
 EXPORTS = (
     "mq_quantize_act", "mq_num_selected", "mq_select_workspace_bytes", "mq_select_blocks",
     "mq_pack_weights", "mq_gemm_workspace_bytes", "mq_gemm_workspace_init", "mq_w4a4_residual_gemm",
-    "mq_w4a4_residual_gemm_noalloc",
+    "mq_w4a4_residual_gemm_noalloc", "mq_gemm_plan",
     "mq_debug_group_dots", "mq_check_device_error", "mq_set_wait_timeout_ns", "mq_debug_wait_timeout",
     "mq_status_string", "mq_last_error", "mq_version",
 )
@@ -58,6 +58,7 @@ def lib() -> ctypes.CDLL:
             "mq_w4a4_residual_gemm": (i32, [P, P, i64, P, i64, i64, P, P, i64, P, P, i32, P, sz, P]),
             "mq_w4a4_residual_gemm_noalloc": (i32, [P, P, i64, P, i64, i64, P, P, i64, P, P, i32, P]),
             "mq_debug_group_dots": (i32, [P, P, i64, P, i64, i64, P, P, i64, P, P, P, P, sz, P]),
+            "mq_gemm_plan": (i32, [i64, i64, i64, P]),
             "mq_check_device_error": (i32, [P]),
             "mq_set_wait_timeout_ns": (None, [u64]),
             "mq_debug_wait_timeout": (i32, [P]),
@@ -220,6 +221,14 @@ def gemm(xq: torch.Tensor, xs: torch.Tensor, M: int, pl: PackedLinear, out: torc
                                        _ptr(out), _dtype_code(out.dtype), _ptr(ws), wsb, _stream(stream)),
            "mq_w4a4_residual_gemm")
     return out
+
+
+def gemm_plan(M: int, N: int, K: int) -> dict:
+    """The kernel the GEMM entry points run for (M, N, K) on the current device."""
+    info = (ctypes.c_int32 * 5)()
+    _check(lib().mq_gemm_plan(M, N, K, ctypes.cast(info, ctypes.c_void_p)), "mq_gemm_plan")
+    return {"decode": bool(info[0]), "tokens_per_tile": info[1], "cluster": info[2], "clusters": info[3],
+            "stages": info[4]}
 
 
 def debug_group_dots(xq, xs, M: int, pl: PackedLinear, stream=None):

@@ -224,6 +224,21 @@ mq_status mq_debug_group_dots(const uint8_t* xq, const uint16_t* xs, int64_t M, 
                               int64_t nnzb, const uint8_t* rpk, int32_t* dw, int32_t* dr, void* ws,
                               size_t ws_bytes, mq_stream_t stream);
 
+/*
+ * Which kernel mq_w4a4_residual_gemm (and the no-alloc and debug forms) runs
+ * for a problem of M tokens, N outputs and K inputs on the current device.
+ *   info  host array of 5 int32, written:
+ *         [0] 1 = the decode kernel (split-K over thread-block clusters, up to
+ *             32 tokens), 0 = the general kernel;
+ *         for the decode kernel, [1] tokens per tile (8, 16 or 32), [2] CTAs
+ *         per cluster, [3] clusters launched, [4] weight stages in shared
+ *         memory; zeros for the general kernel.
+ * MQ_ERR_INVALID_ARG for bad sizes (the same rules as the GEMM) or NULL info;
+ * MQ_ERR_DEVICE if the current device is not compute capability 10.3.
+ * Launches nothing.
+ */
+mq_status mq_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t* info);
+
 /* ------------------------------------------------------------------------ */
 /* Status                                                                    */
 /* ------------------------------------------------------------------------ */

@@ -126,11 +126,24 @@ def test_group_dots_bit_exact(M, N, K, budget):
     xq, xs = mq.quantize_act(dev_half(x))
     dw, dr = mq.debug_group_dots(xq, xs, M, pl)
     mq.check_device_error()
+    assert mq.gemm_plan(M, N, K)["decode"] == (M <= 32)  # which kernel these dots came from
     qx, sx = O.quantize_act(x, False)
     p = O.prepare(w, xcal, False, budget)
     assert np.array_equal(dw.cpu().numpy(), O.group_dots(qx, p.qw))
     if p.ksel:
         assert np.array_equal(dr.cpu().numpy(), O.residual_dots(qx, p.qr, p.col_idx))
+
+
+@pytest.mark.parametrize("lin", synth.LLAMA3_8B + synth.QWEN3_32B, ids=lambda l: f"{l.name}-{l.K}x{l.N}")
+def test_decode_kernel_covers_decode_shapes(lin):
+    """Up to 32 tokens, every layer shape of the two model families runs on
+    the decode kernel (a launch-resource failure would otherwise fall back to
+    the general kernel silently); 33 tokens and more run on the general one."""
+    for M in (1, 4, 8, 9, 16, 17, 32):
+        plan = mq.gemm_plan(M, lin.N, lin.K)
+        assert plan["decode"], (M, plan)
+        assert plan["tokens_per_tile"] >= M and plan["clusters"] > 0 and plan["stages"] >= 6
+    assert not mq.gemm_plan(33, lin.N, lin.K)["decode"]
 
 
 def test_group_dots_extremes():
