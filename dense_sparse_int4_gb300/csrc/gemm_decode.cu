@@ -56,6 +56,8 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 // Timeline probes for profiling builds (compiled out unless MQ_DEC_TRACE is
@@ -75,13 +77,26 @@ __device__ void mq_dec_trace_prof(int w, const long long* acc, int n);
 namespace mq {
 namespace {
 
-constexpr int kSlots = 3;                 // warp sets; set q takes groups q, q+3, q+6, .. of the CTA's list
-constexpr int kMmaWarps = 4 * kSlots;     // warp w: rows 32*(w%4) .. +31 of set w/4
-constexpr int kWarpProducer = kMmaWarps;      // 12: activations, then the base-weight stages
-constexpr int kWarpResidual = kMmaWarps + 1;  // 13: block list, then the residual records
-constexpr int kWarpEpi0 = kMmaWarps + 2;      // epilogue warps 14, 15
 constexpr int kEpiThreads = 64;
-constexpr int kThreads = 32 * kWarpEpi0 + kEpiThreads;  // 512: 4 warps per sub-partition
+// Warp roles of the two variants of the kernel.  Compute warps come in sets
+// of four; set q takes groups q, q + kSets, q + 2 kSets, .. of the CTA's list.
+//   warp-MMA variant: 3 sets; warp w owns rows 32*(w%4) .. +31 of its set's
+//     groups (16 warps in all: 4 per sub-partition, up to 128 registers);
+//   tensor-memory variant: 4 sets (warpgroups); thread t of a warpgroup owns
+//     row t (its tensor-memory lane) (20 warps: 5 per sub-partition, 96
+//     registers).
+// Then one producer warp, one residual-producer warp and two epilogue warps.
+template <bool kTC>
+struct Roles {
+  static constexpr int kSets = kTC ? 4 : 3;
+  static constexpr int kCompute = 4 * kSets;
+  static constexpr int kProducer = kCompute;      // activations, then the base-weight stages
+  static constexpr int kResidual = kCompute + 1;  // block list, then the residual records
+  static constexpr int kEpi0 = kCompute + 2;      // epilogue warps
+  static constexpr int kThreads = 32 * kEpi0 + kEpiThreads;
+  static constexpr int kMaxReg = kTC ? 96 : 128;
+};
+constexpr int kTmemCols = 512;  // tensor-memory variant: per warpgroup A0, A1 (32 columns each), D0, D1 (TN each)
 constexpr int kStageBytes = kWRecBytes;   // one group's base record per stage
 constexpr int kMaxStages = 24;
 constexpr int kRSlots = 6;                // residual-record ring
@@ -118,11 +133,14 @@ struct __align__(8) DecCtl {
   uint64_t work_bar;             // activation fragments converted (one arrival per MMA warp)
   uint64_t epi_bar;              // bounded barrier of the 2 epilogue warps
   uint64_t map_ready;            // residual map and ring positions are built
-  uint64_t chain[kSlots - 1];    // set q has added its partial of the tile
+  uint64_t chain[3];             // set q has added its partial of the tile (q < kSets - 1)
   uint64_t rb_done;              // the last set has added its partial: the CTA's partial is complete
   uint64_t rx_full;              // every rank's rows for this CTA have landed (bytes)
   uint64_t rx_free;              // every owner has consumed this CTA's last push
   uint64_t exit_bar;             // every warp of the CTA is done with its role
+  uint64_t a_ready[4][2];        // tensor-memory variant: A buffer b of warpgroup w is stored (4 warp arrivals)
+  uint64_t d_ready[4][2];        // its MMAs are complete (tcgen05.commit)
+  uint32_t tmem_base;
   int32_t map[kMaxVisits][kMaxSlice][2];   // CSR entry of the slice's residual blocks per tile, or -1
   int32_t rpos[kMaxVisits][kMaxSlice][2];  // position of that block in the residual-ring order
   int32_t sc_off[kMaxVisits + 1], sc_a0[kMaxVisits], sc_a1[kMaxVisits];
@@ -146,6 +164,10 @@ __device__ __forceinline__ uint32_t cluster_index() {
 // Every thread of every CTA of the cluster, together.
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// The same without ordering memory: only that every thread of the cluster got here.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;\n\tbarrier.cluster.wait;" ::: "memory");
 }
 __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
   uint32_t r;
@@ -278,6 +300,31 @@ __device__ __forceinline__ void unpack_u4(uint32_t p, uint32_t& ev, uint32_t& od
   od = (u >> 4) & 0x0F0F0F0Fu;
 }
 
+// Store 16 consecutive 32-bit columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+// Shared-memory matrix descriptor of a K-major operand in 128-byte-swizzled
+// rows (8-row atoms 1024 bytes apart).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (1ull << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// One output element (bf16 or fp32 Y, row-major [M][N]).
+__device__ __forceinline__ void store_y(const DecParams& p, int m, int64_t n, float v) {
+  const int64_t o = static_cast<int64_t>(m) * p.N + n;
+  if (p.y_f32)
+    static_cast<float*>(p.y)[o] = v;
+  else
+    static_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(v);
+}
+
 // Sum of the eight signed codes of a word of packed activations.
 __device__ __forceinline__ int nibble_sum8(uint32_t p) {
   const uint32_t u = p ^ 0x88888888u;  // q + 8 in [1, 15]
@@ -285,8 +332,12 @@ __device__ __forceinline__ int nibble_sum8(uint32_t p) {
   return static_cast<int>((b * 0x01010101u) >> 24) - 64;
 }
 
-template <int TN, bool kDebug>
-__global__ void __maxnreg__(128) w4a4_decode_kernel(const DecParams p) {
+template <int TN, bool kDebug, bool kTC>
+__global__ void __maxnreg__(Roles<kTC>::kMaxReg) w4a4_decode_kernel(const DecParams p) {
+  using RL = Roles<kTC>;
+  constexpr int kSlots = RL::kSets, kMmaWarps = RL::kCompute, kWarpProducer = RL::kProducer;
+  constexpr int kWarpResidual = RL::kResidual, kWarpEpi0 = RL::kEpi0, kThreads = RL::kThreads;
+  static_assert(!kTC || TN % 16 == 0, "tensor-memory MMAs with M = 128 need N a multiple of 16");
   constexpr int NB = TN / 8;                 // 8-token blocks of one MMA
   constexpr int kGroupFrag = 4 * NB * 256;   // activation fragment bytes of one group
   constexpr int kChains = NB == 1 ? 2 : 1;   // accumulator sets per MMA tile, for independent MMAs
@@ -320,25 +371,31 @@ __global__ void __maxnreg__(128) w4a4_decode_kernel(const DecParams p) {
   auto tile_of = [&](int v) { return static_cast<int64_t>(cid) + static_cast<int64_t>(v) * p.nclusters; };
   auto stage_rec = [&](int i) { return p.wpk + (tile_of(i / ns) * G + gs + i % ns) * kWRecBytes; };
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
+  if (warp == 0) {  // barrier initialisation, spread over the lanes of warp 0
+    for (int s = lane; s < NS; s += 32) {
       mbar_init(&ctl.full[s], 1);
       mbar_init(&ctl.empty[s], 4);
     }
-    for (int s = 0; s < kRSlots; ++s) {
-      mbar_init(&ctl.r_full[s], 1);
-      mbar_init(&ctl.r_empty[s], 2);
+    if (lane < kRSlots) {
+      mbar_init(&ctl.r_full[lane], 1);
+      mbar_init(&ctl.r_empty[lane], kTC ? 4 : 2);
     }
-    mbar_init(&ctl.x_full, 1);
-    mbar_init(&ctl.work_bar, kMmaWarps);
-    mbar_init(&ctl.epi_bar, kEpiThreads / 32);
-    mbar_init(&ctl.map_ready, 1);
-    for (int s = 0; s + 1 < kSlots; ++s) mbar_init(&ctl.chain[s], 4);
-    mbar_init(&ctl.rb_done, 4);
-    mbar_init(&ctl.rx_full, 1);
-    mbar_init(&ctl.rx_free, CS);
-    mbar_init(&ctl.exit_bar, kThreads / 32);
-    ctl.abort_flag = 0;
+    if (kTC && lane >= 8 && lane < 16) {
+      mbar_init(&ctl.a_ready[(lane - 8) >> 1][lane & 1], 4);
+      mbar_init(&ctl.d_ready[(lane - 8) >> 1][lane & 1], 1);
+    }
+    if (lane + 1 < kSlots) mbar_init(&ctl.chain[lane], 4);
+    if (lane == 16) mbar_init(&ctl.x_full, 1);
+    if (lane == 17) mbar_init(&ctl.work_bar, kMmaWarps);
+    if (lane == 18) mbar_init(&ctl.epi_bar, kEpiThreads / 32);
+    if (lane == 19) mbar_init(&ctl.map_ready, 1);
+    if (lane == 20) mbar_init(&ctl.rb_done, 4);
+    if (lane == 21) mbar_init(&ctl.rx_full, 1);
+    // With one CTA per cluster the last compute set stores Y itself and frees
+    // the reduction buffer (one arrival per warp); else each owner frees it.
+    if (lane == 22) mbar_init(&ctl.rx_free, CS == 1 && !kDebug ? 4 : CS);
+    if (lane == 23) mbar_init(&ctl.exit_bar, kThreads / 32);
+    if (lane == 24) ctl.abort_flag = 0;
     fence_mbar_init();
   }
   // The next kernel may start launching: everything it reads before its own
@@ -488,6 +545,7 @@ __global__ void __maxnreg__(128) w4a4_decode_kernel(const DecParams p) {
       if (!__all_sync(0xFFFFFFFFu, rok)) break;
     }
   } else if (warp < kMmaWarps) {
+   if constexpr (!kTC) {
     // ---------------- MMA warps ----------------
     const int gq = lane >> 2, tq = lane & 3;   // MMA fragment coordinates: row / token group, thread in group
     const int q = warp >> 2;                   // warp set: stages q, q + kSlots, ...
@@ -500,7 +558,7 @@ __global__ void __maxnreg__(128) w4a4_decode_kernel(const DecParams p) {
     // w + kMmaWarps, ..; each group's packed codes sit in the upper half of
     // its own fragment block, so the warp reads all of them before writing.
     pdl_wait();
-    if (!(ok = mbar_wait_long(&ctl.x_full, 0, abort_flag, tmo, p.err))) {
+    if (!(ok = mbar_wait(&ctl.x_full, 0, abort_flag, tmo, p.err))) {
       // fall through to the arrival below; the abort flag is up
     } else {
       const uint16_t* xs_raw = reinterpret_cast<const uint16_t*>(rb);  // [ns][Mp]
@@ -541,7 +599,7 @@ __global__ void __maxnreg__(128) w4a4_decode_kernel(const DecParams p) {
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&ctl.work_bar);
-    ok = mbar_wait_long(&ctl.work_bar, 0, abort_flag, tmo, p.err) && ok;
+    ok = mbar_wait(&ctl.work_bar, 0, abort_flag, tmo, p.err) && ok;
     if (threadIdx.x == 0) MQ_DTRACE(12);
 
     // accumulators of row tile mt (rows rb0 + 16mt + gq, +8) and token block
@@ -643,8 +701,10 @@ __global__ void __maxnreg__(128) w4a4_decode_kernel(const DecParams p) {
       if (q == 0)  // every owner has consumed the previous tile's push out of this buffer
         passed = v == 0 || mbar_wait_cluster(&ctl.rx_free, (v - 1) & 1, abort_flag, tmo, p.err);
       else
-        passed = mbar_wait_long(&ctl.chain[q - 1], v & 1, abort_flag, tmo, p.err);
+        passed = mbar_wait(&ctl.chain[q - 1], v & 1, abort_flag, tmo, p.err);
       if (!passed) return false;
+      const bool direct = CS == 1 && !kDebug && q + 1 == kSlots;  // the last set stores Y
+      const int64_t n0 = tile_of(v) * kTileN;
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
@@ -659,15 +719,29 @@ __global__ void __maxnreg__(128) w4a4_decode_kernel(const DecParams p) {
             v0 = make_float2(o0.x + v0.x, o0.y + v0.y);
             v1 = make_float2(o1.x + v1.x, o1.y + v1.y);
           }
-          *r0 = v0;
-          *r1 = v1;
+          if (direct) {
+            const int m = 8 * nb + 2 * tq;
+            const int64_t n = n0 + rb0 + 16 * mt + gq;
+            if (m < p.M) store_y(p, m, n, v0.x), store_y(p, m, n + 8, v1.x);
+            if (m + 1 < p.M) store_y(p, m + 1, n, v0.y), store_y(p, m + 1, n + 8, v1.y);
+          } else {
+            *r0 = v0;
+            *r1 = v1;
+          }
           acc[mt][nb][0] = acc[mt][nb][1] = 0ull;
         }
       // the buffer is pushed by bulk copies (the async proxy): order these
       // generic writes before them
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(q + 1 < kSlots ? &ctl.chain[q] : &ctl.rb_done);
+      if (lane == 0) {
+        if (q + 1 < kSlots)
+          mbar_arrive(&ctl.chain[q]);
+        else if (!direct)
+          mbar_arrive(&ctl.rb_done);
+        else if (v + 1 < nvis)
+          mbar_arrive(&ctl.rx_free);  // this warp's rows of the buffer are read
+      }
       if (lane == 0 && v == 0) MQ_DTRACE(13 + warp);
       return true;
     };
@@ -720,6 +794,308 @@ __global__ void __maxnreg__(128) w4a4_decode_kernel(const DecParams p) {
     prof_[8] = (total - q + kSlots - 1) / kSlots;
     if (lane == 0 && warp < 4) mq_dec_trace_prof(warp, prof_, 9);
 #endif
+   } else {
+    // ---------------- tensor-memory converters: warpgroup w owns all 128 rows (thread = row = TMEM lane) ----------------
+    const int w = warp >> 2, quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // weight row of the tile
+    const int half = r >> 6;            // residual block (64 rows) of the row; a warp's rows share it
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    float* sxf = reinterpret_cast<float*>(sxc);  // [ns][TN] 2^9 * activation scales
+    float* cfv = sxf + kMaxSlice * TN;           // [ns][TN] offset terms 2^-9 * 8 * (sum of the codes)
+    bool ok = true;
+    if (warp == 0) tmem_alloc(&ctl.tmem_base, kTmemCols);
+
+    // --- this slice's activations, once: packed codes -> E4M3 rows of the
+    // 128-byte-swizzled, K-major B tile (token m = row m), with the same K
+    // order as the A columns (per 8 codes: the even ones, then the odd ones);
+    // group sums and scales.  Warp w converts groups w, w + 16, ..
+    pdl_wait();
+    if (mbar_wait(&ctl.x_full, 0, abort_flag, tmo, p.err)) {
+      if (threadIdx.x == 0) MQ_DTRACE(55);
+      const uint16_t* xs_raw = reinterpret_cast<const uint16_t*>(rb);  // [ns][Mp]
+      constexpr int kLpt = 32 / TN, kWpl = 16 / kLpt;                   // lanes per token, words per lane
+      const int m = lane / kLpt, t0 = (lane % kLpt) * kWpl;
+      for (int gl = warp; gl < ns; gl += kMmaWarps) {
+        uint8_t* blk = bfrag + gl * (TN * 128);
+        const uint8_t* raw = blk + TN * 64;  // [Mp][64]
+        uint32_t wv[kWpl];
+#pragma unroll
+        for (int u = 0; u < kWpl; ++u)
+          wv[u] = m < p.Mp ? *reinterpret_cast<const uint32_t*>(raw + m * 64 + (t0 + u) * 4) : 0u;
+        __syncwarp();
+        uint8_t* row = blk + (m >> 3) * 1024 + (m & 7) * 128;
+        int sum = 0;
+#pragma unroll
+        for (int u = 0; u < kWpl; ++u) {
+          const int t = t0 + u;  // codes 8t .. 8t+7 -> bytes 8t .. 8t+7 of the row: 16-byte chunk t/2
+          uint32_t lo, hi;
+          int4x8_to_e4m3(wv[u], lo, hi);
+          *reinterpret_cast<uint2*>(row + (((t >> 1) ^ (m & 7)) * 16) + (t & 1) * 8) =
+              make_uint2(prmt(lo, hi, 0x6420u), prmt(lo, hi, 0x7531u));
+          sum += nibble_sum8(wv[u]);
+        }
+        if (kLpt == 2) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+        if (lane % kLpt == 0) {
+          sxf[gl * TN + m] = m < p.Mp ? 512.0f * __half2float(__ushort_as_half(xs_raw[gl * p.Mp + m])) : 0.0f;
+          cfv[gl * TN + m] = static_cast<float>(sum) * (1.0f / 64.0f);
+        }
+      }
+    } else {
+      ok = false;
+    }
+    fence_proxy_async_smem();  // generic writes -> the tensor core's reads
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl.work_bar);
+    ok = mbar_wait(&ctl.work_bar, 0, abort_flag, tmo, p.err) && ok;
+    tc_fence_after();
+    if (threadIdx.x == 0) MQ_DTRACE(12);
+
+    const uint32_t tmem = ctl.tmem_base;
+    // Per warpgroup 128 columns: A buffers b = 0, 1 (32 columns each), then D
+    // buffers (kDCh accumulator chains of TN columns each: K-steps j and
+    // j + kDCh accumulate into chain j; independent chains let the tensor
+    // core overlap their MMAs, and their exact sums are added in the drain).
+    constexpr int kDCh = TN == 16 ? 2 : 1;
+    static_assert(64 + 2 * kDCh * TN <= 128, "tensor-memory columns per warpgroup");
+    const uint32_t colA = tmem + w * 128, colD = tmem + w * 128 + 64;  // buffer b: +32b, +kDCh*TN*b
+    const uint32_t bt = smem_u32(bfrag);
+    // kind::f8f6f4, E4M3 x E4M3 -> f32, K-major A and B, N = TN, M = 128
+    constexpr uint32_t kIdesc =
+        (1u << 4) | (static_cast<uint32_t>(TN >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
+    uint64_t acc[TN / 2];  // row r, tokens 2j, 2j+1
+#pragma unroll
+    for (int j = 0; j < TN / 2; ++j) acc[j] = 0ull;
+#ifdef MQ_DEC_TRACE
+    long long prof_[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0}, pt_ = 0;
+#endif
+    // Per A/D buffer: the item's group, visit, CSR entry (-1: dense; -2:
+    // residual, none in this warp's half) and this row's scale.
+    int fgl0 = 0, fv0 = 0, fe0 = -2, fgl1 = 0, fv1 = 0, fe1 = -2;
+    float fs0 = 0.0f, fs1 = 0.0f;
+    int kis = 0, kdr = 0;  // items issued, items drained by this warpgroup
+
+    // 64 bytes of this row's codes (K-steps jstride apart) -> E4M3 (q + 8) * 2^-9
+    // in A buffer columns a_col .. a_col + 31: word t -> columns 2t (even
+    // codes), 2t + 1 (odd codes).
+    auto convert_row = [&](const uint8_t* src, int jstride, uint32_t a_col) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint4 pk0 = *reinterpret_cast<const uint4*>(src + (2 * hh) * jstride);
+        const uint4 pk1 = *reinterpret_cast<const uint4*>(src + (2 * hh + 1) * jstride);
+        uint32_t ev[16];
+        unpack_u4(pk0.x, ev[0], ev[1]);
+        unpack_u4(pk0.y, ev[2], ev[3]);
+        unpack_u4(pk0.z, ev[4], ev[5]);
+        unpack_u4(pk0.w, ev[6], ev[7]);
+        unpack_u4(pk1.x, ev[8], ev[9]);
+        unpack_u4(pk1.y, ev[10], ev[11]);
+        unpack_u4(pk1.z, ev[12], ev[13]);
+        unpack_u4(pk1.w, ev[14], ev[15]);
+        tmem_st16(a_col + 16 * hh, ev);
+      }
+    };
+    // The converted A of item n is in tensor memory: lane 0 of the
+    // warpgroup's first warp issues its four K=32 MMAs once all four warps
+    // have stored theirs.
+    auto issue = [&](int n, int gl) -> bool {
+      const int b = n & 1;
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      int good = 1;
+      if (lane == 0) {
+        mbar_arrive(&ctl.a_ready[w][b]);
+        if (quarter == 0) {
+          good = mbar_wait(&ctl.a_ready[w][b], (n >> 1) & 1, abort_flag, tmo, p.err);
+          if (good) {
+            tc_fence_after();
+            const uint32_t b_addr = bt + gl * (TN * 128);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              tc_mma_ts(colD + kDCh * TN * b + TN * (j % kDCh), colA + 32 * b + 8 * j, sw128_desc(b_addr + 32 * j),
+                        kIdesc, j >= kDCh);
+            tc_commit(&ctl.d_ready[w][b]);
+          }
+        }
+      }
+      return __shfl_sync(0xFFFFFFFFu, good, 0) != 0;
+    };
+    // Item n's MMAs are complete: acc += 2^9 sx * (s * (D - c)) for this row
+    // (or, as a test hook, store the dots).
+    auto retire = [&](int n) -> bool {
+      const int b = n & 1;
+      MQ_PT();
+      if (!mbar_wait(&ctl.d_ready[w][b], (n >> 1) & 1, abort_flag, tmo, p.err)) return false;
+      MQ_PA(5);
+      MQ_PT();
+      tc_fence_after();
+      const int gl = b ? fgl1 : fgl0, e = b ? fe1 : fe0, vv = b ? fv1 : fv0;
+      const float s = b ? fs1 : fs0;
+      if (e != -2) {  // warp-uniform
+        const float4* sx4 = reinterpret_cast<const float4*>(sxf + gl * TN);
+        const float4* c4 = reinterpret_cast<const float4*>(cfv + gl * TN);
+        const uint64_t s2 = f2pack(s, s), m1 = f2pack(-1.0f, -1.0f);
+#pragma unroll
+        for (int cc = 0; cc < TN / 16; ++cc) {
+          uint32_t dv[16];
+          tmem_ld16(colD + kDCh * TN * b + 16 * cc + lane_base, dv);
+          if (kDCh == 2) {
+            uint32_t dw[16];
+            tmem_ld16(colD + kDCh * TN * b + TN + 16 * cc + lane_base, dw);
+            tc_wait_ld();
+#pragma unroll
+            for (int t = 0; t < 16; ++t) dv[t] = __float_as_uint(__uint_as_float(dv[t]) + __uint_as_float(dw[t]));
+          } else {
+            tc_wait_ld();
+          }
+#pragma unroll
+          for (int j4 = 0; j4 < 4; ++j4) {
+            const float4 sv = sx4[cc * 4 + j4], cv = c4[cc * 4 + j4];  // tokens 16cc + 4j4 .. +3
+            if (kDebug) {
+              const float cvv[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                const int m = 16 * cc + 4 * j4 + t;
+                if (m < p.M) {
+                  const int32_t dd = static_cast<int32_t>((__uint_as_float(dv[4 * j4 + t]) - cvv[t]) * 512.0f);
+                  if (e < 0)
+                    p.dots_w[(static_cast<int64_t>(m) * p.N + tile_of(vv) * kTileN + r) * G + gs + gl] = dd;
+                  else
+                    p.dots_r[(static_cast<int64_t>(m) * p.nnzb + e) * 64 + (r & 63)] = dd;
+                }
+              }
+            } else {
+              // 2^-9 times the dot of q with x: the measured dot minus the offset term, exact
+              const uint64_t d0 = f2fma(f2pack(cv.x, cv.y), m1,
+                                        f2pack(__uint_as_float(dv[4 * j4]), __uint_as_float(dv[4 * j4 + 1])));
+              const uint64_t d1 = f2fma(f2pack(cv.z, cv.w), m1,
+                                        f2pack(__uint_as_float(dv[4 * j4 + 2]), __uint_as_float(dv[4 * j4 + 3])));
+              acc[cc * 8 + 2 * j4] = f2fma(f2pack(sv.x, sv.y), f2mul(s2, d0), acc[cc * 8 + 2 * j4]);
+              acc[cc * 8 + 2 * j4 + 1] = f2fma(f2pack(sv.z, sv.w), f2mul(s2, d1), acc[cc * 8 + 2 * j4 + 1]);
+            }
+          }
+        }
+      }
+      tc_fence_before();  // the loads precede the buffer's reuse
+      MQ_PA(6);
+      return true;
+    };
+    // End of visit vv: add this warpgroup's partial into the CTA's row-major
+    // buffer, warpgroup 0 first, then 1, 2, 3.
+    auto finish_visit = [&](int vv) -> bool {
+      bool passed;
+      if (w == 0)  // every owner has consumed the previous tile's push out of this buffer
+        passed = vv == 0 || mbar_wait_cluster(&ctl.rx_free, (vv - 1) & 1, abort_flag, tmo, p.err);
+      else
+        passed = mbar_wait(&ctl.chain[w - 1], vv & 1, abort_flag, tmo, p.err);
+      if (!passed) return false;
+      const bool direct = CS == 1 && !kDebug && w + 1 == kSlots;  // the last warpgroup stores Y
+      const int64_t n = tile_of(vv) * kTileN + r;
+      float4* row = reinterpret_cast<float4*>(rb + r * TN);
+#pragma unroll
+      for (int k4 = 0; k4 < TN / 4; ++k4) {
+        float4 a;
+        f2unpack(acc[2 * k4], a.x, a.y);
+        f2unpack(acc[2 * k4 + 1], a.z, a.w);
+        if (w != 0) {
+          const float4 o = row[k4];
+          a = make_float4(o.x + a.x, o.y + a.y, o.z + a.z, o.w + a.w);
+        }
+        if (direct) {
+          const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            if (4 * k4 + t < p.M) store_y(p, 4 * k4 + t, n, av[t]);
+        } else {
+          row[k4] = a;
+        }
+        acc[2 * k4] = acc[2 * k4 + 1] = 0ull;
+      }
+      // the buffer is pushed by bulk copies (the async proxy): order these
+      // generic writes before them
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        if (w + 1 < kSlots)
+          mbar_arrive(&ctl.chain[w]);
+        else if (!direct)
+          mbar_arrive(&ctl.rb_done);
+        else if (vv + 1 < nvis)
+          mbar_arrive(&ctl.rx_free);  // this warp's rows of the buffer are read
+      }
+      if (lane == 0 && vv == 0) MQ_DTRACE(13 + warp);
+      return true;
+    };
+
+    bool map_seen = false;
+    int cur_v = 0;
+    // stage i = w, w + 4, ..: group gl of visit v, in slot st whose fill parity is ph
+    int v = w / ns, gl = w - (w / ns) * ns, st = w, ph = 0;
+    for (int i = w; ok && i < total; i += kSlots) {
+      if (v != cur_v) {  // a new tile: drain what is in flight, then close the finished visits
+        while (ok && kdr < kis) ok = retire(kdr++);
+        while (ok && cur_v < v) ok = finish_visit(cur_v++);
+        if (!ok) break;
+      }
+      // dense item
+      if (kis - kdr >= 2 && !(ok = retire(kdr++))) break;
+      MQ_PT();
+      if (!(ok = mbar_wait(&ctl.full[st], ph, abort_flag, tmo, p.err))) break;
+      MQ_PA(1);
+      MQ_PT();
+      {
+        const uint8_t* rec = stages + st * kStageBytes;
+        const float s = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(rec + kWRecScales + 2 * r)));
+        convert_row(rec + r * 16, 2048, colA + 32 * (kis & 1) + lane_base);
+        if (kis & 1) fgl1 = gl, fv1 = v, fe1 = -1, fs1 = s;
+        else fgl0 = gl, fv0 = v, fe0 = -1, fs0 = s;
+      }
+      ok = issue(kis++, gl);
+      if (lane == 0) mbar_arrive(&ctl.empty[st]);  // this warp's reads of the stage are done
+      MQ_PA(2);
+      if (!ok) break;
+      // residual item, if the block list has a block in either half here
+      if (!map_seen) {
+        if (!(ok = mbar_wait(&ctl.map_ready, 0, abort_flag, tmo, p.err))) break;
+        map_seen = true;
+      }
+      const int e0 = ctl.map[v][gl][0], e1 = ctl.map[v][gl][1];
+      if (e0 >= 0 || e1 >= 0) {
+        if (kis - kdr >= 2 && !(ok = retire(kdr++))) break;
+        const int e = half ? e1 : e0;
+        float sr = 0.0f;
+        if (e >= 0) {
+          const int c = ctl.rpos[v][gl][half], slot = c % kRSlots;
+          MQ_PT();
+          if (!(ok = mbar_wait(&ctl.r_full[slot], (c / kRSlots) & 1, abort_flag, tmo, p.err))) break;
+          MQ_PA(3);
+          MQ_PT();
+          const uint8_t* rrec = rring + slot * kRRecBytes;
+          sr = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(rrec + kRRecScales + 2 * (r & 63))));
+          convert_row(rrec + (r & 63) * 16, 1024, colA + 32 * (kis & 1) + lane_base);
+          MQ_PA(4);
+        }
+        if (kis & 1) fgl1 = gl, fv1 = v, fe1 = e >= 0 ? e : -2, fs1 = sr;
+        else fgl0 = gl, fv0 = v, fe0 = e >= 0 ? e : -2, fs0 = sr;
+        ok = issue(kis++, gl);
+        if (lane == 0) {  // each warp releases every ring slot of this group once
+          if (e0 >= 0) mbar_arrive(&ctl.r_empty[ctl.rpos[v][gl][0] % kRSlots]);
+          if (e1 >= 0) mbar_arrive(&ctl.r_empty[ctl.rpos[v][gl][1] % kRSlots]);
+        }
+        if (!ok) break;
+      }
+      for (gl += kSlots; gl >= ns; gl -= ns) ++v;
+      if ((st += kSlots) >= NS) st -= NS, ph ^= 1;
+    }
+    while (ok && kdr < kis) ok = retire(kdr++);
+    while (ok && cur_v < nvis) ok = finish_visit(cur_v++);
+#ifdef MQ_DEC_TRACE
+    prof_[8] = kis;
+    if (lane == 0 && warp < 4) mq_dec_trace_prof(warp, prof_, 9);
+#endif
+   }
+
   } else {
     // ---------------- epilogue: push partial rows to their owners, sum the owned rows, store Y ----------------
     const int et = threadIdx.x - 32 * kWarpEpi0;  // 0 .. kEpiThreads-1
@@ -730,10 +1106,11 @@ __global__ void __maxnreg__(128) w4a4_decode_kernel(const DecParams p) {
     pdl_wait();  // Y may still be in use by the preceding kernel
     int nsync = 0;
     bool ok = true;
-    for (int v = 0; ok && v < nvis; ++v) {
+    // (one CTA per cluster: the last compute set has stored Y)
+    for (int v = 0; ok && v < nvis && !(CS == 1 && !kDebug); ++v) {
       const int64_t tile = tile_of(v);
       if (et == 0 && CS > 1) mbar_arrive_expect_tx(&ctl.rx_full, CS * chunk);
-      if (!mbar_wait_long(&ctl.rb_done, v & 1, abort_flag, tmo, p.err)) { ok = false; break; }
+      if (!mbar_wait(&ctl.rb_done, v & 1, abort_flag, tmo, p.err)) { ok = false; break; }
       if (et == 0 && v < 2) MQ_DTRACE(45 + v);
       const float* src;
       int nsrc;
@@ -742,7 +1119,7 @@ __global__ void __maxnreg__(128) w4a4_decode_kernel(const DecParams p) {
           const uint32_t rx_dst = smem_u32(rx) + rank * chunk, bar = smem_u32(&ctl.rx_full);
           for (int k = 0; k < CS; ++k) bulk_s2peer(mapa(rx_dst, k), rb + k * (R * TN), chunk, mapa(bar, k));
         }
-        if (!mbar_wait_long(&ctl.rx_full, v & 1, abort_flag, tmo, p.err)) { ok = false; break; }
+        if (!mbar_wait(&ctl.rx_full, v & 1, abort_flag, tmo, p.err)) { ok = false; break; }
         src = rx;
         nsrc = CS;
       } else {
@@ -803,7 +1180,7 @@ __global__ void __maxnreg__(128) w4a4_decode_kernel(const DecParams p) {
       if (et == 0 && v < 2) MQ_DTRACE(53 + v);
       __syncwarp();
       if ((et & 31) == 0) mbar_arrive(&ctl.epi_bar);  // every epilogue warp has read the received rows
-      if (!mbar_wait_long(&ctl.epi_bar, nsync & 1, abort_flag, tmo, p.err)) { ok = false; break; }
+      if (!mbar_wait(&ctl.epi_bar, nsync & 1, abort_flag, tmo, p.err)) { ok = false; break; }
       ++nsync;
       if (et == 0 && v < 2) MQ_DTRACE(49 + v);
 #ifdef MQ_DEC_TRACE
@@ -824,7 +1201,7 @@ __global__ void __maxnreg__(128) w4a4_decode_kernel(const DecParams p) {
   // rather than in a hardware barrier, then all threads meet.
   __syncwarp();
   if (lane == 0) mbar_arrive(&ctl.exit_bar);
-  mbar_wait_long(&ctl.exit_bar, 0, abort_flag, tmo, p.err);
+  mbar_wait(&ctl.exit_bar, 0, abort_flag, tmo, p.err);
   __syncthreads();
   if (threadIdx.x == 0) MQ_DTRACE(51);
   if (*abort_flag) {
@@ -837,9 +1214,13 @@ __global__ void __maxnreg__(128) w4a4_decode_kernel(const DecParams p) {
     }
     __syncthreads();
   }
+  if (kTC && warp == 0) {  // every tensor-memory access of the CTA is complete
+    tc_fence_after();
+    tmem_dealloc(ctl.tmem_base, kTmemCols);
+  }
   // Every CTA has received all its rows, so every push out of this CTA's
-  // shared memory has been read.
-  cluster_sync_all();
+  // shared memory has been read (no data passes through this barrier).
+  if (CS > 1) cluster_sync_relaxed();
   if (threadIdx.x == 0) MQ_DTRACE(52);
 }
 
@@ -848,24 +1229,27 @@ __global__ void __maxnreg__(128) w4a4_decode_kernel(const DecParams p) {
 // ---------------------------------------------------------------------------
 
 struct DecPlan {
+  bool tc;  // tensor-memory variant
   int tn, cs, nstages, nclusters;
   uint32_t oSX, oRB, oRX, oR, oStage, smem;
 };
 
-template <int TN, bool kDebug>
+template <int TN, bool kDebug, bool kTC>
 static const void* kernel_ptr() {
-  return reinterpret_cast<const void*>(&w4a4_decode_kernel<TN, kDebug>);
+  return reinterpret_cast<const void*>(&w4a4_decode_kernel<TN, kDebug, kTC>);
 }
 
 // Co-resident clusters of `cs` CTAs of this kernel (one CTA per SM), per device.
-static int max_clusters(int cs) {
+static int max_clusters(int cs, bool tc) {
   static std::mutex mu;
-  static int cache[64][kMaxCS + 1];
+  static int cache[64][2][kMaxCS + 1];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lk(mu);
-  if (cache[dev][cs] != 0) return cache[dev][cs];
-  const void* kern = kernel_ptr<32, false>();
+  int& slot = cache[dev][tc ? 1 : 0][cs];
+  if (slot != 0) return slot;
+  const void* kern = tc ? kernel_ptr<32, false, true>() : kernel_ptr<32, false, false>();
+  const int threads = tc ? Roles<true>::kThreads : Roles<false>::kThreads;
   const int smem = kSmemLimit - kCtlBytes;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
     cudaGetLastError();
@@ -873,7 +1257,7 @@ static int max_clusters(int cs) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(cs * 256), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -887,17 +1271,31 @@ static int max_clusters(int cs) {
     cudaGetLastError();
     n = 0;
   }
-  cache[dev][cs] = n > 0 ? n : -1;
-  return cache[dev][cs];
+  slot = n > 0 ? n : -1;
+  return slot;
 }
 
 static uint32_t up1024(uint32_t b) { return (b + 1023u) / 1024u * 1024u; }
 
+// Which variant runs: the tensor-memory one above 16 tokens (where the
+// warp-level MMAs of a 32-token tile cost more than the tensor-memory round
+// trips), the warp-MMA one up to 16 (measured on GB300: faster on every
+// Llama-3-8B layer shape at 4 and 16 tokens, slower at 32).
+// MQ_DECODE_VARIANT = "warp" or "tc" forces one (benchmarking and tests).
+static bool decode_use_tc(int64_t M) {
+  const char* v = getenv("MQ_DECODE_VARIANT");
+  if (v && strcmp(v, "warp") == 0) return false;
+  if (v && strcmp(v, "tc") == 0) return true;
+  return M > 16;
+}
+
 // Pick the cluster size: the makespan of a CTA is (visits x slice) groups
-// plus a per-visit reduction; the slice's activation fragments must fit.
+// plus a per-visit reduction; the slice's activation tiles must fit.
 static bool decode_plan(int64_t M, int64_t N, int64_t K, DecPlan* out) {
   if (M > 32) return false;
-  const int tn = M <= 8 ? 8 : M <= 16 ? 16 : 32;
+  const bool tc = decode_use_tc(M);
+  const int tn = M <= 8 && !tc ? 8 : M <= 16 ? 16 : 32;
+  const int sets = tc ? Roles<true>::kSets : Roles<false>::kSets;
   const int G = static_cast<int>(K / kGroup), tiles = static_cast<int>(N / kTileN);
   double best = 1e30;
   bool found = false;
@@ -907,6 +1305,7 @@ static bool decode_plan(int64_t M, int64_t N, int64_t K, DecPlan* out) {
     const uint32_t bbytes = static_cast<uint32_t>(ns) * tn * 128;
     if (ns > kMaxSlice || bbytes > static_cast<uint32_t>(kMaxBBytes)) continue;
     DecPlan pl;
+    pl.tc = tc;
     pl.tn = tn;
     pl.cs = cs;
     pl.oSX = bbytes;
@@ -916,9 +1315,9 @@ static bool decode_plan(int64_t M, int64_t N, int64_t K, DecPlan* out) {
     pl.oStage = up1024(pl.oR + kRSlots * kRRecBytes);
     const int avail = kSmemLimit - kCtlBytes - 1024 - static_cast<int>(pl.oStage);
     pl.nstages = std::min(kMaxStages, avail / kStageBytes);
-    if (pl.nstages < 2 * kSlots) continue;
+    if (pl.nstages < sets + 2) continue;  // every set busy, two more in flight
     pl.smem = pl.oStage + pl.nstages * kStageBytes + 1024;
-    const int ncl = max_clusters(cs);
+    const int ncl = max_clusters(cs, tc);
     if (ncl <= 0) continue;
     pl.nclusters = std::min(tiles, ncl);
     const int rounds = (tiles + pl.nclusters - 1) / pl.nclusters;
@@ -933,10 +1332,10 @@ static bool decode_plan(int64_t M, int64_t N, int64_t K, DecPlan* out) {
   return found;
 }
 
-template <int TN, bool kDebug>
+template <int TN, bool kDebug, bool kTC>
 static mq_status launch_decode(const DecParams& dp, const DecPlan& pl, cudaStream_t stream) {
-  const void* kern = kernel_ptr<TN, kDebug>();
-  static bool smem_set[64];  // per device
+  const void* kern = kernel_ptr<TN, kDebug, kTC>();
+  static bool smem_set[64];  // per device, per instantiation
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return launch_status("decode gemm: device");
   if (!smem_set[dev]) {
@@ -947,7 +1346,7 @@ static mq_status launch_decode(const DecParams& dp, const DecPlan& pl, cudaStrea
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(pl.nclusters * pl.cs), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(Roles<kTC>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
@@ -959,20 +1358,21 @@ static mq_status launch_decode(const DecParams& dp, const DecPlan& pl, cudaStrea
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  if (cudaLaunchKernelEx(&cfg, w4a4_decode_kernel<TN, kDebug>, dp) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, w4a4_decode_kernel<TN, kDebug, kTC>, dp) != cudaSuccess)
     return launch_status("decode gemm launch");
   return launch_status("decode gemm");
 }
 
 }  // namespace
 
-// The kernel choice for (M, N, K) on the current device: {1, tokens per
-// tile, cluster size, clusters, stages} for the decode kernel, else zeros.
+// The kernel choice for (M, N, K) on the current device: {1 (warp-MMA
+// variant) or 2 (tensor-memory variant), tokens per tile, cluster size,
+// clusters, stages} for the decode kernel, else zeros.
 mq_status gemm_plan_info(int64_t M, int64_t N, int64_t K, int32_t* info) {
   DecPlan pl;
   for (int i = 0; i < 5; ++i) info[i] = 0;
   if (decode_plan(M, N, K, &pl)) {
-    info[0] = 1;
+    info[0] = pl.tc ? 2 : 1;
     info[1] = pl.tn;
     info[2] = pl.cs;
     info[3] = pl.nclusters;
@@ -1020,9 +1420,16 @@ mq_status gemm_decode_launch(bool* handled, const uint8_t* xq, const uint16_t* x
   dp.err = device_error_word();
   if (!dp.err) return set_error(MQ_ERR_CUDA, "decode gemm: device error word unavailable");
   const bool dbg = dots_w != nullptr;
-  if (pl.tn == 8) return dbg ? launch_decode<8, true>(dp, pl, stream) : launch_decode<8, false>(dp, pl, stream);
-  if (pl.tn == 16) return dbg ? launch_decode<16, true>(dp, pl, stream) : launch_decode<16, false>(dp, pl, stream);
-  return dbg ? launch_decode<32, true>(dp, pl, stream) : launch_decode<32, false>(dp, pl, stream);
+  if (pl.tc) {
+    if (pl.tn == 16)
+      return dbg ? launch_decode<16, true, true>(dp, pl, stream) : launch_decode<16, false, true>(dp, pl, stream);
+    return dbg ? launch_decode<32, true, true>(dp, pl, stream) : launch_decode<32, false, true>(dp, pl, stream);
+  }
+  if (pl.tn == 8)
+    return dbg ? launch_decode<8, true, false>(dp, pl, stream) : launch_decode<8, false, false>(dp, pl, stream);
+  if (pl.tn == 16)
+    return dbg ? launch_decode<16, true, false>(dp, pl, stream) : launch_decode<16, false, false>(dp, pl, stream);
+  return dbg ? launch_decode<32, true, false>(dp, pl, stream) : launch_decode<32, false, false>(dp, pl, stream);
 }
 
 }  // namespace mq

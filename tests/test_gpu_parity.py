@@ -146,6 +146,31 @@ def test_decode_kernel_covers_decode_shapes(lin):
     assert not mq.gemm_plan(33, lin.N, lin.K)["decode"]
 
 
+@pytest.mark.parametrize("variant", ["warp", "tc"])
+@pytest.mark.parametrize("M,N,K,budget", [(9, 384, 1024, 0.3), (16, 512, 2048, 0.2), (24, 256, 768, 1.0)])
+def test_decode_variants_match_oracle(variant, M, N, K, budget, monkeypatch):
+    """Both variants of the decode kernel (forced through MQ_DECODE_VARIANT):
+    dots bit for bit, Y within the fp32 bound, on sizes either may serve."""
+    monkeypatch.setenv("MQ_DECODE_VARIANT", variant)
+    plan = mq.gemm_plan(M, N, K)
+    assert plan["variant"] == {"warp": "warp-mma", "tc": "tensor-memory"}[variant]
+    x, w, xcal = _case(M, N, K, budget, seed=M + N)
+    pl = mq.prepare_linear(dev_half(w), dev_half(xcal), budget)
+    xq, xs = mq.quantize_act(dev_half(x))
+    dw, dr = mq.debug_group_dots(xq, xs, M, pl)
+    y32 = mq.gemm(xq, xs, M, pl, out_dtype=torch.float32)
+    y16 = mq.gemm(xq, xs, M, pl, out_dtype=torch.bfloat16)
+    mq.check_device_error()
+    qx, sx = O.quantize_act(x, False)
+    p = O.prepare(w, xcal, False, budget)
+    assert np.array_equal(dw.cpu().numpy(), O.group_dots(qx, p.qw))
+    if p.ksel:
+        assert np.array_equal(dr.cpu().numpy(), O.residual_dots(qx, p.qr, p.col_idx))
+    y, a = O.linear(qx, sx, p)
+    check_close(y32.cpu().numpy(), y, a)
+    check_bf16(host_u16(y16), y, a)
+
+
 def test_group_dots_extremes():
     """Adversarial codes: every product +49, every product -49, alternating
     cancellation; sums reach +-6272 per group, exactly."""
