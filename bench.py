@@ -530,7 +530,7 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(tmax / args.steps * 1e3, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "int4 (E4M3-exact on tcgen05), fp32 epilogue, bf16 out",
+            "scaling": "weak", "vs_baseline": None, "dtype": "int4 codes (exact E4M3 on mma.sync / tcgen05), fp32 epilogue, bf16 out",
             "data": "synthetic (random-init weights N(0,0.02), activations N(0,1) with 0.1% outlier channels x50)",
             "config": {"workload": WORKLOAD, "linears": {n: [l.K, l.N] for n, l in lins.items()}, "M": list(MS),
                        "budget": BUDGET, "weight_copies": COPIES,
