@@ -5,50 +5,53 @@
 //   Y[m,n] = sum_g sx[m,g] * ( sw[n,g] * Dw[m,n,g] + sr[n,g] * Dr[m,n,g] )
 //
 // in one kernel: the residual product of a selected 64x128 block runs on the
-// same activation fragments as the dense product of its group, and both are
+// same activation operand as the dense product of its group, and both are
 // reduce-added into the same fp32 accumulators.
 //
 // At decode sizes the work is streaming the 4-bit weights.  Every 128-input
 // group has its own scales, so its integer dot must be finished, scaled and
-// added before the next group's; the warp-level FP8 MMA (mma.sync m16n8k32
-// e4m3, fp32 accumulators in registers) runs on sm_103a far faster than
-// decode needs and keeps that per-group step inside one warp, with no
-// hand-offs between roles.  So each MMA warp works alone:
-//   * it owns 32 rows of the tile and every third group of the CTA's list;
-//     per group it loads its rows' packed codes (one 32-bit word per row,
-//     K-step and thread), unpacks them in registers, runs the MMAs against
-//     the resident activation fragments, and scales the exact dots into its
-//     fp32 accumulators;
+// added before the next group's.  One kernel template, two ways to run the
+// per-group products (the compute role), one frame around them:
 //   * unpacking is a mask: a byte 0x00..0x0F read as E4M3 is exactly
 //     b * 2^-9 (subnormals below 8, the lowest normal binade from 8), so the
 //     nibble u = q + 8 (q XOR 8) moved into a byte is u * 2^-9 with no table
 //     (4 operations per 8 codes).  The dot is then 2^-9 * (D + 8 * sum_k
 //     qx[m,k]); the scaling step subtracts the activation term (the group
 //     sums of the resident activations are computed once) and folds 2^9 into
-//     the activation scale.  Every partial sum is a multiple of 2^-9 below 2^14
-//     in magnitude, so the fp32 accumulation is exact;
-//   * K is permuted inside each 32-wide MMA step: the thread that holds MMA
-//     columns 4t..4t+3 gets the even codes 8t, 8t+2, .., 8t+6 of the step and
-//     the one holding 16+4t..16+4t+3 the odd ones, which is the order the
-//     mask leaves them in.  A and B use the same permutation, so the dot is
-//     unchanged.
-// Around the warps:
+//     the activation scale.  Every partial sum is a multiple of 2^-9 below
+//     2^14 in magnitude, so the fp32 accumulation is exact;
+//   * K is permuted inside each 8-code word: the even codes, then the odd
+//     ones, which is the order the mask leaves them in.  The activations use
+//     the same permutation, so the dot is unchanged;
+//   * warp-MMA variant (the default up to 16 tokens): each of 12 warps owns
+//     32 rows and every third group of the CTA's list; per group it unpacks
+//     its rows' codes in registers, runs mma.sync m16n8k32 e4m3 against
+//     resident activation fragments and scales the exact dots into register
+//     accumulators.  No hand-offs between roles;
+//   * tensor-memory variant (above 16 tokens): each of 4 warpgroups owns all
+//     128 rows (thread = row = tensor-memory lane) and every fourth group; it
+//     unpacks into double-buffered tensor-memory A operands, its first warp
+//     issues the group's four tcgen05 MMAs (B = the 128-byte-swizzled
+//     activation tile) once the warpgroup's four warps have stored theirs,
+//     and the warpgroup drains the accumulators two items later.
+// The frame:
 //   * Split-K over a thread-block cluster of CS CTAs.  A cluster owns whole
 //     128-row weight tiles (one after another, persistently); CTA rank j
 //     handles the same K slice [j*G/CS, (j+1)*G/CS) of every tile it visits,
-//     so its activations are converted to E4M3 fragments once, at the start,
-//     and stay in shared memory.
+//     so its activations arrive by bulk copy, are converted once, and stay in
+//     shared memory.
 //   * A producer warp streams the base-weight records (codes and scales side
-//     by side, 8.25 KiB, one bulk copy each) into a ring of stages, and the
-//     residual block records the CSR block list has in this slice into a
-//     small ring.  The block lists of every tile the CTA visits are read once,
-//     up front, into a static map.
-//   * At the end of a tile the three warp sets' partials are added in a fixed
-//     order into a row-major shared-memory buffer; each CTA then pushes the
-//     rows owned by rank k into rank k's shared memory with one bulk copy
-//     (distributed shared memory, counted on the owner's barrier), and each
-//     rank sums its 128/CS rows over the CS partials in rank order and stores
-//     Y.  No global workspace, no atomics: the result is deterministic.
+//     by side, 8.25 KiB, one bulk copy each) into a ring of stages; a second
+//     one reads the block lists of every tile the CTA visits once, up front,
+//     into a static map, and streams the residual block records of this slice
+//     into a small ring.
+//   * At the end of a tile the compute sets' partials are added in a fixed
+//     order.  With one CTA per cluster the last set stores Y from registers;
+//     otherwise each CTA pushes the rows owned by rank k into rank k's shared
+//     memory with one bulk copy (distributed shared memory, counted on the
+//     owner's barrier), and each rank sums its 128/CS rows over the CS
+//     partials in rank order and stores Y.  No global workspace, no atomics:
+//     the result is deterministic.
 // Every wait is bounded (mbar_wait): a wait that runs out records the error,
 // raises the CTA's abort flag, and every role winds down.
 #include "mq_internal.cuh"
@@ -138,8 +141,8 @@ struct __align__(8) DecCtl {
   uint64_t rx_full;              // every rank's rows for this CTA have landed (bytes)
   uint64_t rx_free;              // every owner has consumed this CTA's last push
   uint64_t exit_bar;             // every warp of the CTA is done with its role
-  uint64_t a_ready[4][2];        // tensor-memory variant: A buffer b of warpgroup w is stored (4 warp arrivals)
-  uint64_t d_ready[4][2];        // its MMAs are complete (tcgen05.commit)
+  uint64_t d_ready[4][2];        // tensor-memory variant: the MMAs of A/D buffer b of warpgroup w are complete
+  uint32_t a_cnt[4][2];          // warps of warpgroup w that have stored A buffer b, over all its uses
   uint32_t tmem_base;
   int32_t map[kMaxVisits][kMaxSlice][2];   // CSR entry of the slice's residual blocks per tile, or -1
   int32_t rpos[kMaxVisits][kMaxSlice][2];  // position of that block in the residual-ring order
@@ -164,6 +167,13 @@ __device__ __forceinline__ uint32_t cluster_index() {
 // Every thread of every CTA of the cluster, together.
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// Shared-memory counter increment with acquire-release ordering; returns the old value.
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* ctr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_u32(ctr)), "r"(v)
+               : "memory");
+  return old;
 }
 // The same without ordering memory: only that every thread of the cluster got here.
 __device__ __forceinline__ void cluster_sync_relaxed() {
@@ -381,7 +391,7 @@ __global__ void __maxnreg__(Roles<kTC>::kMaxReg) w4a4_decode_kernel(const DecPar
       mbar_init(&ctl.r_empty[lane], kTC ? 4 : 2);
     }
     if (kTC && lane >= 8 && lane < 16) {
-      mbar_init(&ctl.a_ready[(lane - 8) >> 1][lane & 1], 4);
+      ctl.a_cnt[(lane - 8) >> 1][lane & 1] = 0;
       mbar_init(&ctl.d_ready[(lane - 8) >> 1][lane & 1], 1);
     }
     if (lane + 1 < kSlots) mbar_init(&ctl.chain[lane], 4);
@@ -405,6 +415,50 @@ __global__ void __maxnreg__(Roles<kTC>::kMaxReg) w4a4_decode_kernel(const DecPar
   // pushes into them (also a barrier of this CTA's threads).
   cluster_sync_all();
   if (threadIdx.x == 0) MQ_DTRACE(1);
+
+  // Sum the CS partials of this rank's R rows of tile `tile` (sources in rank
+  // order) and store them to Y: item idx = (4-token block, row), items t0,
+  // t0 + nthr, ..; four items' loads go ahead of their stores.
+  auto store_owned = [&](const float* src, int nsrc, int64_t tile, int t0, int nthr) {
+    const uint32_t src_s = smem_u32(src);
+    const int rsh = __ffs(R) - 1;  // R = 128 / CS is a power of two
+    constexpr int kU = 4;
+    for (int base = t0; base < R * (TN / 4); base += kU * nthr) {
+      float4 acc4[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int idx = base + u * nthr;
+        const int row = idx & (R - 1), m4 = (idx >> rsh) * 4;
+        if (idx < R * (TN / 4) && m4 < p.M) {
+          const uint32_t a = src_s + static_cast<uint32_t>(row * TN + m4) * 4;
+          float4 sv = lds_f4(a);
+          for (int j = 1; j < nsrc; ++j) {  // ascending rank = ascending K slice
+            const float4 t = lds_f4(a + static_cast<uint32_t>(j * R * TN) * 4);
+            sv.x += t.x;
+            sv.y += t.y;
+            sv.z += t.z;
+            sv.w += t.w;
+          }
+          acc4[u] = sv;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int idx = base + u * nthr;
+        const int row = idx & (R - 1), m4 = (idx >> rsh) * 4;
+        if (idx < R * (TN / 4) && m4 < p.M) {
+          const int64_t n = tile * kTileN + rank * R + row;
+          const float vals[4] = {acc4[u].x, acc4[u].y, acc4[u].z, acc4[u].w};
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            if (m4 + t < p.M) store_y(p, m4 + t, n, vals[t]);
+        }
+      }
+    }
+  };
+  // Threads that store the last tile's owned rows (several CTAs per cluster):
+  // the epilogue warps and, having finished their last tile, the compute warps.
+  constexpr int kLastStorers = kEpiThreads + 32 * kMmaWarps;
 
   if (warp == kWarpProducer) {
     // ---------------- producer: activations, then the base-weight stages in order ----------------
@@ -790,6 +844,9 @@ __global__ void __maxnreg__(Roles<kTC>::kMaxReg) w4a4_decode_kernel(const DecPar
       if ((st += kSlots) >= NS) st -= NS, ph ^= 1;
     }
     while (ok && cur_v < nvis) ok = finish_visit(cur_v++);
+    // the last tile's owned rows, with the epilogue warps (several CTAs per cluster)
+    if (ok && CS > 1 && !kDebug && mbar_wait(&ctl.rx_full, (nvis - 1) & 1, abort_flag, tmo, p.err))
+      store_owned(rx, CS, tile_of(nvis - 1), kEpiThreads + threadIdx.x, kLastStorers);
 #ifdef MQ_DEC_TRACE
     prof_[8] = (total - q + kSlots - 1) / kSlots;
     if (lane == 0 && warp < 4) mq_dec_trace_prof(warp, prof_, 9);
@@ -895,31 +952,25 @@ __global__ void __maxnreg__(Roles<kTC>::kMaxReg) w4a4_decode_kernel(const DecPar
         tmem_st16(a_col + 16 * hh, ev);
       }
     };
-    // The converted A of item n is in tensor memory: lane 0 of the
-    // warpgroup's first warp issues its four K=32 MMAs once all four warps
-    // have stored theirs.
+    // The converted A of item n is in tensor memory: the last of the
+    // warpgroup's four warps to store its part issues the item's four K=32
+    // MMAs (the counter of buffer b counts every use: the (n/2)-th use is
+    // complete at 4 (n/2 + 1)), so no warp waits for another here.
     auto issue = [&](int n, int gl) -> bool {
       const int b = n & 1;
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
-      int good = 1;
-      if (lane == 0) {
-        mbar_arrive(&ctl.a_ready[w][b]);
-        if (quarter == 0) {
-          good = mbar_wait(&ctl.a_ready[w][b], (n >> 1) & 1, abort_flag, tmo, p.err);
-          if (good) {
-            tc_fence_after();
-            const uint32_t b_addr = bt + gl * (TN * 128);
+      if (lane == 0 && atom_add_acq_rel(&ctl.a_cnt[w][b], 1u) + 1u == 4u * static_cast<uint32_t>((n >> 1) + 1)) {
+        tc_fence_after();
+        const uint32_t b_addr = bt + gl * (TN * 128);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              tc_mma_ts(colD + kDCh * TN * b + TN * (j % kDCh), colA + 32 * b + 8 * j, sw128_desc(b_addr + 32 * j),
-                        kIdesc, j >= kDCh);
-            tc_commit(&ctl.d_ready[w][b]);
-          }
-        }
+        for (int j = 0; j < 4; ++j)
+          tc_mma_ts(colD + kDCh * TN * b + TN * (j % kDCh), colA + 32 * b + 8 * j, sw128_desc(b_addr + 32 * j), kIdesc,
+                    j >= kDCh);
+        tc_commit(&ctl.d_ready[w][b]);
       }
-      return __shfl_sync(0xFFFFFFFFu, good, 0) != 0;
+      return true;
     };
     // Item n's MMAs are complete: acc += 2^9 sx * (s * (D - c)) for this row
     // (or, as a test hook, store the dots).
@@ -1090,6 +1141,9 @@ __global__ void __maxnreg__(Roles<kTC>::kMaxReg) w4a4_decode_kernel(const DecPar
     }
     while (ok && kdr < kis) ok = retire(kdr++);
     while (ok && cur_v < nvis) ok = finish_visit(cur_v++);
+    // the last tile's owned rows, with the epilogue warps (several CTAs per cluster)
+    if (ok && CS > 1 && !kDebug && mbar_wait(&ctl.rx_full, (nvis - 1) & 1, abort_flag, tmo, p.err))
+      store_owned(rx, CS, tile_of(nvis - 1), kEpiThreads + threadIdx.x, kLastStorers);
 #ifdef MQ_DEC_TRACE
     prof_[8] = kis;
     if (lane == 0 && warp < 4) mq_dec_trace_prof(warp, prof_, 9);
@@ -1128,54 +1182,12 @@ __global__ void __maxnreg__(Roles<kTC>::kMaxReg) w4a4_decode_kernel(const DecPar
       }
       if (et == 0 && v < 2) MQ_DTRACE(47 + v);
       if (!kDebug) {
-        // thread: one owned row, four tokens; sources summed in rank order.
-        // Four items' loads go ahead of their stores.
-        const uint32_t src_s = smem_u32(src);
-        const int rsh = __ffs(R) - 1;  // R = 128 / CS is a power of two
-        constexpr int kU = 4;
-        for (int base = et; base < R * (TN / 4); base += kU * kEpiThreads) {
-          MQ_PT();
-          float4 acc4[kU];
-#pragma unroll
-          for (int u = 0; u < kU; ++u) {
-            const int idx = base + u * kEpiThreads;
-            const int row = idx & (R - 1), m4 = (idx >> rsh) * 4;
-            if (idx < R * (TN / 4) && m4 < p.M) {
-              const uint32_t a = src_s + static_cast<uint32_t>(row * TN + m4) * 4;
-              float4 sv = lds_f4(a);
-              for (int j = 1; j < nsrc; ++j) {  // ascending rank = ascending K slice
-                const float4 t = lds_f4(a + static_cast<uint32_t>(j * R * TN) * 4);
-                sv.x += t.x;
-                sv.y += t.y;
-                sv.z += t.z;
-                sv.w += t.w;
-              }
-              acc4[u] = sv;
-            }
-          }
-          MQ_PA(base == et ? 0 : 2);
-          MQ_PT();
-#pragma unroll
-          for (int u = 0; u < kU; ++u) {
-            const int idx = base + u * kEpiThreads;
-            const int row = idx & (R - 1), m4 = (idx >> rsh) * 4;
-            if (idx < R * (TN / 4) && m4 < p.M) {
-              const int64_t n = tile * kTileN + rank * R + row;
-              const float vals[4] = {acc4[u].x, acc4[u].y, acc4[u].z, acc4[u].w};
-#pragma unroll
-              for (int t = 0; t < 4; ++t) {
-                if (m4 + t < p.M) {
-                  const int64_t o = static_cast<int64_t>(m4 + t) * p.N + n;
-                  if (p.y_f32)
-                    static_cast<float*>(p.y)[o] = vals[t];
-                  else
-                    static_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(vals[t]);
-                }
-              }
-            }
-          }
-          MQ_PA(base == et ? 1 : 3);
-        }
+        MQ_PT();
+        if (v + 1 == nvis && CS > 1)  // the compute warps are done and help
+          store_owned(src, nsrc, tile, et, kLastStorers);
+        else
+          store_owned(src, nsrc, tile, et, kEpiThreads);
+        MQ_PA(0);
       }
       if (et == 0 && v < 2) MQ_DTRACE(53 + v);
       __syncwarp();
