@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmq.so")
-SOURCES = ["abi.cu", "status.cu", "quantize.cu", "select.cu", "pack.cu", "gemm.cu", "gemm_decode.cu", "noalloc.cu"]
+SOURCES = ["abi.cu", "status.cu", "quantize.cu", "select.cu", "pack.cu", "gemm.cu", "gemm_decode.cu", "zipper.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

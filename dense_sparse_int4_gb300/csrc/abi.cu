@@ -3,6 +3,7 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -21,7 +22,16 @@ mq_status pack_weights_launch(const uint16_t* w, int64_t N, int64_t K, const int
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 mq_status gemm_launch(const uint8_t* xq, const uint16_t* xs, int64_t M, const uint8_t* wpk, int64_t N, int64_t K,
                       const int32_t* row_ptr, const int32_t* col_idx, int64_t nnzb, const uint8_t* rpk, void* y,
-                      mq_dtype yt, int32_t* dots_w, int32_t* dots_r, void* ws, size_t ws_bytes, cudaStream_t stream);
+                      int64_t ldy, mq_dtype yt, int32_t* dots_w, int32_t* dots_r, void* ws, size_t ws_bytes,
+                      cudaStream_t stream);
+size_t general_workspace_bytes(int64_t M, int64_t N, int64_t K);
+size_t zipper_workspace_bytes(int64_t M, int64_t tiles, int64_t K);
+mq_status zipper_launch(bool* handled, int nmat, const uint8_t* const* wpk, const int64_t* N,
+                        const int32_t* const* row_ptr, const int32_t* const* col_idx, const int64_t* nnzb,
+                        const uint8_t* const* rpk, void* const* y, const int64_t* ldy, mq_dtype yt, const uint8_t* xq,
+                        const uint16_t* xs, const void* x, mq_dtype xt, int64_t ldx, uint8_t* xq_out,
+                        uint16_t* xs_out, int64_t M, int64_t K, int32_t* dots_w, int32_t* dots_r, void* ws,
+                        size_t ws_bytes, cudaStream_t stream);
 mq_status gemm_plan_info(int64_t M, int64_t N, int64_t K, int32_t* info);
 mq_status wait_timeout_probe_launch(cudaStream_t stream);
 mq_status error_word_address(uint32_t** out);
@@ -44,6 +54,11 @@ mq_status launch_status(const char* what) {
 }
 
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(); }
+
+// Incremented each time mq_check_device_error reports a device-side timeout:
+// after one, workspace counters may have been left nonzero.
+static std::atomic<uint64_t> g_timeout_epoch{0};
+uint64_t timeout_epoch() { return g_timeout_epoch.load(); }
 
 constexpr int kMaxDevices = 64;
 static int g_dev_ok[kMaxDevices];  // 0 unknown, 1 ok, -1 unsupported
@@ -233,7 +248,7 @@ mq_status mq_w4a4_residual_gemm(const uint8_t* xq, const uint16_t* xs, int64_t M
   MQ_CHECK(aligned(y, yt == MQ_F32 ? 4 : 2), MQ_ERR_ALIGNMENT, "gemm: y misaligned");
   if (mq_status s = gemm_common(xq, xs, M, wpk, N, K, row_ptr, col_idx, nnzb, rpk, ws, ws_bytes); s != MQ_OK)
     return s;
-  return gemm_launch(xq, xs, M, wpk, N, K, row_ptr, col_idx, nnzb, rpk, y, yt, nullptr, nullptr, ws, ws_bytes,
+  return gemm_launch(xq, xs, M, wpk, N, K, row_ptr, col_idx, nnzb, rpk, y, N, yt, nullptr, nullptr, ws, ws_bytes,
                      reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -244,8 +259,98 @@ mq_status mq_debug_group_dots(const uint8_t* xq, const uint16_t* xs, int64_t M, 
   MQ_CHECK(dw && (nnzb == 0 || dr), MQ_ERR_INVALID_ARG, "debug_group_dots: NULL output");
   if (mq_status s = gemm_common(xq, xs, M, wpk, N, K, row_ptr, col_idx, nnzb, rpk, ws, ws_bytes); s != MQ_OK)
     return s;
-  return gemm_launch(xq, xs, M, wpk, N, K, row_ptr, col_idx, nnzb, rpk, nullptr, MQ_F32, dw, dr, ws, ws_bytes,
+  return gemm_launch(xq, xs, M, wpk, N, K, row_ptr, col_idx, nnzb, rpk, nullptr, N, MQ_F32, dw, dr, ws, ws_bytes,
                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Workspace of the fused linear: the decode kernel's over all matrices' tiles
+// when it covers the shape, else the quantized activations after the largest
+// general-kernel workspace (whose zeroed prefix stays at the start).
+static size_t linear_ws(int64_t M, int64_t K, int nmat, const int64_t* N, size_t* gen_bytes) {
+  int64_t tiles = 0;
+  size_t gen = 0;
+  for (int i = 0; i < nmat; ++i) {
+    tiles += N[i] / kTileN;
+    gen = std::max(gen, general_workspace_bytes(M, N[i], K));
+  }
+  *gen_bytes = 0;
+  if (const size_t z = zipper_workspace_bytes(M, tiles, K)) return z;
+  const size_t Mp = static_cast<size_t>((M + 7) / 8 * 8), G = static_cast<size_t>(K / kGroup);
+  gen = (gen + 255) / 256 * 256;
+  *gen_bytes = gen;
+  return gen + (G * Mp * 64 + 255) / 256 * 256 + (G * Mp * 2 + 255) / 256 * 256;
+}
+
+size_t mq_linear_workspace_bytes(int64_t M, int64_t K, int nmat, const int64_t* N) {
+  if (nmat < 1 || nmat > 4 || !N) return 0;
+  for (int i = 0; i < nmat; ++i)
+    if (!sizes_ok(M, N[i], K)) return 0;
+  size_t gen = 0;
+  return linear_ws(M, K, nmat, N, &gen);
+}
+
+mq_status mq_w4a4_residual_linear(const void* x, mq_dtype xt, int64_t M, int64_t K, int64_t ldx, int nmat,
+                                  const mq_matrix* mats, mq_dtype yt, uint8_t* xq, uint16_t* xs, void* ws,
+                                  size_t ws_bytes, mq_stream_t stream) {
+  MQ_CHECK(x && mats, MQ_ERR_INVALID_ARG, "linear: NULL pointer");
+  MQ_CHECK(nmat >= 1 && nmat <= 4, MQ_ERR_INVALID_ARG, "linear: 1 to 4 matrices, %d given", nmat);
+  MQ_CHECK(xt == MQ_F16 || xt == MQ_BF16, MQ_ERR_INVALID_ARG, "linear: x must be fp16 or bf16");
+  MQ_CHECK(yt == MQ_BF16 || yt == MQ_F32, MQ_ERR_INVALID_ARG, "linear: y must be bf16 or fp32");
+  MQ_CHECK(ldx >= K, MQ_ERR_INVALID_ARG, "linear: ldx %lld < K %lld", (long long)ldx, (long long)K);
+  MQ_CHECK(aligned(x, 8) && ldx % 4 == 0 && aligned(xq, 16) && aligned(xs, 16), MQ_ERR_ALIGNMENT,
+           "linear: x (and ldx*2 bytes) must be 8-byte aligned, xq and xs 16-byte aligned");
+  const uint8_t* wpk[4];
+  const int32_t* rp[4];
+  const int32_t* ci[4];
+  const uint8_t* rpk[4];
+  void* y[4];
+  int64_t N[4], nz[4], ldy[4];
+  for (int i = 0; i < nmat; ++i) {
+    const mq_matrix& m = mats[i];
+    MQ_CHECK(m.wpk && m.y, MQ_ERR_INVALID_ARG, "linear: matrix %d: NULL pointer", i);
+    MQ_CHECK(sizes_ok(M, m.N, K), MQ_ERR_INVALID_ARG, "linear: matrix %d: bad sizes M=%lld N=%lld K=%lld", i,
+             (long long)M, (long long)m.N, (long long)K);
+    MQ_CHECK(m.nnzb >= 0 && m.nnzb <= (m.N / kBlockRows) * (K / kGroup), MQ_ERR_INVALID_ARG,
+             "linear: matrix %d: bad nnzb %lld", i, (long long)m.nnzb);
+    MQ_CHECK(m.nnzb == 0 || (m.row_ptr && m.col_idx && m.rpk), MQ_ERR_INVALID_ARG,
+             "linear: matrix %d: residual pointers are NULL but nnzb = %lld", i, (long long)m.nnzb);
+    MQ_CHECK(m.ldy >= m.N, MQ_ERR_INVALID_ARG, "linear: matrix %d: ldy %lld < N %lld", i, (long long)m.ldy,
+             (long long)m.N);
+    MQ_CHECK(aligned(m.wpk, 16) && aligned(m.rpk, 16) && aligned(m.row_ptr, 4) && aligned(m.col_idx, 4) &&
+                 aligned(m.y, yt == MQ_F32 ? 4 : 2),
+             MQ_ERR_ALIGNMENT, "linear: matrix %d: wpk and rpk must be 16-byte aligned", i);
+    wpk[i] = m.wpk;
+    rp[i] = m.row_ptr;
+    ci[i] = m.col_idx;
+    rpk[i] = m.rpk;
+    y[i] = m.y;
+    N[i] = m.N;
+    nz[i] = m.nnzb;
+    ldy[i] = m.ldy;
+  }
+  if (mq_status s = check_device(); s != MQ_OK) return s;
+  size_t gen = 0;
+  const size_t need = linear_ws(M, K, nmat, N, &gen);
+  MQ_CHECK(ws && aligned(ws, 256) && ws_bytes >= need, MQ_ERR_WORKSPACE,
+           "linear: workspace of %zu bytes (256-aligned) needed, %zu given", need, ws_bytes);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  bool handled = false;
+  if (gen == 0) {  // one launch: quantize in the prologue, every matrix's tiles in one sequence
+    const mq_status zs = zipper_launch(&handled, nmat, wpk, N, rp, ci, nz, rpk, y, ldy, yt, nullptr, nullptr, x, xt,
+                                       ldx, xq, xs, M, K, nullptr, nullptr, ws, ws_bytes, st);
+    if (zs != MQ_OK || handled) return zs;
+  }
+  // the quantizer, then each matrix's GEMM
+  const size_t Mp = static_cast<size_t>((M + 7) / 8 * 8), G = static_cast<size_t>(K / kGroup);
+  uint8_t* qbuf = xq ? xq : static_cast<uint8_t*>(ws) + gen;
+  uint16_t* sbuf = xs ? xs : reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + gen + (G * Mp * 64 + 255) / 256 * 256);
+  if (mq_status s = quantize_act_launch(x, xt, M, K, ldx, qbuf, sbuf, st); s != MQ_OK) return s;
+  for (int i = 0; i < nmat; ++i)
+    if (mq_status s = gemm_launch(qbuf, sbuf, M, wpk[i], N[i], K, rp[i], ci[i], nz[i], rpk[i], y[i], ldy[i], yt,
+                                  nullptr, nullptr, ws, gen, st);
+        s != MQ_OK)
+      return s;
+  return MQ_OK;
 }
 
 mq_status mq_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t* info) {
@@ -265,7 +370,10 @@ mq_status mq_check_device_error(mq_stream_t stream) {
   if (cudaMemcpy(&h, word, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return launch_status("error word read");
   if (h != 0) {
     if (cudaMemset(word, 0, sizeof(uint32_t)) != cudaSuccess) return launch_status("error word reset");
-    if (h & kDevErrTimeout) return set_error(MQ_ERR_TIMEOUT, "a device-side wait ran out (error word 0x%x)", h);
+    if (h & kDevErrTimeout) {
+      g_timeout_epoch.fetch_add(1);
+      return set_error(MQ_ERR_TIMEOUT, "a device-side wait ran out (error word 0x%x)", h);
+    }
   }
   return MQ_OK;
 }

@@ -55,6 +55,8 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <cstdlib>
+#include <cstring>
 
 // Timeline probes for profiling builds (compiled out unless MQ_GEMM_TRACE is
 // defined, in which case the build supplies mq_trace_stamp).
@@ -124,8 +126,9 @@ struct GemmParams {
   int32_t* dots_w;    // debug
   int32_t* dots_r;    // debug
   float* partials;    // [ctas][2 slots][128 rows][TN]
-  int32_t* counters;  // [tiles]
+  int32_t* counters;  // [ctas]: pieces of the cut tile whose first unit is CTA c's
   int M, Mp, N, K, G, tiles_n, tiles_m, nnzb;
+  int64_t ldy;  // elements between rows of Y
   int64_t units;  // tiles * G / UG
   int ctas;
   uint64_t timeout_ns;
@@ -562,7 +565,7 @@ __global__ void __launch_bounds__(Cfg<TN, UG>::kThreads, 1) w4a4_residual_gemm_k
         for (int h = 0; h < 2; ++h) {
           const int mi = 2 * j + h;
           if (mi < mvalid) {
-            const int64_t off = static_cast<int64_t>(m0 + mi) * p.N + n;
+            const int64_t off = static_cast<int64_t>(m0 + mi) * p.ldy + n;
             if (p.y_f32)
               static_cast<float*>(p.y)[off] = v[h];
             else
@@ -654,7 +657,7 @@ __global__ void __launch_bounds__(Cfg<TN, UG>::kThreads, 1) w4a4_residual_gemm_k
           if (!drain_sync()) { ok = false; break; }
           if (dtid == 0) {
             const int64_t cf = cta_of_unit(tu0, U, P), cl = cta_of_unit(tu1 - 1, U, P);
-            const int old = atomicAdd(&p.counters[tile], 1);
+            const int old = atomicAdd(&p.counters[cf], 1);  // CTA cf starts at most one cut tile
             if (old == static_cast<int>(cl - cf)) ctl.deferred[ctl.ndeferred++] = tile;
           }
         }
@@ -708,7 +711,7 @@ __global__ void __launch_bounds__(Cfg<TN, UG>::kThreads, 1) w4a4_residual_gemm_k
         }
         if (!ok) break;
         store_tile(m0, n, mvalid);
-        if (dtid == 0) p.counters[tile] = 0;  // ready for the next launch
+        if (dtid == 0) p.counters[cf] = 0;  // ready for the next launch
       }
     }
   }
@@ -768,11 +771,31 @@ static Plan make_plan(int64_t M, int64_t N, int64_t K) {
   if (ctas < min_ctas) ctas = min_ctas;
   pl.ctas = static_cast<int>(ctas);
   pl.ws_partials = a256(static_cast<size_t>(pl.ctas) * 2 * pl.tn * kTileN * sizeof(float));
-  pl.ws_counters = a256(static_cast<size_t>(pl.tiles_m) * pl.tiles_n * sizeof(int32_t));
+  pl.ws_counters = kWsZeroBytes;  // counters [ctas] at the start, in the zeroed prefix
   return pl;
 }
 
+size_t zipper_workspace_bytes(int64_t M, int64_t tiles, int64_t K);
+
+// Bytes of workspace of the general kernel alone.
+size_t general_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  const Plan pl = make_plan(M, N, K);
+  return pl.ws_partials + pl.ws_counters;
+}
+
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  const Plan pl = make_plan(M, N, K);
+  return std::max(pl.ws_partials + pl.ws_counters, zipper_workspace_bytes(M, N / kTileN, K));
+}
+
+// Bytes of workspace the kernel that mq_w4a4_residual_gemm will run for
+// (M, N, K) on the current device reads and writes.
+size_t gemm_run_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  const char* impl = getenv("MQ_DECODE_IMPL");
+  if (!(impl && strcmp(impl, "cluster") == 0)) {
+    const size_t z = zipper_workspace_bytes(M, N / kTileN, K);
+    if (z) return z;
+  }
   const Plan pl = make_plan(M, N, K);
   return pl.ws_partials + pl.ws_counters;
 }
@@ -811,15 +834,36 @@ mq_status gemm_decode_launch(bool* handled, const uint8_t* xq, const uint16_t* x
                              const uint8_t* rpk, void* y, mq_dtype yt, int32_t* dots_w, int32_t* dots_r,
                              cudaStream_t stream);
 
+mq_status zipper_launch(bool* handled, int nmat, const uint8_t* const* wpk, const int64_t* N,
+                        const int32_t* const* row_ptr, const int32_t* const* col_idx, const int64_t* nnzb,
+                        const uint8_t* const* rpk, void* const* y, const int64_t* ldy, mq_dtype yt, const uint8_t* xq,
+                        const uint16_t* xs, const void* x, mq_dtype xt, int64_t ldx, uint8_t* xq_out,
+                        uint16_t* xs_out, int64_t M, int64_t K, int32_t* dots_w, int32_t* dots_r, void* ws,
+                        size_t ws_bytes, cudaStream_t stream);
+
 mq_status gemm_launch(const uint8_t* xq, const uint16_t* xs, int64_t M, const uint8_t* wpk, int64_t N, int64_t K,
                       const int32_t* row_ptr, const int32_t* col_idx, int64_t nnzb, const uint8_t* rpk, void* y,
-                      mq_dtype yt, int32_t* dots_w, int32_t* dots_r, void* ws, size_t ws_bytes, cudaStream_t stream) {
-  // Decode batches: the cluster split-K kernel (gemm_decode.cu), when it covers the shape.
+                      int64_t ldy, mq_dtype yt, int32_t* dots_w, int32_t* dots_r, void* ws, size_t ws_bytes,
+                      cudaStream_t stream) {
   bool handled = false;
-  const mq_status ds = gemm_decode_launch(&handled, xq, xs, M, wpk, N, K, row_ptr, col_idx, nnzb, rpk, y, yt, dots_w,
-                                          dots_r, stream);
-  if (handled || ds != MQ_OK) return ds;
+  const char* impl = getenv("MQ_DECODE_IMPL");
+  if (impl && strcmp(impl, "cluster") == 0 && ldy == N) {
+    // Decode batches: the cluster split-K kernel (gemm_decode.cu), when it covers the shape.
+    const mq_status ds = gemm_decode_launch(&handled, xq, xs, M, wpk, N, K, row_ptr, col_idx, nnzb, rpk, y, yt,
+                                            dots_w, dots_r, stream);
+    if (handled || ds != MQ_OK) return ds;
+  } else {
+    // Decode batches: the stream-K tensor-memory kernel (zipper.cu), when it covers the shape.
+    void* yy = y;
+    const mq_status zs = zipper_launch(&handled, 1, &wpk, &N, &row_ptr, &col_idx, &nnzb, &rpk, &yy, &ldy, yt, xq, xs,
+                                       nullptr, MQ_F16, 0, nullptr, nullptr, M, K, dots_w, dots_r, ws, ws_bytes,
+                                       stream);
+    if (handled || zs != MQ_OK) return zs;
+  }
   const Plan pl = make_plan(M, N, K);
+  if (pl.ctas > kWsZeroBytes / 4)
+    return set_error(MQ_ERR_INVALID_ARG, "gemm: M=%lld N=%lld K=%lld is too large for one launch", (long long)M,
+                     (long long)N, (long long)K);
   if (ws_bytes < pl.ws_partials + pl.ws_counters || ws == nullptr)
     return set_error(MQ_ERR_WORKSPACE, "gemm: workspace of %zu bytes needed, %zu given",
                      pl.ws_partials + pl.ws_counters, ws_bytes);
@@ -834,11 +878,12 @@ mq_status gemm_launch(const uint8_t* xq, const uint16_t* xs, int64_t M, const ui
   gp.y_f32 = yt == MQ_F32;
   gp.dots_w = dots_w;
   gp.dots_r = dots_r;
-  gp.partials = static_cast<float*>(ws);
-  gp.counters = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + pl.ws_partials);
+  gp.counters = static_cast<int32_t*>(ws);
+  gp.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + pl.ws_counters);
   gp.M = static_cast<int>(M);
   gp.Mp = static_cast<int>((M + 7) / 8 * 8);
   gp.N = static_cast<int>(N);
+  gp.ldy = ldy;
   gp.K = static_cast<int>(K);
   gp.G = pl.G;
   gp.tiles_n = pl.tiles_n;

@@ -1380,9 +1380,16 @@ static mq_status launch_decode(const DecParams& dp, const DecPlan& pl, cudaStrea
 // The kernel choice for (M, N, K) on the current device: {1 (warp-MMA
 // variant) or 2 (tensor-memory variant), tokens per tile, cluster size,
 // clusters, stages} for the decode kernel, else zeros.
+bool zipper_plan_info(int64_t M, int64_t tiles, int64_t K, int32_t* form, int32_t* tn, int32_t* ctas, int32_t* stages);
+
 mq_status gemm_plan_info(int64_t M, int64_t N, int64_t K, int32_t* info) {
   DecPlan pl;
   for (int i = 0; i < 5; ++i) info[i] = 0;
+  const char* impl = getenv("MQ_DECODE_IMPL");
+  if (!(impl && strcmp(impl, "cluster") == 0)) {
+    if (zipper_plan_info(M, N / kTileN, K, &info[0], &info[1], &info[3], &info[4])) info[2] = 1;
+    return MQ_OK;
+  }
   if (decode_plan(M, N, K, &pl)) {
     info[0] = pl.tc ? 2 : 1;
     info[1] = pl.tn;

@@ -23,6 +23,12 @@ static_assert(kWRecBytes == kWRecScales + 2 * kTileN && kRRecBytes == kRRecScale
 // device error word bits
 constexpr uint32_t kDevErrTimeout = 1u;
 
+// Every GEMM workspace starts with this many bytes that the kernels read as
+// counters and flags: zero before the first use, and left zero by every
+// launch that finishes normally.  Scratch (pieces, activation images) follows,
+// so one workspace can serve GEMMs of any shape run one after another.
+constexpr int kWsZeroBytes = 16384;
+
 // ---------------------------------------------------------------------------
 // host side (abi.cu)
 // ---------------------------------------------------------------------------
@@ -93,17 +99,25 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 // Bounded wait on an mbarrier phase.  Gives up after `timeout_ns` or when the
 // CTA-wide abort flag is raised; on timeout it records the error in the
 // device error word and raises the abort flag.  Returns false on give-up.
+// The global timer and the abort flag are read once every 64 polls only: a
+// waiting warp must notice a completed phase at once (the handoffs between
+// roles sit on the critical path), and those reads are slow.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           uint64_t timeout_ns, uint32_t* err_word) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  while (true) {
+  uint64_t t0 = 0;
+  for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (globaltimer() - t0 > timeout_ns) {
-      atomicOr(err_word, kDevErrTimeout);
-      *abort_flag = 1;
-      return false;
+    if ((n & 63u) == 0) {
+      if (*abort_flag) return false;
+      const uint64_t now = globaltimer();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > timeout_ns) {
+        atomicOr(err_word, kDevErrTimeout);
+        *abort_flag = 1;
+        return false;
+      }
     }
   }
 }

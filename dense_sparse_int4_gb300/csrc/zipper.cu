@@ -1,0 +1,1695 @@
+// The fused W4A4 + block-sparse 4-bit residual GEMM for decode batches (up to
+// 32 tokens): the ZipperEngine of the MosaicQuant summary (Metodologia 3) as a
+// persistent, stream-K, tensor-memory kernel for sm_103a.  It computes
+//
+//   Y[m,n] = sum_g sx[m,g] * ( sw[n,g] * Dw[m,n,g] + sr[n,g] * Dr[m,n,g] )
+//
+// in one launch: the residual product of a selected 64x128 block runs on the
+// same activation tile as the dense product of its group and both are
+// reduce-added into the same fp32 accumulators.
+//
+// Work.  A "unit" is one 128-row weight tile x one 128-input group: one packed
+// base record (8448 bytes) and, where the block list has a block in either
+// 64-row half, one residual item more.  Units are ordered tile-major, over up to
+// four weight matrices that share the activations (a grouped launch), and the
+// CTAs (one per SM) take equal contiguous ranges of them (stream-K), so every SM
+// streams the same number of weight bytes whatever the tile count.
+//
+// Numbers.  INT4 codes run on the tensor cores as E4M3 bytes (sm_103a has no
+// integer tcgen05 kind):
+//   * weights: a byte 0x00..0x0F read as E4M3 is exactly b * 2^-9, so the
+//     nibble u = q + 8 (q XOR 8) moved into a byte is u * 2^-9: a mask and a
+//     shift per 8 codes.  The MMA measures 2^-9 (D + 8 sum_k qx); the drain
+//     subtracts the exact activation term and folds 2^9 into the activation
+//     scale.  Every partial sum is a multiple of 2^-9 below 2^14: exact in fp32.
+//   * activations: E4M3 bytes holding the integer codes exactly, in a
+//     128-byte-swizzled K-major tile (the MMA's B operand), with K permuted
+//     inside each 8-code word (even codes, then odd) as the weight unpack
+//     leaves them.
+//
+// The launch, per CTA (16 warps):
+//   prologue   every group's activation image (B tile, 2^9 sx, offset terms)
+//              is built once per launch by one CTA (group g by CTA g mod P),
+//              from the packed activations or, in the fused form, straight from
+//              X (the quantizer runs here), written to the workspace and
+//              published with a per-group flag;
+//   warp 0     producer: bulk copies of each unit's base record and its
+//              group's activation image into a ring of shared-memory stages;
+//   warp 1     reads the block list of the CTA's tiles once into a residual map,
+//              then streams the residual records into a ring of their own;
+//   warp 2     issues each item's four K=32 tcgen05 MMAs (A = unpacked weights
+//              in tensor memory, B = the stage's activation tile) into a ring
+//              of 8 tensor-memory accumulators;
+//   warps 4-11 unpack: lane quarter q (warp % 4) owns rows 32q..32q+31, the two
+//              warpgroups split each item's four K-steps; codes go from the
+//              stage to registers to tensor memory (no shared-memory round trip);
+//   warps 12-15 drain: per item, load the exact dots from tensor memory and
+//              reduce-add sx * (s * D) into fp32 registers; at a tile's end,
+//              store Y, or hand the CTA's piece of a tile cut by a range
+//              boundary to the workspace, where the last CTA to arrive sums the
+//              pieces in CTA order (deterministic, no floating-point atomics).
+// Every wait is bounded: a wait that runs out sets the device error word,
+// raises the CTA's abort flag, and every role winds down.
+#include "mq_internal.cuh"
+
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+// Timeline probes for profiling builds: compiled out unless MQ_ZTRACE is
+// defined, in which case stamps go to a buffer the host sets: ZT(slot) the
+// global timer, ZC(slot) the SM cycle counter.
+#ifdef MQ_ZTRACE
+__device__ unsigned long long* g_zt_buf;
+__device__ __forceinline__ void zt_put(int slot, unsigned long long v) {
+  if (g_zt_buf && slot < 256) g_zt_buf[blockIdx.x * 256 + slot] = v;
+}
+__device__ __forceinline__ unsigned long long zt_gtime() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+#define ZT_INIT unsigned long long* const zt_b = g_zt_buf ? g_zt_buf + blockIdx.x * 256 : nullptr
+#define ZT(slot)                      \
+  do {                                \
+    if (zt_b) zt_b[slot] = zt_gtime(); \
+  } while (0)
+#define ZC(slot)                                                             \
+  do {                                                                       \
+    if (zt_b) zt_b[slot] = static_cast<unsigned long long>(clock64());       \
+  } while (0)
+extern "C" int mq_zt_set_buffer(void* p) {
+  return cudaMemcpyToSymbol(g_zt_buf, &p, sizeof(p)) == cudaSuccess ? 0 : 1;
+}
+#else
+#define ZT_INIT
+#define ZT(slot) ((void)0)
+#define ZC(slot) ((void)0)
+#endif
+
+namespace mq {
+namespace {
+
+constexpr int kNB = 8;             // items in flight: A/D buffer pairs in tensor memory
+constexpr int kUS = 4;             // units per shared-memory stage (one bulk copy of their base records)
+constexpr int kMinUnits = 8;       // units per CTA at least (bounds the pieces a tile is cut into)
+constexpr int kRS = 8;             // residual-record ring slots
+constexpr int kMaxUnits = 256;     // units per CTA (size of the residual map)
+constexpr int kMaxStages = 8;
+constexpr int kMaxMats = 4;
+constexpr int kWarpProd = 0, kWarpRes = 1, kWarpMma = 2, kWarpConv0 = 4, kWarpDrain0 = 12;
+constexpr int kConvWarps = 8, kDrainWarps = 4;
+constexpr int kThreads = 32 * (kWarpDrain0 + kDrainWarps);
+constexpr int kTmemCols = 512;
+constexpr int kSmemLimit = 227 * 1024;
+
+struct ZMat {
+  const uint8_t* wpk;
+  const int32_t* row_ptr;
+  const int32_t* col_idx;
+  const uint8_t* rpk;
+  void* y;
+  int64_t ldy;  // elements between rows of Y
+  int tile0;    // first tile of this matrix in the launch's tile order
+  int nnzb;
+};
+
+struct ZParams {
+  ZMat mat[kMaxMats];
+  int nmat;
+  const uint8_t* xq;   // [G][Mp][64] packed activations (prologue from codes)
+  const uint16_t* xs;  // [G][Mp] fp16
+  const uint16_t* x;   // [M][ldx] fp16 / bf16 (prologue quantizes)
+  int64_t ldx;
+  int x_bf16;
+  uint8_t* xq_out;     // optional: the quantized activations, as mq_quantize_act writes them
+  uint16_t* xs_out;
+  int M, Mp, G, tiles, ctas, nstages, stage_bytes;
+  int64_t units;
+  int y_f32;
+  int32_t* dots_w;  // test hook (one matrix): raw group dots instead of Y
+  int32_t* dots_r;
+  const uint8_t* act;  // workspace: [G] activation images (written by the image kernel)
+  int32_t* tcount;     // [ctas] pieces that have arrived of the cut tile whose first unit is CTA c's
+  float* part;         // [ctas][2][TN][128] stream-K pieces
+  uint64_t timeout_ns;
+  uint32_t* err;
+};
+
+struct __align__(8) ZCtl {
+  uint64_t full[kMaxStages];   // stage landed: producer arrival + bytes
+  uint64_t empty[kMaxStages];  // 8 unpack warps read the codes, 4 drain warps the scales
+  uint64_t r_full[kRS];
+  uint64_t r_empty[kRS];       // the 4 unpack and 2 drain warps of the record's half
+  uint64_t a_full[kNB];        // 8 unpack warps stored item's A
+  uint64_t d_full[kNB];        // the item's MMAs completed (commit)
+  uint64_t d_empty[kNB];       // 4 drain warps loaded the item's D
+  uint64_t map_ready;
+  uint64_t exit_bar;
+  uint64_t red_bar;            // stream-K pieces copied in for a deferred tile
+  uint64_t drain_bar;          // bounded barrier of the 4 drain warps
+  uint64_t tmem_ready;         // the tensor-memory allocation is published
+  int32_t map[kMaxUnits][2];   // CSR entry of the residual block of (unit, half), or -1
+  int32_t rpos[kMaxUnits][2];  // its position in the residual ring order
+  uint32_t tmem_base;
+  int abort_flag;
+  int ndeferred;
+  int deferred[2];             // cut tiles whose count this CTA completed
+};
+
+// Bytes of one activation image in the workspace and in a stage: the B tile
+// (TN rows x 128 bytes), 2^9 sx and the offset terms (TN fp32 each), padded to
+// a multiple of 1024 so every B tile keeps the 128-byte swizzle's alignment.
+__host__ __device__ constexpr int act_rec_bytes(int tn) { return (tn * 128 + tn * 8 + 1023) / 1024 * 1024; }
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(int32_t* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void named_bar(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+// Bounded wait with back-off, for roles whose waits are long (producers).
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                uint64_t timeout_ns, uint32_t* err_word) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = 0;
+  for (uint32_t n = 1;; ++n) {
+    __nanosleep(32);
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 63u) == 0) {
+      if (*abort_flag) return false;
+      const uint64_t now = globaltimer();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > timeout_ns) {
+        atomicOr(err_word, kDevErrTimeout);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+// Bounded wait for a flag in global memory (written by another CTA) to become nonzero.
+__device__ __forceinline__ bool flag_wait(const int32_t* f, volatile int* abort_flag, uint64_t timeout_ns,
+                                          uint32_t* err_word) {
+  if (ld_acquire_gpu(f) != 0) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    __nanosleep(100);
+    if (ld_acquire_gpu(f) != 0) return true;
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > timeout_ns) {
+      atomicOr(err_word, kDevErrTimeout);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// Shared-memory matrix descriptor of a K-major operand in 128-byte-swizzled
+// rows (8-row atoms 1024 bytes apart).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | (static_cast<uint64_t>(1024 >> 4) << 32) |
+         (1ull << 46) | (2ull << 61);
+}
+
+// Load MLD consecutive 32-bit columns of this thread's tensor-memory lane.
+template <int MLD>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&v)[MLD]) {
+  if constexpr (MLD == 4) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+                 : "r"(taddr)
+                 : "memory");
+  } else if constexpr (MLD == 8) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+                 : "r"(taddr)
+                 : "memory");
+  } else if constexpr (MLD == 16) {
+    tmem_ld16(taddr, v);
+  } else {
+    tmem_ld32(taddr, v);
+  }
+}
+
+// Store 16 consecutive 32-bit columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+// Eight weight codes (two's complement nibbles, element i in bits 4i..4i+3)
+// -> two words of four E4M3 bytes holding (q + 8) * 2^-9 exactly: the even
+// elements 0, 2, 4, 6 in `ev`, the odd ones in `od`.
+__device__ __forceinline__ void unpack_u4(uint32_t p, uint32_t& ev, uint32_t& od) {
+  const uint32_t u = p ^ 0x88888888u;
+  ev = u & 0x0F0F0F0Fu;
+  od = (u >> 4) & 0x0F0F0F0Fu;
+}
+
+// Sum of the eight signed codes of a word of packed activations.
+__device__ __forceinline__ int nibble_sum8(uint32_t p) {
+  const uint32_t u = p ^ 0x88888888u;  // q + 8 in [1, 15]
+  const uint32_t b = (u & 0x0F0F0F0Fu) + ((u >> 4) & 0x0F0F0F0Fu);
+  return static_cast<int>((b * 0x01010101u) >> 24) - 64;
+}
+
+// Byte offset of codes 8t..8t+7 (word t of 16) of token row m inside the
+// activation image's 128-byte-swizzled K-major tile.
+__device__ __forceinline__ int act_word_offset(int m, int t) {
+  return (m >> 3) * 1024 + (m & 7) * 128 + (((t >> 1) ^ (m & 7)) << 4) + ((t & 1) << 3);
+}
+
+// Activation quantization (the quantizer's rule, bit-exact with mq_quantize_act):
+// s = fp16_RNE(amax / 7) saturated, q = clamp(RNE(x / s), -7, 7) in IEEE fp32.
+__device__ __forceinline__ uint16_t act_scale_bits(float amax) {
+  const __half h = __float2half_rn(__fdiv_rn(amax, 7.0f));
+  uint16_t b = __half_as_ushort(h);
+  if ((b & 0x7FFFu) == 0x7C00u) b = (b & 0x8000u) | 0x7BFFu;
+  return b;
+}
+__device__ __forceinline__ int act_code(float v, float s) {
+  if (s == 0.0f) return 0;
+  float t = rintf(__fdiv_rn(v, s));
+  t = fminf(fmaxf(t, -7.0f), 7.0f);
+  return static_cast<int>(t);
+}
+// E4M3 byte of an integer code |q| <= 7.
+__device__ __forceinline__ uint32_t e4m3_of_code(int q) {
+  const uint32_t a = static_cast<uint32_t>(q < 0 ? -q : q);
+  const uint32_t mag = prmt(0x44403800u, 0x4E4C4A48u, a);  // bytes of 0,1,2,3 | 4,5,6,7
+  return (mag & 0xFFu) | (q < 0 ? 0x80u : 0u);
+}
+__device__ __forceinline__ float act_value(const uint16_t* x, int64_t i, bool bf16) {
+  const uint16_t b = x[i];
+  return bf16 ? __uint_as_float(static_cast<uint32_t>(b) << 16) : __half2float(__ushort_as_half(b));
+}
+
+// first unit of CTA c, and the CTA that owns unit u (balanced contiguous ranges)
+__device__ __forceinline__ int64_t first_unit(int64_t c, int64_t U, int64_t P) { return c * U / P; }
+__device__ __forceinline__ int64_t owner_of(int64_t u, int64_t U, int64_t P) { return ((u + 1) * P - 1) / U; }
+
+__device__ __forceinline__ int mat_of_tile(const ZParams& p, int t) {
+  int mi = 0;
+#pragma unroll
+  for (int i = 1; i < kMaxMats; ++i)
+    if (i < p.nmat && t >= p.mat[i].tile0) mi = i;
+  return mi;
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+
+// TN: tokens of the MMA tile (16 or 32); MLD: token columns the drain reads
+// (4, 8, 16 or 32); kDebug: write raw group dots.
+template <int TN, int MLD, bool kDebug>
+__global__ void __launch_bounds__(kThreads, 1) zipper_decode_kernel(const ZParams p) {
+  static_assert(MLD <= TN && TN % 16 == 0, "tile shape");
+  constexpr int kArec = act_rec_bytes(TN);  // activation image: B tile, 2^9 sx, offset terms, padding
+  constexpr int kAct = kUS * kArec;         // a stage: kUS activation images, then kUS base records
+  constexpr uint32_t kIdesc =
+      (1u << 4) | (static_cast<uint32_t>(TN >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ ZCtl ctl;
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int S = p.nstages, SB = p.stage_bytes, G = p.G;
+  uint8_t* stages = smem;                               // [S] stages, 1024-aligned
+  uint8_t* rring = smem + static_cast<size_t>(S) * SB;  // [kRS] residual records
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t U = p.units, P = p.ctas, c = blockIdx.x;
+  const int64_t u0 = first_unit(c, U, P), u1 = first_unit(c + 1, U, P);
+  const int nu = static_cast<int>(u1 - u0);
+  const int nstg = (nu + kUS - 1) / kUS;  // stages this CTA fills
+  volatile int* abort_flag = &ctl.abort_flag;
+  const uint64_t tmo = p.timeout_ns;
+  ZT_INIT;
+
+  if (threadIdx.x == 0) {
+    ZT(0);
+    ZC(6);
+  }
+  if (warp == 0) {
+    for (int s = lane; s < S; s += 32) {
+      mbar_init(&ctl.full[s], 1);
+      mbar_init(&ctl.empty[s], kConvWarps + kDrainWarps);
+    }
+    if (lane < kRS) {
+      mbar_init(&ctl.r_full[lane], 1);
+      mbar_init(&ctl.r_empty[lane], kConvWarps / 2 + kDrainWarps / 2);
+    }
+    if (lane < kNB) {
+      mbar_init(&ctl.a_full[lane], kConvWarps);
+      mbar_init(&ctl.d_full[lane], 1);
+      mbar_init(&ctl.d_empty[lane], kDrainWarps);
+    }
+    if (lane == 8) mbar_init(&ctl.map_ready, 1);
+    if (lane == 9) mbar_init(&ctl.exit_bar, kThreads / 32);
+    if (lane == 10) mbar_init(&ctl.red_bar, 1);
+    if (lane == 13) mbar_init(&ctl.drain_bar, kDrainWarps);
+    if (lane == 14) mbar_init(&ctl.tmem_ready, 1);
+    if (lane == 11) ctl.abort_flag = 0;
+    if (lane == 12) ctl.ndeferred = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();  // barriers initialised
+  if (threadIdx.x == 0) ZC(8);
+  // The next kernel may start launching; it touches nothing this one uses
+  // before its own dependency wait.
+  pdl_trigger();
+  // The tensor-memory allocation (by the MMA warp) is published through
+  // tmem_ready, so the producers start streaming at once.
+  auto tmem_wait = [&]() -> bool {
+    const bool r = mbar_wait(&ctl.tmem_ready, 0, abort_flag, tmo, p.err);
+    tc_fence_after();
+    return r;
+  };
+  auto stage = [&](int s) { return stages + static_cast<size_t>(s) * SB; };
+  auto wrec = [&](int64_t u) -> const uint8_t* {
+    const int t = static_cast<int>(u / G), g = static_cast<int>(u - static_cast<int64_t>(t) * G);
+    const ZMat& mt = p.mat[mat_of_tile(p, t)];
+    return mt.wpk + (static_cast<int64_t>(t - mt.tile0) * G + g) * kWRecBytes;
+  };
+  // first unit after the matrix of unit u (records are contiguous inside one matrix)
+  auto mat_end = [&](int64_t u) -> int64_t {
+    const int mi = mat_of_tile(p, static_cast<int>(u / G));
+    return static_cast<int64_t>(mi + 1 < p.nmat ? p.mat[mi + 1].tile0 : p.tiles) * G;
+  };
+
+  if (warp == kWarpProd) {
+    // ---------------- producer: a stage = kUS units' base records and activation images ----------------
+    // Bulk copies cost the copy engine a fixed time each, so a stage moves
+    // its base records (contiguous within a matrix) in one copy and its
+    // activation images (consecutive groups) in one more.
+    auto stage_bytes = [&](int st) {
+      const int n = min(kUS, nu - st * kUS);
+      return static_cast<uint32_t>(n * (kWRecBytes + kArec));
+    };
+    auto issue_weights = [&](int st, int s) {
+      int64_t ua = u0 + st * kUS;
+      const int64_t ub = min(u1, ua + kUS), us = ua;
+      while (ua < ub) {
+        const int64_t e = min(ub, mat_end(ua));
+        bulk_g2s(stage(s) + kAct + (ua - us) * kWRecBytes, wrec(ua), static_cast<uint32_t>((e - ua) * kWRecBytes),
+                 &ctl.full[s]);
+        ua = e;
+      }
+    };
+    auto issue_act = [&](int st, int s) {
+      int64_t ua = u0 + st * kUS;
+      const int64_t ub = min(u1, ua + kUS), us = ua;
+      while (ua < ub) {
+        const int g = static_cast<int>(ua % G);
+        const int64_t n = min(ub - ua, static_cast<int64_t>(G - g));
+        bulk_g2s(stage(s) + (ua - us) * kArec, p.act + static_cast<int64_t>(g) * kArec,
+                 static_cast<uint32_t>(n * kArec), &ctl.full[s]);
+        ua += n;
+      }
+    };
+    const int pre = min(S, nstg);
+    // The first stages' base records are requested before the dependency wait:
+    // the kernels that may run ahead of it (this library's, which ask for the
+    // next launch early) never write packed weights.
+    if (lane == 0) {
+      for (int st = 0; st < pre; ++st) {
+        mbar_arrive_expect_tx(&ctl.full[st], stage_bytes(st));
+        issue_weights(st, st);
+      }
+    }
+    pdl_wait();  // the activation images are the preceding kernel's output
+    if (lane == 0) ZC(9);
+    bool ok = true;
+    if (lane == 0 && ok) {
+      for (int st = 0; st < nstg; ++st) {
+        const int s = st % S;
+        if (st >= S) {
+          if (!mbar_wait_sleep(&ctl.empty[s], ((st / S) - 1) & 1, abort_flag, tmo, p.err)) break;
+          mbar_arrive_expect_tx(&ctl.full[s], stage_bytes(st));
+          issue_weights(st, s);
+        }
+        issue_act(st, s);
+        if (st < 16) ZC(16 + st);
+      }
+    }
+  } else if (warp == kWarpRes) {
+    // ---------------- residual map, then the residual records in order ----------------
+    pdl_wait();
+    for (int i = lane; i < nu * 2; i += 32) (&ctl.map[0][0])[i] = -1;
+    __syncwarp();
+    if (nu > 0) {
+      const int t_lo = static_cast<int>(u0 / G), t_hi = static_cast<int>((u1 - 1) / G);
+      for (int t = t_lo; t <= t_hi; ++t) {
+        const ZMat& mt = p.mat[mat_of_tile(p, t)];
+        if (mt.nnzb == 0) continue;
+        const int64_t br = 2 * static_cast<int64_t>(t - mt.tile0);
+        const int a0 = max(0, min(mt.nnzb, mt.row_ptr[br]));
+        const int a1 = max(a0, min(mt.nnzb, mt.row_ptr[br + 1]));
+        const int a2 = max(a1, min(mt.nnzb, mt.row_ptr[br + 2]));
+        for (int e = a0 + lane; e < a2; e += 32) {
+          const int g = mt.col_idx[e];
+          if (g < 0 || g >= G) continue;
+          const int64_t u = static_cast<int64_t>(t) * G + g;
+          if (u >= u0 && u < u1) ctl.map[u - u0][e >= a1 ? 1 : 0] = e;
+        }
+      }
+    }
+    __syncwarp();
+    {  // ring positions: residual records in (unit, half) order; lane l counts a chunk of it
+      const int nf = nu * 2;
+      const int chunk = (nf + 31) / 32, f0 = min(nf, lane * chunk), f1 = min(nf, f0 + chunk);
+      int cnt = 0;
+      for (int f = f0; f < f1; ++f) cnt += (&ctl.map[0][0])[f] >= 0;
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int pos = incl - cnt;
+      for (int f = f0; f < f1; ++f)
+        if ((&ctl.map[0][0])[f] >= 0) (&ctl.rpos[0][0])[f] = pos++;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(&ctl.map_ready);
+      ZC(11);
+      for (int f = 0; f < nu * 2; ++f) {
+        const int e = (&ctl.map[0][0])[f];
+        if (e < 0) continue;
+        const int cpos = (&ctl.rpos[0][0])[f], slot = cpos % kRS;
+        if (cpos >= kRS && !mbar_wait_sleep(&ctl.r_empty[slot], ((cpos / kRS) - 1) & 1, abort_flag, tmo, p.err))
+          break;
+        const int t = static_cast<int>((u0 + f / 2) / G);
+        const ZMat& mt = p.mat[mat_of_tile(p, t)];
+        mbar_arrive_expect_tx(&ctl.r_full[slot], kRRecBytes);
+        bulk_g2s(rring + slot * kRRecBytes, mt.rpk + static_cast<int64_t>(e) * kRRecBytes, kRRecBytes,
+                 &ctl.r_full[slot]);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ---------------- MMA issue: four K=32 MMAs per item ----------------
+    tmem_alloc(&ctl.tmem_base, kTmemCols);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl.tmem_ready);
+    const uint32_t tmem = ctl.tmem_base;
+    tc_fence_after();
+    if (lane == 0 && mbar_wait(&ctl.map_ready, 0, abort_flag, tmo, p.err)) {
+      int i = 0;
+      bool ok = true;
+      for (int ui = 0; ui < nu && ok; ++ui) {
+        if (i < 16) ZC(64 + 8 * i + 7);
+        const int st = ui / kUS, j = ui - st * kUS, s = st % S;
+        const uint32_t bsm = smem_u32(stage(s) + j * kArec);
+        const int nitems = (ctl.map[ui][0] >= 0 || ctl.map[ui][1] >= 0) ? 2 : 1;
+        // the activation tile the MMAs read landed by bulk copy (long complete by now)
+        if (j == 0 && !(ok = mbar_wait(&ctl.full[s], (st / S) & 1, abort_flag, tmo, p.err))) break;
+        for (int it = 0; it < nitems; ++it, ++i) {
+          const int b = i % kNB, k = i / kNB;
+          if (i < 16) ZC(64 + 8 * i + 0);
+          if (!(ok = mbar_wait(&ctl.a_full[b], k & 1, abort_flag, tmo, p.err))) break;
+          if (i < 16) ZC(64 + 8 * i + 1);
+          if (k > 0 && !(ok = mbar_wait(&ctl.d_empty[b], (k - 1) & 1, abort_flag, tmo, p.err))) break;
+          if (i < 16) ZC(64 + 8 * i + 2);
+          tc_fence_after();
+          if (i < 16) ZC(64 + 8 * i + 3);
+          const uint32_t a_col = tmem + 32 * b, d_col = tmem + 32 * kNB + TN * b;
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj)
+            tc_mma_ts(d_col, a_col + 8 * jj, sw128_desc(bsm + 32 * jj), kIdesc, jj > 0);
+          if (i < 16) ZC(64 + 8 * i + 4);
+          tc_commit(&ctl.d_full[b]);
+          if (i < 16) ZC(64 + 8 * i + 5);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp >= kWarpConv0 && warp < kWarpDrain0) {
+    // ---------------- unpack warps ----------------
+    const int cw = warp - kWarpConv0, q = warp & 3, kh = cw >> 2;
+    const int r = 32 * q + lane, half = q >> 1;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    const int ct = cw * 32 + lane;  // 0..255
+    bool ok = tmem_wait();
+    const uint32_t tmem = ctl.tmem_base;
+    // --- main loop: items in order ---
+    ok = ok && mbar_wait(&ctl.map_ready, 0, abort_flag, tmo, p.err);
+    int i = 0;
+    for (int ui = 0; ui < nu && ok; ++ui) {
+      const int st = ui / kUS, j = ui - st * kUS, s = st % S;
+      {  // base item
+        const int b = i % kNB, k = i / kNB;
+        if (k > 0 && !(ok = mbar_wait(&ctl.d_full[b], (k - 1) & 1, abort_flag, tmo, p.err))) break;
+        if (j == 0 && !(ok = mbar_wait(&ctl.full[s], (st / S) & 1, abort_flag, tmo, p.err))) break;
+        if (ct == 0 && j == 0 && st < 16) ZC(32 + st);
+        const uint8_t* src = stage(s) + kAct + j * kWRecBytes + (2 * kh) * 2048 + r * 16;
+        const uint4 w0 = *reinterpret_cast<const uint4*>(src);
+        const uint4 w1 = *reinterpret_cast<const uint4*>(src + 2048);
+        if (j == kUS - 1 || ui == nu - 1) {  // this warp's reads of the stage are done
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl.empty[s]);
+        }
+        uint32_t v[16];
+        unpack_u4(w0.x, v[0], v[1]);
+        unpack_u4(w0.y, v[2], v[3]);
+        unpack_u4(w0.z, v[4], v[5]);
+        unpack_u4(w0.w, v[6], v[7]);
+        unpack_u4(w1.x, v[8], v[9]);
+        unpack_u4(w1.y, v[10], v[11]);
+        unpack_u4(w1.z, v[12], v[13]);
+        unpack_u4(w1.w, v[14], v[15]);
+        tmem_st16(tmem + 32 * b + 16 * kh + lane_base, v);
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.a_full[b]);
+        ++i;
+      }
+      const int e0 = ctl.map[ui][0], e1 = ctl.map[ui][1];
+      if (e0 >= 0 || e1 >= 0) {  // residual item
+        const int b = i % kNB, k = i / kNB;
+        if (k > 0 && !(ok = mbar_wait(&ctl.d_full[b], (k - 1) & 1, abort_flag, tmo, p.err))) break;
+        if ((half ? e1 : e0) >= 0) {
+          const int cpos = ctl.rpos[ui][half], slot = cpos % kRS;
+          if (!(ok = mbar_wait(&ctl.r_full[slot], (cpos / kRS) & 1, abort_flag, tmo, p.err))) break;
+          const uint8_t* src = rring + slot * kRRecBytes + (2 * kh) * 1024 + (r & 63) * 16;
+          const uint4 w0 = *reinterpret_cast<const uint4*>(src);
+          const uint4 w1 = *reinterpret_cast<const uint4*>(src + 1024);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl.r_empty[slot]);
+          uint32_t v[16];
+          unpack_u4(w0.x, v[0], v[1]);
+          unpack_u4(w0.y, v[2], v[3]);
+          unpack_u4(w0.z, v[4], v[5]);
+          unpack_u4(w0.w, v[6], v[7]);
+          unpack_u4(w1.x, v[8], v[9]);
+          unpack_u4(w1.y, v[10], v[11]);
+          unpack_u4(w1.z, v[12], v[13]);
+          unpack_u4(w1.w, v[14], v[15]);
+          tmem_st16(tmem + 32 * b + 16 * kh + lane_base, v);
+          tc_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.a_full[b]);
+        ++i;
+      }
+    }
+  } else if (warp >= kWarpDrain0) {
+    // ---------------- drain warps: thread = weight row ----------------
+    const int q = warp & 3, r = 32 * q + lane, half = q >> 1;
+    const int dt = threadIdx.x - 32 * kWarpDrain0;  // 0..127
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    uint64_t acc[MLD / 2];
+#pragma unroll
+    for (int j = 0; j < MLD / 2; ++j) acc[j] = 0ull;
+    bool ok = tmem_wait() && mbar_wait(&ctl.map_ready, 0, abort_flag, tmo, p.err);
+    const uint32_t tmem = ctl.tmem_base;
+    pdl_wait();  // Y and the workspace pieces may still be in use by the preceding kernel
+    // Barrier of the 4 drain warps, bounded like every other wait (a warp that
+    // gave up never leaves the others waiting).
+    int nsync = 0;
+    auto drain_sync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.drain_bar);
+      return mbar_wait(&ctl.drain_bar, (nsync++) & 1, abort_flag, tmo, p.err);
+    };
+
+    // One item's dots of this row: acc += 2^9 sx * (s * (D - c)), or the test hook's raw dots.
+    auto drain_item = [&](int i, const float* sx2, const float* cc, const uint16_t* sp, bool use, int ui,
+                          int e) -> bool {
+      const int b = i % kNB, k = i / kNB;
+      if (!mbar_wait(&ctl.d_full[b], k & 1, abort_flag, tmo, p.err)) return false;
+      tc_fence_after();
+      const float s = use ? __half2float(__ushort_as_half(*sp)) : 0.0f;  // read only now: the copy has landed
+      uint32_t d[MLD];
+      tmem_ld_cols<MLD>(tmem + 32 * kNB + TN * b + lane_base, d);
+      tc_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.d_empty[b]);
+      if (!use) return true;
+      if constexpr (kDebug) {
+        const int64_t u = u0 + ui;
+        const int t = static_cast<int>(u / G), g = static_cast<int>(u % G);
+#pragma unroll
+        for (int m = 0; m < MLD; ++m) {
+          if (m < p.M) {
+            const int32_t dd = static_cast<int32_t>((__uint_as_float(d[m]) - cc[m]) * 512.0f);
+            if (e < 0)
+              p.dots_w[(static_cast<int64_t>(m) * (p.tiles * kTileN) + static_cast<int64_t>(t) * kTileN + r) * G + g] = dd;
+            else
+              p.dots_r[(static_cast<int64_t>(m) * p.mat[0].nnzb + e) * 64 + (r & 63)] = dd;
+          }
+        }
+      } else {
+        const uint64_t s2 = f2pack(s, s), m1 = f2pack(-1.0f, -1.0f);
+        const float4* sx4 = reinterpret_cast<const float4*>(sx2);
+        const float4* c4 = reinterpret_cast<const float4*>(cc);
+#pragma unroll
+        for (int j4 = 0; j4 < MLD / 4; ++j4) {
+          const float4 sv = sx4[j4], cv = c4[j4];
+          const uint64_t d0 = f2fma(f2pack(cv.x, cv.y), m1, f2pack(__uint_as_float(d[4 * j4]), __uint_as_float(d[4 * j4 + 1])));
+          const uint64_t d1 =
+              f2fma(f2pack(cv.z, cv.w), m1, f2pack(__uint_as_float(d[4 * j4 + 2]), __uint_as_float(d[4 * j4 + 3])));
+          acc[2 * j4] = f2fma(f2pack(sv.x, sv.y), f2mul(s2, d0), acc[2 * j4]);
+          acc[2 * j4 + 1] = f2fma(f2pack(sv.z, sv.w), f2mul(s2, d1), acc[2 * j4 + 1]);
+        }
+      }
+      return true;
+    };
+    auto store_y = [&](const ZMat& mt, int64_t n, int m, float v) {
+      const int64_t o = static_cast<int64_t>(m) * mt.ldy + n;
+      if (p.y_f32)
+        static_cast<float*>(mt.y)[o] = v;
+      else
+        static_cast<__nv_bfloat16*>(mt.y)[o] = __float2bfloat16_rn(v);
+    };
+    auto piece_of = [&](int64_t cc, int t) -> const float* {  // CTA cc's piece of tile t
+      const int wc = (t == static_cast<int>(first_unit(cc, U, P) / G)) ? 0 : 1;
+      return p.part + ((cc * 2 + wc) * TN) * static_cast<int64_t>(kTileN);
+    };
+    // Tile t is finished in this CTA's range: store it whole, or write this
+    // CTA's piece and count it in; the CTA that completes the count sums the
+    // pieces after its own range (deferred: no stall here).
+    auto finish_tile = [&](int t) -> bool {
+      const ZMat& mt = p.mat[mat_of_tile(p, t)];
+      const int64_t n = static_cast<int64_t>(t - mt.tile0) * kTileN + r;
+      const int64_t tu0 = static_cast<int64_t>(t) * G, tu1 = tu0 + G;
+      if (tu0 >= u0 && tu1 <= u1) {  // the whole tile is this CTA's
+#pragma unroll
+        for (int j = 0; j < MLD / 2; ++j) {
+          float lo, hi;
+          f2unpack(acc[j], lo, hi);
+          acc[j] = 0ull;
+          if (2 * j < p.M) store_y(mt, n, 2 * j, lo);
+          if (2 * j + 1 < p.M) store_y(mt, n, 2 * j + 1, hi);
+        }
+        return true;
+      }
+      float* mine = const_cast<float*>(piece_of(c, t));
+#pragma unroll
+      for (int j = 0; j < MLD / 2; ++j) {
+        float lo, hi;
+        f2unpack(acc[j], lo, hi);
+        acc[j] = 0ull;
+        if (2 * j < p.M) __stcg(mine + (2 * j) * kTileN + r, lo);
+        if (2 * j + 1 < p.M) __stcg(mine + (2 * j + 1) * kTileN + r, hi);
+      }
+      __threadfence();
+      if (!drain_sync()) return false;
+      if (dt == 0) {  // a CTA is the first contributor of at most one cut tile: count it there
+        const int64_t c_lo = owner_of(tu0, U, P), c_hi = owner_of(tu1 - 1, U, P);
+        if (atomicAdd(p.tcount + c_lo, 1) == static_cast<int>(c_hi - c_lo)) ctl.deferred[ctl.ndeferred++] = t;
+      }
+      return true;
+    };
+
+    int i = 0;
+    for (int ui = 0; ui < nu && ok; ++ui) {
+      const int st = ui / kUS, j = ui - st * kUS, s = st % S;
+      const int64_t u = u0 + ui;
+      const int t = static_cast<int>(u / G), g = static_cast<int>(u - static_cast<int64_t>(t) * G);
+      const uint8_t* sg = stage(s);
+      const float* sx2 = reinterpret_cast<const float*>(sg + j * kArec + TN * 128);
+      const float* cc = sx2 + TN;
+      // the stage's bytes (activation scales, offset terms, row scales) were
+      // written by the bulk copy: wait on its barrier too (long complete)
+      if (j == 0 && !(ok = mbar_wait(&ctl.full[s], (st / S) & 1, abort_flag, tmo, p.err))) break;
+      const uint16_t* swp = reinterpret_cast<const uint16_t*>(sg + kAct + j * kWRecBytes + kWRecScales + 2 * r);
+      if (!(ok = drain_item(i++, sx2, cc, swp, true, ui, -1))) break;
+      const int e0 = ctl.map[ui][0], e1 = ctl.map[ui][1];
+      if (e0 >= 0 || e1 >= 0) {
+        const int e = half ? e1 : e0;
+        int slot = 0;
+        const uint16_t* srp = nullptr;
+        if (e >= 0) {
+          const int cpos = ctl.rpos[ui][half];
+          slot = cpos % kRS;
+          if (!(ok = mbar_wait(&ctl.r_full[slot], (cpos / kRS) & 1, abort_flag, tmo, p.err))) break;
+          srp = reinterpret_cast<const uint16_t*>(rring + slot * kRRecBytes + kRRecScales + 2 * (r & 63));
+        }
+        if (!(ok = drain_item(i++, sx2, cc, srp, e >= 0, ui, e))) break;
+        __syncwarp();
+        if (lane == 0 && e >= 0) mbar_arrive(&ctl.r_empty[slot]);
+      }
+      if (j == kUS - 1 || ui == nu - 1) {  // the stage's scales are read
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.empty[s]);
+      }
+      if (!kDebug && (g == G - 1 || ui == nu - 1) && !(ok = finish_tile(t))) break;
+    }
+
+    // Finish the tiles this CTA completed the count of: bring every piece
+    // into the (now idle) stage memory with bulk copies, sum in CTA order,
+    // store Y, and reset the tile's counter for the next launch.
+    if (!kDebug && ok && (ok = drain_sync())) {
+      const int nd = ctl.ndeferred;
+      const uint32_t piece_bytes = static_cast<uint32_t>(p.M) * kTileN * 4;  // rows 0..M-1 of a piece
+      const int per_round = max(1, static_cast<int>((static_cast<size_t>(S) * SB) / piece_bytes));
+      int nred = 0;
+      for (int di = 0; di < nd && ok; ++di) {
+        const int t = ctl.deferred[di];
+        const ZMat& mt = p.mat[mat_of_tile(p, t)];
+        const int64_t n = static_cast<int64_t>(t - mt.tile0) * kTileN + r;
+        const int64_t tu0 = static_cast<int64_t>(t) * G, tu1 = tu0 + G;
+        const int64_t c_lo = owner_of(tu0, U, P), c_hi = owner_of(tu1 - 1, U, P);
+        float sum[MLD];
+        for (int64_t cb = c_lo; cb <= c_hi && ok; cb += per_round) {
+          const int np = static_cast<int>(min(static_cast<int64_t>(per_round), c_hi - cb + 1));
+          if (dt == 0) {
+            __threadfence();
+            fence_proxy_async_global();  // other CTAs' generic writes -> this bulk (async) read
+            mbar_arrive_expect_tx(&ctl.red_bar, np * piece_bytes);
+            for (int k = 0; k < np; ++k) bulk_g2s(stages + k * piece_bytes, piece_of(cb + k, t), piece_bytes, &ctl.red_bar);
+          }
+          if (!(ok = mbar_wait(&ctl.red_bar, nred & 1, abort_flag, tmo, p.err))) break;
+          ++nred;
+          for (int k = 0; k < np; ++k) {
+            const float* pc = reinterpret_cast<const float*>(stages + k * piece_bytes) + r;
+#pragma unroll
+            for (int m = 0; m < MLD; ++m) {
+              if (m < p.M) {
+                const float v = pc[m * kTileN];
+                sum[m] = (cb == c_lo && k == 0) ? v : sum[m] + v;  // ascending CTA order
+              }
+            }
+          }
+          if (!(ok = drain_sync())) break;  // the stage memory is free for the next round
+        }
+        if (!ok) break;
+#pragma unroll
+        for (int m = 0; m < MLD; ++m)
+          if (m < p.M) store_y(mt, n, m, sum[m]);
+        if (dt == 0) p.tcount[c_lo] = 0;
+      }
+    }
+  }
+
+  // Every role is done.
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&ctl.exit_bar);
+  mbar_wait(&ctl.exit_bar, 0, abort_flag, tmo, p.err);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    ZT(5);
+    ZC(7);
+  }
+  if (*abort_flag) {
+    // A wait gave up: copies and MMAs may still be in flight; give them 200 us.
+    if (threadIdx.x == 0) {
+      const uint64_t t0 = globaltimer();
+      while (globaltimer() - t0 < 200000ull) {
+      }
+    }
+    __syncthreads();
+  }
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(ctl.tmem_base, kTmemCols);
+  }
+}
+
+
+// ---------------------------------------------------------------------------
+// The warp-MMA form (the default up to 32 tokens).
+//
+// Measured on GB300: a tcgen05.mma of M = 128, K = 32 costs the tensor pipe
+// about 46 cycles at any N up to 64, and passing items between warps through
+// mbarriers (unpack -> MMA issue -> drain) costs about 500 cycles per item even
+// with no work in it -- more than the ~430 SM-cycles of HBM time a 128 x 128
+// group of 4-bit weights is worth.  So here every warp carries its own rows
+// through a whole group with no hand-off: unpack its codes into registers, run
+// mma.sync m16n8k32 e4m3 against the activation fragments of the stage, and
+// scale the exact dots into its own fp32 accumulators.  Warps meet only once
+// per 4-unit stage (and at tile ends, to add their partials in a fixed order).
+//
+// Warps 0..15: four sets of four; set q takes unit q of every stage, warp w of
+// a set owns rows 32w..32w+31 (two 16-row MMA tiles).  Warp 16: producer;
+// warp 17: residual map and records.
+// ---------------------------------------------------------------------------
+
+// Units per stage (= sets of 4 compute warps): 4 up to 16 tokens; 3 at 32
+// tokens, whose accumulators need more registers per thread (the warps of a
+// block share each scheduler's register file).
+__host__ __device__ constexpr int w_sets(int tn) { return tn == 32 ? 3 : 4; }
+__host__ __device__ constexpr int w_threads(int tn) { return 32 * (4 * w_sets(tn) + 1); }
+constexpr int kWMaxSets = 4;
+
+struct __align__(8) WCtl {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];  // the compute warps are done with the stage
+  uint64_t r_full[kRS];
+  uint64_t r_empty[kRS];       // the 2 warps of the record's half
+  uint64_t chain[kWMaxSets][2];  // tile flush f (buffer f % 2): set q has added its partial
+  uint64_t red_free[2];        // the last set is done with buffer b
+  uint64_t piece_bar;          // the last set's 4 warps wrote their piece rows
+  uint64_t map_ready;
+  uint64_t fix_bar;            // all compute warps are past the main loop (stage memory idle)
+  uint64_t red_bar;            // stream-K pieces copied in for a deferred tile
+  uint64_t exit_bar;
+  int32_t map[kMaxUnits][2];
+  int32_t rpos[kMaxUnits][2];
+  int abort_flag;
+  int ndeferred;
+  int deferred[2];
+};
+
+// D(16x8, fp32) += A(16x32, E4M3, row-major) * B(32x8, E4M3, column-major).
+__device__ __forceinline__ void mma_e4m3(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// The same with a zero accumulator in (the first K-step of a group).
+__device__ __forceinline__ void mma_e4m3_z(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%10, %10, %10, %10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+// TN: tokens per tile (8, 16 or 32); kDebug: write raw group dots.
+template <int TN, bool kDebug>
+__global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZParams p) {
+  constexpr int NB = TN / 8;           // 8-token blocks of one MMA
+  constexpr int US = w_sets(TN);       // units per stage = sets of compute warps
+  constexpr int kWSets = US, kWCompute = 4 * US, kWProd = kWCompute, kWThreads = w_threads(TN);
+  constexpr int kArec = TN * 136;      // activation image: B fragments, then {2^9 sx, c} pairs
+  constexpr int kAct = US * kArec;     // a stage: US activation images, then US base records
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ WCtl ctl;
+  uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+  const int S = p.nstages, SB = p.stage_bytes, G = p.G;
+  uint8_t* stages = smem;
+  uint8_t* rring = smem + static_cast<size_t>(S) * SB;
+  float* red = reinterpret_cast<float*>(rring + kRS * kRRecBytes);  // [2][128 rows][TN]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t U = p.units, P = p.ctas, c = blockIdx.x;
+  const int64_t u0 = first_unit(c, U, P), u1 = first_unit(c + 1, U, P);
+  const int nu = static_cast<int>(u1 - u0);
+  const int nstg = (nu + US - 1) / US;
+  volatile int* abort_flag = &ctl.abort_flag;
+  const uint64_t tmo = p.timeout_ns;
+
+  if (warp == 0) {
+    for (int s = lane; s < S; s += 32) {
+      mbar_init(&ctl.full[s], 1);
+      mbar_init(&ctl.empty[s], kWCompute);
+    }
+    if (lane < kRS) {
+      mbar_init(&ctl.r_full[lane], 1);
+      mbar_init(&ctl.r_empty[lane], 2);
+    }
+    if (lane < 2 * kWSets) mbar_init(&ctl.chain[lane >> 1][lane & 1], 4);
+    if (lane == 8 || lane == 9) mbar_init(&ctl.red_free[lane - 8], 4);
+    if (lane == 10) mbar_init(&ctl.piece_bar, 4);
+    if (lane == 11) mbar_init(&ctl.map_ready, 1);
+    if (lane == 12) mbar_init(&ctl.fix_bar, kWCompute);
+    if (lane == 13) mbar_init(&ctl.red_bar, 1);
+    if (lane == 14) mbar_init(&ctl.exit_bar, kWThreads / 32);
+    if (lane == 15) ctl.abort_flag = 0;
+    if (lane == 16) ctl.ndeferred = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_trigger();
+  auto stage = [&](int s) { return stages + static_cast<size_t>(s) * SB; };
+  auto wrec = [&](int64_t u) -> const uint8_t* {
+    const int t = static_cast<int>(u / G), g = static_cast<int>(u - static_cast<int64_t>(t) * G);
+    const ZMat& mt = p.mat[mat_of_tile(p, t)];
+    return mt.wpk + (static_cast<int64_t>(t - mt.tile0) * G + g) * kWRecBytes;
+  };
+  auto mat_end = [&](int64_t u) -> int64_t {
+    const int mi = mat_of_tile(p, static_cast<int>(u / G));
+    return static_cast<int64_t>(mi + 1 < p.nmat ? p.mat[mi + 1].tile0 : p.tiles) * G;
+  };
+
+  if (warp == kWProd) {
+    // ---------------- producer: a stage = US units' base records and activation images, then the
+    // residual records of those units ----------------
+    auto stage_bytes = [&](int st) {
+      const int n = min(US, nu - st * US);
+      return static_cast<uint32_t>(n * (kWRecBytes + kArec));
+    };
+    auto issue_weights = [&](int st, int s) {
+      int64_t ua = u0 + st * US;
+      const int64_t ub = min(u1, ua + US), us = ua;
+      while (ua < ub) {
+        const int64_t e = min(ub, mat_end(ua));
+        bulk_g2s(stage(s) + kAct + (ua - us) * kWRecBytes, wrec(ua), static_cast<uint32_t>((e - ua) * kWRecBytes),
+                 &ctl.full[s]);
+        ua = e;
+      }
+    };
+    auto issue_act = [&](int st, int s) {
+      int64_t ua = u0 + st * US;
+      const int64_t ub = min(u1, ua + US), us = ua;
+      while (ua < ub) {
+        const int g = static_cast<int>(ua % G);
+        const int64_t n = min(ub - ua, static_cast<int64_t>(G - g));
+        bulk_g2s(stage(s) + (ua - us) * kArec, p.act + static_cast<int64_t>(g) * kArec,
+                 static_cast<uint32_t>(n * kArec), &ctl.full[s]);
+        ua += n;
+      }
+    };
+    const int pre = min(S, nstg);
+    // The first stages' base records, the block lists and the residual
+    // records are read before the dependency wait: the kernels that may run
+    // ahead of it (this library's, which ask for the next launch early) never
+    // write packed weights or block lists.
+    if (lane == 0) {
+      for (int st = 0; st < pre; ++st) {
+        mbar_arrive_expect_tx(&ctl.full[st], stage_bytes(st));
+        issue_weights(st, st);
+      }
+    }
+    // residual map of the CTA's units and the records' ring positions
+    for (int i = lane; i < nu * 2; i += 32) (&ctl.map[0][0])[i] = -1;
+    __syncwarp();
+    if (nu > 0) {
+      const int t_lo = static_cast<int>(u0 / G), t_hi = static_cast<int>((u1 - 1) / G);
+      for (int t = t_lo; t <= t_hi; ++t) {
+        const ZMat& mt = p.mat[mat_of_tile(p, t)];
+        if (mt.nnzb == 0) continue;
+        const int64_t br = 2 * static_cast<int64_t>(t - mt.tile0);
+        const int a0 = max(0, min(mt.nnzb, mt.row_ptr[br]));
+        const int a1 = max(a0, min(mt.nnzb, mt.row_ptr[br + 1]));
+        const int a2 = max(a1, min(mt.nnzb, mt.row_ptr[br + 2]));
+        for (int e = a0 + lane; e < a2; e += 32) {
+          const int g = mt.col_idx[e];
+          if (g < 0 || g >= G) continue;
+          const int64_t u = static_cast<int64_t>(t) * G + g;
+          if (u >= u0 && u < u1) ctl.map[u - u0][e >= a1 ? 1 : 0] = e;
+        }
+      }
+    }
+    __syncwarp();
+    {
+      const int nf = nu * 2;
+      const int chunk = (nf + 31) / 32, f0 = min(nf, lane * chunk), f1 = min(nf, f0 + chunk);
+      int cnt = 0;
+      for (int f = f0; f < f1; ++f) cnt += (&ctl.map[0][0])[f] >= 0;
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int pos = incl - cnt;
+      for (int f = f0; f < f1; ++f)
+        if ((&ctl.map[0][0])[f] >= 0) (&ctl.rpos[0][0])[f] = pos++;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl.map_ready);
+    pdl_wait();  // the activation images are the preceding kernel's output
+    if (lane == 0) {
+      bool ok = true;
+      for (int st = 0; ok && st < nstg; ++st) {
+        const int s = st % S;
+        if (st >= S) {
+          if (!(ok = mbar_wait_sleep(&ctl.empty[s], ((st / S) - 1) & 1, abort_flag, tmo, p.err))) break;
+          mbar_arrive_expect_tx(&ctl.full[s], stage_bytes(st));
+          issue_weights(st, s);
+        }
+        issue_act(st, s);
+        for (int f = 2 * st * US; ok && f < min(2 * nu, 2 * (st + 1) * US); ++f) {
+          const int e = (&ctl.map[0][0])[f];
+          if (e < 0) continue;
+          const int cpos = (&ctl.rpos[0][0])[f], slot = cpos % kRS;
+          if (cpos >= kRS && !(ok = mbar_wait_sleep(&ctl.r_empty[slot], ((cpos / kRS) - 1) & 1, abort_flag, tmo, p.err)))
+            break;
+          const ZMat& mt = p.mat[mat_of_tile(p, static_cast<int>((u0 + f / 2) / G))];
+          mbar_arrive_expect_tx(&ctl.r_full[slot], kRRecBytes);
+          bulk_g2s(rring + slot * kRRecBytes, mt.rpk + static_cast<int64_t>(e) * kRRecBytes, kRRecBytes,
+                   &ctl.r_full[slot]);
+        }
+      }
+    }
+  } else {
+    // ---------------- compute warps ----------------
+    const int q = warp >> 2, wq = warp & 3;      // set, row quarter
+    const int g = lane >> 2, t = lane & 3;       // MMA fragment coordinates
+    const int rw = 32 * wq, half = wq >> 1;      // first row of this warp, its residual half
+    bool ok = mbar_wait(&ctl.map_ready, 0, abort_flag, tmo, p.err);
+    pdl_wait();  // Y and the workspace pieces may still be in use by the preceding kernel
+    // accumulators: [mt][nb] pairs {row r, tokens 8nb+2t, +1}, {row r+8, same tokens}
+    uint64_t acc[2][NB][2];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) acc[mt][nb][0] = acc[mt][nb][1] = 0ull;
+
+    // One group's product for this warp's rows: codes (K-steps jstride apart,
+    // 16 bytes per row, first row row0), fragments and scale pairs of the
+    // group's activation image, row scales sc; into acc, or the test hook's dots.
+    auto group_product = [&](const uint8_t* codes, int jstride, int row0, const uint16_t* sc, const uint8_t* img,
+                             int64_t u, int e) {
+      float d[2][NB][4];
+      const uint8_t* wr = codes + (row0 + g) * 16 + t * 4;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t a[2][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(wr + j * jstride + mt * 256);        // row +0
+          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(wr + j * jstride + mt * 256 + 128);  // row +8
+          unpack_u4(w0, a[mt][0], a[mt][2]);
+          unpack_u4(w1, a[mt][1], a[mt][3]);
+        }
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          const uint2 b = *reinterpret_cast<const uint2*>(img + ((j * NB + nb) * 32 + lane) * 8);
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            if (j == 0)
+              mma_e4m3_z(d[mt][nb], a[mt], b.x, b.y);
+            else
+              mma_e4m3(d[mt][nb], a[mt], b.x, b.y);
+          }
+        }
+      }
+      const float4* sg = reinterpret_cast<const float4*>(img + TN * 128) + t;  // token pairs 2t, 2t+1 of block nb
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const float s0 = __half2float(__ushort_as_half(sc[row0 + 16 * mt + g]));
+        const float s1 = __half2float(__ushort_as_half(sc[row0 + 16 * mt + 8 + g]));
+        const uint64_t s20 = f2pack(s0, s0), s21 = f2pack(s1, s1), m1 = f2pack(-1.0f, -1.0f);
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          const float4 f = sg[4 * nb];  // 2^9 sx (tokens 8nb+2t, +1), c (same tokens)
+          if constexpr (kDebug) {
+            const int tile = static_cast<int>(u / G), gg = static_cast<int>(u % G);
+            const float ev[2][2] = {{d[mt][nb][0] - f.z, d[mt][nb][1] - f.w}, {d[mt][nb][2] - f.z, d[mt][nb][3] - f.w}};
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int cc = 0; cc < 2; ++cc) {
+                const int m = 8 * nb + 2 * t + cc, r = rw + 16 * mt + 8 * h + g;
+                if (m < p.M) {
+                  const int32_t dv = static_cast<int32_t>(ev[h][cc] * 512.0f);
+                  if (e < 0)
+                    p.dots_w[(static_cast<int64_t>(m) * (p.tiles * kTileN) + static_cast<int64_t>(tile) * kTileN + r) * G +
+                             gg] = dv;
+                  else
+                    p.dots_r[(static_cast<int64_t>(m) * p.mat[0].nnzb + e) * 64 + (r & 63)] = dv;
+                }
+              }
+          } else {
+            const uint64_t sx2 = f2pack(f.x, f.y), c2 = f2pack(f.z, f.w);
+            const uint64_t e0 = f2fma(c2, m1, f2pack(d[mt][nb][0], d[mt][nb][1]));  // row +0: exact 2^-9 D
+            const uint64_t e1 = f2fma(c2, m1, f2pack(d[mt][nb][2], d[mt][nb][3]));  // row +8
+            acc[mt][nb][0] = f2fma(sx2, f2mul(s20, e0), acc[mt][nb][0]);
+            acc[mt][nb][1] = f2fma(sx2, f2mul(s21, e1), acc[mt][nb][1]);
+          }
+        }
+      }
+    };
+    auto store_y = [&](const ZMat& mt, int64_t n, int m, float v) {
+      const int64_t o = static_cast<int64_t>(m) * mt.ldy + n;
+      if (p.y_f32)
+        static_cast<float*>(mt.y)[o] = v;
+      else
+        static_cast<__nv_bfloat16*>(mt.y)[o] = __float2bfloat16_rn(v);
+    };
+    auto piece_of = [&](int64_t cc, int tile) -> float* {  // CTA cc's piece of the tile: [TN][128]
+      const int wc = (tile == static_cast<int>(first_unit(cc, U, P) / G)) ? 0 : 1;
+      return p.part + ((cc * 2 + wc) * TN) * static_cast<int64_t>(kTileN);
+    };
+    // End of tile `tile` (the f-th tile of this CTA): the sets add their
+    // partials into red[f % 2] in set order; the last set stores Y (whole
+    // tile) or writes this CTA's stream-K piece and counts it in.
+    int npiece = 0;  // pieces this CTA has written (phases of piece_bar)
+    auto flush = [&](int tile, int f) -> bool {
+      const int bsel = f & 1;
+      float* rb = red + bsel * (kTileN * TN);
+      bool pass = true;
+      if (q == 0)
+        pass = f < 2 || mbar_wait(&ctl.red_free[bsel], ((f >> 1) - 1) & 1, abort_flag, tmo, p.err);
+      else
+        pass = mbar_wait(&ctl.chain[q - 1][bsel], (f >> 1) & 1, abort_flag, tmo, p.err);
+      if (!pass) return false;
+      const bool last = q == kWSets - 1;
+      const ZMat& mt = p.mat[mat_of_tile(p, tile)];
+      const int64_t nbase = static_cast<int64_t>(tile - mt.tile0) * kTileN;
+      const int64_t tu0 = static_cast<int64_t>(tile) * G, tu1 = tu0 + G;
+      const bool whole = tu0 >= u0 && tu1 <= u1;
+      float* piece = whole || !last ? nullptr : piece_of(c, tile);
+#pragma unroll
+      for (int mt2 = 0; mt2 < 2; ++mt2)
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int r = rw + 16 * mt2 + 8 * h + g, m0 = 8 * nb + 2 * t;
+            float2* slot = reinterpret_cast<float2*>(rb + r * TN + m0);
+            float2 v;
+            f2unpack(acc[mt2][nb][h], v.x, v.y);
+            acc[mt2][nb][h] = 0ull;
+            if (q != 0) {
+              const float2 o = *slot;
+              v = make_float2(o.x + v.x, o.y + v.y);  // ascending set order
+            }
+            if (!last) {
+              *slot = v;
+            } else if (whole) {
+              if (m0 < p.M) store_y(mt, nbase + r, m0, v.x);
+              if (m0 + 1 < p.M) store_y(mt, nbase + r, m0 + 1, v.y);
+            } else {
+              if (m0 < p.M) __stcg(piece + m0 * kTileN + r, v.x);
+              if (m0 + 1 < p.M) __stcg(piece + (m0 + 1) * kTileN + r, v.y);
+            }
+          }
+      __syncwarp();
+      if (!last) {
+        if (lane == 0) mbar_arrive(&ctl.chain[q][bsel]);
+        return true;
+      }
+      if (lane == 0) mbar_arrive(&ctl.red_free[bsel]);  // this warp's reads of the buffer are done
+      if (!whole) {
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.piece_bar);
+        // a barrier of the last set's 4 warps: the piece is complete
+        if (!mbar_wait(&ctl.piece_bar, npiece++ & 1, abort_flag, tmo, p.err)) return false;
+        if (wq == 0 && lane == 0) {  // count it in
+          const int64_t c_lo = owner_of(tu0, U, P), c_hi = owner_of(tu1 - 1, U, P);
+          if (atomicAdd(p.tcount + c_lo, 1) == static_cast<int>(c_hi - c_lo)) {
+            const int nd = ctl.ndeferred;  // only this thread writes the list
+            ctl.deferred[nd] = tile;
+            ctl.ndeferred = nd + 1;
+          }
+        }
+      }
+      return true;
+    };
+
+    // the sets walk the CTA's units tile by tile; set q takes the units ui = q (mod US)
+    int f = 0;
+    const int t_lo = nu > 0 ? static_cast<int>(u0 / G) : 0, t_hi = nu > 0 ? static_cast<int>((u1 - 1) / G) : -1;
+    for (int tile = t_lo; ok && tile <= t_hi; ++tile, ++f) {
+      const int64_t ua = max(u0, static_cast<int64_t>(tile) * G), ub = min(u1, static_cast<int64_t>(tile + 1) * G);
+      int ui = static_cast<int>(ua - u0);
+      ui += (q - ui % US + US) % US;  // this set's first unit in the tile
+      for (; ok && ui < static_cast<int>(ub - u0); ui += US) {
+        const int st = ui / US, s = st % S;
+        if (!(ok = mbar_wait(&ctl.full[s], (st / S) & 1, abort_flag, tmo, p.err))) break;
+        const uint8_t* sg = stage(s);
+        const uint8_t* img = sg + q * kArec;
+        const uint8_t* rec = sg + kAct + q * kWRecBytes;
+        group_product(rec, 2048, rw, reinterpret_cast<const uint16_t*>(rec + kWRecScales), img, u0 + ui, -1);
+        const int e = ctl.map[ui][half];
+        if (e >= 0) {  // the residual block of this warp's half
+          const int cpos = ctl.rpos[ui][half], slot = cpos % kRS;
+          if (!(ok = mbar_wait(&ctl.r_full[slot], (cpos / kRS) & 1, abort_flag, tmo, p.err))) break;
+          const uint8_t* rrec = rring + slot * kRRecBytes;
+          group_product(rrec, 1024, rw - 64 * half, reinterpret_cast<const uint16_t*>(rrec + kRRecScales), img,
+                        u0 + ui, e);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl.r_empty[slot]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.empty[s]);  // this warp is done with the stage
+      }
+      if (ok && !kDebug) ok = flush(tile, f);
+    }
+
+    // Finish the tiles whose count this CTA completed: once every compute
+    // warp is past its main loop the stage memory is idle; the last set brings
+    // every piece into it with bulk copies, sums in CTA order, stores Y and
+    // resets the tile's counter for the next launch.
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl.fix_bar);
+    if (!kDebug && ok && q == kWSets - 1 && (ok = mbar_wait(&ctl.fix_bar, 0, abort_flag, tmo, p.err))) {
+      const int r = rw + lane;
+      const int nd = ctl.ndeferred;
+      const uint32_t piece_bytes = static_cast<uint32_t>(p.M) * kTileN * 4;  // rows 0..M-1 of a piece
+      const int per_round = max(1, static_cast<int>((static_cast<size_t>(S) * SB) / piece_bytes));
+      int nred = 0, nfin = 0;
+      for (int di = 0; di < nd && ok; ++di) {
+        const int tile = ctl.deferred[di];
+        const ZMat& mt = p.mat[mat_of_tile(p, tile)];
+        const int64_t n = static_cast<int64_t>(tile - mt.tile0) * kTileN + r;
+        const int64_t tu0 = static_cast<int64_t>(tile) * G, tu1 = tu0 + G;
+        const int64_t c_lo = owner_of(tu0, U, P), c_hi = owner_of(tu1 - 1, U, P);
+        float sum[TN];
+        for (int64_t cb = c_lo; cb <= c_hi && ok; cb += per_round) {
+          const int np = static_cast<int>(min(static_cast<int64_t>(per_round), c_hi - cb + 1));
+          if (wq == 0 && lane == 0) {
+            __threadfence();
+            fence_proxy_async_global();  // other CTAs' generic writes -> this bulk (async) read
+            mbar_arrive_expect_tx(&ctl.red_bar, np * piece_bytes);
+            for (int k = 0; k < np; ++k) bulk_g2s(stages + k * piece_bytes, piece_of(cb + k, tile), piece_bytes, &ctl.red_bar);
+          }
+          if (!(ok = mbar_wait(&ctl.red_bar, nred & 1, abort_flag, tmo, p.err))) break;
+          ++nred;
+          for (int k = 0; k < np; ++k) {
+            const float* pc = reinterpret_cast<const float*>(stages + k * piece_bytes) + r;
+#pragma unroll
+            for (int m = 0; m < TN; ++m) {
+              if (m < p.M) {
+                const float v = pc[m * kTileN];
+                sum[m] = (cb == c_lo && k == 0) ? v : sum[m] + v;  // ascending CTA order
+              }
+            }
+          }
+          // the stage memory is free for the next round once all 4 warps read it
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl.piece_bar);
+          if (!(ok = mbar_wait(&ctl.piece_bar, (npiece + nfin++) & 1, abort_flag, tmo, p.err))) break;
+        }
+        if (!ok) break;
+#pragma unroll
+        for (int m = 0; m < TN; ++m)
+          if (m < p.M) store_y(mt, n, m, sum[m]);
+        if (wq == 0 && lane == 0) p.tcount[c_lo] = 0;
+      }
+    }
+  }
+
+  // Every role is done.
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&ctl.exit_bar);
+  mbar_wait(&ctl.exit_bar, 0, abort_flag, tmo, p.err);
+  __syncthreads();
+  if (*abort_flag) {
+    // A wait gave up: copies may still be in flight; give them 200 us.
+    if (threadIdx.x == 0) {
+      const uint64_t t0 = globaltimer();
+      while (globaltimer() - t0 < 200000ull) {
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// The activation images of one launch, written to the workspace for the GEMM
+// to bulk-copy: for group g, the MMA's B operand (the integer codes as E4M3
+// bytes in the 128-byte-swizzled, K-major tile, K permuted inside each 8-code
+// word like the weight unpack), 2^9 sx and the offset terms 2^-9 * 8 * sum_k qx.
+// From packed codes (xq, xs), or straight from X (kQuant: quantized here with
+// mq_quantize_act's rule and bits; xq / xs written too when asked).  One CTA of
+// 256 threads per group.
+struct ImgParams {
+  const uint8_t* xq;
+  const uint16_t* xs;
+  const uint16_t* x;
+  int64_t ldx;
+  int x_bf16;
+  uint8_t* xq_out;
+  uint16_t* xs_out;
+  int M, Mp;
+  uint8_t* act;
+};
+
+// kFrag: the warp-MMA form's layout (per K-step j and 8-token block nb, lane
+// 4g + t holds token 8nb + g: the even codes 8t, 8t+2, .., 8t+6 of the K-step,
+// then the odd ones; then {2^9 sx, 2^9 sx', c, c'} per token pair); else the
+// tensor-memory form's swizzled tile (then 2^9 sx [TN], c [TN], padding).
+template <int TN, bool kQuant, bool kFrag>
+__global__ void __launch_bounds__(256) act_image_kernel(const ImgParams p) {
+  constexpr int kArec = kFrag ? TN * 136 : act_rec_bytes(TN);
+  constexpr int NB = TN / 8;
+  // byte offset of codes 8w..8w+7 (word w of 16) of token m, and of its two scale values
+  auto word_off = [](int m, int w) {
+    return kFrag ? ((((w >> 2) * NB + (m >> 3)) * 32 + 4 * (m & 7) + (w & 3)) * 8) : act_word_offset(m, w);
+  };
+  auto sx_idx = [](int m) { return kFrag ? (m >> 1) * 4 + (m & 1) : m; };
+  auto c_idx = [](int m) { return kFrag ? (m >> 1) * 4 + 2 + (m & 1) : TN + m; };
+  pdl_trigger();
+  // the inputs are the preceding kernel's output, and the previous GEMM may
+  // still be reading the images this overwrites
+  pdl_wait();
+  const int64_t g = blockIdx.x;
+  const int ct = threadIdx.x;
+  uint8_t* rec = p.act + g * kArec;
+  float* sco = reinterpret_cast<float*>(rec + TN * 128);
+  if constexpr (!kQuant) {
+    // from packed codes: item = (token m, word t), 16 words per token
+    for (int idx = ct; idx < TN * 16; idx += 256) {
+      const int m = idx >> 4, t = idx & 15;
+      const uint32_t wv = m < p.Mp ? *reinterpret_cast<const uint32_t*>(p.xq + (g * p.Mp + m) * 64 + t * 4) : 0u;
+      uint32_t lo, hi;
+      int4x8_to_e4m3(wv, lo, hi);
+      *reinterpret_cast<uint2*>(rec + word_off(m, t)) = make_uint2(prmt(lo, hi, 0x6420u), prmt(lo, hi, 0x7531u));
+      int sum = nibble_sum8(wv);
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+      if (t == 0) {
+        sco[sx_idx(m)] = m < p.Mp ? 512.0f * __half2float(__ushort_as_half(p.xs[g * p.Mp + m])) : 0.0f;
+        sco[c_idx(m)] = static_cast<float>(sum) * (1.0f / 64.0f);
+      }
+    }
+  } else {
+    // from X: threads of one token: 16 (TN <= 16) or 8 (TN = 32), each on 128 / that inputs
+    // (whole 8-code words); threads past the tile's tokens have nothing to do
+    constexpr int kTpt = TN == 32 ? 8 : 16, kEpt = 128 / kTpt, kWpt = kEpt / 8;
+    static_assert(kWpt >= 1 && kTpt * TN <= 256, "quantizer thread mapping");
+    const int m = ct / kTpt, part = ct % kTpt;
+    if (m >= TN) return;
+    float v[kEpt];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kEpt; ++i) {
+      v[i] = m < p.M ? act_value(p.x, static_cast<int64_t>(m) * p.ldx + g * kGroup + part * kEpt + i, p.x_bf16) : 0.0f;
+      amax = fmaxf(amax, fabsf(v[i]));
+    }
+#pragma unroll
+    for (int o = 1; o < kTpt; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const uint16_t sb = m < p.M ? act_scale_bits(amax) : static_cast<uint16_t>(0);
+    const float sf = __half2float(__ushort_as_half(sb));
+    int sum = 0;
+#pragma unroll
+    for (int w = 0; w < kWpt; ++w) {
+      uint32_t ev = 0, od = 0, pk = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int qv = act_code(v[w * 8 + e], sf);
+        sum += qv;
+        pk |= (static_cast<uint32_t>(qv) & 0xFu) << (4 * e);
+        const uint32_t byte = e4m3_of_code(qv);
+        if (e & 1)
+          od |= byte << (8 * (e >> 1));
+        else
+          ev |= byte << (8 * (e >> 1));
+      }
+      const int t = part * kWpt + w;  // word of the token's 16
+      *reinterpret_cast<uint2*>(rec + word_off(m, t)) = make_uint2(ev, od);
+      if (p.xq_out && m < p.Mp) *reinterpret_cast<uint32_t*>(p.xq_out + (g * p.Mp + m) * 64 + t * 4) = pk;
+    }
+#pragma unroll
+    for (int o = 1; o < kTpt; o <<= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+    if (part == 0) {
+      sco[sx_idx(m)] = 512.0f * sf;
+      sco[c_idx(m)] = static_cast<float>(sum) * (1.0f / 64.0f);
+      if (p.xs_out && m < p.Mp) p.xs_out[g * p.Mp + m] = sb;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+size_t a256(size_t b) { return (b + 255) / 256 * 256; }
+
+int sm_count_current() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
+struct ZPlan {
+  bool tc;  // the tensor-memory form (else warp-MMA)
+  int tn, mld, ctas, nstages, stage_bytes, smem, arec;
+  int64_t units;
+  size_t o_act, o_part, bytes;  // workspace layout after the zeroed prefix
+};
+
+// The tensor-memory form when MQ_DECODE_VARIANT = "tc" (benchmarks and tests), else the warp-MMA form.
+bool use_tc_variant() {
+  const char* v = getenv("MQ_DECODE_VARIANT");
+  return v && strcmp(v, "tc") == 0;
+}
+
+// Plan for M tokens over `tiles` 128-row tiles of K inputs; false if the
+// decode kernel does not cover the shape.
+bool zplan(int64_t M, int64_t tiles, int64_t K, ZPlan* out) {
+  if (M < 1 || M > 32) return false;
+  ZPlan pl;
+  pl.tc = use_tc_variant();
+  pl.tn = pl.tc ? (M <= 16 ? 16 : 32) : (M <= 8 ? 8 : M <= 16 ? 16 : 32);
+  pl.mld = M <= 4 ? 4 : M <= 8 ? 8 : M <= 16 ? 16 : 32;
+  const int64_t G = K / kGroup;
+  pl.units = tiles * G;
+  const int sms = sm_count_current();
+  if (sms <= 0 || sms > kWsZeroBytes / 4) return false;
+  pl.ctas = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms, pl.units / kMinUnits)));
+  if ((pl.units + pl.ctas - 1) / pl.ctas > kMaxUnits) return false;
+  int ctl_bytes, fixed;
+  if (pl.tc) {
+    pl.arec = act_rec_bytes(pl.tn);
+    pl.stage_bytes = kUS * (pl.arec + kWRecBytes);  // a multiple of 1024
+    ctl_bytes = (static_cast<int>(sizeof(ZCtl)) + 127) / 128 * 128;
+    fixed = 1024 + kRS * kRRecBytes;
+  } else {
+    pl.arec = pl.tn * 136;
+    pl.stage_bytes = (w_sets(pl.tn) * (pl.arec + kWRecBytes) + 127) / 128 * 128;
+    ctl_bytes = (static_cast<int>(sizeof(WCtl)) + 127) / 128 * 128;
+    fixed = 128 + kRS * kRRecBytes + 2 * kTileN * pl.tn * 4;  // alignment, residual ring, tile-sum buffers
+  }
+  pl.nstages = std::min(kMaxStages, (kSmemLimit - ctl_bytes - fixed) / pl.stage_bytes);
+  if (pl.nstages < 2) return false;
+  pl.smem = pl.nstages * pl.stage_bytes + fixed;
+  // workspace: the zeroed prefix (tile counters [ctas]), the activation
+  // images, the stream-K pieces
+  pl.o_act = kWsZeroBytes;
+  pl.o_part = pl.o_act + a256(static_cast<size_t>(G) * pl.arec);
+  pl.bytes = pl.o_part + a256(static_cast<size_t>(pl.ctas) * 2 * pl.tn * kTileN * sizeof(float));
+  *out = pl;
+  return true;
+}
+
+template <int TN, int MLD, bool kDebug>
+mq_status zlaunch(const ZParams& zp, const ZPlan& pl, cudaStream_t stream) {
+  auto kern = zipper_decode_kernel<TN, MLD, kDebug>;
+  static std::mutex mu;
+  static bool attr_set[64];  // per device, per instantiation
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return launch_status("zipper: device");
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (!attr_set[dev]) {
+      // static shared memory (the control block) and dynamic together stay within the per-block limit
+      const int ctl_bytes = (static_cast<int>(sizeof(ZCtl)) + 127) / 128 * 128;
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit - ctl_bytes) != cudaSuccess)
+        return launch_status("zipper: smem attribute");
+      attr_set[dev] = true;
+    }
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(pl.ctas), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, zp) != cudaSuccess) return launch_status("zipper launch");
+  return launch_status("zipper");
+}
+
+template <bool kDebug>
+mq_status zdispatch(const ZParams& zp, const ZPlan& pl, cudaStream_t stream) {
+  switch (pl.mld) {
+    case 4: return zlaunch<16, 4, kDebug>(zp, pl, stream);
+    case 8: return zlaunch<16, 8, kDebug>(zp, pl, stream);
+    case 16: return zlaunch<16, 16, kDebug>(zp, pl, stream);
+    default: return zlaunch<32, 32, kDebug>(zp, pl, stream);
+  }
+}
+
+template <int TN, bool kDebug>
+mq_status wlaunch(const ZParams& zp, const ZPlan& pl, cudaStream_t stream) {
+  auto kern = zipper_warp_kernel<TN, kDebug>;
+  static std::mutex mu;
+  static bool attr_set[64];  // per device, per instantiation
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return launch_status("zipper: device");
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (!attr_set[dev]) {
+      const int ctl_bytes = (static_cast<int>(sizeof(WCtl)) + 127) / 128 * 128;
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit - ctl_bytes) != cudaSuccess)
+        return launch_status("zipper: smem attribute");
+      attr_set[dev] = true;
+    }
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(pl.ctas), 1, 1);
+  cfg.blockDim = dim3(w_threads(TN), 1, 1);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, zp) != cudaSuccess) return launch_status("zipper launch");
+  return launch_status("zipper");
+}
+
+template <bool kDebug>
+mq_status wdispatch(const ZParams& zp, const ZPlan& pl, cudaStream_t stream) {
+  switch (pl.tn) {
+    case 8: return wlaunch<8, kDebug>(zp, pl, stream);
+    case 16: return wlaunch<16, kDebug>(zp, pl, stream);
+    default: return wlaunch<32, kDebug>(zp, pl, stream);
+  }
+}
+
+template <int TN, bool kQuant, bool kFrag>
+mq_status image_launch(const ImgParams& ip, int G, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(G), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, act_image_kernel<TN, kQuant, kFrag>, ip) != cudaSuccess) return launch_status("image launch");
+  return launch_status("image");
+}
+
+}  // namespace
+
+// Workspace bytes of the decode kernel for M tokens over `tiles` tiles of K
+// inputs on the current device, or 0 when it does not cover the shape.
+size_t zipper_workspace_bytes(int64_t M, int64_t tiles, int64_t K) {
+  ZPlan pl;
+  return zplan(M, tiles, K, &pl) ? pl.bytes : 0;
+}
+
+// Plan summary for mq_gemm_plan: {form (3 tensor-memory, 4 warp-MMA), tokens per tile, CTAs, stages}.
+bool zipper_plan_info(int64_t M, int64_t tiles, int64_t K, int32_t* form, int32_t* tn, int32_t* ctas, int32_t* stages) {
+  ZPlan pl;
+  if (!zplan(M, tiles, K, &pl)) return false;
+  *form = pl.tc ? 3 : 4;
+  *tn = pl.tn;
+  *ctas = pl.ctas;
+  *stages = pl.nstages;
+  return true;
+}
+
+// One launch of the decode kernel over `nmat` matrices that share the
+// activations: from packed activations (xq, xs) or, when x is given, from X
+// (quantized in the prologue; xq_out / xs_out optional).  `handled` is false
+// when the shape is not covered (the caller runs the general kernel).
+mq_status zipper_launch(bool* handled, int nmat, const uint8_t* const* wpk, const int64_t* N,
+                        const int32_t* const* row_ptr, const int32_t* const* col_idx, const int64_t* nnzb,
+                        const uint8_t* const* rpk, void* const* y, const int64_t* ldy, mq_dtype yt, const uint8_t* xq,
+                        const uint16_t* xs, const void* x, mq_dtype xt, int64_t ldx, uint8_t* xq_out,
+                        uint16_t* xs_out, int64_t M, int64_t K, int32_t* dots_w, int32_t* dots_r, void* ws,
+                        size_t ws_bytes, cudaStream_t stream) {
+  *handled = false;
+  if (nmat < 1 || nmat > kMaxMats) return set_error(MQ_ERR_INVALID_ARG, "zipper: 1 to %d matrices", kMaxMats);
+  int64_t tiles = 0;
+  for (int i = 0; i < nmat; ++i) tiles += N[i] / kTileN;
+  ZPlan pl;
+  if (!zplan(M, tiles, K, &pl)) return MQ_OK;
+  *handled = true;
+  if (ws == nullptr || ws_bytes < pl.bytes || !aligned(ws, 256))
+    return set_error(MQ_ERR_WORKSPACE, "gemm: workspace of %zu bytes (256-aligned) needed, %zu given", pl.bytes,
+                     ws_bytes);
+  ZParams zp = {};
+  int64_t t0 = 0;
+  for (int i = 0; i < nmat; ++i) {
+    zp.mat[i].wpk = wpk[i];
+    zp.mat[i].row_ptr = row_ptr[i];
+    zp.mat[i].col_idx = col_idx[i];
+    zp.mat[i].rpk = rpk[i];
+    zp.mat[i].y = y ? y[i] : nullptr;
+    zp.mat[i].ldy = ldy ? ldy[i] : N[i];
+    zp.mat[i].tile0 = static_cast<int>(t0);
+    zp.mat[i].nnzb = static_cast<int>(nnzb[i]);
+    t0 += N[i] / kTileN;
+  }
+  zp.nmat = nmat;
+  zp.xq = xq;
+  zp.xs = xs;
+  zp.x = static_cast<const uint16_t*>(x);
+  zp.ldx = ldx;
+  zp.x_bf16 = xt == MQ_BF16;
+  zp.xq_out = xq_out;
+  zp.xs_out = xs_out;
+  zp.M = static_cast<int>(M);
+  zp.Mp = static_cast<int>((M + 7) / 8 * 8);
+  zp.G = static_cast<int>(K / kGroup);
+  zp.tiles = static_cast<int>(tiles);
+  zp.ctas = pl.ctas;
+  zp.nstages = pl.nstages;
+  zp.stage_bytes = pl.stage_bytes;
+  zp.units = pl.units;
+  zp.y_f32 = yt == MQ_F32;
+  zp.dots_w = dots_w;
+  zp.dots_r = dots_r;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  zp.act = w + pl.o_act;
+  zp.tcount = reinterpret_cast<int32_t*>(w);
+  zp.part = reinterpret_cast<float*>(w + pl.o_part);
+  ImgParams ip;
+  ip.xq = xq;
+  ip.xs = xs;
+  ip.x = static_cast<const uint16_t*>(x);
+  ip.ldx = ldx;
+  ip.x_bf16 = xt == MQ_BF16;
+  ip.xq_out = xq_out;
+  ip.xs_out = xs_out;
+  ip.M = zp.M;
+  ip.Mp = zp.Mp;
+  ip.act = w + pl.o_act;
+  zp.timeout_ns = wait_timeout_ns();
+  zp.err = device_error_word();
+  if (!zp.err) return set_error(MQ_ERR_CUDA, "zipper: device error word unavailable");
+  const bool quant = x != nullptr;
+  mq_status st;
+  if (pl.tc)
+    st = pl.tn == 16 ? (quant ? image_launch<16, true, false>(ip, zp.G, stream) : image_launch<16, false, false>(ip, zp.G, stream))
+                     : (quant ? image_launch<32, true, false>(ip, zp.G, stream) : image_launch<32, false, false>(ip, zp.G, stream));
+  else if (pl.tn == 8)
+    st = quant ? image_launch<8, true, true>(ip, zp.G, stream) : image_launch<8, false, true>(ip, zp.G, stream);
+  else if (pl.tn == 16)
+    st = quant ? image_launch<16, true, true>(ip, zp.G, stream) : image_launch<16, false, true>(ip, zp.G, stream);
+  else
+    st = quant ? image_launch<32, true, true>(ip, zp.G, stream) : image_launch<32, false, true>(ip, zp.G, stream);
+  if (st != MQ_OK) return st;
+  if (pl.tc) return dots_w ? zdispatch<true>(zp, pl, stream) : zdispatch<false>(zp, pl, stream);
+  return dots_w ? wdispatch<true>(zp, pl, stream) : wdispatch<false>(zp, pl, stream);
+}
+
+}  // namespace mq

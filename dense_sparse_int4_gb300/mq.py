@@ -24,7 +24,7 @@ RREC_BYTES, RREC_SCALES = 4224, 4096  # residual record: 64x128 codes, then 64 f
 EXPORTS = (
     "mq_quantize_act", "mq_num_selected", "mq_select_workspace_bytes", "mq_select_blocks",
     "mq_pack_weights", "mq_gemm_workspace_bytes", "mq_gemm_workspace_init", "mq_w4a4_residual_gemm",
-    "mq_w4a4_residual_gemm_noalloc", "mq_gemm_plan",
+    "mq_w4a4_residual_gemm_noalloc", "mq_gemm_plan", "mq_linear_workspace_bytes", "mq_w4a4_residual_linear",
     "mq_debug_group_dots", "mq_check_device_error", "mq_set_wait_timeout_ns", "mq_debug_wait_timeout",
     "mq_status_string", "mq_last_error", "mq_version",
 )
@@ -59,6 +59,8 @@ def lib() -> ctypes.CDLL:
             "mq_w4a4_residual_gemm_noalloc": (i32, [P, P, i64, P, i64, i64, P, P, i64, P, P, i32, P]),
             "mq_debug_group_dots": (i32, [P, P, i64, P, i64, i64, P, P, i64, P, P, P, P, sz, P]),
             "mq_gemm_plan": (i32, [i64, i64, i64, P]),
+            "mq_linear_workspace_bytes": (sz, [i64, i64, i32, P]),
+            "mq_w4a4_residual_linear": (i32, [P, i32, i64, i64, i64, i32, P, i32, P, P, P, sz, P]),
             "mq_check_device_error": (i32, [P]),
             "mq_set_wait_timeout_ns": (None, [u64]),
             "mq_debug_wait_timeout": (i32, [P]),
@@ -223,11 +225,59 @@ def gemm(xq: torch.Tensor, xs: torch.Tensor, M: int, pl: PackedLinear, out: torc
     return out
 
 
+class Matrix(ctypes.Structure):
+    """mq_matrix: one weight matrix of a fused (grouped) linear call."""
+    _fields_ = [("wpk", ctypes.c_void_p), ("N", ctypes.c_int64), ("row_ptr", ctypes.c_void_p),
+                ("col_idx", ctypes.c_void_p), ("nnzb", ctypes.c_int64), ("rpk", ctypes.c_void_p),
+                ("y", ctypes.c_void_p), ("ldy", ctypes.c_int64)]
+
+
+def linear_workspace(M: int, K: int, Ns, device) -> tuple[torch.Tensor, int]:
+    """A zeroed workspace for mq_w4a4_residual_linear over matrices of N in Ns, cached per device and size."""
+    arr = (ctypes.c_int64 * len(Ns))(*Ns)
+    nbytes = int(lib().mq_linear_workspace_bytes(M, K, len(Ns), ctypes.cast(arr, ctypes.c_void_p)))
+    if nbytes == 0:
+        raise ValueError(f"no fused linear for M={M} K={K} N={list(Ns)}")
+    key = (torch.device(device).index, nbytes)
+    ws = _ws_cache.get(key)
+    if ws is None:
+        ws = torch.zeros(nbytes + 256, dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    return ws, nbytes
+
+
+def fused_linear(x: torch.Tensor, pls, outs=None, out_dtype=torch.bfloat16, ws: torch.Tensor | None = None,
+                 xq: torch.Tensor | None = None, xs: torch.Tensor | None = None, stream=None):
+    """Y_i = Q(x) (Q(W_i) + R_i)^T for the packed matrices pls (1..4, sharing x), quantizer included.
+    outs: optional list of [M, N_i] tensors (views with row stride >= N_i are allowed)."""
+    M, K = x.shape
+    if x.stride(1) != 1:
+        raise ValueError("x must have unit stride along K")
+    dev = x.device
+    if outs is None:
+        outs = [torch.empty((M, pl.N), dtype=out_dtype, device=dev) for pl in pls]
+    mats = (Matrix * len(pls))()
+    for i, (pl, y) in enumerate(zip(pls, outs)):
+        nz = pl.nnzb > 0
+        mats[i] = Matrix(pl.wpk.data_ptr(), pl.N, pl.row_ptr.data_ptr(), pl.col_idx.data_ptr() if nz else None, pl.nnzb,
+                         pl.rpk.data_ptr() if nz else None, y.data_ptr(), y.stride(0))
+    if ws is None:
+        ws, wsb = linear_workspace(M, K, [pl.N for pl in pls], dev)
+    else:
+        wsb = ws.numel()
+    _check(lib().mq_w4a4_residual_linear(_ptr(x), _dtype_code(x.dtype), M, K, x.stride(0), len(pls),
+                                         ctypes.cast(mats, ctypes.c_void_p), _dtype_code(outs[0].dtype), _ptr(xq),
+                                         _ptr(xs), _ptr(ws), wsb, _stream(stream)), "mq_w4a4_residual_linear")
+    return outs
+
+
 def gemm_plan(M: int, N: int, K: int) -> dict:
     """The kernel the GEMM entry points run for (M, N, K) on the current device."""
     info = (ctypes.c_int32 * 5)()
     _check(lib().mq_gemm_plan(M, N, K, ctypes.cast(info, ctypes.c_void_p)), "mq_gemm_plan")
-    return {"decode": bool(info[0]), "variant": {0: "general", 1: "warp-mma", 2: "tensor-memory"}[info[0]],
+    return {"decode": bool(info[0]),
+            "variant": {0: "general", 1: "cluster-warp-mma", 2: "cluster-tensor-memory", 3: "tensor-memory",
+                        4: "warp-mma"}[info[0]],
             "tokens_per_tile": info[1], "cluster": info[2], "clusters": info[3], "stages": info[4]}
 
 

@@ -180,9 +180,12 @@ mq_status mq_gemm_workspace_init(void* ws, size_t ws_bytes, mq_stream_t stream);
  *   wpk, row_ptr, col_idx, nnzb, rpk   from mq_select_blocks /
  *            mq_pack_weights (nnzb == 0: row_ptr, col_idx and rpk may be NULL).
  *   y        [M, N] row-major, MQ_BF16 (round to nearest even) or MQ_F32.
- *   ws       at least mq_gemm_workspace_bytes(M, N, K) bytes, 256-byte
- *            aligned, zeroed once by mq_gemm_workspace_init; one workspace
- *            must not be used by two GEMMs in flight at the same time.
+ *   ws       at least mq_gemm_workspace_bytes(M, N, K) bytes on the current
+ *            device, 256-byte aligned, zeroed once by mq_gemm_workspace_init
+ *            (and again after an MQ_ERR_TIMEOUT).  Every call that finishes
+ *            normally leaves it ready for the next, so one workspace can serve
+ *            GEMMs of any shape run one after another on a stream; it must not
+ *            be used by two GEMMs in flight at the same time.
  */
 mq_status mq_w4a4_residual_gemm(const uint8_t* xq, const uint16_t* xs, int64_t M,
                                 const uint8_t* wpk, int64_t N, int64_t K, const int32_t* row_ptr,
@@ -197,20 +200,73 @@ mq_status mq_w4a4_residual_gemm(const uint8_t* xq, const uint16_t* xs, int64_t M
  * has no counterpart in the paper; it is a deployment convenience.
  *   Arguments and results as mq_w4a4_residual_gemm, without ws / ws_bytes.
  *   Scratch: one fixed 8 MiB array in the library's device memory (held on
- *     every GPU that loads the library until the process exits).  That covers
- *     up to 32 tokens at any N and K; larger problems return MQ_ERR_WORKSPACE.
+ *     every GPU that loads the library until the process exits).  Any shape
+ *     whose kernel needs at most that much (mq_gemm_workspace_bytes on the
+ *     current device, for the kernel the shape runs on) is served: every
+ *     decode batch of up to 32 tokens at K up to about 600k on a 152-SM GPU,
+ *     and small larger-M problems; others return MQ_ERR_WORKSPACE.
  *   The first call on a device resolves the array's device address (with that
  *     device current); make that first call before any stream capture.
- *   The array is shared by every call and keeps the last call's contents; each
- *     call clears the part it uses on `stream` before the kernel.  Calls that
- *     overlap on the GPU (two streams, or two devices' threads racing on one
- *     device) race on the array: serialize them.
+ *   The array is shared by every call and keeps the last call's contents.
+ *     The kernels leave its counter prefix zeroed; after a device-side wait
+ *     has run out (mq_check_device_error returned MQ_ERR_TIMEOUT), the next
+ *     call clears that prefix on `stream` first.  Calls that overlap on the
+ *     GPU (two streams, or several host threads on one device) race on the
+ *     array: serialize them.
  *   Allocates nothing (no cudaMalloc / cudaFree, no allocating library call).
  */
 mq_status mq_w4a4_residual_gemm_noalloc(const uint8_t* xq, const uint16_t* xs, int64_t M,
                                         const uint8_t* wpk, int64_t N, int64_t K,
                                         const int32_t* row_ptr, const int32_t* col_idx, int64_t nnzb,
                                         const uint8_t* rpk, void* y, mq_dtype yt, mq_stream_t stream);
+
+/*
+ * One weight matrix of a grouped call (mq_w4a4_residual_linear): its packed
+ * form from mq_select_blocks / mq_pack_weights and its output.
+ *   wpk, N, row_ptr, col_idx, nnzb, rpk  as for mq_w4a4_residual_gemm (all
+ *         matrices of one call share K); nnzb == 0: row_ptr, col_idx, rpk may be NULL.
+ *   y     [M, ldy] row-major, columns 0..N-1 written (MQ_BF16 or MQ_F32, the
+ *         call's yt); ldy >= N, so several matrices may write slices of one
+ *         wider output.
+ */
+typedef struct {
+  const uint8_t* wpk;
+  int64_t N;
+  const int32_t* row_ptr;
+  const int32_t* col_idx;
+  int64_t nnzb;
+  const uint8_t* rpk;
+  void* y;
+  int64_t ldy;
+} mq_matrix;
+
+/* Bytes of workspace mq_w4a4_residual_linear needs for M tokens, K inputs and
+ * the nmat matrices of N[i] outputs each (0 for invalid sizes). */
+size_t mq_linear_workspace_bytes(int64_t M, int64_t K, int nmat, const int64_t* N);
+
+/*
+ * The whole linear layer from unquantized activations, for up to 4 matrices
+ * that read the same X (for example the q, k and v projections, or gate and
+ * up):  Y_i = Q(X) (Q(W_i) + R_i)^T.
+ * The activation quantizer is the ZipperEngine pipeline's first stage
+ * (Metodologia 3); with at most 32 tokens it runs inside the GEMM launch: each
+ * 128-input group of X is quantized once (by one CTA, with the same rule and
+ * bits as mq_quantize_act), published to the workspace, and every weight tile
+ * of every matrix reduce-adds its dense and residual products against it.
+ * One kernel launch, no xq round trip through the caller.  Above 32 tokens it
+ * runs mq_quantize_act's kernel, then the GEMM of each matrix.
+ *   x     [M, ldx] MQ_F16 or MQ_BF16 (xt), ldx >= K, 8-byte aligned rows.
+ *   mats  host array of nmat (1..4) mq_matrix; the matrices' tiles are
+ *         processed as one sequence, so small matrices share the launch.
+ *   xq, xs  optional (NULL: not written): the quantized activations in
+ *         mq_quantize_act's layout, bit-identical to what it writes.
+ *   ws    at least mq_linear_workspace_bytes(M, K, nmat, N) bytes, 256-byte
+ *         aligned, zeroed once by mq_gemm_workspace_init (as for the GEMM).
+ * Errors as mq_w4a4_residual_gemm.
+ */
+mq_status mq_w4a4_residual_linear(const void* x, mq_dtype xt, int64_t M, int64_t K, int64_t ldx, int nmat,
+                                  const mq_matrix* mats, mq_dtype yt, uint8_t* xq, uint16_t* xs, void* ws,
+                                  size_t ws_bytes, mq_stream_t stream);
 
 /*
  * Test hook: the same kernel, but instead of the fp32 reduce-add it writes the
@@ -237,7 +293,7 @@ mq_status mq_debug_group_dots(const uint8_t* xq, const uint16_t* xs, int64_t M, 
  *         per cluster, [3] clusters launched, [4] weight stages in shared
  *         memory; zeros for the general kernel.
  * MQ_ERR_INVALID_ARG for bad sizes (the same rules as the GEMM) or NULL info;
- * MQ_ERR_DEVICE if the current device is not compute capability 10.3.
+ * MQ_ERR_UNSUPPORTED_DEVICE if the current device is not compute capability 10.3.
  * Launches nothing.
  */
 mq_status mq_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t* info);
