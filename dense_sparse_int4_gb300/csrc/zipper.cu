@@ -97,7 +97,7 @@ constexpr int kNB = 8;             // items in flight: A/D buffer pairs in tenso
 constexpr int kUS = 4;             // units per shared-memory stage (one bulk copy of their base records)
 constexpr int kMinUnits = 8;       // units per CTA at least (bounds the pieces a tile is cut into)
 constexpr int kRS = 8;             // residual-record ring slots
-constexpr int kMaxUnits = 256;     // units per CTA (size of the residual map)
+constexpr int kMaxUnits = 128;     // units per CTA (size of the residual map)
 constexpr int kMaxStages = 8;
 constexpr int kMaxMats = 4;
 constexpr int kWarpProd = 0, kWarpRes = 1, kWarpMma = 2, kWarpConv0 = 4, kWarpDrain0 = 12;
@@ -875,7 +875,18 @@ __host__ __device__ constexpr int w_sets(int tn) { return tn == 32 ? 3 : 4; }
 __host__ __device__ constexpr int w_threads(int tn) { return 32 * (4 * w_sets(tn) + 1); }
 constexpr int kWMaxSets = 4;
 
-struct __align__(8) WCtl {
+// One bulk copy of the producer's schedule: source, offset in the stage, bytes.
+struct __align__(16) CopyDesc {
+  const uint8_t* src;
+  uint32_t dst;
+  uint32_t bytes;
+};
+constexpr int kMaxStg = kMaxUnits / 3 + 1;  // stages per CTA at most (3 or 4 units each)
+constexpr int kCopiesPerStage = 8;          // weight runs + activation runs of a stage (4 units: at most 4 + 4)
+
+struct __align__(16) WCtl {
+  CopyDesc cp[kMaxStg][kCopiesPerStage];  // the stage's copies (bytes 0: none)
+  uint32_t stage_tx[kMaxStg];             // bytes a stage's copies bring
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];  // the compute warps are done with the stage
   uint64_t r_full[kRS];
@@ -889,6 +900,7 @@ struct __align__(8) WCtl {
   uint64_t exit_bar;
   int32_t map[kMaxUnits][2];
   int32_t rpos[kMaxUnits][2];
+  const uint8_t* rsrc[kMaxUnits];  // residual records of the unit's matrix
   int abort_flag;
   int ndeferred;
   int deferred[2];
@@ -931,6 +943,11 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
   const int nstg = (nu + US - 1) / US;
   volatile int* abort_flag = &ctl.abort_flag;
   const uint64_t tmo = p.timeout_ns;
+  ZT_INIT;
+  if (threadIdx.x == 0) {
+    ZT(0);
+    ZC(6);
+  }
 
   if (warp == 0) {
     for (int s = lane; s < S; s += 32) {
@@ -951,8 +968,10 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
     if (lane == 15) ctl.abort_flag = 0;
     if (lane == 16) ctl.ndeferred = 0;
     fence_mbar_init();
+    if (lane == 0) ZC(11);
   }
   __syncthreads();
+  if (threadIdx.x == 0) ZC(12);
   pdl_trigger();
   auto stage = [&](int s) { return stages + static_cast<size_t>(s) * SB; };
   auto wrec = [&](int64_t u) -> const uint8_t* {
@@ -968,68 +987,138 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
   if (warp == kWProd) {
     // ---------------- producer: a stage = US units' base records and activation images, then the
     // residual records of those units ----------------
-    auto stage_bytes = [&](int st) {
-      const int n = min(US, nu - st * US);
-      return static_cast<uint32_t>(n * (kWRecBytes + kArec));
-    };
-    auto issue_weights = [&](int st, int s) {
-      int64_t ua = u0 + st * US;
-      const int64_t ub = min(u1, ua + US), us = ua;
-      while (ua < ub) {
-        const int64_t e = min(ub, mat_end(ua));
-        bulk_g2s(stage(s) + kAct + (ua - us) * kWRecBytes, wrec(ua), static_cast<uint32_t>((e - ua) * kWRecBytes),
-                 &ctl.full[s]);
-        ua = e;
+    // The issue loop is on the critical path and one thread's scalar work is
+    // slow (dependent chains), so the lanes first lay out every stage's copies
+    // in a table: the base records of a run of units inside one matrix are one
+    // copy, the activation images of a run of consecutive groups another.
+    for (int st = lane; st < nstg; st += 32) {
+      const int64_t ua = u0 + static_cast<int64_t>(st) * US, ub = min(u1, ua + US);
+      int nc = 0;
+      uint32_t tx = 0;
+      for (int64_t a = ua; a < ub;) {  // base records
+        const int t = static_cast<int>(a / G);
+        const int mi = mat_of_tile(p, t);
+        const int64_t e = min(ub, static_cast<int64_t>(mi + 1 < p.nmat ? p.mat[mi + 1].tile0 : p.tiles) * G);
+        const ZMat& mt = p.mat[mi];
+        if (nc < kCopiesPerStage) {
+          ctl.cp[st][nc].src = mt.wpk + (a - static_cast<int64_t>(mt.tile0) * G) * kWRecBytes;
+          ctl.cp[st][nc].dst = static_cast<uint32_t>(kAct + (a - ua) * kWRecBytes);
+          ctl.cp[st][nc].bytes = static_cast<uint32_t>((e - a) * kWRecBytes);
+          tx += ctl.cp[st][nc].bytes;
+          ++nc;
+        }
+        a = e;
       }
-    };
-    auto issue_act = [&](int st, int s) {
-      int64_t ua = u0 + st * US;
-      const int64_t ub = min(u1, ua + US), us = ua;
-      while (ua < ub) {
-        const int g = static_cast<int>(ua % G);
-        const int64_t n = min(ub - ua, static_cast<int64_t>(G - g));
-        bulk_g2s(stage(s) + (ua - us) * kArec, p.act + static_cast<int64_t>(g) * kArec,
-                 static_cast<uint32_t>(n * kArec), &ctl.full[s]);
-        ua += n;
+      for (int64_t a = ua; a < ub;) {  // activation images
+        const int gg = static_cast<int>(a % G);
+        const int64_t e = min(ub, a + (G - gg));
+        if (nc < kCopiesPerStage) {
+          ctl.cp[st][nc].src = p.act + static_cast<int64_t>(gg) * kArec;
+          ctl.cp[st][nc].dst = static_cast<uint32_t>((a - ua) * kArec);
+          ctl.cp[st][nc].bytes = static_cast<uint32_t>((e - a) * kArec);
+          tx += ctl.cp[st][nc].bytes;
+          ++nc;
+        }
+        a = e;
       }
-    };
+      for (int j = nc; j < kCopiesPerStage; ++j) ctl.cp[st][j].bytes = 0;
+      ctl.stage_tx[st] = tx;
+    }
+    __syncwarp();
     const int pre = min(S, nstg);
-    // The first stages' base records, the block lists and the residual
-    // records are read before the dependency wait: the kernels that may run
-    // ahead of it (this library's, which ask for the next launch early) never
-    // write packed weights or block lists.
-    if (lane == 0) {
-      for (int st = 0; st < pre; ++st) {
-        mbar_arrive_expect_tx(&ctl.full[st], stage_bytes(st));
-        issue_weights(st, st);
+    // A stage's copies are issued by several lanes in one instruction (lane j:
+    // copy j of the stage), and so are the residual records of its units.
+    // The first stages' base records are requested before the dependency wait:
+    // the kernels that may run ahead of it (this library's, which ask for the
+    // next launch early) never write packed weights.
+    if (lane < pre) mbar_arrive_expect_tx(&ctl.full[lane], ctl.stage_tx[lane]);
+    __syncwarp();
+    if (lane == 0) ZC(13);
+    for (int st = 0; st < pre; ++st) {
+      if (lane < kCopiesPerStage) {
+        const CopyDesc d = ctl.cp[st][lane];
+        if (d.bytes && d.dst >= static_cast<uint32_t>(kAct)) bulk_g2s(stage(st) + d.dst, d.src, d.bytes, &ctl.full[st]);
       }
     }
-    // residual map of the CTA's units and the records' ring positions
-    for (int i = lane; i < nu * 2; i += 32) (&ctl.map[0][0])[i] = -1;
     __syncwarp();
-    if (nu > 0) {
-      const int t_lo = static_cast<int>(u0 / G), t_hi = static_cast<int>((u1 - 1) / G);
-      for (int t = t_lo; t <= t_hi; ++t) {
-        const ZMat& mt = p.mat[mat_of_tile(p, t)];
-        if (mt.nnzb == 0) continue;
-        const int64_t br = 2 * static_cast<int64_t>(t - mt.tile0);
-        const int a0 = max(0, min(mt.nnzb, mt.row_ptr[br]));
-        const int a1 = max(a0, min(mt.nnzb, mt.row_ptr[br + 1]));
-        const int a2 = max(a1, min(mt.nnzb, mt.row_ptr[br + 2]));
-        for (int e = a0 + lane; e < a2; e += 32) {
-          const int g = mt.col_idx[e];
-          if (g < 0 || g >= G) continue;
-          const int64_t u = static_cast<int64_t>(t) * G + g;
-          if (u >= u0 && u < u1) ctl.map[u - u0][e >= a1 ? 1 : 0] = e;
+    if (lane == 0) ZC(8);
+    pdl_wait();  // the activation images are the preceding kernel's output
+    if (lane == 0) ZC(10);
+    bool ok = true;
+    for (int st = 0, s = 0, ph = 0; ok && st < nstg; ++st) {
+      if (lane == 0 && st < 16) ZC(104 + 4 * st);
+      const bool refill = st >= S;
+      if (refill) {
+        if (lane == 0) {
+          ok = mbar_wait_sleep(&ctl.empty[s], ph ^ 1, abort_flag, tmo, p.err);
+          if (ok) mbar_arrive_expect_tx(&ctl.full[s], ctl.stage_tx[st]);
+        }
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (!ok) break;
+      }
+      if (lane < kCopiesPerStage) {
+        const CopyDesc d = ctl.cp[st][lane];
+        if (d.bytes && (refill || d.dst < static_cast<uint32_t>(kAct))) bulk_g2s(stage(s) + d.dst, d.src, d.bytes, &ctl.full[s]);
+      }
+      if (lane == 0 && st < 16) ZC(16 + st);
+      if (st == 0) {
+        ok = mbar_wait(&ctl.map_ready, 0, abort_flag, tmo, p.err);
+        if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      }
+      if (lane == 0 && st < 16) ZC(105 + 4 * st);
+      // the residual records of the stage's units (lane = unit and half)
+      const int f = 2 * st * US + lane;
+      if (lane < 2 * US && f < 2 * nu) {
+        const int e = (&ctl.map[0][0])[f];
+        if (e >= 0) {
+          const int cpos = (&ctl.rpos[0][0])[f], slot = cpos % kRS;
+          if (cpos < kRS || (ok = mbar_wait_sleep(&ctl.r_empty[slot], ((cpos / kRS) - 1) & 1, abort_flag, tmo, p.err))) {
+            mbar_arrive_expect_tx(&ctl.r_full[slot], kRRecBytes);
+            bulk_g2s(rring + slot * kRRecBytes, ctl.rsrc[f >> 1] + static_cast<int64_t>(e) * kRRecBytes, kRRecBytes,
+                     &ctl.r_full[slot]);
+          }
         }
       }
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      if (lane == 0 && st < 16) ZC(106 + 4 * st);
+      if (++s == S) s = 0, ph ^= 1;
     }
-    __syncwarp();
-    {
+  } else {
+    // ---------------- compute warps ----------------
+    const int q = warp >> 2, wq = warp & 3;      // set, row quarter
+    const int g = lane >> 2, t = lane & 3;       // MMA fragment coordinates
+    const int rw = 32 * wq, half = wq >> 1;      // first row of this warp, its residual half
+    if (warp == 0) {
+      // Residual map of the CTA's units (CSR entry per unit and half) and the
+      // records' ring positions.  The block lists are read before the
+      // dependency wait, like the weights.
+      for (int i = lane; i < nu * 2; i += 32) (&ctl.map[0][0])[i] = -1;
+      __syncwarp();
+      if (nu > 0) {
+        const int t_lo = static_cast<int>(u0 / G), t_hi = static_cast<int>((u1 - 1) / G);
+        for (int tt = t_lo; tt <= t_hi; ++tt) {
+          const ZMat& mt = p.mat[mat_of_tile(p, tt)];
+          if (mt.nnzb == 0) continue;
+          const int64_t br = 2 * static_cast<int64_t>(tt - mt.tile0);
+          const int a0 = max(0, min(mt.nnzb, mt.row_ptr[br]));
+          const int a1 = max(a0, min(mt.nnzb, mt.row_ptr[br + 1]));
+          const int a2 = max(a1, min(mt.nnzb, mt.row_ptr[br + 2]));
+          for (int e = a0 + lane; e < a2; e += 32) {
+            const int gg = mt.col_idx[e];
+            if (gg < 0 || gg >= G) continue;
+            const int64_t u = static_cast<int64_t>(tt) * G + gg;
+            if (u >= u0 && u < u1) {
+              ctl.map[u - u0][e >= a1 ? 1 : 0] = e;
+              ctl.rsrc[u - u0] = mt.rpk;
+            }
+          }
+        }
+      }
+      __syncwarp();
       const int nf = nu * 2;
       const int chunk = (nf + 31) / 32, f0 = min(nf, lane * chunk), f1 = min(nf, f0 + chunk);
       int cnt = 0;
-      for (int f = f0; f < f1; ++f) cnt += (&ctl.map[0][0])[f] >= 0;
+      for (int fx = f0; fx < f1; ++fx) cnt += (&ctl.map[0][0])[fx] >= 0;
       int incl = cnt;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -1037,40 +1126,14 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
         if (lane >= o) incl += v;
       }
       int pos = incl - cnt;
-      for (int f = f0; f < f1; ++f)
-        if ((&ctl.map[0][0])[f] >= 0) (&ctl.rpos[0][0])[f] = pos++;
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&ctl.map_ready);
-    pdl_wait();  // the activation images are the preceding kernel's output
-    if (lane == 0) {
-      bool ok = true;
-      for (int st = 0; ok && st < nstg; ++st) {
-        const int s = st % S;
-        if (st >= S) {
-          if (!(ok = mbar_wait_sleep(&ctl.empty[s], ((st / S) - 1) & 1, abort_flag, tmo, p.err))) break;
-          mbar_arrive_expect_tx(&ctl.full[s], stage_bytes(st));
-          issue_weights(st, s);
-        }
-        issue_act(st, s);
-        for (int f = 2 * st * US; ok && f < min(2 * nu, 2 * (st + 1) * US); ++f) {
-          const int e = (&ctl.map[0][0])[f];
-          if (e < 0) continue;
-          const int cpos = (&ctl.rpos[0][0])[f], slot = cpos % kRS;
-          if (cpos >= kRS && !(ok = mbar_wait_sleep(&ctl.r_empty[slot], ((cpos / kRS) - 1) & 1, abort_flag, tmo, p.err)))
-            break;
-          const ZMat& mt = p.mat[mat_of_tile(p, static_cast<int>((u0 + f / 2) / G))];
-          mbar_arrive_expect_tx(&ctl.r_full[slot], kRRecBytes);
-          bulk_g2s(rring + slot * kRRecBytes, mt.rpk + static_cast<int64_t>(e) * kRRecBytes, kRRecBytes,
-                   &ctl.r_full[slot]);
-        }
+      for (int fx = f0; fx < f1; ++fx)
+        if ((&ctl.map[0][0])[fx] >= 0) (&ctl.rpos[0][0])[fx] = pos++;
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&ctl.map_ready);
+        ZC(9);
       }
     }
-  } else {
-    // ---------------- compute warps ----------------
-    const int q = warp >> 2, wq = warp & 3;      // set, row quarter
-    const int g = lane >> 2, t = lane & 3;       // MMA fragment coordinates
-    const int rw = 32 * wq, half = wq >> 1;      // first row of this warp, its residual half
     bool ok = mbar_wait(&ctl.map_ready, 0, abort_flag, tmo, p.err);
     pdl_wait();  // Y and the workspace pieces may still be in use by the preceding kernel
     // accumulators: [mt][nb] pairs {row r, tokens 8nb+2t, +1}, {row r+8, same tokens}
@@ -1225,15 +1288,16 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
     };
 
     // the sets walk the CTA's units tile by tile; set q takes the units ui = q (mod US)
-    int f = 0;
+    // set q takes units ui = q, q + US, ..: stage st = ui / US, one per step,
+    // in slot s with fill parity ph (counters, not divisions)
+    int f = 0, ui = q, st = 0, s = 0, ph = 0;
     const int t_lo = nu > 0 ? static_cast<int>(u0 / G) : 0, t_hi = nu > 0 ? static_cast<int>((u1 - 1) / G) : -1;
-    for (int tile = t_lo; ok && tile <= t_hi; ++tile, ++f) {
-      const int64_t ua = max(u0, static_cast<int64_t>(tile) * G), ub = min(u1, static_cast<int64_t>(tile + 1) * G);
-      int ui = static_cast<int>(ua - u0);
-      ui += (q - ui % US + US) % US;  // this set's first unit in the tile
-      for (; ok && ui < static_cast<int>(ub - u0); ui += US) {
-        const int st = ui / US, s = st % S;
-        if (!(ok = mbar_wait(&ctl.full[s], (st / S) & 1, abort_flag, tmo, p.err))) break;
+    int tile_end = static_cast<int>(min(u1, static_cast<int64_t>(t_lo + 1) * G) - u0);  // first unit past the tile
+    for (int tile = t_lo; ok && tile <= t_hi; ++tile, ++f, tile_end = min(nu, tile_end + G)) {
+      for (; ok && ui < tile_end; ui += US) {
+        if (!(ok = mbar_wait(&ctl.full[s], ph, abort_flag, tmo, p.err))) break;
+        if (warp == 0 && lane == 0 && st < 16) ZC(32 + st);
+        if (warp == kWCompute - 4 && lane == 0 && st < 16) ZC(48 + st);
         const uint8_t* sg = stage(s);
         const uint8_t* img = sg + q * kArec;
         const uint8_t* rec = sg + kAct + q * kWRecBytes;
@@ -1250,8 +1314,13 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl.empty[s]);  // this warp is done with the stage
+        ++st;
+        if (++s == S) s = 0, ph ^= 1;
       }
+      if (warp == 0 && lane == 0 && f < 8) ZC(64 + f);
+      if (warp == kWCompute - 4 && lane == 0 && f < 8) ZC(72 + f);
       if (ok && !kDebug) ok = flush(tile, f);
+      if (warp == kWCompute - 4 && lane == 0 && f < 8) ZC(80 + f);
     }
 
     // Finish the tiles whose count this CTA completed: once every compute
@@ -1260,7 +1329,9 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
     // resets the tile's counter for the next launch.
     __syncwarp();
     if (lane == 0) mbar_arrive(&ctl.fix_bar);
+    if (warp == kWCompute - 4 && lane == 0) ZC(88);
     if (!kDebug && ok && q == kWSets - 1 && (ok = mbar_wait(&ctl.fix_bar, 0, abort_flag, tmo, p.err))) {
+      if (warp == kWCompute - 4 && lane == 0) ZC(89);
       const int r = rw + lane;
       const int nd = ctl.ndeferred;
       const uint32_t piece_bytes = static_cast<uint32_t>(p.M) * kTileN * 4;  // rows 0..M-1 of a piece
@@ -1308,10 +1379,15 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
   }
 
   // Every role is done.
+  if (warp == kWCompute - 4 && lane == 0) ZC(90);
   __syncwarp();
   if (lane == 0) mbar_arrive(&ctl.exit_bar);
   mbar_wait(&ctl.exit_bar, 0, abort_flag, tmo, p.err);
   __syncthreads();
+  if (threadIdx.x == 0) {
+    ZT(5);
+    ZC(7);
+  }
   if (*abort_flag) {
     // A wait gave up: copies may still be in flight; give them 200 us.
     if (threadIdx.x == 0) {
