@@ -177,6 +177,9 @@ __device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
 __device__ __forceinline__ void st_release_gpu(int32_t* p, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+__device__ __forceinline__ void st_relaxed_gpu(int32_t* p, int v) {
+  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ void named_bar(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -872,7 +875,7 @@ __global__ void __launch_bounds__(kThreads, 1) zipper_decode_kernel(const ZParam
 // tokens, whose accumulators need more registers per thread (the warps of a
 // block share each scheduler's register file).
 __host__ __device__ constexpr int w_sets(int tn) { return tn == 32 ? 3 : 4; }
-__host__ __device__ constexpr int w_threads(int tn) { return 32 * (4 * w_sets(tn) + 1); }
+__host__ __device__ constexpr int w_threads(int tn) { return 32 * (4 * w_sets(tn) + 2); }  // + producer, epilogue
 constexpr int kWMaxSets = 4;
 
 // One bulk copy of the producer's schedule: source, offset in the stage, bytes.
@@ -891,19 +894,17 @@ struct __align__(16) WCtl {
   uint64_t empty[kMaxStages];  // the compute warps are done with the stage
   uint64_t r_full[kRS];
   uint64_t r_empty[kRS];       // the 2 warps of the record's half
-  uint64_t chain[kWMaxSets][2];  // tile flush f (buffer f % 2): set q has added its partial
-  uint64_t red_free[2];        // the last set is done with buffer b
-  uint64_t piece_bar;          // the last set's 4 warps wrote their piece rows
+  uint64_t tile_bar;           // bounded barrier of the compute warps (tile ends)
   uint64_t map_ready;
-  uint64_t fix_bar;            // all compute warps are past the main loop (stage memory idle)
-  uint64_t red_bar;            // stream-K pieces copied in for a deferred tile
+  uint64_t piece_written;      // every compute warp wrote its share of this CTA's stream-K piece
+  uint64_t slot_free[kMaxStages];  // the producer handed the epilogue stage slot k (single use)
+  uint64_t pieces_in;          // the other CTAs' pieces of the tile this CTA finishes are readable
   uint64_t exit_bar;
   int32_t map[kMaxUnits][2];
   int32_t rpos[kMaxUnits][2];
   const uint8_t* rsrc[kMaxUnits];  // residual records of the unit's matrix
   int abort_flag;
-  int ndeferred;
-  int deferred[2];
+  uint32_t piece_slot[kMaxStages];  // shared-memory offset of handed-over slot k
 };
 
 // D(16x8, fp32) += A(16x32, E4M3, row-major) * B(32x8, E4M3, column-major).
@@ -925,8 +926,10 @@ __device__ __forceinline__ void mma_e4m3_z(float (&d)[4], const uint32_t (&a)[4]
 template <int TN, bool kDebug>
 __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZParams p) {
   constexpr int NB = TN / 8;           // 8-token blocks of one MMA
+  constexpr int kRedPasses = TN == 8 ? 1 : 2, kRedTok = TN / kRedPasses;  // tile sums: tokens per pass
+  constexpr int kRedLd = kTileN + 4;  // token stride of a partial buffer: fragment writes hit distinct banks
   constexpr int US = w_sets(TN);       // units per stage = sets of compute warps
-  constexpr int kWSets = US, kWCompute = 4 * US, kWProd = kWCompute, kWThreads = w_threads(TN);
+  constexpr int kWCompute = 4 * US, kWProd = kWCompute, kWEpi = kWCompute + 1, kWThreads = w_threads(TN);
   constexpr int kArec = TN * 136;      // activation image: B fragments, then {2^9 sx, c} pairs
   constexpr int kAct = US * kArec;     // a stage: US activation images, then US base records
   extern __shared__ uint8_t smem_raw[];
@@ -935,12 +938,30 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
   const int S = p.nstages, SB = p.stage_bytes, G = p.G;
   uint8_t* stages = smem;
   uint8_t* rring = smem + static_cast<size_t>(S) * SB;
-  float* red = reinterpret_cast<float*>(rring + kRS * kRRecBytes);  // [2][128 rows][TN]
+  float* red = reinterpret_cast<float*>(rring + kRS * kRRecBytes);  // [US sets][kRedTok][kRedLd] tile partials
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t U = p.units, P = p.ctas, c = blockIdx.x;
   const int64_t u0 = first_unit(c, U, P), u1 = first_unit(c + 1, U, P);
   const int nu = static_cast<int>(u1 - u0);
   const int nstg = (nu + US - 1) / US;
+  // Stream-K roles.  A cut tile is finished by the CTA holding its first
+  // groups (its head); every other CTA on it publishes a piece (its share of
+  // the tile's sums) and a flag.  A CTA publishes at most one piece (for its
+  // first tile, when its range starts inside it) and finishes at most one
+  // tile (its last, when its range holds that tile's head but not its end).
+  // The pieces of the tile it finishes are the tails of later CTAs' ranges,
+  // computed first there: usually in place long before they are needed.
+  const int t_first = static_cast<int>(u0 / G), t_last = static_cast<int>((u1 - 1) / G);
+  const bool publishes = !kDebug && u0 > static_cast<int64_t>(t_first) * G;
+  const bool finishes =
+      !kDebug && u0 <= static_cast<int64_t>(t_last) * G && u1 < static_cast<int64_t>(t_last + 1) * G;
+  const int npc = finishes ? static_cast<int>(owner_of(static_cast<int64_t>(t_last + 1) * G - 1, U, P) - c) : 0;
+  const uint32_t piece_bytes = static_cast<uint32_t>(p.M) * kTileN * 4;  // tokens 0..M-1 of a [TN][128] piece
+  // the pieces go into stage slots no stage needs any more, per_slot to a slot, if they fit in all slots
+  const int per_slot = SB / static_cast<int>(piece_bytes);
+  const int need_slots = per_slot > 0 ? (npc + per_slot - 1) / per_slot : S + 1;
+  const bool pieces_in_smem = need_slots <= S;
+  auto piece_of = [&](int64_t cc) -> float* { return p.part + cc * (TN * static_cast<int64_t>(kTileN)); };
   volatile int* abort_flag = &ctl.abort_flag;
   const uint64_t tmo = p.timeout_ns;
   ZT_INIT;
@@ -958,15 +979,13 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
       mbar_init(&ctl.r_full[lane], 1);
       mbar_init(&ctl.r_empty[lane], 2);
     }
-    if (lane < 2 * kWSets) mbar_init(&ctl.chain[lane >> 1][lane & 1], 4);
-    if (lane == 8 || lane == 9) mbar_init(&ctl.red_free[lane - 8], 4);
-    if (lane == 10) mbar_init(&ctl.piece_bar, 4);
+    if (lane == 10) mbar_init(&ctl.tile_bar, kWCompute);
     if (lane == 11) mbar_init(&ctl.map_ready, 1);
-    if (lane == 12) mbar_init(&ctl.fix_bar, kWCompute);
-    if (lane == 13) mbar_init(&ctl.red_bar, 1);
+    if (lane == 12) mbar_init(&ctl.piece_written, kWCompute);
+    if (lane < kMaxStages) mbar_init(&ctl.slot_free[lane], 1);
+    if (lane == 17) mbar_init(&ctl.pieces_in, 1);
     if (lane == 14) mbar_init(&ctl.exit_bar, kWThreads / 32);
     if (lane == 15) ctl.abort_flag = 0;
-    if (lane == 16) ctl.ndeferred = 0;
     fence_mbar_init();
     if (lane == 0) ZC(11);
   }
@@ -987,50 +1006,60 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
   if (warp == kWProd) {
     // ---------------- producer: a stage = US units' base records and activation images, then the
     // residual records of those units ----------------
-    // The issue loop is on the critical path and one thread's scalar work is
-    // slow (dependent chains), so the lanes first lay out every stage's copies
-    // in a table: the base records of a run of units inside one matrix are one
-    // copy, the activation images of a run of consecutive groups another.
-    for (int st = lane; st < nstg; st += 32) {
-      const int64_t ua = u0 + static_cast<int64_t>(st) * US, ub = min(u1, ua + US);
-      int nc = 0;
-      uint32_t tx = 0;
-      for (int64_t a = ua; a < ub;) {  // base records
-        const int t = static_cast<int>(a / G);
-        const int mi = mat_of_tile(p, t);
-        const int64_t e = min(ub, static_cast<int64_t>(mi + 1 < p.nmat ? p.mat[mi + 1].tile0 : p.tiles) * G);
-        const ZMat& mt = p.mat[mi];
-        if (nc < kCopiesPerStage) {
-          ctl.cp[st][nc].src = mt.wpk + (a - static_cast<int64_t>(mt.tile0) * G) * kWRecBytes;
-          ctl.cp[st][nc].dst = static_cast<uint32_t>(kAct + (a - ua) * kWRecBytes);
-          ctl.cp[st][nc].bytes = static_cast<uint32_t>((e - a) * kWRecBytes);
-          tx += ctl.cp[st][nc].bytes;
-          ++nc;
-        }
-        a = e;
+    // The lanes first lay out every stage's copies in a table, one lane per
+    // unit (a pass of 32 - 32 % US units never splits a stage): a unit opens
+    // a base-record run when it is its stage's first or the first of its
+    // matrix, an activation run when it is its stage's first or group 0 of a
+    // tile; a run ends where the next of its kind opens.  The base records of
+    // a run are one copy, so are its activation images.
+    constexpr int kUnitsPerPass = 32 - 32 % US;
+    for (int j0 = 0; j0 < nu; j0 += kUnitsPerPass) {
+      const int k = lane % US, first = lane - k;  // unit in stage, first lane of the stage
+      const bool live = lane < kUnitsPerPass && j0 + lane < nu;
+      int mi = 0, tt = 0, gg = 0;
+      if (live) {
+        const int u = static_cast<int>(u0) + j0 + lane;  // the planner keeps unit indexes below 2^31
+        tt = u / G;
+        gg = u - tt * G;
+        mi = mat_of_tile(p, tt);
       }
-      for (int64_t a = ua; a < ub;) {  // activation images
-        const int gg = static_cast<int>(a % G);
-        const int64_t e = min(ub, a + (G - gg));
-        if (nc < kCopiesPerStage) {
-          ctl.cp[st][nc].src = p.act + static_cast<int64_t>(gg) * kArec;
-          ctl.cp[st][nc].dst = static_cast<uint32_t>((a - ua) * kArec);
-          ctl.cp[st][nc].bytes = static_cast<uint32_t>((e - a) * kArec);
-          tx += ctl.cp[st][nc].bytes;
-          ++nc;
+      const int mi_prev = __shfl_up_sync(0xFFFFFFFFu, mi, 1);
+      const unsigned wm = __ballot_sync(0xFFFFFFFFu, live && (k == 0 || mi != mi_prev));
+      const unsigned am = __ballot_sync(0xFFFFFFFFu, live && (k == 0 || gg == 0));
+      if (live) {
+        const int st = j0 / US + lane / US;
+        const int last = min(first + US, nu - j0);  // one past the stage's last lane
+        const unsigned smask = ((1u << US) - 1u) << first, below = (1u << lane) - 1u, above = ~below & ~(1u << lane);
+        const int nw = __popc(wm & smask);
+        if ((wm >> lane) & 1u) {
+          const unsigned nxt = wm & smask & above;
+          const int end = nxt ? __ffs(nxt) - 1 : last;
+          const ZMat& mt = p.mat[mi];
+          CopyDesc& d = ctl.cp[st][__popc(wm & smask & below)];
+          d.src = mt.wpk + (static_cast<int64_t>(tt - mt.tile0) * G + gg) * kWRecBytes;
+          d.dst = static_cast<uint32_t>(kAct + k * kWRecBytes);
+          d.bytes = static_cast<uint32_t>((end - lane) * kWRecBytes);
         }
-        a = e;
+        if ((am >> lane) & 1u) {
+          const unsigned nxt = am & smask & above;
+          const int end = nxt ? __ffs(nxt) - 1 : last;
+          CopyDesc& d = ctl.cp[st][nw + __popc(am & smask & below)];
+          d.src = p.act + static_cast<int64_t>(gg) * kArec;
+          d.dst = static_cast<uint32_t>(k * kArec);
+          d.bytes = static_cast<uint32_t>((end - lane) * kArec);
+        }
+        if (k == 0) {
+          for (int i = nw + __popc(am & smask); i < kCopiesPerStage; ++i) ctl.cp[st][i].bytes = 0;
+          ctl.stage_tx[st] = static_cast<uint32_t>((last - first) * (kWRecBytes + kArec));
+        }
       }
-      for (int j = nc; j < kCopiesPerStage; ++j) ctl.cp[st][j].bytes = 0;
-      ctl.stage_tx[st] = tx;
     }
     __syncwarp();
     const int pre = min(S, nstg);
-    // A stage's copies are issued by several lanes in one instruction (lane j:
-    // copy j of the stage), and so are the residual records of its units.
     // The first stages' base records are requested before the dependency wait:
     // the kernels that may run ahead of it (this library's, which ask for the
-    // next launch early) never write packed weights.
+    // next launch early) never write packed weights.  Then the activation
+    // images of those stages, all in one instruction (lane: stage, copy).
     if (lane < pre) mbar_arrive_expect_tx(&ctl.full[lane], ctl.stage_tx[lane]);
     __syncwarp();
     if (lane == 0) ZC(13);
@@ -1044,44 +1073,138 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
     if (lane == 0) ZC(8);
     pdl_wait();  // the activation images are the preceding kernel's output
     if (lane == 0) ZC(10);
-    bool ok = true;
-    for (int st = 0, s = 0, ph = 0; ok && st < nstg; ++st) {
-      if (lane == 0 && st < 16) ZC(104 + 4 * st);
-      const bool refill = st >= S;
-      if (refill) {
-        if (lane == 0) {
-          ok = mbar_wait_sleep(&ctl.empty[s], ph ^ 1, abort_flag, tmo, p.err);
-          if (ok) mbar_arrive_expect_tx(&ctl.full[s], ctl.stage_tx[st]);
+    for (int i = lane; i < pre * kCopiesPerStage; i += 32) {
+      const int st = i / kCopiesPerStage;
+      const CopyDesc d = ctl.cp[st][i % kCopiesPerStage];
+      if (d.bytes && d.dst < static_cast<uint32_t>(kAct)) bulk_g2s(stage(st) + d.dst, d.src, d.bytes, &ctl.full[st]);
+    }
+    __syncwarp();
+    if (lane == 0) ZC(16);
+    bool ok = mbar_wait(&ctl.map_ready, 0, abort_flag, tmo, p.err);
+    ok = __all_sync(0xFFFFFFFFu, ok);
+    // Two cursors, neither waiting on the other: the residual records in ring
+    // order (those of issued stages, each once its ring slot is free), and
+    // the refills of stage slots as the compute warps free them.
+    int bst = pre, bs = 0, bph = 1;  // next stage, its slot, the slot's fill parity
+    int rf = 0;                       // next (unit, half) whose residual record is due
+    const int nf = 2 * nu;
+    uint64_t idle_since = 0;
+    for (int idle = 0; ok && (bst < nstg || rf < nf);) {
+      bool progress = false;
+      const int rlim = min(nf, 2 * US * bst);
+      if (rf < rlim) {
+        const int f = rf + lane;
+        bool ready = false;
+        int e = -1, cpos = 0;
+        if (f < rlim) {
+          e = (&ctl.map[0][0])[f];
+          cpos = e >= 0 ? (&ctl.rpos[0][0])[f] : 0;
+          // the slot's previous record (cpos - kRS) has been issued, so the
+          // slot's phase is one of two and the parity test is exact
+          ready = e < 0 || cpos < kRS || mbar_test_wait(&ctl.r_empty[cpos % kRS], ((cpos / kRS) - 1) & 1);
         }
-        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-        if (!ok) break;
+        const unsigned blocked = __ballot_sync(0xFFFFFFFFu, !ready);
+        const int n = blocked ? __ffs(blocked) - 1 : 32;  // the ready prefix, in ring order
+        if (lane < n && e >= 0) {
+          const int slot = cpos % kRS;
+          mbar_arrive_expect_tx(&ctl.r_full[slot], kRRecBytes);
+          bulk_g2s(rring + slot * kRRecBytes, ctl.rsrc[f >> 1] + static_cast<int64_t>(e) * kRRecBytes, kRRecBytes,
+                   &ctl.r_full[slot]);
+        }
+        rf += n;
+        progress = n > 0;
       }
-      if (lane < kCopiesPerStage) {
-        const CopyDesc d = ctl.cp[st][lane];
-        if (d.bytes && (refill || d.dst < static_cast<uint32_t>(kAct))) bulk_g2s(stage(s) + d.dst, d.src, d.bytes, &ctl.full[s]);
+      if (bst < nstg) {
+        int go = 0;
+        if (lane == 0 && mbar_test_wait(&ctl.empty[bs], bph ^ 1)) {
+          mbar_arrive_expect_tx(&ctl.full[bs], ctl.stage_tx[bst]);
+          go = 1;
+        }
+        if (__shfl_sync(0xFFFFFFFFu, go, 0)) {
+          if (lane < kCopiesPerStage) {
+            const CopyDesc d = ctl.cp[bst][lane];
+            if (d.bytes) bulk_g2s(stage(bs) + d.dst, d.src, d.bytes, &ctl.full[bs]);
+          }
+          if (lane == 0 && bst < 16) ZC(16 + bst);
+          ++bst;
+          if (++bs == S) bs = 0, bph ^= 1;
+          progress = true;
+        }
       }
-      if (lane == 0 && st < 16) ZC(16 + st);
-      if (st == 0) {
-        ok = mbar_wait(&ctl.map_ready, 0, abort_flag, tmo, p.err);
-        if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      if (progress) {
+        idle = 0;
+        continue;
       }
-      if (lane == 0 && st < 16) ZC(105 + 4 * st);
-      // the residual records of the stage's units (lane = unit and half)
-      const int f = 2 * st * US + lane;
-      if (lane < 2 * US && f < 2 * nu) {
-        const int e = (&ctl.map[0][0])[f];
-        if (e >= 0) {
-          const int cpos = (&ctl.rpos[0][0])[f], slot = cpos % kRS;
-          if (cpos < kRS || (ok = mbar_wait_sleep(&ctl.r_empty[slot], ((cpos / kRS) - 1) & 1, abort_flag, tmo, p.err))) {
-            mbar_arrive_expect_tx(&ctl.r_full[slot], kRRecBytes);
-            bulk_g2s(rring + slot * kRRecBytes, ctl.rsrc[f >> 1] + static_cast<int64_t>(e) * kRRecBytes, kRRecBytes,
-                     &ctl.r_full[slot]);
+      __nanosleep(32);
+      if ((++idle & 15) == 0) {  // bounded: give up after the timeout without progress
+        int give_up = 0;
+        if (lane == 0) {
+          const uint64_t now = globaltimer();
+          if (*abort_flag) {
+            give_up = 1;
+          } else if (idle == 16) {
+            idle_since = now;
+          } else if (now - idle_since > tmo) {
+            atomicOr(p.err, kDevErrTimeout);
+            *abort_flag = 1;
+            give_up = 1;
           }
         }
+        ok = !__shfl_sync(0xFFFFFFFFu, give_up, 0);
       }
-      if (!__all_sync(0xFFFFFFFFu, ok)) break;
-      if (lane == 0 && st < 16) ZC(106 + 4 * st);
-      if (++s == S) s = 0, ph ^= 1;
+    }
+    // The slots stages nstg, nstg + 1, .. would take are free once the compute
+    // warps are done with their last stages (at once if never filled): they
+    // take the pieces of the tile this CTA finishes, handed over one by one.
+    if (ok && finishes && pieces_in_smem && lane == 0) {
+      for (int k = 0; k < need_slots; ++k) {
+        const int v = nstg + k, slot = v % S;  // the slot's last fill was stage v - S; its phases are waited in order
+        if (v >= S && !mbar_wait_sleep(&ctl.empty[slot], ((v / S) - 1) & 1, abort_flag, tmo, p.err)) break;
+        ctl.piece_slot[k] = static_cast<uint32_t>(slot) * SB;
+        mbar_arrive(&ctl.slot_free[k]);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWEpi) {
+    // ---------------- epilogue: stream-K pieces off the compute warps' path ----------------
+    pdl_wait();  // the flags and pieces in the workspace may still be in use by the preceding kernel
+    bool ok = true;
+    if (publishes) {  // release this CTA's piece once every compute warp has written its share
+      if (lane == 0) {
+        ok = mbar_wait_sleep(&ctl.piece_written, 0, abort_flag, tmo, p.err);
+        if (ok) {
+          fence_acq_rel_gpu();
+          st_relaxed_gpu(p.tcount + c, 1);
+          ZC(88);
+        }
+      }
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    }
+    if (finishes && ok) {
+      // the flags of the other pieces (lane j: CTA c + 1 + j), then the pieces
+      // into the free slot; each flag is cleared for the next launch once seen
+      for (int j0 = 0; ok && j0 < npc; j0 += 32) {
+        const int j = j0 + lane;
+        bool seen = true;
+        if (j < npc && (seen = flag_wait(p.tcount + c + 1 + j, abort_flag, tmo, p.err))) p.tcount[c + 1 + j] = 0;
+        ok = __all_sync(0xFFFFFFFFu, seen);
+      }
+      if (lane == 0) ZC(89);
+      if (ok && pieces_in_smem) {
+        if (lane == 0) mbar_arrive_expect_tx(&ctl.pieces_in, npc * piece_bytes);
+        for (int k = 0; ok && k < need_slots; ++k) {  // slot k: pieces k * per_slot ..
+          if (lane == 0) ok = mbar_wait_sleep(&ctl.slot_free[k], 0, abort_flag, tmo, p.err);
+          if (!(ok = __shfl_sync(0xFFFFFFFFu, ok, 0))) break;
+          const int j = k * per_slot + lane;
+          if (lane < per_slot && j < npc) {
+            fence_proxy_async_global();  // the pieces were written through the generic proxy
+            bulk_g2s(stages + ctl.piece_slot[k] + lane * piece_bytes, piece_of(c + 1 + j), piece_bytes,
+                     &ctl.pieces_in);
+          }
+        }
+      } else if (ok && lane == 0) {
+        mbar_arrive(&ctl.pieces_in);  // the compute warps read the pieces in place
+      }
     }
   } else {
     // ---------------- compute warps ----------------
@@ -1215,85 +1338,82 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
       else
         static_cast<__nv_bfloat16*>(mt.y)[o] = __float2bfloat16_rn(v);
     };
-    auto piece_of = [&](int64_t cc, int tile) -> float* {  // CTA cc's piece of the tile: [TN][128]
-      const int wc = (tile == static_cast<int>(first_unit(cc, U, P) / G)) ? 0 : 1;
-      return p.part + ((cc * 2 + wc) * TN) * static_cast<int64_t>(kTileN);
+    // End of tile `tile`: every warp writes its partial into its set's
+    // buffer, then each warp adds the sets' partials of its slice of the rows
+    // in set order (and, for the tile this CTA finishes, the other CTAs'
+    // pieces in CTA order) and stores Y, or this CTA's piece.
+    int nsync = 0;  // phases of tile_bar
+    auto tile_sync = [&]() -> bool {  // all compute warps (bounded)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.tile_bar);
+      return mbar_wait(&ctl.tile_bar, (nsync++) & 1, abort_flag, tmo, p.err);
     };
-    // End of tile `tile` (the f-th tile of this CTA): the sets add their
-    // partials into red[f % 2] in set order; the last set stores Y (whole
-    // tile) or writes this CTA's stream-K piece and counts it in.
-    int npiece = 0;  // pieces this CTA has written (phases of piece_bar)
-    auto flush = [&](int tile, int f) -> bool {
-      const int bsel = f & 1;
-      float* rb = red + bsel * (kTileN * TN);
-      bool pass = true;
-      if (q == 0)
-        pass = f < 2 || mbar_wait(&ctl.red_free[bsel], ((f >> 1) - 1) & 1, abort_flag, tmo, p.err);
-      else
-        pass = mbar_wait(&ctl.chain[q - 1][bsel], (f >> 1) & 1, abort_flag, tmo, p.err);
-      if (!pass) return false;
-      const bool last = q == kWSets - 1;
+    auto flush = [&](int tile) -> bool {
       const ZMat& mt = p.mat[mat_of_tile(p, tile)];
       const int64_t nbase = static_cast<int64_t>(tile - mt.tile0) * kTileN;
-      const int64_t tu0 = static_cast<int64_t>(tile) * G, tu1 = tu0 + G;
-      const bool whole = tu0 >= u0 && tu1 <= u1;
-      float* piece = whole || !last ? nullptr : piece_of(c, tile);
-#pragma unroll
-      for (int mt2 = 0; mt2 < 2; ++mt2)
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int r = rw + 16 * mt2 + 8 * h + g, m0 = 8 * nb + 2 * t;
-            float2* slot = reinterpret_cast<float2*>(rb + r * TN + m0);
-            float2 v;
-            f2unpack(acc[mt2][nb][h], v.x, v.y);
-            acc[mt2][nb][h] = 0ull;
-            if (q != 0) {
-              const float2 o = *slot;
-              v = make_float2(o.x + v.x, o.y + v.y);  // ascending set order
-            }
-            if (!last) {
-              *slot = v;
-            } else if (whole) {
-              if (m0 < p.M) store_y(mt, nbase + r, m0, v.x);
-              if (m0 + 1 < p.M) store_y(mt, nbase + r, m0 + 1, v.y);
-            } else {
-              if (m0 < p.M) __stcg(piece + m0 * kTileN + r, v.x);
-              if (m0 + 1 < p.M) __stcg(piece + (m0 + 1) * kTileN + r, v.y);
-            }
-          }
-      __syncwarp();
-      if (!last) {
-        if (lane == 0) mbar_arrive(&ctl.chain[q][bsel]);
-        return true;
+      const bool pub = publishes && tile == t_first;  // write this CTA's piece
+      const bool fin = finishes && tile == t_last;    // add the other CTAs' pieces
+      float* piece = pub ? piece_of(c) : nullptr;
+      float* mine = red + q * (kRedTok * kRedLd);
+      if (fin) {
+        if (!mbar_wait(&ctl.pieces_in, 0, abort_flag, tmo, p.err)) return false;
+        if (warp == 0 && lane == 0) ZC(92);
       }
-      if (lane == 0) mbar_arrive(&ctl.red_free[bsel]);  // this warp's reads of the buffer are done
-      if (!whole) {
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl.piece_bar);
-        // a barrier of the last set's 4 warps: the piece is complete
-        if (!mbar_wait(&ctl.piece_bar, npiece++ & 1, abort_flag, tmo, p.err)) return false;
-        if (wq == 0 && lane == 0) {  // count it in
-          const int64_t c_lo = owner_of(tu0, U, P), c_hi = owner_of(tu1 - 1, U, P);
-          if (atomicAdd(p.tcount + c_lo, 1) == static_cast<int>(c_hi - c_lo)) {
-            const int nd = ctl.ndeferred;  // only this thread writes the list
-            ctl.deferred[nd] = tile;
-            ctl.ndeferred = nd + 1;
+#pragma unroll
+      for (int pass = 0; pass < kRedPasses; ++pass) {  // tokens [pass * kRedTok, +kRedTok)
+#pragma unroll
+        for (int nb = pass * (NB / kRedPasses); nb < (pass + 1) * (NB / kRedPasses); ++nb)
+#pragma unroll
+          for (int mt2 = 0; mt2 < 2; ++mt2)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int r = rw + 16 * mt2 + 8 * h + g, m0 = 8 * nb + 2 * t - pass * kRedTok;
+              float v0, v1;
+              f2unpack(acc[mt2][nb][h], v0, v1);
+              acc[mt2][nb][h] = 0ull;
+              mine[m0 * kRedLd + r] = v0;
+              mine[(m0 + 1) * kRedLd + r] = v1;
+            }
+        if (warp == kWCompute - 4 && lane == 0) ZC(170 + 4 * pass);
+        if (!tile_sync()) return false;
+        if (warp == kWCompute - 4 && lane == 0) ZC(171 + 4 * pass);
+        // this warp's slice: the (row, token) entries e = q, q + US, .. of its 32-row block, token-major
+        // (consecutive lanes take consecutive rows: coalesced stores)
+        for (int e = q * 32 + lane; e < 32 * kRedTok; e += 32 * US) {
+          const int mr = e >> 5, m = pass * kRedTok + mr, r = rw + (e & 31);
+          if (m >= p.M) continue;
+          float v = red[mr * kRedLd + r];
+#pragma unroll
+          for (int qq = 1; qq < US; ++qq) v += red[(qq * kRedTok + mr) * kRedLd + r];  // set order
+          if (fin && pieces_in_smem) {
+            for (int j = 0; j < npc; ++j)  // CTA order
+              v += reinterpret_cast<const float*>(stages + ctl.piece_slot[j / per_slot] +
+                                                  (j % per_slot) * piece_bytes)[m * kTileN + r];
+          } else if (fin) {
+#pragma unroll 8
+            for (int j = 0; j < npc; ++j) v += __ldcg(piece_of(c + 1 + j) + m * kTileN + r);  // CTA order
           }
+          if (pub)
+            __stcg(piece + m * kTileN + r, v);
+          else
+            store_y(mt, nbase + r, m, v);
         }
+        if (warp == kWCompute - 4 && lane == 0) ZC(172 + 4 * pass);
+        if (pass + 1 < kRedPasses && !tile_sync()) return false;  // the buffers are free again
+        if (warp == kWCompute - 4 && lane == 0) ZC(173 + 4 * pass);
       }
-      return true;
+      if (pub) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.piece_written);
+      }
+      return tile_sync();  // the buffers are free again
     };
 
-    // the sets walk the CTA's units tile by tile; set q takes the units ui = q (mod US)
     // set q takes units ui = q, q + US, ..: stage st = ui / US, one per step,
     // in slot s with fill parity ph (counters, not divisions)
     int f = 0, ui = q, st = 0, s = 0, ph = 0;
-    const int t_lo = nu > 0 ? static_cast<int>(u0 / G) : 0, t_hi = nu > 0 ? static_cast<int>((u1 - 1) / G) : -1;
-    int tile_end = static_cast<int>(min(u1, static_cast<int64_t>(t_lo + 1) * G) - u0);  // first unit past the tile
-    for (int tile = t_lo; ok && tile <= t_hi; ++tile, ++f, tile_end = min(nu, tile_end + G)) {
+    int tile_end = static_cast<int>(min(u1, static_cast<int64_t>(t_first + 1) * G) - u0);  // first unit past the tile
+    for (int tile = t_first; ok && tile <= t_last; ++tile, ++f, tile_end = min(nu, tile_end + G)) {
       for (; ok && ui < tile_end; ui += US) {
         if (!(ok = mbar_wait(&ctl.full[s], ph, abort_flag, tmo, p.err))) break;
         if (warp == 0 && lane == 0 && st < 16) ZC(32 + st);
@@ -1319,63 +1439,13 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
       }
       if (warp == 0 && lane == 0 && f < 8) ZC(64 + f);
       if (warp == kWCompute - 4 && lane == 0 && f < 8) ZC(72 + f);
-      if (ok && !kDebug) ok = flush(tile, f);
+      if (ok && !kDebug) ok = flush(tile);
       if (warp == kWCompute - 4 && lane == 0 && f < 8) ZC(80 + f);
     }
 
-    // Finish the tiles whose count this CTA completed: once every compute
-    // warp is past its main loop the stage memory is idle; the last set brings
-    // every piece into it with bulk copies, sums in CTA order, stores Y and
-    // resets the tile's counter for the next launch.
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&ctl.fix_bar);
-    if (warp == kWCompute - 4 && lane == 0) ZC(88);
-    if (!kDebug && ok && q == kWSets - 1 && (ok = mbar_wait(&ctl.fix_bar, 0, abort_flag, tmo, p.err))) {
-      if (warp == kWCompute - 4 && lane == 0) ZC(89);
-      const int r = rw + lane;
-      const int nd = ctl.ndeferred;
-      const uint32_t piece_bytes = static_cast<uint32_t>(p.M) * kTileN * 4;  // rows 0..M-1 of a piece
-      const int per_round = max(1, static_cast<int>((static_cast<size_t>(S) * SB) / piece_bytes));
-      int nred = 0, nfin = 0;
-      for (int di = 0; di < nd && ok; ++di) {
-        const int tile = ctl.deferred[di];
-        const ZMat& mt = p.mat[mat_of_tile(p, tile)];
-        const int64_t n = static_cast<int64_t>(tile - mt.tile0) * kTileN + r;
-        const int64_t tu0 = static_cast<int64_t>(tile) * G, tu1 = tu0 + G;
-        const int64_t c_lo = owner_of(tu0, U, P), c_hi = owner_of(tu1 - 1, U, P);
-        float sum[TN];
-        for (int64_t cb = c_lo; cb <= c_hi && ok; cb += per_round) {
-          const int np = static_cast<int>(min(static_cast<int64_t>(per_round), c_hi - cb + 1));
-          if (wq == 0 && lane == 0) {
-            __threadfence();
-            fence_proxy_async_global();  // other CTAs' generic writes -> this bulk (async) read
-            mbar_arrive_expect_tx(&ctl.red_bar, np * piece_bytes);
-            for (int k = 0; k < np; ++k) bulk_g2s(stages + k * piece_bytes, piece_of(cb + k, tile), piece_bytes, &ctl.red_bar);
-          }
-          if (!(ok = mbar_wait(&ctl.red_bar, nred & 1, abort_flag, tmo, p.err))) break;
-          ++nred;
-          for (int k = 0; k < np; ++k) {
-            const float* pc = reinterpret_cast<const float*>(stages + k * piece_bytes) + r;
-#pragma unroll
-            for (int m = 0; m < TN; ++m) {
-              if (m < p.M) {
-                const float v = pc[m * kTileN];
-                sum[m] = (cb == c_lo && k == 0) ? v : sum[m] + v;  // ascending CTA order
-              }
-            }
-          }
-          // the stage memory is free for the next round once all 4 warps read it
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&ctl.piece_bar);
-          if (!(ok = mbar_wait(&ctl.piece_bar, (npiece + nfin++) & 1, abort_flag, tmo, p.err))) break;
-        }
-        if (!ok) break;
-#pragma unroll
-        for (int m = 0; m < TN; ++m)
-          if (m < p.M) store_y(mt, n, m, sum[m]);
-        if (wq == 0 && lane == 0) p.tcount[c_lo] = 0;
-      }
-    }
+    // Finish the tiles whose count this CTA completed: after every compute
+    // warp's last tile end the stage memory is idle; every piece is brought
+    // into it with bulk copies (one per lane), summed in CTA order, stored.
   }
 
   // Every role is done.
@@ -1542,7 +1612,7 @@ bool zplan(int64_t M, int64_t tiles, int64_t K, ZPlan* out) {
   const int sms = sm_count_current();
   if (sms <= 0 || sms > kWsZeroBytes / 4) return false;
   pl.ctas = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms, pl.units / kMinUnits)));
-  if ((pl.units + pl.ctas - 1) / pl.ctas > kMaxUnits) return false;
+  if ((pl.units + pl.ctas - 1) / pl.ctas > kMaxUnits || pl.units >= (int64_t{1} << 31)) return false;
   int ctl_bytes, fixed;
   if (pl.tc) {
     pl.arec = act_rec_bytes(pl.tn);
@@ -1553,7 +1623,8 @@ bool zplan(int64_t M, int64_t tiles, int64_t K, ZPlan* out) {
     pl.arec = pl.tn * 136;
     pl.stage_bytes = (w_sets(pl.tn) * (pl.arec + kWRecBytes) + 127) / 128 * 128;
     ctl_bytes = (static_cast<int>(sizeof(WCtl)) + 127) / 128 * 128;
-    fixed = 128 + kRS * kRRecBytes + 2 * kTileN * pl.tn * 4;  // alignment, residual ring, tile-sum buffers
+    // alignment, residual ring, tile partials (one pass over 8 tokens, two over 16 or 32)
+    fixed = 128 + kRS * kRRecBytes + w_sets(pl.tn) * (kTileN + 4) * (pl.tn == 8 ? 8 : pl.tn / 2) * 4;
   }
   pl.nstages = std::min(kMaxStages, (kSmemLimit - ctl_bytes - fixed) / pl.stage_bytes);
   if (pl.nstages < 2) return false;
