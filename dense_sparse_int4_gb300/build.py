@@ -1,9 +1,11 @@
-"""Build the sm_103a shared library (libmq.so) in-tree with nvcc.
+"""Build the sm_103a shared libraries in-tree with nvcc.
 
 Each CUDA translation unit compiles in parallel; the objects link into
 ``dense_sparse_int4_gb300/_build/libmq.so`` with the CUDA runtime linked
 statically, so the library loads without a GPU driver (CPU-only hosts can
-still inspect its exported symbols).
+still inspect its exported symbols).  The rate microbenchmarks that the
+roofline peaks come from (``csrc/peaks.cu``) build into their own
+``_build/libmq_peaks.so``, apart from the product library.
 """
 from __future__ import annotations
 
@@ -18,7 +20,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmq.so")
-SOURCES = ["abi.cu", "status.cu", "quantize.cu", "select.cu", "pack.cu", "gemm.cu", "gemm_decode.cu", "zipper.cu", "noalloc.cu"]
+PEAKS_LIB = os.path.join(BUILD, "libmq_peaks.so")
+PEAKS_SOURCE = "peaks.cu"
+SOURCES = ["abi.cu", "status.cu", "quantize.cu", "select.cu", "pack.cu", "gemm.cu", "zipper.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -56,6 +60,14 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = N
         if force or verbose_ptxas or _stale(obj, src):
             todo.append([cc, *_flags(verbose_ptxas), "-c", src, "-o", obj])
 
+    peaks_src = os.path.join(CSRC, PEAKS_SOURCE)
+    if force or _stale(PEAKS_LIB, peaks_src):
+        tmp_peaks = PEAKS_LIB + f".tmp{os.getpid()}"
+        todo.append([cc, *ARCH, "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-shared", "-o", tmp_peaks, peaks_src,
+                     "-cudart", "static"])
+    else:
+        tmp_peaks = None
+
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
         return cmd, r
@@ -67,6 +79,9 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = N
                     sys.stderr.write(r.stdout + r.stderr)
                 if r.returncode != 0:
                     raise RuntimeError(f"nvcc failed: {' '.join(cmd)}")
+    if tmp_peaks:
+        os.replace(tmp_peaks, PEAKS_LIB)
+        todo = [c for c in todo if tmp_peaks not in c]
     if todo or not os.path.exists(LIB):
         tmp = LIB + f".tmp{os.getpid()}"
         cmd = [cc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *objs, "-cudart", "static"]

@@ -791,11 +791,7 @@ size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 // Bytes of workspace the kernel that mq_w4a4_residual_gemm will run for
 // (M, N, K) on the current device reads and writes.
 size_t gemm_run_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  const char* impl = getenv("MQ_DECODE_IMPL");
-  if (!(impl && strcmp(impl, "cluster") == 0)) {
-    const size_t z = zipper_workspace_bytes(M, N / kTileN, K);
-    if (z) return z;
-  }
+  if (const size_t z = zipper_workspace_bytes(M, N / kTileN, K)) return z;
   const Plan pl = make_plan(M, N, K);
   return pl.ws_partials + pl.ws_counters;
 }
@@ -829,11 +825,6 @@ static mq_status launch_tn(const GemmParams& gp, const Plan& pl, cudaStream_t st
   return pl.ug == 2 ? launch_cfg<TN, (TN <= 64 ? 2 : 1), kDebug>(gp, pl, stream) : launch_cfg<TN, 1, kDebug>(gp, pl, stream);
 }
 
-mq_status gemm_decode_launch(bool* handled, const uint8_t* xq, const uint16_t* xs, int64_t M, const uint8_t* wpk,
-                             int64_t N, int64_t K, const int32_t* row_ptr, const int32_t* col_idx, int64_t nnzb,
-                             const uint8_t* rpk, void* y, mq_dtype yt, int32_t* dots_w, int32_t* dots_r,
-                             cudaStream_t stream);
-
 mq_status zipper_launch(bool* handled, int nmat, const uint8_t* const* wpk, const int64_t* N,
                         const int32_t* const* row_ptr, const int32_t* const* col_idx, const int64_t* nnzb,
                         const uint8_t* const* rpk, void* const* y, const int64_t* ldy, mq_dtype yt, const uint8_t* xq,
@@ -846,14 +837,8 @@ mq_status gemm_launch(const uint8_t* xq, const uint16_t* xs, int64_t M, const ui
                       int64_t ldy, mq_dtype yt, int32_t* dots_w, int32_t* dots_r, void* ws, size_t ws_bytes,
                       cudaStream_t stream) {
   bool handled = false;
-  const char* impl = getenv("MQ_DECODE_IMPL");
-  if (impl && strcmp(impl, "cluster") == 0 && ldy == N) {
-    // Decode batches: the cluster split-K kernel (gemm_decode.cu), when it covers the shape.
-    const mq_status ds = gemm_decode_launch(&handled, xq, xs, M, wpk, N, K, row_ptr, col_idx, nnzb, rpk, y, yt,
-                                            dots_w, dots_r, stream);
-    if (handled || ds != MQ_OK) return ds;
-  } else {
-    // Decode batches: the stream-K tensor-memory kernel (zipper.cu), when it covers the shape.
+  {
+    // Decode batches: the stream-K kernel (zipper.cu), when it covers the shape.
     void* yy = y;
     const mq_status zs = zipper_launch(&handled, 1, &wpk, &N, &row_ptr, &col_idx, &nnzb, &rpk, &yy, &ldy, yt, xq, xs,
                                        nullptr, MQ_F16, 0, nullptr, nullptr, M, K, dots_w, dots_r, ws, ws_bytes,

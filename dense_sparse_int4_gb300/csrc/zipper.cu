@@ -180,6 +180,21 @@ __device__ __forceinline__ void st_release_gpu(int32_t* p, int v) {
 __device__ __forceinline__ void st_relaxed_gpu(int32_t* p, int v) {
   asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+
+// Self-checks, compiled in with MQ_ZCHECK only: a failed bounds check records
+// bit 8 + site in the device error word and skips the access; a wait that gave
+// up records bit 24 + site.
+#ifdef MQ_ZCHECK
+__device__ __forceinline__ bool zcheck(bool ok, int bit, uint32_t* err) {
+  if (!ok) atomicOr(err, 1u << bit);
+  return ok;
+}
+#define ZOK(cond, site) zcheck((cond), 8 + (site), p.err)
+#define ZW(ok, site) zcheck((ok), 24 + (site), p.err)
+#else
+#define ZOK(cond, site) true
+#define ZW(ok, site) (ok)
+#endif
 __device__ __forceinline__ void named_bar(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -194,6 +209,26 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, 
   for (uint32_t n = 1;; ++n) {
     __nanosleep(32);
     if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 63u) == 0) {
+      if (*abort_flag) return false;
+      const uint64_t now = globaltimer();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > timeout_ns) {
+        atomicOr(err_word, kDevErrTimeout);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+// Bounded wait until a shared-memory counter (advanced by another warp of the CTA) exceeds `target`.
+__device__ __forceinline__ bool count_wait(volatile int* v, int target, volatile int* abort_flag, uint64_t timeout_ns,
+                                           uint32_t* err_word) {
+  if (*v > target) return true;
+  uint64_t t0 = 0;
+  for (uint32_t n = 1;; ++n) {
+    if (*v > target) return true;
     if ((n & 63u) == 0) {
       if (*abort_flag) return false;
       const uint64_t now = globaltimer();
@@ -331,12 +366,18 @@ __device__ __forceinline__ float act_value(const uint16_t* x, int64_t i, bool bf
 __device__ __forceinline__ int64_t first_unit(int64_t c, int64_t U, int64_t P) { return c * U / P; }
 __device__ __forceinline__ int64_t owner_of(int64_t u, int64_t U, int64_t P) { return ((u + 1) * P - 1) / U; }
 
+__device__ __forceinline__ int mat_end_tile(const ZParams& p, int t);
 __device__ __forceinline__ int mat_of_tile(const ZParams& p, int t) {
   int mi = 0;
 #pragma unroll
   for (int i = 1; i < kMaxMats; ++i)
     if (i < p.nmat && t >= p.mat[i].tile0) mi = i;
   return mi;
+}
+
+__device__ __forceinline__ int mat_end_tile(const ZParams& p, int t) {  // one past the matrix's last tile
+  const int mi = mat_of_tile(p, t);
+  return mi + 1 < p.nmat ? p.mat[mi + 1].tile0 : p.tiles;
 }
 
 // ---------------------------------------------------------------------------
@@ -904,7 +945,7 @@ struct __align__(16) WCtl {
   int32_t rpos[kMaxUnits][2];
   const uint8_t* rsrc[kMaxUnits];  // residual records of the unit's matrix
   int abort_flag;
-  uint32_t piece_slot[kMaxStages];  // shared-memory offset of handed-over slot k
+  volatile int r_issued;  // residual records issued so far (the producer issues them in ring order)
 };
 
 // D(16x8, fp32) += A(16x32, E4M3, row-major) * B(32x8, E4M3, column-major).
@@ -960,7 +1001,10 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
   // the pieces go into stage slots no stage needs any more, per_slot to a slot, if they fit in all slots
   const int per_slot = SB / static_cast<int>(piece_bytes);
   const int need_slots = per_slot > 0 ? (npc + per_slot - 1) / per_slot : S + 1;
-  const bool pieces_in_smem = need_slots <= S;
+  // (a partial last stage's slot is never released by the sets without a unit in it: not handed over)
+  const bool pieces_in_smem = need_slots <= S - (nu % US != 0 ? 1 : 0);
+  // the k-th handed-over slot is the one stage nstg + k would take
+  auto piece_slot = [&](int k) -> uint32_t { return static_cast<uint32_t>((nstg + k) % S) * SB; };
   auto piece_of = [&](int64_t cc) -> float* { return p.part + cc * (TN * static_cast<int64_t>(kTileN)); };
   volatile int* abort_flag = &ctl.abort_flag;
   const uint64_t tmo = p.timeout_ns;
@@ -986,6 +1030,7 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
     if (lane == 17) mbar_init(&ctl.pieces_in, 1);
     if (lane == 14) mbar_init(&ctl.exit_bar, kWThreads / 32);
     if (lane == 15) ctl.abort_flag = 0;
+    if (lane == 16) ctl.r_issued = 0;
     fence_mbar_init();
     if (lane == 0) ZC(11);
   }
@@ -993,6 +1038,11 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
   if (threadIdx.x == 0) ZC(12);
   pdl_trigger();
   auto stage = [&](int s) { return stages + static_cast<size_t>(s) * SB; };
+  auto copy_ok = [&](const CopyDesc& d) {  // a stage copy stays inside its slot, 16-byte aligned
+    return ZOK(d.dst + d.bytes <= static_cast<uint32_t>(SB) && (d.bytes & 15u) == 0 && (d.dst & 15u) == 0 &&
+                   (reinterpret_cast<uintptr_t>(d.src) & 15u) == 0,
+               1);
+  };
   auto wrec = [&](int64_t u) -> const uint8_t* {
     const int t = static_cast<int>(u / G), g = static_cast<int>(u - static_cast<int64_t>(t) * G);
     const ZMat& mt = p.mat[mat_of_tile(p, t)];
@@ -1035,7 +1085,8 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
           const unsigned nxt = wm & smask & above;
           const int end = nxt ? __ffs(nxt) - 1 : last;
           const ZMat& mt = p.mat[mi];
-          CopyDesc& d = ctl.cp[st][__popc(wm & smask & below)];
+          const int ix = __popc(wm & smask & below);
+          CopyDesc& d = ctl.cp[ZOK(st < kMaxStg && ix < kCopiesPerStage, 0) ? st : 0][ix & (kCopiesPerStage - 1)];
           d.src = mt.wpk + (static_cast<int64_t>(tt - mt.tile0) * G + gg) * kWRecBytes;
           d.dst = static_cast<uint32_t>(kAct + k * kWRecBytes);
           d.bytes = static_cast<uint32_t>((end - lane) * kWRecBytes);
@@ -1043,7 +1094,8 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
         if ((am >> lane) & 1u) {
           const unsigned nxt = am & smask & above;
           const int end = nxt ? __ffs(nxt) - 1 : last;
-          CopyDesc& d = ctl.cp[st][nw + __popc(am & smask & below)];
+          const int ix = nw + __popc(am & smask & below);
+          CopyDesc& d = ctl.cp[ZOK(st < kMaxStg && ix < kCopiesPerStage, 0) ? st : 0][ix & (kCopiesPerStage - 1)];
           d.src = p.act + static_cast<int64_t>(gg) * kArec;
           d.dst = static_cast<uint32_t>(k * kArec);
           d.bytes = static_cast<uint32_t>((end - lane) * kArec);
@@ -1066,7 +1118,8 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
     for (int st = 0; st < pre; ++st) {
       if (lane < kCopiesPerStage) {
         const CopyDesc d = ctl.cp[st][lane];
-        if (d.bytes && d.dst >= static_cast<uint32_t>(kAct)) bulk_g2s(stage(st) + d.dst, d.src, d.bytes, &ctl.full[st]);
+        if (d.bytes && d.dst >= static_cast<uint32_t>(kAct) && copy_ok(d))
+          bulk_g2s(stage(st) + d.dst, d.src, d.bytes, &ctl.full[st]);
       }
     }
     __syncwarp();
@@ -1076,11 +1129,12 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
     for (int i = lane; i < pre * kCopiesPerStage; i += 32) {
       const int st = i / kCopiesPerStage;
       const CopyDesc d = ctl.cp[st][i % kCopiesPerStage];
-      if (d.bytes && d.dst < static_cast<uint32_t>(kAct)) bulk_g2s(stage(st) + d.dst, d.src, d.bytes, &ctl.full[st]);
+      if (d.bytes && d.dst < static_cast<uint32_t>(kAct) && copy_ok(d))
+        bulk_g2s(stage(st) + d.dst, d.src, d.bytes, &ctl.full[st]);
     }
     __syncwarp();
     if (lane == 0) ZC(16);
-    bool ok = mbar_wait(&ctl.map_ready, 0, abort_flag, tmo, p.err);
+    bool ok = ZW(mbar_wait(&ctl.map_ready, 0, abort_flag, tmo, p.err), 7);
     ok = __all_sync(0xFFFFFFFFu, ok);
     // Two cursors, neither waiting on the other: the residual records in ring
     // order (those of issued stages, each once its ring slot is free), and
@@ -1111,6 +1165,8 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
           bulk_g2s(rring + slot * kRRecBytes, ctl.rsrc[f >> 1] + static_cast<int64_t>(e) * kRRecBytes, kRRecBytes,
                    &ctl.r_full[slot]);
         }
+        const int nrec = __popc(__ballot_sync(0xFFFFFFFFu, lane < n && e >= 0));
+        if (lane == 0 && nrec) ctl.r_issued = ctl.r_issued + nrec;
         rf += n;
         progress = n > 0;
       }
@@ -1123,7 +1179,7 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
         if (__shfl_sync(0xFFFFFFFFu, go, 0)) {
           if (lane < kCopiesPerStage) {
             const CopyDesc d = ctl.cp[bst][lane];
-            if (d.bytes) bulk_g2s(stage(bs) + d.dst, d.src, d.bytes, &ctl.full[bs]);
+            if (d.bytes && copy_ok(d)) bulk_g2s(stage(bs) + d.dst, d.src, d.bytes, &ctl.full[bs]);
           }
           if (lane == 0 && bst < 16) ZC(16 + bst);
           ++bst;
@@ -1145,6 +1201,7 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
           } else if (idle == 16) {
             idle_since = now;
           } else if (now - idle_since > tmo) {
+            ZW(false, 7);
             atomicOr(p.err, kDevErrTimeout);
             *abort_flag = 1;
             give_up = 1;
@@ -1159,8 +1216,7 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
     if (ok && finishes && pieces_in_smem && lane == 0) {
       for (int k = 0; k < need_slots; ++k) {
         const int v = nstg + k, slot = v % S;  // the slot's last fill was stage v - S; its phases are waited in order
-        if (v >= S && !mbar_wait_sleep(&ctl.empty[slot], ((v / S) - 1) & 1, abort_flag, tmo, p.err)) break;
-        ctl.piece_slot[k] = static_cast<uint32_t>(slot) * SB;
+        if (v >= S && !ZW(mbar_wait_sleep(&ctl.empty[slot], ((v / S) - 1) & 1, abort_flag, tmo, p.err), 7)) break;
         mbar_arrive(&ctl.slot_free[k]);
       }
     }
@@ -1171,7 +1227,7 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
     bool ok = true;
     if (publishes) {  // release this CTA's piece once every compute warp has written its share
       if (lane == 0) {
-        ok = mbar_wait_sleep(&ctl.piece_written, 0, abort_flag, tmo, p.err);
+        ok = ZW(mbar_wait_sleep(&ctl.piece_written, 0, abort_flag, tmo, p.err), 4);
         if (ok) {
           fence_acq_rel_gpu();
           st_relaxed_gpu(p.tcount + c, 1);
@@ -1186,19 +1242,20 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
       for (int j0 = 0; ok && j0 < npc; j0 += 32) {
         const int j = j0 + lane;
         bool seen = true;
-        if (j < npc && (seen = flag_wait(p.tcount + c + 1 + j, abort_flag, tmo, p.err))) p.tcount[c + 1 + j] = 0;
+        if (j < npc && ZOK(c + 1 + j < P, 4) && (seen = ZW(flag_wait(p.tcount + c + 1 + j, abort_flag, tmo, p.err), 5)))
+          p.tcount[c + 1 + j] = 0;
         ok = __all_sync(0xFFFFFFFFu, seen);
       }
       if (lane == 0) ZC(89);
       if (ok && pieces_in_smem) {
         if (lane == 0) mbar_arrive_expect_tx(&ctl.pieces_in, npc * piece_bytes);
         for (int k = 0; ok && k < need_slots; ++k) {  // slot k: pieces k * per_slot ..
-          if (lane == 0) ok = mbar_wait_sleep(&ctl.slot_free[k], 0, abort_flag, tmo, p.err);
+          if (lane == 0) ok = ZW(mbar_wait_sleep(&ctl.slot_free[k], 0, abort_flag, tmo, p.err), 6);
           if (!(ok = __shfl_sync(0xFFFFFFFFu, ok, 0))) break;
           const int j = k * per_slot + lane;
-          if (lane < per_slot && j < npc) {
+          if (lane < per_slot && j < npc && ZOK(piece_slot(k) + (lane + 1) * piece_bytes <= static_cast<uint32_t>(S) * SB, 5)) {
             fence_proxy_async_global();  // the pieces were written through the generic proxy
-            bulk_g2s(stages + ctl.piece_slot[k] + lane * piece_bytes, piece_of(c + 1 + j), piece_bytes,
+            bulk_g2s(stages + piece_slot(k) + lane * piece_bytes, piece_of(c + 1 + j), piece_bytes,
                      &ctl.pieces_in);
           }
         }
@@ -1257,7 +1314,7 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
         ZC(9);
       }
     }
-    bool ok = mbar_wait(&ctl.map_ready, 0, abort_flag, tmo, p.err);
+    bool ok = ZW(mbar_wait(&ctl.map_ready, 0, abort_flag, tmo, p.err), 0);
     pdl_wait();  // Y and the workspace pieces may still be in use by the preceding kernel
     // accumulators: [mt][nb] pairs {row r, tokens 8nb+2t, +1}, {row r+8, same tokens}
     uint64_t acc[2][NB][2];
@@ -1346,7 +1403,7 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
     auto tile_sync = [&]() -> bool {  // all compute warps (bounded)
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.tile_bar);
-      return mbar_wait(&ctl.tile_bar, (nsync++) & 1, abort_flag, tmo, p.err);
+      return ZW(mbar_wait(&ctl.tile_bar, (nsync++) & 1, abort_flag, tmo, p.err), 2);
     };
     auto flush = [&](int tile) -> bool {
       const ZMat& mt = p.mat[mat_of_tile(p, tile)];
@@ -1356,7 +1413,7 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
       float* piece = pub ? piece_of(c) : nullptr;
       float* mine = red + q * (kRedTok * kRedLd);
       if (fin) {
-        if (!mbar_wait(&ctl.pieces_in, 0, abort_flag, tmo, p.err)) return false;
+        if (!ZW(mbar_wait(&ctl.pieces_in, 0, abort_flag, tmo, p.err), 3)) return false;
         if (warp == 0 && lane == 0) ZC(92);
       }
 #pragma unroll
@@ -1387,16 +1444,19 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
           for (int qq = 1; qq < US; ++qq) v += red[(qq * kRedTok + mr) * kRedLd + r];  // set order
           if (fin && pieces_in_smem) {
             for (int j = 0; j < npc; ++j)  // CTA order
-              v += reinterpret_cast<const float*>(stages + ctl.piece_slot[j / per_slot] +
-                                                  (j % per_slot) * piece_bytes)[m * kTileN + r];
+              if (ZOK(piece_slot(j / per_slot) + (j % per_slot) * piece_bytes + (m * kTileN + r) * 4u <
+                          static_cast<uint32_t>(S) * SB, 6))
+                v += reinterpret_cast<const float*>(stages + piece_slot(j / per_slot) +
+                                                    (j % per_slot) * piece_bytes)[m * kTileN + r];
           } else if (fin) {
 #pragma unroll 8
             for (int j = 0; j < npc; ++j) v += __ldcg(piece_of(c + 1 + j) + m * kTileN + r);  // CTA order
           }
-          if (pub)
-            __stcg(piece + m * kTileN + r, v);
-          else
+          if (pub) {
+            if (ZOK(c < P && m < TN, 9)) __stcg(piece + m * kTileN + r, v);
+          } else if (ZOK(tile >= mt.tile0 && tile < mat_end_tile(p, tile) && m < p.M, 8)) {
             store_y(mt, nbase + r, m, v);
+          }
         }
         if (warp == kWCompute - 4 && lane == 0) ZC(172 + 4 * pass);
         if (pass + 1 < kRedPasses && !tile_sync()) return false;  // the buffers are free again
@@ -1415,7 +1475,7 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
     int tile_end = static_cast<int>(min(u1, static_cast<int64_t>(t_first + 1) * G) - u0);  // first unit past the tile
     for (int tile = t_first; ok && tile <= t_last; ++tile, ++f, tile_end = min(nu, tile_end + G)) {
       for (; ok && ui < tile_end; ui += US) {
-        if (!(ok = mbar_wait(&ctl.full[s], ph, abort_flag, tmo, p.err))) break;
+        if (!(ok = ZW(mbar_wait(&ctl.full[s], ph, abort_flag, tmo, p.err), 0))) break;
         if (warp == 0 && lane == 0 && st < 16) ZC(32 + st);
         if (warp == kWCompute - 4 && lane == 0 && st < 16) ZC(48 + st);
         const uint8_t* sg = stage(s);
@@ -1425,7 +1485,11 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
         const int e = ctl.map[ui][half];
         if (e >= 0) {  // the residual block of this warp's half
           const int cpos = ctl.rpos[ui][half], slot = cpos % kRS;
-          if (!(ok = mbar_wait(&ctl.r_full[slot], (cpos / kRS) & 1, abort_flag, tmo, p.err))) break;
+          // Sets run up to a few stages apart, so this slot may still hold (or await) a record two
+          // laps older: its parity would alias.  Once record cpos is issued, every older record of
+          // the slot has been consumed and the newer one waits for this warp: the parity is exact.
+          if (!(ok = ZW(count_wait(&ctl.r_issued, cpos, abort_flag, tmo, p.err), 1))) break;
+          if (!(ok = ZW(mbar_wait(&ctl.r_full[slot], (cpos / kRS) & 1, abort_flag, tmo, p.err), 1))) break;
           const uint8_t* rrec = rring + slot * kRRecBytes;
           group_product(rrec, 1024, rw - 64 * half, reinterpret_cast<const uint16_t*>(rrec + kRRecScales), img,
                         u0 + ui, e);
@@ -1751,6 +1815,15 @@ bool zipper_plan_info(int64_t M, int64_t tiles, int64_t K, int32_t* form, int32_
   *ctas = pl.ctas;
   *stages = pl.nstages;
   return true;
+}
+
+// The kernel choice for (M, N, K) on the current device: {form (3: tensor
+// memory, 4: warp MMA), tokens per tile, 1, CTAs, stages} for the decode
+// kernel, else zeros (the general kernel runs).
+mq_status gemm_plan_info(int64_t M, int64_t N, int64_t K, int32_t* info) {
+  for (int i = 0; i < 5; ++i) info[i] = 0;
+  if (zipper_plan_info(M, N / kTileN, K, &info[0], &info[1], &info[3], &info[4])) info[2] = 1;
+  return MQ_OK;
 }
 
 // One launch of the decode kernel over `nmat` matrices that share the

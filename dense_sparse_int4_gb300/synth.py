@@ -98,6 +98,26 @@ def device_weights(N: int, K: int, seed: int, device, sigma: float = 0.02):
     return (torch.randn((N, K), generator=g, device=device, dtype=torch.float32) * sigma).to(torch.float16)
 
 
+def inject_concentrated_device(w, seed: int, frac: float = 0.02, value: float = 1.0):
+    """In place on a device [N, K] fp16 tensor: a seeded `frac` of the 64x128
+    blocks get one +-value entry per row (the device counterpart of
+    inject_concentrated, drawn with torch's seeded generator: for timing
+    workloads too large to draw on the host)."""
+    import torch
+    N, K = w.shape
+    nbr, G = N // 64, K // 128
+    g = torch.Generator(device=w.device)
+    g.manual_seed(int(seed) + 7919)
+    nblk = max(1, int(round(frac * nbr * G)))
+    blocks = torch.randperm(nbr * G, generator=g, device=w.device)[:nblk]
+    br, gg = blocks // G, blocks % G
+    rows = br[:, None] * 64 + torch.arange(64, device=w.device)[None, :]
+    cols = gg[:, None] * 128 + torch.randint(0, 128, (nblk, 64), generator=g, device=w.device)
+    signs = torch.randint(0, 2, (nblk, 64), generator=g, device=w.device).to(torch.float16) * 2 - 1
+    w[rows.reshape(-1), cols.reshape(-1)] = (signs * value).reshape(-1)
+    return w
+
+
 # --------------------------------------------------------------------------
 # The workloads
 # --------------------------------------------------------------------------

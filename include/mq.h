@@ -284,14 +284,13 @@ mq_status mq_debug_group_dots(const uint8_t* xq, const uint16_t* xs, int64_t M, 
  * Which kernel mq_w4a4_residual_gemm (and the no-alloc and debug forms) runs
  * for a problem of M tokens, N outputs and K inputs on the current device.
  *   info  host array of 5 int32, written:
- *         [0] the decode kernel (split-K over thread-block clusters, up to
- *             32 tokens): 1 = its warp-MMA variant (default up to 16 tokens),
- *             2 = its tensor-memory variant (default above 16); 0 = the
- *             general kernel.  The environment variable MQ_DECODE_VARIANT =
- *             "warp" or "tc" forces one variant;
- *         for the decode kernel, [1] tokens per tile (8, 16 or 32), [2] CTAs
- *         per cluster, [3] clusters launched, [4] weight stages in shared
- *         memory; zeros for the general kernel.
+ *         [0] the decode kernel (stream-K over every SM, up to 32 tokens):
+ *             4 = its warp-MMA form (the default), 3 = its tensor-memory form
+ *             (taken when the environment variable MQ_DECODE_VARIANT is
+ *             "tc"); 0 = the general kernel;
+ *         for the decode kernel, [1] tokens per tile (8, 16 or 32), [2] 1,
+ *         [3] CTAs launched, [4] weight stages in shared memory; zeros for
+ *         the general kernel.
  * MQ_ERR_INVALID_ARG for bad sizes (the same rules as the GEMM) or NULL info;
  * MQ_ERR_UNSUPPORTED_DEVICE if the current device is not compute capability 10.3.
  * Launches nothing.

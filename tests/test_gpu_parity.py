@@ -309,6 +309,38 @@ def test_fused_linear_matches_oracle(M, K, Ns, budget, x_dtype):
     assert mq.gemm_plan(M, sum(Ns), K)["decode"] == (M <= 32)
 
 
+@pytest.mark.parametrize("variant", ["warp", "tc"])
+def test_dense_residual_back_to_back(variant, monkeypatch):
+    """Every block residual (budget 1): each stage fills the residual ring a
+    full lap, and with ~4 stages per CTA the compute sets drift apart.  Twelve
+    calls back to back on one stream and workspace (each launch overlapping
+    the previous one's tail) must all equal the oracle: a set must never take
+    a ring slot's older record for its own."""
+    monkeypatch.setenv("MQ_DECODE_VARIANT", variant)
+    M, N, K = 4 if variant == "warp" else 32, 8192, 4096
+    x = synth.activations(M, K, seed=91, count=synth.n_outliers(K))
+    w = synth.weights(N, K, seed=92)
+    xcal = synth.calibration(K, seed=93, count=synth.n_outliers(K))
+    pl = mq.prepare_linear(dev_half(w), dev_half(xcal), 1.0)
+    p = O.prepare(w, xcal, False, 1.0)
+    assert pl.nnzb == p.ksel == (N // 64) * (K // 128)
+    xt = dev_half(x)
+    ys = [torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda") for _ in range(12)]
+    ws, _ = mq.linear_workspace(M, K, [N], "cuda")
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for y in ys:
+            mq.fused_linear(xt, [pl], outs=[y], ws=ws, stream=stream)
+    stream.synchronize()
+    mq.check_device_error()
+    qx, sx = O.quantize_act(x, False)
+    yo, a = O.linear(qx, sx, p)
+    for y in ys:
+        check_close(y.cpu().numpy(), yo, a)
+    assert mq.gemm_plan(M, N, K)["variant"] == ("warp-mma" if variant == "warp" else "tensor-memory")
+
+
 # ----------------------------------------------------------------------------
 # full-size workloads, sampled outputs
 # ----------------------------------------------------------------------------

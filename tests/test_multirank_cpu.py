@@ -58,7 +58,8 @@ def _ref_worker(rank: int, ws: int, port: int, q):
     class Args:
         steps, warmup, gpus = 1, 0, ws
     called = []
-    bench.oracle_sample = lambda seconds=0.0, max_pairs=None: (called.append(1) or (1.0, 0.5, ["q@M4"]))
+    bench.oracle_prepare = lambda names: {n: None for n in names}
+    bench.oracle_run = lambda preps, pairs, seconds, max_pairs=None: (called.append(1) or (1e9, 0.5, ["q@M4"]))
     line = bench.run_reference(Args())
     q.put((rank, line is not None, len(called)))
 
