@@ -2,17 +2,24 @@
 
 Default workload: the decode linears of a Llama-3-8B-shaped layer (q, k, v, o,
 gate, up, down; random-init weights) at M = 4, 8, 16 and 32 tokens, 10 %
-residual budget.  One step = for each M: quantize the four distinct layer
-inputs, then the seven fused GEMMs, each on its own copy of the packed weights
-(4 copies rotate, so every step streams ~0.5 GB of weights: inputs larger than
-L2).  The step is captured once in a CUDA graph and replayed.
+residual budget.  One step = for each M, the layer's four fused calls
+(``mq_w4a4_residual_linear``, quantizer included): q/k/v on the attention
+input, o, gate/up on the MLP input, down.  Each M streams its own copy of the
+packed weights (4 copies, ~0.47 GB per step: inputs larger than L2).  The step
+is captured once in a CUDA graph; the timed region replays it, nothing else.
 
-Printed: one JSON line.  value = aggregate weight GB/s (base + residual bytes
-streamed by the GEMMs / step time, all ranks); roofline = the GEMM kernel's
-algorithmic bytes per launch / its average event-timed duration vs the
-measured HBM copy bandwidth; cpu_baseline = the oracle on host cores on a
-bounded sample; e2e = the same metric with host buffers (H2D of the inputs,
-D2H of the outputs inside every step).
+Printed: one JSON line.  value = aggregate weight GB/s (base + residual +
+block-list bytes streamed per step / step time, all ranks).  roofline: the
+fused GEMM's algorithmic bytes per launch (weights + X + Y) over its time per
+launch, taken from the timed step itself (step time / launches: the
+activation-image launches and gaps are charged to it, a lower bound), against
+the measured HBM copy bandwidth.  cpu_baseline: the oracle on the host cores,
+single-threaded and on every core.  e2e: the same metric with host buffers
+(H2D of the inputs, D2H of the outputs inside every step).  extra: per-call and
+per-linear event timings, the residual overhead against the budget-0 kernel,
+the prefill shape against a measured E4M3 tensor peak, the 32-layer stack, the
+Qwen3-32B sweep, distortion recovered against budget, a W16A16 (torch bf16)
+context and the legacy mma.sync rates.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -22,6 +29,7 @@ import argparse
 import ctypes
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -38,9 +46,11 @@ WORKLOAD = "llama3-8b-decode-linears"
 MS = (4, 8, 16, 32)
 BUDGET = 0.10
 COPIES = len(MS)
-INPUTS = {"attn": ("q", "k", "v"), "o": ("o",), "mlp": ("gate", "up"), "down": ("down",)}
+# the layer's fused calls: input name -> the linears that share it
+CALLS = (("attn", ("q", "k", "v")), ("o", ("o",)), ("mlp", ("gate", "up")), ("down", ("down",)))
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+E4M3_PER_BF16 = 2.0  # nominal dense-rate ratio, used only when the E4M3 microbenchmark cannot run
 
 
 # ---------------------------------------------------------------------------
@@ -90,26 +100,59 @@ def aggregate(per_rank_units: float, elapsed_s: float, device=None) -> tuple[flo
 
 
 # ---------------------------------------------------------------------------
-# clocks during the timed region
+# clocks during the timed region: NVML polled every few ms (a timed region of
+# tens of ms still gets samples), else nvidia-smi at 100 ms.  Read-only.
 # ---------------------------------------------------------------------------
 
-CLOCK_Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-           "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-           "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
 
 
 class ClockSampler:
-    def __init__(self, gpu_index: int, period_ms: int = 100):
-        self.gpu = gpu_index
-        self.period = period_ms
-        self.samples = []  # (t, sm, max, reasons)
+    def __init__(self, device_index: int, period_ms: float = 2.0):
+        self.dev = device_index
+        self.period = period_ms / 1e3
+        self.samples = []  # (t, sm_mhz, max_mhz, reasons)
         self._stop = threading.Event()
         self._th = None
+        self.source = None
 
-    def _run(self):
+    def _nvml_handle(self):
+        import torch
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit")
+        h = ctypes.c_void_p()
+        uuid = str(getattr(torch.cuda.get_device_properties(self.dev), "uuid", "") or "")
+        ok = False
+        if uuid:
+            for u in (uuid, "GPU-" + uuid):
+                if nv.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(h)) == 0:
+                    ok = True
+                    break
+        if not ok and nv.nvmlDeviceGetHandleByIndex_v2(self.dev, ctypes.byref(h)) != 0:
+            raise OSError("nvml handle")
+        return nv, h
+
+    def _run_nvml(self, nv, h):
+        clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and \
+                    nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                reasons = []
+                if get_reasons(h, ctypes.byref(rs)) == 0:
+                    reasons = [n for b, n in REASON_BITS.items() if rs.value & b]
+                self.samples.append((time.perf_counter(), float(clk.value), float(mx.value), reasons))
+            time.sleep(self.period)
+
+    def _run_smi(self):
+        q = ("index,clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
         try:
-            p = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={CLOCK_Q}", "--format=csv,noheader,nounits",
-                                  f"-lms={self.period}"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            p = subprocess.Popen(["nvidia-smi", f"--id={self.dev}", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                  "-lms=100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             return
         try:
@@ -117,16 +160,12 @@ class ClockSampler:
                 if self._stop.is_set():
                     break
                 f = [x.strip() for x in line.split(",")]
-                if len(f) < 9:
-                    continue
                 try:
                     sm, mx = float(f[1]), float(f[2])
-                except ValueError:
+                except (ValueError, IndexError):
                     continue
-                reasons = []
-                for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), f[5:9]):
-                    if v.lower() == "active":
-                        reasons.append(name)
+                names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+                reasons = [n for n, v in zip(names, f[3:7]) if v.lower() == "active"]
                 self.samples.append((time.perf_counter(), sm, mx, reasons))
         finally:
             p.terminate()
@@ -136,7 +175,13 @@ class ClockSampler:
                 p.kill()
 
     def start(self):
-        self._th = threading.Thread(target=self._run, daemon=True)
+        try:
+            nv, h = self._nvml_handle()
+            self.source = "nvml, 2 ms"
+            self._th = threading.Thread(target=self._run_nvml, args=(nv, h), daemon=True)
+        except (OSError, AttributeError):
+            self.source = "nvidia-smi, 100 ms"
+            self._th = threading.Thread(target=self._run_smi, daemon=True)
         self._th.start()
 
     def stop(self):
@@ -150,18 +195,18 @@ class ClockSampler:
         if not used and self.samples:  # region shorter than the sampling period: nearest samples
             used = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:2]
         if not used:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": self.source}
         reasons = sorted({r for s in used for r in s[3]})
         return {"sm_mhz": statistics.median(s[1] for s in used), "sm_max_mhz": max(s[2] for s in used),
-                "reasons": reasons, "samples": len(inside)}
+                "reasons": reasons, "samples": len(inside), "source": self.source}
 
 
 # ---------------------------------------------------------------------------
-# peaks
+# peaks and the committed ncu traffic figure
 # ---------------------------------------------------------------------------
 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_gemm_traffic.json")
-TRAFFIC_SOURCES = ("dense_sparse_int4_gb300/csrc/gemm_decode.cu", "dense_sparse_int4_gb300/csrc/mq_internal.cuh")
+TRAFFIC_SOURCES = ("dense_sparse_int4_gb300/csrc/zipper.cu", "dense_sparse_int4_gb300/csrc/mq_internal.cuh")
 
 
 def kernel_source_sha256() -> str:
@@ -174,8 +219,8 @@ def kernel_source_sha256() -> str:
 
 
 def measured_traffic():
-    """DRAM bytes per decode-GEMM launch (mean over one step's launches) from the
-    committed ncu capture, or None when that capture is of another kernel source."""
+    """DRAM bytes per fused-GEMM launch from the committed ncu capture, or None
+    when that capture is of another kernel source."""
     try:
         with open(TRAFFIC_FILE) as f:
             d = json.load(f)
@@ -194,6 +239,35 @@ def peaks() -> dict:
     except (OSError, KeyError, ValueError):
         return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS, "bf16_tflops_sustained": 1700.0,
                 "source": "fallback"}
+
+
+def rate_microbenchmarks() -> dict:
+    """Measured tensor rates on this GPU (libmq_peaks.so): dense tcgen05 E4M3 and legacy mma.sync."""
+    from dense_sparse_int4_gb300 import build as b
+    out = {}
+    try:
+        L = ctypes.CDLL(b.PEAKS_LIB)
+    except OSError as e:
+        return {"error": str(e)}
+    L.mqp_tc_e4m3.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
+    L.mqp_mma_sync.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_double)]
+    f, cyc = ctypes.c_double(), ctypes.c_double()
+    best = 0.0
+    for _ in range(3):
+        rc = L.mqp_tc_e4m3(40000, ctypes.byref(f), ctypes.byref(cyc))
+        if rc != 0:
+            out["tc_e4m3_error"] = rc
+            break
+        best = max(best, f.value)
+    if best:
+        out["tcgen05_e4m3_dense_tflops"] = round(best / 1e12, 1)
+        out["tcgen05_e4m3_how"] = "128x256x32 kind::f8f6f4 MMAs from shared memory, one CTA per SM, best of 3 (CUDA events)"
+    for kind, name in ((0, "mma_sync_e4m3_m16n8k32_tflops"), (1, "mma_sync_s8_m16n8k32_tops"),
+                       (2, "mma_sync_s4_m16n8k64_tops")):
+        o = ctypes.c_double()
+        rc = L.mqp_mma_sync(kind, 4000, ctypes.byref(o))
+        out[name] = round(o.value / 1e12, 1) if rc == 0 else f"error {rc}"
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -221,102 +295,6 @@ class GraphEvents:
         return out.value
 
 
-# ---------------------------------------------------------------------------
-# the workload
-# ---------------------------------------------------------------------------
-
-def linear_by_name():
-    from dense_sparse_int4_gb300 import synth
-    return {l.name: l for l in synth.LLAMA3_8B}
-
-
-def setup(dev, budget=BUDGET):
-    import torch
-    from dense_sparse_int4_gb300 import mq, synth
-    lins = linear_by_name()
-    base = {}
-    for i, (name, lin) in enumerate(lins.items()):
-        w = synth.device_weights(lin.N, lin.K, seed=1000 + i, device=dev)
-        xcal = torch.from_numpy(synth.calibration(lin.K, seed=i, count=synth.n_outliers(lin.K)).view(np.float16)).to(dev)
-        base[name] = mq.prepare_linear(w, xcal, budget)
-        del w
-    torch.cuda.synchronize()
-    copies = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(COPIES - 1)]
-    xs_host, xs_dev = {}, {}
-    for M in MS:
-        for inp, users in INPUTS.items():
-            K = lins[users[0]].K
-            h = synth.activations(M, K, seed=M * 10 + len(inp), count=synth.n_outliers(K))
-            t = torch.from_numpy(h.view(np.float16)).pin_memory()
-            xs_host[(M, inp)] = t
-            xs_dev[(M, inp)] = t.to(dev)
-    return lins, copies, xs_host, xs_dev
-
-
-class Step:
-    """Buffers and launch sequence of one step; capturable in a CUDA graph."""
-
-    def __init__(self, dev, lins, copies, xs_dev, budget0=False):
-        import torch
-        from dense_sparse_int4_gb300 import mq
-        self.mq = mq
-        self.lins, self.xs_dev = lins, xs_dev
-        self.copies = copies
-        if budget0:  # same base weights, no residual: the budget-0 kernel
-            self.copies = [{k: mq.PackedLinear(v.N, v.K, 0, v.wpk, v.row_ptr, v.col_idx, v.rpk)
-                            for k, v in c.items()} for c in copies]
-        self.q = {}
-        for M in MS:
-            for inp, users in INPUTS.items():
-                K = lins[users[0]].K
-                self.q[(M, inp)] = (torch.empty((K // 128, mq.padded_tokens(M), 64), dtype=torch.uint8, device=dev),
-                                    torch.empty((K // 128, mq.padded_tokens(M)), dtype=torch.float16, device=dev))
-        self.y = {(M, n): torch.empty((M, l.N), dtype=torch.bfloat16, device=dev) for M in MS for n, l in lins.items()}
-        wsb = max(int(mq.lib().mq_gemm_workspace_bytes(M, l.N, l.K)) for M in MS for l in lins.values())
-        self.ws = torch.zeros(max(wsb, 256), dtype=torch.uint8, device=dev)
-        self.wsb = wsb
-        self.gemm_order = [(ci, M, n) for ci, M in enumerate(MS) for inp, users in INPUTS.items() for n in users]
-
-    def run(self, stream, events: GraphEvents | None = None, ev_base: int = 0):
-        mq = self.mq
-        j = 0
-        for ci, M in enumerate(MS):
-            for inp, users in INPUTS.items():
-                xq, xs = self.q[(M, inp)]
-                mq.quantize_act(self.xs_dev[(M, inp)], xq, xs, stream=stream)
-                for n in users:
-                    if events is not None:
-                        events.record(ev_base + 2 * j, stream)
-                    mq.gemm(xq, xs, M, self.copies[ci][n], out=self.y[(M, n)], ws=self.ws, stream=stream)
-                    if events is not None:
-                        events.record(ev_base + 2 * j + 1, stream)
-                    j += 1
-
-    def launches(self) -> int:
-        return len(MS) * len(INPUTS) + len(self.gemm_order)
-
-    def gemm_bytes(self, j: int) -> int:
-        """Algorithmic bytes of GEMM j: weights (base + residual + CSR), packed activations + scales, bf16 output."""
-        ci, M, n = self.gemm_order[j]
-        pl = self.copies[ci][n]
-        K, N = pl.K, pl.N
-        Mp = self.mq.padded_tokens(M)
-        return pl.weight_bytes() + Mp * K // 2 + 2 * Mp * (K // 128) + 2 * M * N
-
-    def weight_bytes_per_step(self) -> int:
-        return sum(self.copies[ci][n].weight_bytes() for ci, M, n in self.gemm_order)
-
-    def ops_per_step(self) -> int:
-        """2*M*N*K dense + 2*M*64*128 per residual block."""
-        return sum(2 * M * self.lins[n].N * self.lins[n].K + 2 * M * 8192 * self.copies[ci][n].nnzb
-                   for ci, M, n in self.gemm_order)
-
-    def io_bytes(self) -> tuple[int, int]:
-        h2d = sum(t.numel() * 2 for t in self.xs_dev.values())
-        d2h = sum(t.numel() * 2 for t in self.y.values())
-        return h2d, d2h
-
-
 def capture(fn, stream):
     import torch
     g = torch.cuda.CUDAGraph()
@@ -325,77 +303,493 @@ def capture(fn, stream):
     return g
 
 
+def replay_ms(graph, stream, reps: int) -> float:
+    """Mean ms of `reps` back-to-back replays (after one untimed replay)."""
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        graph.replay()
+        e0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(stream)
+    stream.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
 # ---------------------------------------------------------------------------
-# CPU baseline: the oracle on host cores
+# the workload
 # ---------------------------------------------------------------------------
 
-_ORACLE_PREPS: dict = {}
+def linear_table(model: str = "llama"):
+    from dense_sparse_int4_gb300 import synth
+    return {l.name: l for l in (synth.LLAMA3_8B if model == "llama" else synth.QWEN3_32B)}
 
 
-def oracle_sample(seconds: float = 12.0, max_pairs: int | None = None):
-    """Time the oracle (as it stands) on (linear, M) pairs of the workload until
-    `seconds` of CPU work are done; returns (weight GB/s, description)."""
+def prepare_layer(dev, lins, seed: int, budget=BUDGET, placement: str = "uniform"):
+    """The packed linears of one layer (GPU selector + packer)."""
+    import torch
+    from dense_sparse_int4_gb300 import mq, synth
+    out = {}
+    for i, (name, lin) in enumerate(lins.items()):
+        w = synth.device_weights(lin.N, lin.K, seed=seed + i, device=dev)
+        if placement == "concentrated":
+            synth.inject_concentrated_device(w, seed=seed + i)
+        xcal = torch.from_numpy(synth.calibration(lin.K, seed=seed + i, count=synth.n_outliers(lin.K))
+                                .view(np.float16)).to(dev)
+        out[name] = mq.prepare_linear(w, xcal, budget)
+        del w
+    return out
+
+
+def call_bytes(pls, M: int, K: int) -> int:
+    """Algorithmic HBM bytes of one fused call: packed weights (base, residual, block lists), X (fp16), Y (bf16)."""
+    return sum(pl.weight_bytes() for pl in pls) + 2 * M * K + sum(2 * M * pl.N for pl in pls)
+
+
+def call_ops(pls, M: int) -> int:
+    """2*M*N*K dense + 2*M*64*128 per residual block."""
+    return sum(2 * M * pl.N * pl.K + 2 * M * 8192 * pl.nnzb for pl in pls)
+
+
+class Step:
+    """One step's fused calls (for each M: q/k/v, o, gate/up, down) on its own weight copy; capturable."""
+
+    def __init__(self, dev, lins, copies, xs_dev, budget0=False, calls=CALLS, ms=MS):
+        import torch
+        from dense_sparse_int4_gb300 import mq
+        self.mq = mq
+        self.lins, self.xs_dev = lins, xs_dev
+        if budget0:  # same base weights, no residual: the budget-0 kernel
+            copies = [{k: mq.PackedLinear(v.N, v.K, 0, v.wpk, v.row_ptr, v.col_idx, v.rpk) for k, v in c.items()}
+                      for c in copies]
+        self.copies = copies
+        self.calls = [(M, ci % len(copies), inp, names) for ci, M in enumerate(ms) for inp, names in calls]
+        self.y = {(M, n): torch.empty((M, lins[n].N), dtype=torch.bfloat16, device=dev)
+                  for M, _, _, names in self.calls for n in names}
+        lib = mq.lib()
+        wsb = 0
+        for M, ci, inp, names in self.calls:
+            Ns = (ctypes.c_int64 * len(names))(*[lins[n].N for n in names])
+            wsb = max(wsb, int(lib.mq_linear_workspace_bytes(M, lins[names[0]].K, len(names),
+                                                              ctypes.cast(Ns, ctypes.c_void_p))))
+        self.ws = torch.zeros(max(wsb, 256), dtype=torch.uint8, device=dev)
+
+    def pls(self, j):
+        M, ci, inp, names = self.calls[j]
+        return [self.copies[ci][n] for n in names]
+
+    def run(self, stream, events: GraphEvents | None = None, ev_base: int = 0):
+        for j, (M, ci, inp, names) in enumerate(self.calls):
+            if events is not None:
+                events.record(ev_base + 2 * j, stream)
+            self.mq.fused_linear(self.xs_dev[(M, inp)], self.pls(j), outs=[self.y[(M, n)] for n in names],
+                                 ws=self.ws, stream=stream)
+            if events is not None:
+                events.record(ev_base + 2 * j + 1, stream)
+
+    def launches(self) -> int:
+        return 2 * len(self.calls)  # the activation-image kernel and the fused GEMM per call
+
+    def bytes_per_step(self) -> int:
+        return sum(call_bytes(self.pls(j), M, self.lins[names[0]].K) for j, (M, _, _, names) in enumerate(self.calls))
+
+    def weight_bytes_per_step(self) -> int:
+        return sum(pl.weight_bytes() for j in range(len(self.calls)) for pl in self.pls(j))
+
+    def ops_per_step(self) -> int:
+        return sum(call_ops(self.pls(j), M) for j, (M, _, _, _) in enumerate(self.calls))
+
+    def io_bytes(self) -> tuple[int, int]:
+        h2d = sum(self.xs_dev[(M, inp)].numel() * 2 for M, _, inp, _ in self.calls)
+        d2h = sum(t.numel() * 2 for t in self.y.values())
+        return h2d, d2h
+
+    def event_times_us(self, stream, reps: int = 3) -> list[float]:
+        """Per-call µs from an instrumented replay of the same calls (median of reps)."""
+        ev = GraphEvents(2 * len(self.calls))
+        g = capture(lambda: self.run(stream, ev), stream)
+        per = [[] for _ in self.calls]
+        with torch_stream(stream):
+            g.replay()
+        stream.synchronize()
+        for _ in range(reps):
+            with torch_stream(stream):
+                g.replay()
+            stream.synchronize()
+            for j in range(len(self.calls)):
+                per[j].append(ev.ms(2 * j, 2 * j + 1) * 1e3)
+        return [statistics.median(p) for p in per]
+
+
+def torch_stream(stream):
+    import torch
+    return torch.cuda.stream(stream)
+
+
+def after_allocations(stream):
+    """Order `stream` after the work on the current stream (the zero-fills and copies of
+    freshly allocated buffers) before launching on it."""
+    import torch
+    stream.wait_stream(torch.cuda.current_stream())
+
+
+def make_inputs(dev, lins, ms=MS, calls=CALLS, seed_base: int = 0):
+    """Pinned host and device activations per (M, input)."""
+    import torch
+    from dense_sparse_int4_gb300 import synth
+    host, devx = {}, {}
+    for M in ms:
+        for inp, names in calls:
+            K = lins[names[0]].K
+            h = synth.activations(M, K, seed=seed_base + M * 10 + len(inp), count=synth.n_outliers(K))
+            t = torch.from_numpy(h.view(np.float16)).pin_memory()
+            host[(M, inp)] = t
+            devx[(M, inp)] = t.to(dev)
+    return host, devx
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle on the host cores
+# ---------------------------------------------------------------------------
+
+STEP_PAIRS = [(n, M) for M in MS for _, names in CALLS for n in names]  # (linear, M) in step order
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.processor() or platform.machine()
+
+
+def oracle_weight_bytes(lin, ksel: int) -> int:
+    """The bytes the oracle's linear reads as weights, counted like the GPU's packed records:
+    int4 codes, fp16 group scales, residual blocks (codes + scales) and the block lists."""
+    return lin.N * lin.K // 2 + 2 * lin.N * (lin.K // 128) + ksel * (4096 + 128 + 4) + 4 * (lin.N // 64 + 1)
+
+
+def oracle_prepare(names):
+    """The oracle's offline products for the named Llama-3-8B linears (untimed), residual dropped."""
     import oracle as O
     from dense_sparse_int4_gb300 import synth
-    lins = linear_by_name()
-    # the attention linears of every M, in step order, repeated until `seconds`
-    # (the MLP matrices would add minutes of untimed offline packing)
-    base_order = [(n, M) for M in MS for n in ("q", "k", "v", "o")]
-    order = (base_order[i % len(base_order)] for i in range(10 ** 6))
-    done, wbytes, t_total = [], 0, 0.0
-    preps = _ORACLE_PREPS
-    for n, M in order:
+    lins = linear_table()
+    preps = {}
+    for n in names:
         lin = lins[n]
-        if n not in preps:  # offline packing is not part of the timed online path
-            w = synth.weights(lin.N, lin.K, seed=7)
-            xcal = synth.calibration(lin.K, seed=7, count=synth.n_outliers(lin.K))
-            preps[n] = O.prepare(w, xcal, False, BUDGET)
-        p = preps[n]
+        w = synth.weights(lin.N, lin.K, seed=7)
+        xcal = synth.calibration(lin.K, seed=7, count=synth.n_outliers(lin.K))
+        p = O.prepare(w, xcal, False, BUDGET)
+        p.r = p.h = p.delta = np.zeros(0)  # not read by the online path
+        preps[n] = p
+    return preps
+
+
+def oracle_run(preps, pairs, seconds: float, max_pairs: int | None = None):
+    """Quantize + linear through the oracle over `pairs` (cycled) until `seconds` of work.
+    Returns (weight bytes, seconds, pairs done)."""
+    import oracle as O
+    from dense_sparse_int4_gb300 import synth
+    lins = linear_table()
+    done, wbytes, t_total = [], 0, 0.0
+    i = 0
+    while True:
+        n, M = pairs[i % len(pairs)]
+        i += 1
+        lin = lins[n]
         x = synth.activations(M, lin.K, seed=M, count=synth.n_outliers(lin.K))
         t0 = time.perf_counter()
         qx, sx = O.quantize_act(x, False)
-        O.linear(qx, sx, p)
-        dt = time.perf_counter() - t0
-        t_total += dt
-        wbytes += lin.N * lin.K // 2 + 2 * lin.N * (lin.K // 128) + p.ksel * (4096 + 128 + 4) + 4 * (lin.N // 64 + 1)
+        O.linear(qx, sx, preps[n])
+        t_total += time.perf_counter() - t0
+        wbytes += oracle_weight_bytes(lin, preps[n].ksel)
         done.append(f"{n}@M{M}")
         if t_total >= seconds or (max_pairs and len(done) >= max_pairs):
-            break
-    return wbytes / t_total / 1e9, t_total, done
+            return wbytes, t_total, done
+
+
+def _oracle_worker(pairs, seconds, start, q):
+    """Child process of the all-cores run: pack (untimed), wait for the common start, run."""
+    sys.path.insert(0, ROOT)
+    try:
+        os.sched_setaffinity(0, os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        pass
+    preps = oracle_prepare(sorted({n for n, _ in pairs}))
+    start.wait(timeout=600)  # every worker has packed: all start together
+    t0 = time.perf_counter()
+    b, secs, done = oracle_run(preps, pairs, seconds)
+    q.put((b, secs, time.perf_counter() - t0, len(done)))
+
+
+def oracle_all_cores(seconds: float, workers: int):
+    """The oracle on `workers` processes at once (spawned: no CUDA state is inherited), each on
+    one linear of the step cycling over M; throughput = all bytes / the slowest worker's wall time."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    lins = list(linear_table())
+    start, q = ctx.Barrier(workers + 1), ctx.Queue()
+    procs = []
+    for i in range(workers):
+        n = lins[i % len(lins)]
+        pairs = [(n, M) for M in MS]
+        p = ctx.Process(target=_oracle_worker, args=(pairs, seconds, start, q), daemon=True)
+        p.start()
+        procs.append(p)
+    start.wait(timeout=600)
+    res = [q.get(timeout=600) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+    total = sum(r[0] for r in res)
+    wall = max(r[2] for r in res)
+    return total / wall / 1e9, wall, sum(r[3] for r in res)
+
+
+def cpu_baseline(seconds: float, all_cores: bool = True) -> dict:
+    single_preps = oracle_prepare(sorted({n for n, _ in STEP_PAIRS}))
+    b, secs, done = oracle_run(single_preps, STEP_PAIRS, seconds)
+    v1 = b / secs / 1e9
+    out = {"value": round(v1, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "nproc": os.cpu_count(), "cpu_model": cpu_model(),
+           "sample": (f"oracle (plain C, float64/int64) single-threaded on {len(done)} (linear, M) pairs taken in "
+                      f"step order over all seven linears ({len(set(done))} distinct): activation quantization + "
+                      f"linear, {secs:.1f} s of CPU; packing untimed")}
+    if all_cores and (os.cpu_count() or 1) > 1:
+        workers = os.cpu_count()
+        v, wall, npairs = oracle_all_cores(seconds, workers)
+        out.update({"value": round(v, 6), "cores": workers,
+                    "single_thread": {"value": round(v1, 6), "cores": 1},
+                    "sample": out["sample"] + (f"; then {workers} processes at once (one per core; worker i on "
+                                                f"linear i mod 7 cycling over M = {list(MS)}), {npairs} pairs in "
+                                                f"{wall:.1f} s wall: value = all bytes / wall")})
+    return out
 
 
 # ---------------------------------------------------------------------------
-# prefill extra: M = 2048, K = 4096, N = 14336
+# extras (outside the timed region)
 # ---------------------------------------------------------------------------
 
-def prefill_extra(dev, stream, reps: int = 20):
+SINGLE_CALLS = tuple((inp, (n,)) for inp, names in CALLS for n in names)  # each linear alone
+
+
+def per_call_table(step: Step, stream, peak_gbs: float, reps: int = 3) -> dict:
+    """Event-timed µs of each call of a step (an instrumented replay of the same calls)."""
+    us = step.event_times_us(stream, reps)
+    out = {}
+    for j, (M, _, _, names) in enumerate(step.calls):
+        pls = step.pls(j)
+        wb = sum(pl.weight_bytes() for pl in pls)
+        gbs = wb / (us[j] * 1e-6) / 1e9
+        out[f"{'+'.join(names)}@M{M}"] = {"us": round(us[j], 2), "weight_GBps": round(gbs, 1),
+                                          "frac_hbm": round(gbs / peak_gbs, 4)}
+    return out
+
+
+def prefill_extra(dev, stream, tc_peak_tflops: float | None, reps: int = 20) -> dict:
+    """M = 2048, K = 4096, N = 14336 at budgets 0.10 and 0: the GEMM alone (event-timed, L2-warm:
+    a compute-bound shape) against the measured dense E4M3 tensor rate, and the fused call."""
     import torch
     from dense_sparse_int4_gb300 import mq, synth
     M, K, N = 2048, 4096, 14336
     w = synth.device_weights(N, K, seed=77, device=dev)
     xcal = torch.from_numpy(synth.calibration(K, seed=2, count=8, dtype="bf16").view(np.int16)).to(dev).view(torch.bfloat16)
-    out = {}
     x = torch.from_numpy(synth.activations(M, K, seed=2, count=8, dtype="bf16").view(np.int16)).to(dev).view(torch.bfloat16)
+    out = {}
     for budget in (0.10, 0.0):
         pl = mq.prepare_linear(w, xcal, budget)
         xq, xs = mq.quantize_act(x)
         y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         ws, _ = mq.gemm_workspace(M, N, K, dev)
-        for _ in range(3):
-            mq.gemm(xq, xs, M, pl, out=y, ws=ws)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(reps):
-            mq.gemm(xq, xs, M, pl, out=y, ws=ws)
-        e1.record()
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / reps
+        mq.linear_workspace(M, K, [N], dev)  # allocated (zeroed) before the stream uses it
+        after_allocations(stream)
+        with torch_stream(stream):
+            mq.fused_linear(x, [pl], outs=[y], stream=stream)  # allocates its workspace before capture
+            g = capture(lambda: [mq.gemm(xq, xs, M, pl, out=y, ws=ws, stream=stream) for _ in range(reps)], stream)
+            gf = capture(lambda: [mq.fused_linear(x, [pl], outs=[y], stream=stream) for _ in range(reps)], stream)
+        ms = replay_ms(g, stream, 3) / reps
+        ms_fused = replay_ms(gf, stream, 3) / reps
         ops = 2 * M * N * K + 2 * M * 8192 * pl.nnzb
-        out[f"budget_{budget:.2f}"] = {"ms": round(ms, 4), "tops": round(ops / ms / 1e9, 1),
-                                       "dense_tops": round(2 * M * N * K / ms / 1e9, 1)}
+        d = {"ms": round(ms, 4), "tops": round(ops / ms / 1e9, 1), "dense_tops": round(2 * M * N * K / ms / 1e9, 1),
+             "fused_call_ms": round(ms_fused, 4), "nnzb": pl.nnzb}
+        if tc_peak_tflops:
+            d["roofline"] = {"bound": "tensor", "achieved": d["tops"], "peak": tc_peak_tflops, "unit": "TFLOP/s",
+                             "frac": round(d["tops"] / tc_peak_tflops, 4),
+                             "peak_source": "measured dense tcgen05 E4M3 rate (libmq_peaks)"}
+        out[f"budget_{budget:.2f}"] = d
     mq.check_device_error()
     out["residual_overhead"] = round(out["budget_0.10"]["ms"] / out["budget_0.00"]["ms"] - 1, 4)
+    out["roofline"] = out["budget_0.10"].get("roofline")
+    return out
+
+
+def stack32_extra(dev, stream, peak_gbs: float, layers: int = 32, M: int = 32) -> dict:
+    """All linears of a 32-layer Llama-3-8B-shaped decoder at M = 32, 10 % budget, back to back:
+    per layer its four fused calls (per-layer quantization inside), per-layer weights and block lists."""
+    lins = linear_table()
+    t0 = time.perf_counter()
+    stack = [prepare_layer(dev, lins, seed=5000 + 16 * l) for l in range(layers)]
+    prep_s = time.perf_counter() - t0
+    _, xs = make_inputs(dev, lins, ms=(M,), seed_base=900)
+    xs_layer = {}
+    for l in range(layers):  # distinct activations per layer: a seeded permutation of the rows' values
+        for (m, inp), t in xs.items():
+            xs_layer[(l, inp)] = t.roll(shifts=l, dims=1).contiguous()
+    step = Step(dev, lins, stack, xs_layer, ms=(M,) * layers)
+    after_allocations(stream)
+    step.run = _layer_run(step, xs_layer)
+    g = capture(lambda: step.run(stream), stream)
+    ms = min(replay_ms(g, stream, 5) for _ in range(3))
+    wb = step.weight_bytes_per_step()
+    from dense_sparse_int4_gb300 import mq
+    mq.check_device_error(stream)
+    return {"layers": layers, "M": M, "calls": len(step.calls), "launches": step.launches(), "ms": round(ms, 4),
+            "weight_bytes": wb, "weight_GBps": round(wb / ms / 1e6, 1), "frac_hbm": round(wb / ms / 1e6 / peak_gbs, 4),
+            "tops": round(step.ops_per_step() / ms / 1e9, 2), "prepare_s": round(prep_s, 1),
+            "note": "one CUDA graph of the 128 fused calls; each layer has its own packed weights and block lists"}
+
+
+def _layer_run(step: Step, xs_layer):
+    def run(stream, events=None, ev_base=0):
+        for j, (M, ci, inp, names) in enumerate(step.calls):
+            if events is not None:
+                events.record(ev_base + 2 * j, stream)
+            step.mq.fused_linear(xs_layer[(ci, inp)], step.pls(j), outs=[step.y[(M, n)] for n in names],
+                                 ws=step.ws, stream=stream)
+            if events is not None:
+                events.record(ev_base + 2 * j + 1, stream)
+    return run
+
+
+def qwen3_extra(dev, stream, peak_gbs: float, tc_peak_tflops: float | None,
+                budgets=(0.0, 0.05, 0.10, 0.20), ms=(4, 32, 512)) -> dict:
+    """Qwen3-32B-shaped linears, each alone, at M in {4, 32, 512} x budgets x {concentrated, uniform}:
+    event-timed µs per linear (the 7 calls of a (placement, budget, M) in one graph, ~0.25 GB of
+    weights: larger than L2), weight GB/s, TOPS, and the overhead against budget 0."""
+    import torch
+    from dense_sparse_int4_gb300 import mq, synth
+    lins = linear_table("qwen")
+    res = {"linears": {n: [l.K, l.N] for n, l in lins.items()}}
+    t0 = time.perf_counter()
+    for placement in ("concentrated", "uniform"):
+        sets = {b: {} for b in budgets}
+        for i, (name, lin) in enumerate(lins.items()):
+            w = synth.device_weights(lin.N, lin.K, seed=3000 + i, device=dev)
+            if placement == "concentrated":  # errors injected into 2 % of the blocks
+                synth.inject_concentrated_device(w, seed=3000 + i)
+            xcal = torch.from_numpy(synth.calibration(lin.K, seed=i, count=synth.n_outliers(lin.K))
+                                    .view(np.float16)).to(dev)
+            for b in budgets:
+                sets[b][name] = mq.prepare_linear(w, xcal, b)
+            del w
+        pr = res[placement] = {}
+        for b in budgets:
+            for M in ms:
+                _, xs = make_inputs(dev, lins, ms=(M,), seed_base=700)
+                step = Step(dev, lins, [sets[b]], xs, calls=SINGLE_CALLS, ms=(M,))
+                after_allocations(stream)
+                with torch_stream(stream):
+                    step.run(stream)  # eager first: workspace and attributes outside capture
+                us = step.event_times_us(stream)
+                tot = sum(us)
+                wb = step.weight_bytes_per_step()
+                d = {"us": {names[0]: round(u, 2) for u, (_, _, _, names) in zip(us, step.calls)},
+                     "total_us": round(tot, 2), "weight_GBps": round(wb / (tot * 1e-6) / 1e9, 1),
+                     "frac_hbm": round(wb / (tot * 1e-6) / 1e9 / peak_gbs, 4),
+                     "tops": round(step.ops_per_step() / (tot * 1e-6) / 1e12, 2),
+                     "nnzb": {names[0]: step.pls(j)[0].nnzb for j, (_, _, _, names) in enumerate(step.calls)}}
+                if tc_peak_tflops:
+                    d["frac_tensor"] = round(d["tops"] / tc_peak_tflops, 4)
+                pr[f"b{b:.2f}/M{M}"] = d
+                del step
+        for b in budgets:
+            for M in ms:
+                base = pr[f"b{budgets[0]:.2f}/M{M}"]["total_us"]
+                pr[f"b{b:.2f}/M{M}"]["overhead_vs_b0"] = round(pr[f"b{b:.2f}/M{M}"]["total_us"] / base - 1, 4)
+        del sets
+        torch.cuda.empty_cache()
+    mq.check_device_error(stream)
+    res["seconds"] = round(time.perf_counter() - t0, 1)
+    return res
+
+
+def distortion_extra(dev, budgets=(0.0, 0.05, 0.10, 0.20)) -> dict:
+    """Output distortion recovered against budget, from the GPU selector's packed output:
+    1 - ||Xcal (W - W_b)^T||^2 / ||Xcal (W - W_0)^T||^2 with W_b = Q(W) + R_b, the effective weights
+    the fused kernel applies.  W_b is read back through the product path: X = 7 I quantizes exactly
+    (group scale 1, code 7), so Y / 7 = W_b^T.  Llama-3-8B gate shape, concentrated and uniform."""
+    import torch
+    from dense_sparse_int4_gb300 import mq, synth
+    N, K = 14336, 4096
+    eye7 = (torch.eye(K, device=dev, dtype=torch.float32) * 7).to(torch.float16)
+    out = {"shape": [N, K], "calibration_rows": 256}
+    for placement in ("concentrated", "uniform"):
+        w = synth.device_weights(N, K, seed=4242, device=dev)
+        if placement == "concentrated":
+            synth.inject_concentrated_device(w, seed=4242)
+        xcal = torch.from_numpy(synth.calibration(K, seed=11, count=synth.n_outliers(K)).view(np.float16)).to(dev)
+        xf, wf = xcal.float(), w.float()
+        d = {}
+        for b in budgets:
+            pl = mq.prepare_linear(w, xcal, b)
+            y = mq.fused_linear(eye7, [pl], out_dtype=torch.float32)[0]  # [K, N]
+            e = wf - y.t() / 7
+            d[b] = float((xf @ e.t()).double().pow(2).sum())
+            del y, e
+        out[placement] = {f"{b:.2f}": {"distortion": d[b], "recovered": round(1 - d[b] / d[budgets[0]], 4)}
+                          for b in budgets}
+        del w, wf
+    mq.check_device_error()
+    return out
+
+
+def w16a16_extra(dev, stream, ours: dict) -> dict:
+    """Context: torch bf16 GEMMs (cuBLAS) at the same Llama-3-8B shapes and M, each linear alone,
+    event-timed in one graph over the seven linears (~0.44 GB of bf16 weights per M)."""
+    import torch
+    lins = linear_table()
+    g = torch.Generator(device=dev)
+    g.manual_seed(16)
+    ws = {n: (torch.randn((l.N, l.K), generator=g, device=dev) * 0.02).to(torch.bfloat16) for n, l in lins.items()}
+    order = [(M, n) for M in MS for n in lins]
+    xs = {(M, n): torch.randn((M, lins[n].K), generator=g, device=dev).to(torch.bfloat16) for M, n in order}
+    ys = {(M, n): torch.empty((M, lins[n].N), device=dev, dtype=torch.bfloat16) for M, n in order}
+    ev = GraphEvents(2 * len(order))
+    after_allocations(stream)
+
+    def run(events=True):
+        for j, (M, n) in enumerate(order):
+            if events:
+                ev.record(2 * j, stream)
+            torch.mm(xs[(M, n)], ws[n].t(), out=ys[(M, n)])
+            if events:
+                ev.record(2 * j + 1, stream)
+    with torch_stream(stream):
+        run(events=False)  # eager first: cuBLAS handles and workspaces outside capture
+    stream.synchronize()
+    gr = capture(run, stream)
+    per = {k: [] for k in order}
+    for _ in range(4):
+        with torch_stream(stream):
+            gr.replay()
+        stream.synchronize()
+        for j, k in enumerate(order):
+            per[k].append(ev.ms(2 * j, 2 * j + 1) * 1e3)
+    out = {}
+    for (M, n), v in per.items():
+        us = statistics.median(v[1:])
+        d = {"us": round(us, 2)}
+        o = ours.get(f"{n}@M{M}")
+        if o:
+            d["speedup_of_w4a4"] = round(us / o["us"], 3)
+        out[f"{n}@M{M}"] = d
+    tot16 = sum(statistics.median(v[1:]) for v in per.values())
+    tot4 = sum(ours[f"{n}@M{M}"]["us"] for M, n in order if f"{n}@M{M}" in ours)
+    out["total_speedup_of_w4a4"] = round(tot16 / tot4, 3) if tot4 else None
+    del ws, xs, ys
     return out
 
 
@@ -415,30 +809,26 @@ def run_ours(args):
     barrier()
     from dense_sparse_int4_gb300 import mq
 
-    lins, copies, xs_host, xs_dev = setup(dev)
+    lins = linear_table()
+    base = prepare_layer(dev, lins, seed=1000)
+    copies = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(COPIES - 1)]
+    xs_host, xs_dev = make_inputs(dev, lins)
+    torch.cuda.synchronize()
     stream = torch.cuda.Stream(device=dev)
     step = Step(dev, lins, copies, xs_dev)
     step0 = Step(dev, lins, copies, xs_dev, budget0=True)
-    ngemm = len(step.gemm_order)
-    R = max(1, min(args.steps, 4))  # instrumented steps at the start of the timed region
-    gev = GraphEvents(2 * ngemm * R + 4 * ngemm)
-
-    with torch.cuda.stream(stream):
+    after_allocations(stream)
+    with torch_stream(stream):
         for _ in range(2):  # eager warm-up: one-time attributes, workspace, module load
             step.run(stream)
             step0.run(stream)
     stream.synchronize()
     mq.check_device_error(stream)
     plain = capture(lambda: step.run(stream), stream)
-    instr = [capture(lambda r=r: step.run(stream, gev, 2 * ngemm * r), stream) for r in range(R)]
     plain0 = capture(lambda: step0.run(stream), stream)
-    instr0 = capture(lambda: step0.run(stream, gev, 2 * ngemm * R), stream)
-    instr10 = capture(lambda: step.run(stream, gev, 2 * ngemm * R + 2 * ngemm), stream)
-
-    # e2e: host inputs -> device, the step, outputs -> host, all in one graph
     y_host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in step.y.items()}
 
-    def e2e_body():
+    def e2e_body():  # host inputs -> device, the step, outputs -> host
         for k, t in xs_host.items():
             xs_dev[k].copy_(t, non_blocking=True)
         step.run(stream)
@@ -446,61 +836,53 @@ def run_ours(args):
             y_host[k].copy_(t, non_blocking=True)
     e2e_graph = capture(e2e_body, stream)
 
+    # ---- the timed region: K plain replays of the step graph, nothing else ----
     clocks = ClockSampler(local)
     clocks.start()
-    time.sleep(0.3)
-    for _ in range(args.warmup):
-        plain.replay()
+    time.sleep(0.2)
+    with torch_stream(stream):
+        for _ in range(args.warmup):
+            plain.replay()
     stream.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
+    with torch_stream(stream):
         ev0.record(stream)
-        for s in range(args.steps):
-            (instr[s] if s < R else plain).replay()
+        for _ in range(args.steps):
+            plain.replay()
         ev1.record(stream)
     stream.synchronize()
     torch.cuda.synchronize(dev)
     t1 = time.perf_counter()
     barrier()
-    time.sleep(0.25)
+    time.sleep(0.05)
     clocks.stop()
     mq.check_device_error(stream)
     elapsed = ev0.elapsed_time(ev1) / 1e3
     value, tmax = aggregate(step.weight_bytes_per_step() * args.steps / 1e9, elapsed, dev)
-
-    # GEMM launches inside the timed region: durations from the in-graph events
-    gemm_ms = [gev.ms(2 * j, 2 * j + 1) for r in range(R) for j in range(r * ngemm, (r + 1) * ngemm)]
-    gemm_bytes = [step.gemm_bytes(j % ngemm) for r in range(R) for j in range(r * ngemm, (r + 1) * ngemm)]
-    achieved = sum(gemm_bytes) / (sum(gemm_ms) / 1e3) / 1e9
+    ms_step = tmax / args.steps * 1e3
     pk = peaks()
+    ncalls = len(step.calls)
+    achieved = step.bytes_per_step() / (ms_step * 1e-3) / 1e9  # per launch: bytes/ncalls over ms/ncalls
 
-    # residual overhead: the budget-0 kernel on the same base weights, same protocol
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            plain0.replay()
-            plain.replay()
-        instr0.replay()
-        instr10.replay()
-    stream.synchronize()
-    b = 2 * ngemm * R
-    t10 = sum(gev.ms(b + 2 * ngemm + 2 * j, b + 2 * ngemm + 2 * j + 1) for j in range(ngemm))
-    t0g = sum(gev.ms(b + 2 * j, b + 2 * j + 1) for j in range(ngemm))
-    per_linear = {}
-    for j, (ci, M, n) in enumerate(step.gemm_order):
-        d = per_linear.setdefault(f"{n}@M{M}", {})
-        d["us"] = round(gev.ms(b + 2 * ngemm + 2 * j, b + 2 * ngemm + 2 * j + 1) * 1e3, 2)
-        d["us_budget0"] = round(gev.ms(b + 2 * j, b + 2 * j + 1) * 1e3, 2)
-        d["weight_GBps"] = round(step.copies[ci][n].weight_bytes() / (d["us"] * 1e-6) / 1e9, 1)
-
-    # e2e through the public API with host buffers
-    for _ in range(max(1, args.warmup // 2)):
-        e2e_graph.replay()
+    # ---- outside the timed region ----
+    ms10 = min(replay_ms(plain, stream, 10) for _ in range(3))
+    ms0 = min(replay_ms(plain0, stream, 10) for _ in range(3))
+    per_call = per_call_table(step, stream, pk["hbm_gbs"])
+    single = Step(dev, lins, copies, xs_dev, calls=SINGLE_CALLS)
+    after_allocations(stream)
+    with torch_stream(stream):
+        single.run(stream)
+    per_linear = per_call_table(single, stream, pk["hbm_gbs"])
+    del single
+    with torch_stream(stream):
+        for _ in range(max(1, args.warmup // 2)):
+            e2e_graph.replay()
     stream.synchronize()
     e2e_steps = max(3, min(args.steps, 50))
-    with torch.cuda.stream(stream):
+    with torch_stream(stream):
         ev0.record(stream)
         for _ in range(e2e_steps):
             e2e_graph.replay()
@@ -509,11 +891,27 @@ def run_ours(args):
     e2e_val, _ = aggregate(step.weight_bytes_per_step() * e2e_steps / 1e9, ev0.elapsed_time(ev1) / 1e3, dev)
     h2d, d2h = step.io_bytes()
 
-    extra = {"per_linear": per_linear, "gemm_us_budget10": round(t10 * 1e3, 2), "gemm_us_budget0": round(t0g * 1e3, 2),
-             "residual_overhead": round(t10 / t0g - 1, 4),
-             "tops": round(step.ops_per_step() * args.steps / elapsed / 1e12, 2)}
-    if not args.no_prefill and rank == 0:
-        extra["prefill_2048x4096x14336"] = prefill_extra(dev, stream)
+    extra = {"per_call": per_call, "per_linear": per_linear,
+             "step_ms_budget10": round(ms10, 4), "step_ms_budget0": round(ms0, 4),
+             "residual_overhead": round(ms10 / ms0 - 1, 4),
+             "tops": round(step.ops_per_step() * args.steps / elapsed / 1e12, 2),
+             "event_sum_us_per_step": round(sum(v["us"] for v in per_call.values()), 2)}
+    rates = {}
+    if rank == 0 and not args.no_extras:
+        rates = rate_microbenchmarks()
+        extra["rates"] = rates
+    tc_peak = rates.get("tcgen05_e4m3_dense_tflops") or (pk["bf16_tflops"] * E4M3_PER_BF16)
+    if rank == 0 and not args.no_prefill:
+        extra["prefill_2048x4096x14336"] = prefill_extra(dev, stream, tc_peak)
+    if rank == 0 and not args.no_extras:
+        for name, fn in (("stack32", lambda: stack32_extra(dev, stream, pk["hbm_gbs"])),
+                         ("qwen3", lambda: qwen3_extra(dev, stream, pk["hbm_gbs"], tc_peak)),
+                         ("distortion", lambda: distortion_extra(dev)),
+                         ("w16a16", lambda: w16a16_extra(dev, stream, per_linear))):
+            t = time.perf_counter()
+            extra[name] = fn()
+            extra[name + "_bench_s"] = round(time.perf_counter() - t, 1)
+            torch.cuda.empty_cache()
 
     tr = measured_traffic()
     traffic = args.traffic if args.traffic is not None else (tr["dram_bytes_per_launch"] if tr else None)
@@ -521,32 +919,36 @@ def run_ours(args):
     if rank == 0:
         cpu = None
         if ws == 1 and not args.no_cpu_baseline:
-            v, secs, done = oracle_sample(args.cpu_seconds)
-            cpu = {"value": round(v, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                   "sample": f"oracle (single-threaded C, float64/int64) on {len(done)} (linear, M) pairs of the same "
-                             f"workload, cycling in step order over {len(set(done))} distinct ones "
-                             f"({', '.join(sorted(set(done)))}): activation quantization + linear, {secs:.1f} s of CPU"}
+            cpu = cpu_baseline(args.cpu_seconds)
         ck = clocks.summary(t0, t1)
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(tmax / args.steps * 1e3, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "int4 codes (exact E4M3 on mma.sync / tcgen05), fp32 epilogue, bf16 out",
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "int4 codes (exact E4M3 on mma.sync / tcgen05), fp32 epilogue, bf16 out",
             "data": "synthetic (random-init weights N(0,0.02), activations N(0,1) with 0.1% outlier channels x50)",
             "config": {"workload": WORKLOAD, "linears": {n: [l.K, l.N] for n, l in lins.items()}, "M": list(MS),
-                       "budget": BUDGET, "weight_copies": COPIES,
+                       "budget": BUDGET, "weight_copies": COPIES, "calls_per_step": ncalls,
+                       "calls": [f"{'+'.join(names)}@M{M}" for M, _, _, names in step.calls],
                        "weight_bytes_per_step": step.weight_bytes_per_step(),
-                       "l2": "inputs larger than L2: 4 rotating weight copies, ~0.5 GB streamed per step",
-                       "graph": "each step replayed from one CUDA graph", "parallelism": f"replica x{ws}"},
+                       "algorithmic_bytes_per_step": step.bytes_per_step(),
+                       "l2": "inputs larger than L2: one packed-weight copy per M, ~0.47 GB streamed per step",
+                       "graph": "each step replayed from one CUDA graph (plain replays only in the timed region)",
+                       "parallelism": f"replica x{ws}"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": traffic,
-                         "algorithmic_bytes_per_launch": round(sum(gemm_bytes) / len(gemm_bytes)),
-                         "peak_source": pk["source"], "kernel": "w4a4_decode_kernel",
-                         "launches_timed": len(gemm_ms)},
+                         "algorithmic_bytes_per_launch": round(step.bytes_per_step() / ncalls),
+                         "launch_ms": round(ms_step / ncalls, 6),
+                         "duration_from": "timed step / fused-GEMM launches per step (the activation-image "
+                                          "launches and gaps are charged to the GEMM: a lower bound)",
+                         "peak_source": f"{pk['source']} HBM copy (MEASURED_PEAKS.json hbm_gbs), burst",
+                         "kernel": "zipper_warp_kernel (fused W4A4 + residual stream-K GEMM)",
+                         "launches_per_step": ncalls},
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": step.launches() * args.steps,
             "clocks": {"sm_mhz": ck["sm_mhz"], "sm_max_mhz": ck["sm_max_mhz"], "reasons": ck["reasons"],
-                       "samples_in_region": ck["samples"]},
+                       "samples_in_region": ck["samples"], "source": ck["source"]},
             "extra": extra,
         }
         print(json.dumps(line), flush=True)
@@ -555,33 +957,37 @@ def run_ours(args):
 
 
 def run_reference(args):
+    """The oracle as it stands, on the host cores: each step one (linear, M) pair of the workload,
+    taken in step order over all seven linears and four M (single-threaded)."""
     ws, rank, _ = dist_env()
     if rank != 0:
         return None
-    v_steps = []
-    total_bytes, total_s = 0.0, 0.0
-    desc = None
+    preps = oracle_prepare(sorted({n for n, _ in STEP_PAIRS}))
+    total_bytes, total_s, seen = 0, 0.0, []
     for s in range(args.warmup + args.steps):
-        v, secs, done = oracle_sample(seconds=0.0, max_pairs=1)  # one (linear, M) pair per step
+        pair = STEP_PAIRS[s % len(STEP_PAIRS)]
+        b, secs, done = oracle_run(preps, [pair], 0.0, max_pairs=1)
         if s >= args.warmup:
-            total_bytes += v * secs
+            total_bytes += b
             total_s += secs
-            desc = done
-    value = total_bytes / total_s
+            seen += done
+    value = total_bytes / total_s / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_s / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "float64/int64 (CPU oracle)",
             "data": "synthetic", "config": {"workload": WORKLOAD, "M": list(MS), "budget": BUDGET},
             "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": f"each step: the oracle on one (linear, M) pair of the workload ({desc[0]}), "
-                                       f"activation quantization + linear, single-threaded"},
+                             "nproc": os.cpu_count(), "cpu_model": cpu_model(),
+                             "sample": f"each step: the oracle on one (linear, M) pair, in step order "
+                                       f"({len(set(seen))} distinct of {len(STEP_PAIRS)}: {', '.join(seen[:6])}, ...), "
+                                       f"activation quantization + linear, single-threaded; packing untimed"},
             "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return line
 
 
 def run_single(args):
-    """One linear at one M, eager launches (for profiler captures of one GEMM shape)."""
+    """One linear at one M through the fused call, eager launches (for profiler captures of one shape)."""
     import torch
     from dense_sparse_int4_gb300 import mq, synth
     name, M, *rest = args.single.split(":")
@@ -600,22 +1006,19 @@ def run_single(args):
     pl = mq.prepare_linear(w, xcal, budget)
     del w
     x = torch.from_numpy(synth.activations(M, lin.K, seed=5, count=synth.n_outliers(lin.K)).view(np.float16)).to(dev)
-    xq, xs = mq.quantize_act(x)
     y = torch.empty((M, lin.N), dtype=torch.bfloat16, device=dev)
-    ws, _ = mq.gemm_workspace(M, lin.N, lin.K, dev)
     for _ in range(args.warmup):
-        mq.quantize_act(x, xq, xs)
-        mq.gemm(xq, xs, M, pl, out=y, ws=ws)
+        mq.fused_linear(x, [pl], outs=[y])
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(args.steps):
-        mq.gemm(xq, xs, M, pl, out=y, ws=ws)
+        mq.fused_linear(x, [pl], outs=[y])
     e1.record()
     torch.cuda.synchronize()
     mq.check_device_error()
     us = e0.elapsed_time(e1) * 1e3 / args.steps
-    print(json.dumps({"single": args.single, "N": lin.N, "K": lin.K, "M": M, "nnzb": pl.nnzb, "us_per_gemm": round(us, 3),
+    print(json.dumps({"single": args.single, "N": lin.N, "K": lin.K, "M": M, "nnzb": pl.nnzb, "us_per_call": round(us, 3),
                       "weight_GBps": round(pl.weight_bytes() / us / 1e3, 1), "note": "L2-warm when the weights fit in L2"}))
 
 
@@ -625,11 +1028,12 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the rates, stack32, qwen3, distortion and w16a16 extras")
     ap.add_argument("--traffic", type=float, default=None,
-                    help="dram bytes per GEMM launch from an ncu capture of the current kernel (else null)")
+                    help="dram bytes per fused-GEMM launch from an ncu capture of the current kernel (else the committed one)")
     ap.add_argument("--single", default=None, help="LINEAR:M[:budget], e.g. gate:32, qwen-gate:4, prefill:2048 (profiling helper)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
