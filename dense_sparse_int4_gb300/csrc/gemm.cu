@@ -57,6 +57,7 @@
 #include <algorithm>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 // Timeline probes for profiling builds (compiled out unless MQ_GEMM_TRACE is
 // defined, in which case the build supplies mq_trace_stamp).
@@ -69,10 +70,20 @@ __device__ void mq_trace_stamp(int slot);
 
 namespace mq {
 
+constexpr int kGemmMaxDevices = 64;
+
+// SMs of the current device, 0 when none is current.
+static int current_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
 // warps: 0 and 2 producers (alternating units), 1 block list + MMA, then converters, then drain
 constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpProducer2 = 2, kWarpConv0 = 3;
 constexpr int kMaxGroupsPerCta = 1024;  // size of the CTA's residual map
-constexpr int kPlanCtas = 152;          // persistent CTAs (one per GB300 SM)
+constexpr int kPlanCtasNoDevice = 152;  // persistent CTAs when no device is current (workspace sizing): GB300's SMs
 constexpr int kMinUnitsPerCta = 4;
 constexpr int kRSlots = 6;              // residual-code ring: 6 x 4 KiB
 
@@ -766,7 +777,8 @@ static Plan make_plan(int64_t M, int64_t N, int64_t K) {
   pl.ug = (pl.tn <= 64 && pl.G % 2 == 0) ? 2 : 1;
   pl.units = static_cast<int64_t>(pl.tiles_m) * pl.tiles_n * (pl.G / pl.ug);
   // at least kMinUnitsPerCta units per CTA bounds the pieces a tile is cut into
-  int64_t ctas = std::min<int64_t>(kPlanCtas, std::max<int64_t>(1, pl.units / kMinUnitsPerCta));
+  const int sms = current_sms();  // one persistent CTA per SM of the current device
+  int64_t ctas = std::min<int64_t>(sms > 0 ? sms : kPlanCtasNoDevice, std::max<int64_t>(1, pl.units / kMinUnitsPerCta));
   const int64_t min_ctas = (pl.units * pl.ug + kMaxGroupsPerCta - 1) / kMaxGroupsPerCta;
   if (ctas < min_ctas) ctas = min_ctas;
   pl.ctas = static_cast<int>(ctas);
@@ -800,11 +812,17 @@ template <int TN, int UG, bool kDebug>
 static mq_status launch_cfg(const GemmParams& gp, const Plan& pl, cudaStream_t stream) {
   using C = Cfg<TN, UG>;
   auto kern = w4a4_residual_gemm_kernel<TN, UG, kDebug>;
-  static bool attr_set = false;  // per template instance
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
-      return launch_status("gemm: smem attribute");
-    attr_set = true;
+  static std::mutex mu;
+  static bool attr_set[kGemmMaxDevices] = {};  // per device, per template instance
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kGemmMaxDevices) return launch_status("gemm: device");
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!attr_set[dev]) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
+        return launch_status("gemm: smem attribute");
+      attr_set[dev] = true;
+    }
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(pl.ctas), 1, 1);

@@ -171,11 +171,16 @@ def test_decode_variants_match_oracle(variant, M, N, K, budget, monkeypatch):
     check_bf16(host_u16(y16), y, a)
 
 
-@pytest.mark.parametrize("M", [32, 8, 4, 1, 33, 128])
-def test_group_dots_extremes(M):
+@pytest.mark.parametrize("M,variant", [(32, "warp"), (32, "tc"), (16, "tc"), (8, "warp"), (8, "tc"), (4, "warp"),
+                                       (1, "warp"), (1, "tc"), (33, None), (128, None)])
+def test_group_dots_extremes(M, variant, monkeypatch):
     """Adversarial codes: every product +49, every product -49, alternating
     cancellation; sums reach +-6272 per group, exactly.  Up to 32 tokens this
-    runs the decode kernel (16- and 32-token tiles), above it the general one."""
+    runs the decode kernel, in its warp-MMA form (mask-and-offset unpack to
+    E4M3, fp32 MMA accumulators) and its tensor-memory form; above 32 tokens
+    the general kernel (exact-integer E4M3 table)."""
+    if variant:
+        monkeypatch.setenv("MQ_DECODE_VARIANT", variant)
     N, K = 128, 256
     x = np.full((M, K), 7.0, np.float32)
     w = np.full((N, K), 7.0 * 0.01, np.float32)
@@ -191,7 +196,8 @@ def test_group_dots_extremes(M):
     p = O.prepare(wb, xcal, False, 1.0)
     ref = O.group_dots(qx, p.qw)
     assert ref.max() == 6272 and ref.min() == -6272 and (ref == 0).any() == (M > 1)
-    assert mq.gemm_plan(M, N, K)["decode"] == (M <= 32)
+    plan = mq.gemm_plan(M, N, K)
+    assert plan["variant"] == {"warp": "warp-mma", "tc": "tensor-memory", None: "general"}[variant]
     assert np.array_equal(dw.cpu().numpy(), ref)
 
 
@@ -369,6 +375,99 @@ def _sampled_parity(M, lin, budget, x_dtype, seed, conc=False, nsamp=384):
     y, a = O.linear_entries(qx, sx, p, ms, ns)
     check_close(y32.cpu().numpy()[ms, ns], y, a)
     check_bf16(host_u16(y16)[ms, ns], y, a)
+
+
+@pytest.mark.parametrize("name,M,variant", [("gate", 8, "warp"), ("gate", 16, "warp"), ("gate", 32, "tc"),
+                                            ("down", 4, "warp")])
+def test_full_size_whole_output(name, M, variant, monkeypatch):
+    """One full-size Llama-3-8B linear through the fused call, every output
+    (fp32 and bf16) against the oracle: the whole matrix, not a sample."""
+    monkeypatch.setenv("MQ_DECODE_VARIANT", variant)
+    lin = {l.name: l for l in synth.LLAMA3_8B}[name]
+    x, w, xcal = _case(M, lin.N, lin.K, 0.10, seed=M * 13 + lin.N)
+    pl = mq.prepare_linear(dev_half(w), dev_half(xcal), 0.10)
+    xt = dev_half(x)
+    y32 = mq.fused_linear(xt, [pl], out_dtype=torch.float32)[0]
+    y16 = mq.fused_linear(xt, [pl])[0]
+    mq.check_device_error()
+    assert mq.gemm_plan(M, lin.N, lin.K)["variant"] == ("warp-mma" if variant == "warp" else "tensor-memory")
+    qx, sx = O.quantize_act(x, False)
+    y, a = O.linear(qx, sx, O.prepare(w, xcal, False, 0.10))
+    check_close(y32.cpu().numpy(), y, a)
+    check_bf16(host_u16(y16), y, a)
+
+
+def test_prefill_row_slab_whole_rows():
+    """M = 2048, K = 4096, N = 14336 (the general kernel): 48 whole output rows
+    across a 128-token tile boundary, and the last token's row, against the oracle."""
+    M, K, N, budget = 2048, 4096, 14336, 0.10
+    x = synth.activations(M, K, seed=2, count=8, dtype="bf16")
+    w = synth.weights(N, K, seed=77)
+    xcal = synth.calibration(K, seed=2, count=8, dtype="bf16")
+    pl = mq.prepare_linear(dev_half(w), dev_act(xcal, True), budget)
+    y32 = mq.fused_linear(dev_act(x, True), [pl], out_dtype=torch.float32)[0]
+    mq.check_device_error()
+    assert not mq.gemm_plan(M, N, K)["decode"]
+    rows = np.concatenate([np.arange(1000, 1048), [M - 1]])
+    ms, ns = np.repeat(rows, N), np.tile(np.arange(N), rows.size)
+    qx, sx = O.quantize_act(x[rows], True)
+    # the oracle's activation quantization is per token: the slab's rows quantize alone
+    y, a = O.linear_entries(qx, sx, O.prepare(w, xcal, True, budget), np.repeat(np.arange(rows.size), N), ns)
+    check_close(y32.cpu().numpy()[ms, ns], y, a)
+
+
+def _oracle_budgets(w, xcal, budgets):
+    """O.prepare for several budgets of one matrix: the base products once, then per budget
+    the selection and the residual codes (the oracle's own steps, in its order)."""
+    N, K = w.shape
+    qw, sw, r = O.base_quant(w)
+    h = O.hessian_diag(xcal, False)
+    d = O.delta_scores(r, h)
+    out = {}
+    for b in budgets:
+        ksel = O.num_selected(N, K, b)
+        rp, ci = O.select_topk(d, N, K, ksel)
+        qr, sr = O.residual_quant(r, rp, ci)
+        out[b] = O.Prepared(N, K, qw, sw, r, h, d, ksel, rp, ci, qr, sr, O.sel_of(rp, ci, N, K))
+    return out
+
+
+@pytest.mark.parametrize("placement", ["concentrated", "uniform"])
+@pytest.mark.parametrize("lin", synth.QWEN3_32B, ids=lambda l: l.name)
+def test_qwen3_sweep_sampled(lin, placement):
+    """Qwen3-32B shapes: every linear x M in {4, 32, 512} x budgets {0, 5, 10, 20} %,
+    errors injected into 2 % of the blocks or not: block lists bit for bit, and
+    sampled outputs (plus a selected block row) against the oracle."""
+    N, K = lin.N, lin.K
+    seed = sum(map(ord, lin.name)) + (7 if placement == "concentrated" else 0)
+    w = synth.weights(N, K, seed=seed)
+    if placement == "concentrated":
+        w = synth.inject_concentrated(w, seed=seed)
+    xcal = synth.calibration(K, seed=seed, count=synth.n_outliers(K))
+    budgets = (0.0, 0.05, 0.10, 0.20)
+    preps = _oracle_budgets(w, xcal, budgets)
+    wt, ct = dev_half(w), dev_half(xcal)
+    rng = np.random.default_rng(seed)
+    xs_host = {M: synth.activations(M, K, seed=seed + M, count=synth.n_outliers(K)) for M in (4, 32, 512)}
+    qxs = {M: O.quantize_act(x, False) for M, x in xs_host.items()}
+    xdev = {M: mq.quantize_act(dev_half(x)) for M, x in xs_host.items()}
+    for b in budgets:
+        p = preps[b]
+        pl = mq.prepare_linear(wt, ct, b)
+        assert np.array_equal(pl.row_ptr.cpu().numpy(), p.row_ptr)
+        assert np.array_equal(pl.col_idx[: pl.nnzb].cpu().numpy(), p.col_idx)
+        for M in (4, 32, 512):
+            xq, xs = xdev[M]
+            y32 = mq.gemm(xq, xs, M, pl, out_dtype=torch.float32)
+            mq.check_device_error()
+            ms, ns = rng.integers(0, M, 192), rng.integers(0, N, 192)
+            if p.ksel:
+                br = int(O.csr_block_rows(p.row_ptr)[rng.integers(0, p.ksel)])
+                ns = np.concatenate([ns, np.arange(br * 64, br * 64 + 64)])
+                ms = np.concatenate([ms, np.full(64, M - 1)])
+            y, a = O.linear_entries(*qxs[M], p, ms, ns)
+            check_close(y32.cpu().numpy()[ms, ns], y, a)
+            del y32
 
 
 @pytest.mark.parametrize("lin", synth.LLAMA3_8B, ids=lambda l: l.name)

@@ -176,6 +176,54 @@ def test_qz_codes_exact_property():
             assert np.abs(q).max() == 7
 
 
+def test_residual_qz_exact_fraction():
+    """The residual codes and scales (float64 inputs R = W^ - Q(W^)) against
+    exact rationals: the scale is the fp16 nearest to amax/7 (ties to even),
+    every code the integer nearest to r/s (ties to even), clamped to +-7.
+    Real residual rows of a packed matrix, and rows with planted exact ties."""
+    N, K = 128, 512
+    w = synth.weights(N, K, seed=21)
+    w = synth.inject_concentrated(w, seed=21, frac=0.25)
+    xcal = synth.calibration(K, seed=21, count=4)
+    p = O.prepare(w, xcal, False, 0.5)
+    assert p.ksel > 0
+    rng = np.random.default_rng(5)
+    rows = []
+    for e in range(p.ksel):  # the selected blocks' rows, as the residual quantizer saw them
+        br = int(np.searchsorted(p.row_ptr, e, side="right") - 1)
+        g = int(p.col_idx[e])
+        for i in rng.choice(64, 4, replace=False):
+            rows.append((p.r[br * 64 + i, g * 128:(g + 1) * 128].copy(), (e, int(i))))
+    for trial in range(40):  # planted ties: k + 1/2 of the scale, exactly in float64
+        v = rng.standard_normal(128) * 10.0 ** rng.uniform(-6, -2)
+        sb, _ = O.quantize_group(v)
+        sf = float(np.uint16(sb).view(np.float16))
+        if sf > 0:
+            k = rng.integers(-6, 6, 24)
+            cand = (k + 0.5) * sf
+            keep = np.abs(cand) <= np.abs(v).max()
+            v[:24][keep] = cand[keep]
+        rows.append((v, None))
+    checked_ties = 0
+    for vd, where in rows:
+        sb, q = O.quantize_group(vd)
+        t = max(abs(Fraction(float(x))) for x in vd) / 7  # amax / 7, exactly
+        assert _is_nearest_f16(sb, t) or (t >= 65520 and sb == 0x7BFF)
+        s = _f16(sb)
+        for x, qq in zip(vd, q):
+            if s == 0:
+                assert qq == 0
+                continue
+            quo = Fraction(float(x)) / s
+            want = max(-7, min(7, _nearest_int_even(quo)))
+            assert qq == want, (x, float(s), int(qq), want)
+            checked_ties += (quo - (quo.numerator // quo.denominator)) == Fraction(1, 2)
+        if where is not None:  # the packed residual holds exactly these codes and this scale
+            e, i = where
+            assert np.array_equal(p.qr[e, i], q) and p.sr[e, i] == sb
+    assert checked_ties > 50
+
+
 def _read_cases(path):
     cases, cur = [], None
     for line in open(path):
