@@ -177,6 +177,21 @@ __device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
 __device__ __forceinline__ void st_release_gpu(int32_t* p, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+__device__ __forceinline__ float ld_shared_f32(const float* p) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
+  return v;
+}
+__device__ __forceinline__ void st_shared_f32(float* p, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "f"(v)
+               : "memory");
+}
+__device__ __forceinline__ void st_global_f32(float* p, float v) {
+  asm volatile("st.global.cg.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_global_b16(void* p, unsigned short v) {
+  asm volatile("st.global.b16 [%0], %1;" ::"l"(p), "h"(v) : "memory");
+}
 __device__ __forceinline__ void st_relaxed_gpu(int32_t* p, int v) {
   asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -1326,74 +1341,89 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
     // One group's product for this warp's rows: codes (K-steps jstride apart,
     // 16 bytes per row, first row row0), fragments and scale pairs of the
     // group's activation image, row scales sc; into acc, or the test hook's dots.
+    // The 8-token blocks are taken at most two at a time (the weight
+    // fragments are unpacked again for the second pair): 32 tokens would
+    // otherwise hold 32 MMA results next to the 32 accumulators and spill.
     auto group_product = [&](const uint8_t* codes, int jstride, int row0, const uint16_t* sc, const uint8_t* img,
                              int64_t u, int e) {
-      float d[2][NB][4];
+      constexpr int NBH = NB < 2 ? NB : 2;  // 8-token blocks per pass
       const uint8_t* wr = codes + (row0 + g) * 16 + t * 4;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t a[2][4];
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(wr + j * jstride + mt * 256);        // row +0
-          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(wr + j * jstride + mt * 256 + 128);  // row +8
-          unpack_u4(w0, a[mt][0], a[mt][2]);
-          unpack_u4(w1, a[mt][1], a[mt][3]);
-        }
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-          const uint2 b = *reinterpret_cast<const uint2*>(img + ((j * NB + nb) * 32 + lane) * 8);
-#pragma unroll
-          for (int mt = 0; mt < 2; ++mt) {
-            if (j == 0)
-              mma_e4m3_z(d[mt][nb], a[mt], b.x, b.y);
-            else
-              mma_e4m3(d[mt][nb], a[mt], b.x, b.y);
-          }
-        }
-      }
       const float4* sg = reinterpret_cast<const float4*>(img + TN * 128) + t;  // token pairs 2t, 2t+1 of block nb
+      float s[2][2];
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
-        const float s0 = __half2float(__ushort_as_half(sc[row0 + 16 * mt + g]));
-        const float s1 = __half2float(__ushort_as_half(sc[row0 + 16 * mt + 8 + g]));
-        const uint64_t s20 = f2pack(s0, s0), s21 = f2pack(s1, s1), m1 = f2pack(-1.0f, -1.0f);
+        s[mt][0] = __half2float(__ushort_as_half(sc[row0 + 16 * mt + g]));
+        s[mt][1] = __half2float(__ushort_as_half(sc[row0 + 16 * mt + 8 + g]));
+      }
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-          const float4 f = sg[4 * nb];  // 2^9 sx (tokens 8nb+2t, +1), c (same tokens)
-          if constexpr (kDebug) {
-            const int tile = static_cast<int>(u / G), gg = static_cast<int>(u % G);
-            const float ev[2][2] = {{d[mt][nb][0] - f.z, d[mt][nb][1] - f.w}, {d[mt][nb][2] - f.z, d[mt][nb][3] - f.w}};
+      for (int nh = 0; nh < NB; nh += NBH) {
+        float d[2][NBH][4];
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
+        for (int j = 0; j < 4; ++j) {
+          uint32_t a[2][4];
 #pragma unroll
-              for (int cc = 0; cc < 2; ++cc) {
-                const int m = 8 * nb + 2 * t + cc, r = rw + 16 * mt + 8 * h + g;
-                if (m < p.M) {
-                  const int32_t dv = static_cast<int32_t>(ev[h][cc] * 512.0f);
-                  if (e < 0)
-                    p.dots_w[(static_cast<int64_t>(m) * (p.tiles * kTileN) + static_cast<int64_t>(tile) * kTileN + r) * G +
-                             gg] = dv;
-                  else
-                    p.dots_r[(static_cast<int64_t>(m) * p.mat[0].nnzb + e) * 64 + (r & 63)] = dv;
+          for (int mt = 0; mt < 2; ++mt) {
+            const uint32_t w0 = *reinterpret_cast<const uint32_t*>(wr + j * jstride + mt * 256);        // row +0
+            const uint32_t w1 = *reinterpret_cast<const uint32_t*>(wr + j * jstride + mt * 256 + 128);  // row +8
+            unpack_u4(w0, a[mt][0], a[mt][2]);
+            unpack_u4(w1, a[mt][1], a[mt][3]);
+          }
+#pragma unroll
+          for (int i = 0; i < NBH; ++i) {
+            const uint2 b = *reinterpret_cast<const uint2*>(img + ((j * NB + nh + i) * 32 + lane) * 8);
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+              if (j == 0)
+                mma_e4m3_z(d[mt][i], a[mt], b.x, b.y);
+              else
+                mma_e4m3(d[mt][i], a[mt], b.x, b.y);
+            }
+          }
+        }
+        const uint64_t m1 = f2pack(-1.0f, -1.0f);
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+          for (int i = 0; i < NBH; ++i) {
+            const int nb = nh + i;
+            const float4 f = sg[4 * nb];  // 2^9 sx (tokens 8nb+2t, +1), c (same tokens)
+            if constexpr (kDebug) {
+              const int tile = static_cast<int>(u / G), gg = static_cast<int>(u % G);
+              const float ev[2][2] = {{d[mt][i][0] - f.z, d[mt][i][1] - f.w}, {d[mt][i][2] - f.z, d[mt][i][3] - f.w}};
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                  const int m = 8 * nb + 2 * t + cc, r = rw + 16 * mt + 8 * h + g;
+                  if (m < p.M) {
+                    const int32_t dv = static_cast<int32_t>(ev[h][cc] * 512.0f);
+                    if (e < 0)
+                      p.dots_w[(static_cast<int64_t>(m) * (p.tiles * kTileN) + static_cast<int64_t>(tile) * kTileN + r) *
+                                   G +
+                               gg] = dv;
+                    else
+                      p.dots_r[(static_cast<int64_t>(m) * p.mat[0].nnzb + e) * 64 + (r & 63)] = dv;
+                  }
                 }
-              }
-          } else {
-            const uint64_t sx2 = f2pack(f.x, f.y), c2 = f2pack(f.z, f.w);
-            const uint64_t e0 = f2fma(c2, m1, f2pack(d[mt][nb][0], d[mt][nb][1]));  // row +0: exact 2^-9 D
-            const uint64_t e1 = f2fma(c2, m1, f2pack(d[mt][nb][2], d[mt][nb][3]));  // row +8
-            acc[mt][nb][0] = f2fma(sx2, f2mul(s20, e0), acc[mt][nb][0]);
-            acc[mt][nb][1] = f2fma(sx2, f2mul(s21, e1), acc[mt][nb][1]);
+            } else {
+              const uint64_t sx2 = f2pack(f.x, f.y), c2 = f2pack(f.z, f.w);
+              const uint64_t e0 = f2fma(c2, m1, f2pack(d[mt][i][0], d[mt][i][1]));  // row +0: exact 2^-9 D
+              const uint64_t e1 = f2fma(c2, m1, f2pack(d[mt][i][2], d[mt][i][3]));  // row +8
+              acc[mt][nb][0] = f2fma(sx2, f2mul(f2pack(s[mt][0], s[mt][0]), e0), acc[mt][nb][0]);
+              acc[mt][nb][1] = f2fma(sx2, f2mul(f2pack(s[mt][1], s[mt][1]), e1), acc[mt][nb][1]);
+            }
           }
         }
       }
     };
+    // Explicit global stores and shared loads in the tile ends: a generic load
+    // after a generic store that might alias it waits for the store to land.
     auto store_y = [&](const ZMat& mt, int64_t n, int m, float v) {
       const int64_t o = static_cast<int64_t>(m) * mt.ldy + n;
       if (p.y_f32)
-        static_cast<float*>(mt.y)[o] = v;
+        st_global_f32(static_cast<float*>(mt.y) + o, v);
       else
-        static_cast<__nv_bfloat16*>(mt.y)[o] = __float2bfloat16_rn(v);
+        st_global_b16(static_cast<__nv_bfloat16*>(mt.y) + o, __bfloat16_as_ushort(__float2bfloat16_rn(v)));
     };
     // End of tile `tile`: every warp writes its partial into its set's
     // buffer, then each warp adds the sets' partials of its slice of the rows
@@ -1412,6 +1442,7 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
       const bool fin = finishes && tile == t_last;    // add the other CTAs' pieces
       float* piece = pub ? piece_of(c) : nullptr;
       float* mine = red + q * (kRedTok * kRedLd);
+      const int slot0 = nstg % S;  // the first slot handed over for pieces
       if (fin) {
         if (!ZW(mbar_wait(&ctl.pieces_in, 0, abort_flag, tmo, p.err), 3)) return false;
         if (warp == 0 && lane == 0) ZC(92);
@@ -1428,8 +1459,8 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
               float v0, v1;
               f2unpack(acc[mt2][nb][h], v0, v1);
               acc[mt2][nb][h] = 0ull;
-              mine[m0 * kRedLd + r] = v0;
-              mine[(m0 + 1) * kRedLd + r] = v1;
+              st_shared_f32(mine + m0 * kRedLd + r, v0);
+              st_shared_f32(mine + (m0 + 1) * kRedLd + r, v1);
             }
         if (warp == kWCompute - 4 && lane == 0) ZC(170 + 4 * pass);
         if (!tile_sync()) return false;
@@ -1439,21 +1470,29 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
         for (int e = q * 32 + lane; e < 32 * kRedTok; e += 32 * US) {
           const int mr = e >> 5, m = pass * kRedTok + mr, r = rw + (e & 31);
           if (m >= p.M) continue;
-          float v = red[mr * kRedLd + r];
+          float v = ld_shared_f32(red + mr * kRedLd + r);
 #pragma unroll
-          for (int qq = 1; qq < US; ++qq) v += red[(qq * kRedTok + mr) * kRedLd + r];  // set order
+          for (int qq = 1; qq < US; ++qq) v += ld_shared_f32(red + (qq * kRedTok + mr) * kRedLd + r);  // set order
           if (fin && pieces_in_smem) {
-            for (int j = 0; j < npc; ++j)  // CTA order
-              if (ZOK(piece_slot(j / per_slot) + (j % per_slot) * piece_bytes + (m * kTileN + r) * 4u <
-                          static_cast<uint32_t>(S) * SB, 6))
-                v += reinterpret_cast<const float*>(stages + piece_slot(j / per_slot) +
-                                                    (j % per_slot) * piece_bytes)[m * kTileN + r];
+            // piece j sits at slot (nstg + j / per_slot) % S, (j % per_slot) pieces in: walked, not divided
+            uint32_t off = static_cast<uint32_t>(slot0) * SB;
+            for (int j = 0, in = 0, sl = slot0; j < npc; ++j) {  // CTA order
+              if (ZOK(off + (m * kTileN + r) * 4u < static_cast<uint32_t>(S) * SB, 6))
+                v += ld_shared_f32(reinterpret_cast<const float*>(stages + off) + m * kTileN + r);
+              if (++in == per_slot) {
+                in = 0;
+                sl = sl + 1 == S ? 0 : sl + 1;
+                off = static_cast<uint32_t>(sl) * SB;
+              } else {
+                off += piece_bytes;
+              }
+            }
           } else if (fin) {
 #pragma unroll 8
             for (int j = 0; j < npc; ++j) v += __ldcg(piece_of(c + 1 + j) + m * kTileN + r);  // CTA order
           }
           if (pub) {
-            if (ZOK(c < P && m < TN, 9)) __stcg(piece + m * kTileN + r, v);
+            if (ZOK(c < P && m < TN, 9)) st_global_f32(piece + m * kTileN + r, v);
           } else if (ZOK(tile >= mt.tile0 && tile < mat_end_tile(p, tile) && m < p.M, 8)) {
             store_y(mt, nbase + r, m, v);
           }
