@@ -927,12 +927,15 @@ __global__ void __launch_bounds__(kThreads, 1) zipper_decode_kernel(const ZParam
 // warp 17: residual map and records.
 // ---------------------------------------------------------------------------
 
-// Units per stage (= sets of 4 compute warps): 4 up to 16 tokens; 3 at 32
-// tokens, whose accumulators need more registers per thread (the warps of a
-// block share each scheduler's register file).
-__host__ __device__ constexpr int w_sets(int tn) { return tn == 32 ? 3 : 4; }
-__host__ __device__ constexpr int w_threads(int tn) { return 32 * (4 * w_sets(tn) + 2); }  // + producer, epilogue
-constexpr int kWMaxSets = 4;
+// 16 compute warps in sets; a set takes one unit (128 rows) of every stage.
+// Up to 16 tokens a warp owns 32 rows (two 16-row MMA tiles): sets of 4 warps,
+// 4 units per stage.  At 32 tokens a warp owns 16 rows: its accumulators then
+// fit the 96 registers a thread gets when 18 warps share the schedulers'
+// register files, with sets of 8 warps and 2 units per stage.
+__host__ __device__ constexpr int w_mt(int tn) { return tn == 32 ? 1 : 2; }  // 16-row MMA tiles per warp
+__host__ __device__ constexpr int w_wps(int tn) { return 8 / w_mt(tn); }     // warps per set
+__host__ __device__ constexpr int w_sets(int tn) { return 16 / w_wps(tn); }  // sets = units per stage
+__host__ __device__ constexpr int w_threads(int tn) { return 32 * (16 + 2); }  // + producer, epilogue
 
 // One bulk copy of the producer's schedule: source, offset in the stage, bytes.
 struct __align__(16) CopyDesc {
@@ -940,9 +943,10 @@ struct __align__(16) CopyDesc {
   uint32_t dst;
   uint32_t bytes;
 };
-constexpr int kMaxStg = kMaxUnits / 3 + 1;  // stages per CTA at most (3 or 4 units each)
+
 constexpr int kCopiesPerStage = 8;          // weight runs + activation runs of a stage (4 units: at most 4 + 4)
 
+template <int kMaxStg>  // stages per CTA at most: kMaxUnits / units per stage, + 1
 struct __align__(16) WCtl {
   CopyDesc cp[kMaxStg][kCopiesPerStage];  // the stage's copies (bytes 0: none)
   uint32_t stage_tx[kMaxStg];             // bytes a stage's copies bring
@@ -984,12 +988,14 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
   constexpr int NB = TN / 8;           // 8-token blocks of one MMA
   constexpr int kRedPasses = TN == 8 ? 1 : 2, kRedTok = TN / kRedPasses;  // tile sums: tokens per pass
   constexpr int kRedLd = kTileN + 4;  // token stride of a partial buffer: fragment writes hit distinct banks
+  constexpr int MT = w_mt(TN), WPS = w_wps(TN);  // 16-row MMA tiles per warp, warps per set
   constexpr int US = w_sets(TN);       // units per stage = sets of compute warps
-  constexpr int kWCompute = 4 * US, kWProd = kWCompute, kWEpi = kWCompute + 1, kWThreads = w_threads(TN);
+  constexpr int kWCompute = 16, kWProd = kWCompute, kWEpi = kWCompute + 1, kWThreads = w_threads(TN);
+  constexpr int kMaxStg = kMaxUnits / US + 1;  // stages per CTA at most
   constexpr int kArec = TN * 136;      // activation image: B fragments, then {2^9 sx, c} pairs
   constexpr int kAct = US * kArec;     // a stage: US activation images, then US base records
   extern __shared__ uint8_t smem_raw[];
-  __shared__ WCtl ctl;
+  __shared__ WCtl<kMaxStg> ctl;
   uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
   const int S = p.nstages, SB = p.stage_bytes, G = p.G;
   uint8_t* stages = smem;
@@ -1036,7 +1042,7 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
     }
     if (lane < kRS) {
       mbar_init(&ctl.r_full[lane], 1);
-      mbar_init(&ctl.r_empty[lane], 2);
+      mbar_init(&ctl.r_empty[lane], WPS / 2);  // the warps of the record's 64-row half
     }
     if (lane == 10) mbar_init(&ctl.tile_bar, kWCompute);
     if (lane == 11) mbar_init(&ctl.map_ready, 1);
@@ -1206,7 +1212,8 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
         idle = 0;
         continue;
       }
-      __nanosleep(32);
+      // back off (32 ns doubling to 512 ns): the polls share a scheduler with compute warps
+      __nanosleep(32u << min(idle >> 2, 4));
       if ((++idle & 15) == 0) {  // bounded: give up after the timeout without progress
         int give_up = 0;
         if (lane == 0) {
@@ -1280,9 +1287,9 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
     }
   } else {
     // ---------------- compute warps ----------------
-    const int q = warp >> 2, wq = warp & 3;      // set, row quarter
+    const int q = warp / WPS, wq = warp % WPS;  // set, row block within the set
     const int g = lane >> 2, t = lane & 3;       // MMA fragment coordinates
-    const int rw = 32 * wq, half = wq >> 1;      // first row of this warp, its residual half
+    const int rw = 16 * MT * wq, half = rw >> 6;  // first row of this warp, its residual half
     if (warp == 0) {
       // Residual map of the CTA's units (CSR entry per unit and half) and the
       // records' ring positions.  The block lists are read before the
@@ -1332,37 +1339,37 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
     bool ok = ZW(mbar_wait(&ctl.map_ready, 0, abort_flag, tmo, p.err), 0);
     pdl_wait();  // Y and the workspace pieces may still be in use by the preceding kernel
     // accumulators: [mt][nb] pairs {row r, tokens 8nb+2t, +1}, {row r+8, same tokens}
-    uint64_t acc[2][NB][2];
+    uint64_t acc[MT][NB][2];
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
+    for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb) acc[mt][nb][0] = acc[mt][nb][1] = 0ull;
 
     // One group's product for this warp's rows: codes (K-steps jstride apart,
     // 16 bytes per row, first row row0), fragments and scale pairs of the
     // group's activation image, row scales sc; into acc, or the test hook's dots.
-    // The 8-token blocks are taken at most two at a time (the weight
-    // fragments are unpacked again for the second pair): 32 tokens would
-    // otherwise hold 32 MMA results next to the 32 accumulators and spill.
+    // The 8-token blocks are taken one at a time (the weight fragments are
+    // unpacked again for each): the MMA results then never hold more than 8
+    // registers next to the accumulators, and nothing spills.
     auto group_product = [&](const uint8_t* codes, int jstride, int row0, const uint16_t* sc, const uint8_t* img,
                              int64_t u, int e) {
-      constexpr int NBH = NB < 2 ? NB : 2;  // 8-token blocks per pass
+      constexpr int NBH = 1;  // 8-token blocks per pass
       const uint8_t* wr = codes + (row0 + g) * 16 + t * 4;
       const float4* sg = reinterpret_cast<const float4*>(img + TN * 128) + t;  // token pairs 2t, 2t+1 of block nb
-      float s[2][2];
+      float s[MT][2];
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
+      for (int mt = 0; mt < MT; ++mt) {
         s[mt][0] = __half2float(__ushort_as_half(sc[row0 + 16 * mt + g]));
         s[mt][1] = __half2float(__ushort_as_half(sc[row0 + 16 * mt + 8 + g]));
       }
 #pragma unroll
       for (int nh = 0; nh < NB; nh += NBH) {
-        float d[2][NBH][4];
+        float d[MT][NBH][4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          uint32_t a[2][4];
+          uint32_t a[MT][4];
 #pragma unroll
-          for (int mt = 0; mt < 2; ++mt) {
+          for (int mt = 0; mt < MT; ++mt) {
             const uint32_t w0 = *reinterpret_cast<const uint32_t*>(wr + j * jstride + mt * 256);        // row +0
             const uint32_t w1 = *reinterpret_cast<const uint32_t*>(wr + j * jstride + mt * 256 + 128);  // row +8
             unpack_u4(w0, a[mt][0], a[mt][2]);
@@ -1372,7 +1379,7 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
           for (int i = 0; i < NBH; ++i) {
             const uint2 b = *reinterpret_cast<const uint2*>(img + ((j * NB + nh + i) * 32 + lane) * 8);
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
+            for (int mt = 0; mt < MT; ++mt) {
               if (j == 0)
                 mma_e4m3_z(d[mt][i], a[mt], b.x, b.y);
               else
@@ -1382,7 +1389,7 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
         }
         const uint64_t m1 = f2pack(-1.0f, -1.0f);
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
+        for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
           for (int i = 0; i < NBH; ++i) {
             const int nb = nh + i;
@@ -1452,7 +1459,7 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
 #pragma unroll
         for (int nb = pass * (NB / kRedPasses); nb < (pass + 1) * (NB / kRedPasses); ++nb)
 #pragma unroll
-          for (int mt2 = 0; mt2 < 2; ++mt2)
+          for (int mt2 = 0; mt2 < MT; ++mt2)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int r = rw + 16 * mt2 + 8 * h + g, m0 = 8 * nb + 2 * t - pass * kRedTok;
@@ -1462,13 +1469,13 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
               st_shared_f32(mine + m0 * kRedLd + r, v0);
               st_shared_f32(mine + (m0 + 1) * kRedLd + r, v1);
             }
-        if (warp == kWCompute - 4 && lane == 0) ZC(170 + 4 * pass);
+        if (warp == kWCompute - WPS && lane == 0) ZC(170 + 4 * pass);
         if (!tile_sync()) return false;
-        if (warp == kWCompute - 4 && lane == 0) ZC(171 + 4 * pass);
-        // this warp's slice: the (row, token) entries e = q, q + US, .. of its 32-row block, token-major
-        // (consecutive lanes take consecutive rows: coalesced stores)
-        for (int e = q * 32 + lane; e < 32 * kRedTok; e += 32 * US) {
-          const int mr = e >> 5, m = pass * kRedTok + mr, r = rw + (e & 31);
+        if (warp == kWCompute - WPS && lane == 0) ZC(171 + 4 * pass);
+        // the pass's (row, token) entries of the tile, spread over the compute warps, row-major
+        // within a token (consecutive lanes take consecutive rows: coalesced stores)
+        for (int e = warp * 32 + lane; e < kTileN * kRedTok; e += 32 * kWCompute) {
+          const int mr = e >> 7, m = pass * kRedTok + mr, r = e & (kTileN - 1);
           if (m >= p.M) continue;
           float v = ld_shared_f32(red + mr * kRedLd + r);
 #pragma unroll
@@ -1497,9 +1504,9 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
             store_y(mt, nbase + r, m, v);
           }
         }
-        if (warp == kWCompute - 4 && lane == 0) ZC(172 + 4 * pass);
+        if (warp == kWCompute - WPS && lane == 0) ZC(172 + 4 * pass);
         if (pass + 1 < kRedPasses && !tile_sync()) return false;  // the buffers are free again
-        if (warp == kWCompute - 4 && lane == 0) ZC(173 + 4 * pass);
+        if (warp == kWCompute - WPS && lane == 0) ZC(173 + 4 * pass);
       }
       if (pub) {
         __syncwarp();
@@ -1516,11 +1523,12 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
       for (; ok && ui < tile_end; ui += US) {
         if (!(ok = ZW(mbar_wait(&ctl.full[s], ph, abort_flag, tmo, p.err), 0))) break;
         if (warp == 0 && lane == 0 && st < 16) ZC(32 + st);
-        if (warp == kWCompute - 4 && lane == 0 && st < 16) ZC(48 + st);
+        if (warp == kWCompute - WPS && lane == 0 && st < 16) ZC(48 + st);
         const uint8_t* sg = stage(s);
         const uint8_t* img = sg + q * kArec;
         const uint8_t* rec = sg + kAct + q * kWRecBytes;
         group_product(rec, 2048, rw, reinterpret_cast<const uint16_t*>(rec + kWRecScales), img, u0 + ui, -1);
+        if (warp == 0 && lane == 0 && st < 16) ZC(230 + st);
         const int e = ctl.map[ui][half];
         if (e >= 0) {  // the residual block of this warp's half
           const int cpos = ctl.rpos[ui][half], slot = cpos % kRS;
@@ -1536,14 +1544,15 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
           if (lane == 0) mbar_arrive(&ctl.r_empty[slot]);
         }
         __syncwarp();
+        if (warp == 0 && lane == 0 && st < 8) ZC(246 + st);
         if (lane == 0) mbar_arrive(&ctl.empty[s]);  // this warp is done with the stage
         ++st;
         if (++s == S) s = 0, ph ^= 1;
       }
       if (warp == 0 && lane == 0 && f < 8) ZC(64 + f);
-      if (warp == kWCompute - 4 && lane == 0 && f < 8) ZC(72 + f);
+      if (warp == kWCompute - WPS && lane == 0 && f < 8) ZC(72 + f);
       if (ok && !kDebug) ok = flush(tile);
-      if (warp == kWCompute - 4 && lane == 0 && f < 8) ZC(80 + f);
+      if (warp == kWCompute - WPS && lane == 0 && f < 8) ZC(80 + f);
     }
 
     // Finish the tiles whose count this CTA completed: after every compute
@@ -1552,7 +1561,7 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
   }
 
   // Every role is done.
-  if (warp == kWCompute - 4 && lane == 0) ZC(90);
+  if (warp == kWCompute - WPS && lane == 0) ZC(90);
   __syncwarp();
   if (lane == 0) mbar_arrive(&ctl.exit_bar);
   mbar_wait(&ctl.exit_bar, 0, abort_flag, tmo, p.err);
@@ -1704,6 +1713,12 @@ bool use_tc_variant() {
 
 // Plan for M tokens over `tiles` 128-row tiles of K inputs; false if the
 // decode kernel does not cover the shape.
+// Static shared memory of the warp-MMA form's control block (with its alignment slack).
+template <int TN>
+int w_ctl_bytes() {
+  return (static_cast<int>(sizeof(WCtl<kMaxUnits / w_sets(TN) + 1>)) + 127) / 128 * 128;
+}
+
 bool zplan(int64_t M, int64_t tiles, int64_t K, ZPlan* out) {
   if (M < 1 || M > 32) return false;
   ZPlan pl;
@@ -1725,7 +1740,7 @@ bool zplan(int64_t M, int64_t tiles, int64_t K, ZPlan* out) {
   } else {
     pl.arec = pl.tn * 136;
     pl.stage_bytes = (w_sets(pl.tn) * (pl.arec + kWRecBytes) + 127) / 128 * 128;
-    ctl_bytes = (static_cast<int>(sizeof(WCtl)) + 127) / 128 * 128;
+    ctl_bytes = pl.tn == 32 ? w_ctl_bytes<32>() : w_ctl_bytes<8>();
     // alignment, residual ring, tile partials (one pass over 8 tokens, two over 16 or 32)
     fixed = 128 + kRS * kRRecBytes + w_sets(pl.tn) * (kTileN + 4) * (pl.tn == 8 ? 8 : pl.tn / 2) * 4;
   }
@@ -1792,7 +1807,7 @@ mq_status wlaunch(const ZParams& zp, const ZPlan& pl, cudaStream_t stream) {
   {
     std::lock_guard<std::mutex> lk(mu);
     if (!attr_set[dev]) {
-      const int ctl_bytes = (static_cast<int>(sizeof(WCtl)) + 127) / 128 * 128;
+      const int ctl_bytes = w_ctl_bytes<TN>();
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit - ctl_bytes) != cudaSuccess)
         return launch_status("zipper: smem attribute");
       attr_set[dev] = true;
