@@ -380,6 +380,10 @@ __device__ __forceinline__ float act_value(const uint16_t* x, int64_t i, bool bf
 // first unit of CTA c, and the CTA that owns unit u (balanced contiguous ranges)
 __device__ __forceinline__ int64_t first_unit(int64_t c, int64_t U, int64_t P) { return c * U / P; }
 __device__ __forceinline__ int64_t owner_of(int64_t u, int64_t U, int64_t P) { return ((u + 1) * P - 1) / U; }
+// The same in 32-bit arithmetic, for the warp-MMA form: its planner keeps units per CTA at most kMaxUnits
+// and CTAs at most kWsZeroBytes / 4, so c * U and (u + 1) * P stay below 2^31.
+__device__ __forceinline__ uint32_t first_unit32(uint32_t c, uint32_t U, uint32_t P) { return c * U / P; }
+__device__ __forceinline__ uint32_t owner_of32(uint32_t u, uint32_t U, uint32_t P) { return ((u + 1) * P - 1) / U; }
 
 __device__ __forceinline__ int mat_end_tile(const ZParams& p, int t);
 __device__ __forceinline__ int mat_of_tile(const ZParams& p, int t) {
@@ -1002,8 +1006,9 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
   uint8_t* rring = smem + static_cast<size_t>(S) * SB;
   float* red = reinterpret_cast<float*>(rring + kRS * kRRecBytes);  // [US sets][kRedTok][kRedLd] tile partials
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t U = p.units, P = p.ctas, c = blockIdx.x;
-  const int64_t u0 = first_unit(c, U, P), u1 = first_unit(c + 1, U, P);
+  const uint32_t U32 = static_cast<uint32_t>(p.units), P32 = static_cast<uint32_t>(p.ctas), c32 = blockIdx.x;
+  const int64_t U = U32, P = P32, c = c32;
+  const int64_t u0 = first_unit32(c32, U32, P32), u1 = first_unit32(c32 + 1, U32, P32);
   const int nu = static_cast<int>(u1 - u0);
   const int nstg = (nu + US - 1) / US;
   // Stream-K roles.  A cut tile is finished by the CTA holding its first
@@ -1013,11 +1018,13 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
   // tile (its last, when its range holds that tile's head but not its end).
   // The pieces of the tile it finishes are the tails of later CTAs' ranges,
   // computed first there: usually in place long before they are needed.
-  const int t_first = static_cast<int>(u0 / G), t_last = static_cast<int>((u1 - 1) / G);
+  const int t_first = static_cast<int>(static_cast<uint32_t>(u0) / static_cast<uint32_t>(G));
+  const int t_last = static_cast<int>(static_cast<uint32_t>(u1 - 1) / static_cast<uint32_t>(G));
   const bool publishes = !kDebug && u0 > static_cast<int64_t>(t_first) * G;
   const bool finishes =
       !kDebug && u0 <= static_cast<int64_t>(t_last) * G && u1 < static_cast<int64_t>(t_last + 1) * G;
-  const int npc = finishes ? static_cast<int>(owner_of(static_cast<int64_t>(t_last + 1) * G - 1, U, P) - c) : 0;
+  const int npc =
+      finishes ? static_cast<int>(owner_of32(static_cast<uint32_t>((t_last + 1) * G - 1), U32, P32) - c32) : 0;
   const uint32_t piece_bytes = static_cast<uint32_t>(p.M) * kTileN * 4;  // tokens 0..M-1 of a [TN][128] piece
   // the pieces go into stage slots no stage needs any more, per_slot to a slot, if they fit in all slots
   const int per_slot = SB / static_cast<int>(piece_bytes);
@@ -1064,15 +1071,6 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
                    (reinterpret_cast<uintptr_t>(d.src) & 15u) == 0,
                1);
   };
-  auto wrec = [&](int64_t u) -> const uint8_t* {
-    const int t = static_cast<int>(u / G), g = static_cast<int>(u - static_cast<int64_t>(t) * G);
-    const ZMat& mt = p.mat[mat_of_tile(p, t)];
-    return mt.wpk + (static_cast<int64_t>(t - mt.tile0) * G + g) * kWRecBytes;
-  };
-  auto mat_end = [&](int64_t u) -> int64_t {
-    const int mi = mat_of_tile(p, static_cast<int>(u / G));
-    return static_cast<int64_t>(mi + 1 < p.nmat ? p.mat[mi + 1].tile0 : p.tiles) * G;
-  };
 
   if (warp == kWProd) {
     // ---------------- producer: a stage = US units' base records and activation images, then the
@@ -1111,6 +1109,9 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
           d.src = mt.wpk + (static_cast<int64_t>(tt - mt.tile0) * G + gg) * kWRecBytes;
           d.dst = static_cast<uint32_t>(kAct + k * kWRecBytes);
           d.bytes = static_cast<uint32_t>((end - lane) * kWRecBytes);
+          // the first stages' base records leave at once (their stage's count is posted
+          // below: a transfer may complete before it, the phase cannot)
+          if (st < S && copy_ok(d)) bulk_g2s(stage(st) + d.dst, d.src, d.bytes, &ctl.full[st]);
         }
         if ((am >> lane) & 1u) {
           const unsigned nxt = am & smask & above;
@@ -1124,26 +1125,18 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
         if (k == 0) {
           for (int i = nw + __popc(am & smask); i < kCopiesPerStage; ++i) ctl.cp[st][i].bytes = 0;
           ctl.stage_tx[st] = static_cast<uint32_t>((last - first) * (kWRecBytes + kArec));
+          if (st < S) mbar_arrive_expect_tx(&ctl.full[st], ctl.stage_tx[st]);
         }
       }
     }
     __syncwarp();
     const int pre = min(S, nstg);
-    // The first stages' base records are requested before the dependency wait:
-    // the kernels that may run ahead of it (this library's, which ask for the
-    // next launch early) never write packed weights.  Then the activation
-    // images of those stages, all in one instruction (lane: stage, copy).
-    if (lane < pre) mbar_arrive_expect_tx(&ctl.full[lane], ctl.stage_tx[lane]);
-    __syncwarp();
+    // The first stages' base records left during the table pass, before the
+    // dependency wait: the kernels that may run ahead of it (this library's,
+    // which ask for the next launch early) never write packed weights.  Then
+    // the activation images of those stages, all in one instruction (lane:
+    // stage, copy).
     if (lane == 0) ZC(13);
-    for (int st = 0; st < pre; ++st) {
-      if (lane < kCopiesPerStage) {
-        const CopyDesc d = ctl.cp[st][lane];
-        if (d.bytes && d.dst >= static_cast<uint32_t>(kAct) && copy_ok(d))
-          bulk_g2s(stage(st) + d.dst, d.src, d.bytes, &ctl.full[st]);
-      }
-    }
-    __syncwarp();
     if (lane == 0) ZC(8);
     pdl_wait();  // the activation images are the preceding kernel's output
     if (lane == 0) ZC(10);
@@ -1297,8 +1290,7 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
       for (int i = lane; i < nu * 2; i += 32) (&ctl.map[0][0])[i] = -1;
       __syncwarp();
       if (nu > 0) {
-        const int t_lo = static_cast<int>(u0 / G), t_hi = static_cast<int>((u1 - 1) / G);
-        for (int tt = t_lo; tt <= t_hi; ++tt) {
+        for (int tt = t_first; tt <= t_last; ++tt) {
           const ZMat& mt = p.mat[mat_of_tile(p, tt)];
           if (mt.nnzb == 0) continue;
           const int64_t br = 2 * static_cast<int64_t>(tt - mt.tile0);
