@@ -828,12 +828,31 @@ def run_ours(args):
     plain0 = capture(lambda: step0.run(stream), stream)
     y_host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in step.y.items()}
 
-    def e2e_body():  # host inputs -> device, the step, outputs -> host
-        for k, t in xs_host.items():
-            xs_dev[k].copy_(t, non_blocking=True)
-        step.run(stream)
-        for k, t in step.y.items():
-            y_host[k].copy_(t, non_blocking=True)
+    copy_stream = torch.cuda.Stream(device=dev)
+
+    def e2e_body():
+        # Host inputs -> device, the step, outputs -> host, every step.  The copies run on a second
+        # stream of the same graph: each call waits only for its own input, and its outputs go to
+        # the host while the next call computes.
+        copy_stream.wait_stream(stream)
+        ready = {}
+        with torch.cuda.stream(copy_stream):
+            for M, _, inp, _ in step.calls:
+                if (M, inp) not in ready:
+                    xs_dev[(M, inp)].copy_(xs_host[(M, inp)], non_blocking=True)
+                    ready[(M, inp)] = torch.cuda.Event()
+                    ready[(M, inp)].record(copy_stream)
+        for j, (M, _, inp, names) in enumerate(step.calls):
+            stream.wait_event(ready[(M, inp)])
+            mq.fused_linear(xs_dev[(M, inp)], step.pls(j), outs=[step.y[(M, n)] for n in names], ws=step.ws,
+                            stream=stream)
+            done = torch.cuda.Event()
+            done.record(stream)
+            copy_stream.wait_event(done)
+            with torch.cuda.stream(copy_stream):
+                for n in names:
+                    y_host[(M, n)].copy_(step.y[(M, n)], non_blocking=True)
+        stream.wait_stream(copy_stream)
     e2e_graph = capture(e2e_body, stream)
 
     # ---- the timed region: K plain replays of the step graph, nothing else ----
@@ -945,7 +964,9 @@ def run_ours(args):
                          "kernel": "zipper_warp_kernel (fused W4A4 + residual stream-K GEMM)",
                          "launches_per_step": ncalls},
             "cpu_baseline": cpu,
-            "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "how": "one graph per step: H2D of every input from pinned host memory and D2H of every output "
+                           "on a copy stream, each call waiting for its own input (copies overlap other calls)"},
             "gpu_launches": step.launches() * args.steps,
             "clocks": {"sm_mhz": ck["sm_mhz"], "sm_max_mhz": ck["sm_max_mhz"], "reasons": ck["reasons"],
                        "samples_in_region": ck["samples"], "source": ck["source"]},
