@@ -389,7 +389,13 @@ class Step:
                 events.record(ev_base + 2 * j + 1, stream)
 
     def launches(self) -> int:
-        return 2 * len(self.calls)  # the activation-image kernel and the fused GEMM per call
+        # per call: the fused GEMM, plus the activation-image kernel unless the column form runs
+        # (it quantizes inside; the step's inputs are 16-byte aligned rows)
+        n = 0
+        for M, _, _, names in self.calls:
+            plan = self.mq.gemm_plan(M, sum(self.lins[k].N for k in names), self.lins[names[0]].K)
+            n += 1 if plan["variant"] == "column" else 2
+        return n
 
     def bytes_per_step(self) -> int:
         return sum(call_bytes(self.pls(j), M, self.lins[names[0]].K) for j, (M, _, _, names) in enumerate(self.calls))

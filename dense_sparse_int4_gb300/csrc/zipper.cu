@@ -130,6 +130,7 @@ struct ZParams {
   int M, Mp, G, tiles, ctas, nstages, stage_bytes;
   int64_t units;
   int y_f32;
+  int raw;          // column form: the stages take X rows (else packed codes and scales)
   int32_t* dots_w;  // test hook (one matrix): raw group dots instead of Y
   int32_t* dots_r;
   const uint8_t* act;  // workspace: [G] activation images (written by the image kernel)
@@ -1573,13 +1574,635 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
   }
 }
 
+// ---------------------------------------------------------------------------
+// Decode GEMM, column form (warp MMA, quantizer inside; the default for M <= 32)
+// ---------------------------------------------------------------------------
+// The launch's tiles are taken T at a time (T = the sets of compute warps: 4
+// up to 16 tokens, 2 at 32), and a "column" is one 128-input group of such a
+// tile-group.  One shared-memory stage holds one column: the T tiles' base
+// records of the group and the group's activations (X rows as they are, or
+// packed codes and scales).  Set q owns tile q of every tile-group, so its
+// accumulators stay on one tile for the CTA's whole share of the tile-group,
+// and the group's activation image (E4M3 codes in the MMA's B-fragment order,
+// 2^9 sx, offset terms) is built once per stage in shared memory by all 16
+// compute warps: the activation quantizer runs inside the GEMM, one stage
+// ahead of the MMAs, on data the producer has already brought in.
+//
+// CTAs take equal contiguous ranges of columns (stream-K over every SM).  A
+// tile-group cut by range boundaries is finished by the CTA holding its first
+// group: every other CTA on it publishes a piece (its fp32 partial sums, in
+// register-fragment order, so writes and reads are whole 256-byte rows per
+// warp) and a flag; the finisher adds the pieces in CTA order (deterministic).
+
+template <int TN>
+struct ColGeo {
+  static constexpr int T = w_sets(TN);                       // tiles per tile-group
+  static constexpr int kImg = TN * 136;                      // B fragments, then {2^9 sx, c} per token pair
+  static constexpr int kOffRec = (kImg + 127) / 128 * 128;   // T base records
+  static constexpr int kOffRaw = kOffRec + T * kWRecBytes;   // X rows [TN][128] x 2 bytes, or codes [TN][64] + scales
+  static constexpr int kRaw = TN * 256;
+  static constexpr int kOffScales = TN * 64;                 // packed input: the scales after the codes
+  static constexpr int kStage = (kOffRaw + kRaw + 127) / 128 * 128;
+  static constexpr int kMaxCols = kMaxUnits / T;             // columns per CTA at most (residual map size)
+  static constexpr int kPieceU64 = T * TN * 64;              // a piece: T tiles x 128 rows x TN tokens, fp32 pairs
+};
+static_assert(kWRecBytes % 128 == 0, "base records keep 128-byte alignment in a stage");
+
+template <int kMaxCols, int T>
+struct __align__(16) CCtl {
+  uint64_t full[kMaxStages];    // the stage's base records landed
+  uint64_t xfull[kMaxStages];   // the stage's activations landed
+  uint64_t built[kMaxStages];   // every compute warp wrote its share of the stage's image
+  uint64_t empty[kMaxStages];   // every compute warp is done with the stage
+  uint64_t r_full[kRS];
+  uint64_t r_empty[kRS];        // the warps of the record's 64-row half
+  uint64_t map_ready;
+  uint64_t piece_written;       // every compute warp wrote its share of this CTA's piece
+  uint64_t pieces_in;           // the other CTAs' pieces of the tile-group this CTA finishes are readable
+  uint64_t exit_bar;
+  int32_t map[kMaxCols][T][2];  // CSR entry of the residual block of (column, tile, half), or -1
+  int32_t rpos[kMaxCols][T][2]; // its position in the residual ring order
+  const uint8_t* rsrc[kMaxCols][T];  // residual records of the tile's matrix
+  int abort_flag;
+  volatile int r_issued;        // residual records issued so far (in ring order)
+};
+
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t ld_global_cg_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.global.cg.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_global_cg_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.global.cg.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+// Two floats holding integers |q| <= 7 -> their E4M3 bytes (exact), `lo` in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2_of(float hi, float lo) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Eight inputs of one token (inputs 8k..8k+7 of a group) quantized with the
+// token's scale s (an fp16 value, nonzero) and r = 1/s rounded to fp32:
+// q = clamp(RNE(v / s), -7, 7), as the quantizer's IEEE division gives it.
+// The quotient is refined once, q1 = q0 + (v - q0 s) r with q0 = v r (the
+// residual exact in the fma), which puts q1 within 2^-20 of v / s and equal
+// to it where v / s is a half-integer; an input and a scale of at most 11
+// significant bits never put v / s closer than 2^-13 to a half-integer of
+// magnitude 1/2 or more unless it is one, so rint(q1) is the exact
+// round-half-even.  Out: the codes as floats.
+__device__ __forceinline__ void quant8(const float (&v)[8], float s, float r, float (&q)[8]) {
+  const uint64_t r2 = f2pack(r, r), ns2 = f2pack(-s, -s);
+#pragma unroll
+  for (int i = 0; i < 8; i += 2) {
+    const uint64_t v2 = f2pack(v[i], v[i + 1]);
+    const uint64_t q0 = f2mul(v2, r2);
+    const uint64_t e = f2fma(q0, ns2, v2);
+    const uint64_t q1 = f2fma(e, r2, q0);
+    float a, b;
+    f2unpack(q1, a, b);
+    q[i] = fminf(fmaxf(rintf(a), -7.0f), 7.0f);
+    q[i + 1] = fminf(fmaxf(rintf(b), -7.0f), 7.0f);
+  }
+}
+
+// TN: tokens per tile (8, 16 or 32); kDebug: write raw group dots.
+template <int TN, bool kDebug>
+__global__ void __launch_bounds__(w_threads(TN), 1) zipper_col_kernel(const ZParams p) {
+  using Geo = ColGeo<TN>;
+  constexpr int NB = TN / 8;                                // 8-token blocks of one MMA
+  constexpr int MT = w_mt(TN), WPS = w_wps(TN), T = Geo::T;  // 16-row MMA tiles per warp, warps per set, sets
+  constexpr int kWCompute = 16, kWProd = kWCompute, kWEpi = kWCompute + 1, kWThreads = w_threads(TN);
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ CCtl<Geo::kMaxCols, T> ctl;
+  uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+  const int S = p.nstages, SB = p.stage_bytes, G = p.G;
+  uint8_t* stages = smem;
+  uint8_t* rring = smem + static_cast<size_t>(S) * SB;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t C32 = static_cast<uint32_t>(p.units), P32 = static_cast<uint32_t>(p.ctas), c32 = blockIdx.x;
+  const int64_t P = P32, c = c32;
+  const int col0 = static_cast<int>(first_unit32(c32, C32, P32)), col1 = static_cast<int>(first_unit32(c32 + 1, C32, P32));
+  const int nstg = col1 - col0;  // one stage per column
+  // Stream-K roles (per tile-group): a CTA publishes at most one piece (its
+  // first tile-group, when its range starts inside it) and finishes at most
+  // one tile-group (its last, when its range holds that tile-group's first
+  // group but not its last).
+  const int t_first = col0 / G, t_last = (col1 - 1) / G;
+  const bool publishes = !kDebug && col0 > t_first * G;
+  const bool finishes = !kDebug && col0 <= t_last * G && col1 < (t_last + 1) * G;
+  const int npc =
+      finishes ? static_cast<int>(owner_of32(static_cast<uint32_t>((t_last + 1) * G - 1), C32, P32) - c32) : 0;
+  auto piece_of = [&](int64_t cc) { return reinterpret_cast<uint64_t*>(p.part) + cc * Geo::kPieceU64; };
+  volatile int* abort_flag = &ctl.abort_flag;
+  const uint64_t tmo = p.timeout_ns;
+  const uint32_t xbytes = p.raw ? static_cast<uint32_t>(p.M) * 256u : static_cast<uint32_t>(p.Mp) * 66u;
+
+  if (warp == 0) {
+    for (int s = lane; s < S; s += 32) {
+      mbar_init(&ctl.full[s], 1);
+      mbar_init(&ctl.xfull[s], 1);
+      mbar_init(&ctl.built[s], kWCompute);
+      mbar_init(&ctl.empty[s], kWCompute);
+    }
+    if (lane < kRS) {
+      mbar_init(&ctl.r_full[lane], 1);
+      mbar_init(&ctl.r_empty[lane], WPS / 2);  // the warps of the record's 64-row half
+    }
+    if (lane == 11) mbar_init(&ctl.map_ready, 1);
+    if (lane == 12) mbar_init(&ctl.piece_written, kWCompute);
+    if (lane == 13) mbar_init(&ctl.pieces_in, 1);
+    if (lane == 14) mbar_init(&ctl.exit_bar, kWThreads / 32);
+    if (lane == 15) ctl.abort_flag = 0;
+    if (lane == 16) ctl.r_issued = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_trigger();
+  auto stage = [&](int s) { return stages + static_cast<size_t>(s) * SB; };
+
+  if (warp == kWProd) {
+    // ---------------- producer: a stage = one column's T base records and its group's activations;
+    // then the residual records, in ring order ----------------
+    auto issue_w = [&](int st, int sl) {  // the stage's base records (lane q: tile q of the tile-group)
+      const int cc = col0 + st, tg = cc / G, gg = cc - tg * G;
+      const int nt = min(T, p.tiles - tg * T);
+      if (lane < nt) {
+        const int tt = tg * T + lane;
+        const ZMat& mt = p.mat[mat_of_tile(p, tt)];
+        const uint8_t* src = mt.wpk + (static_cast<int64_t>(tt - mt.tile0) * G + gg) * kWRecBytes;
+        if (ZOK((reinterpret_cast<uintptr_t>(src) & 15u) == 0, 1))
+          bulk_g2s(stage(sl) + Geo::kOffRec + lane * kWRecBytes, src, kWRecBytes, &ctl.full[sl]);
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&ctl.full[sl], static_cast<uint32_t>(nt) * kWRecBytes);
+    };
+    auto issue_x = [&](int st, int sl) {  // the stage's activations: X rows (lane m), or codes + scales
+      const int gg = (col0 + st) % G;
+      uint8_t* raw = stage(sl) + Geo::kOffRaw;
+      if (p.raw) {
+        if (lane < p.M)
+          bulk_g2s(raw + lane * 256, p.x + static_cast<int64_t>(lane) * p.ldx + static_cast<int64_t>(gg) * kGroup, 256u,
+                   &ctl.xfull[sl]);
+      } else {
+        if (lane == 0)
+          bulk_g2s(raw, p.xq + static_cast<int64_t>(gg) * p.Mp * 64, static_cast<uint32_t>(p.Mp) * 64u, &ctl.xfull[sl]);
+        if (lane == 1)
+          bulk_g2s(raw + Geo::kOffScales, p.xs + static_cast<int64_t>(gg) * p.Mp, static_cast<uint32_t>(p.Mp) * 2u,
+                   &ctl.xfull[sl]);
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&ctl.xfull[sl], xbytes);
+    };
+    const int pre = min(S, nstg);
+    // The first stages' base records leave before the dependency wait (the
+    // kernels that may run ahead of it never write packed weights); their
+    // activations after it.
+    for (int st = 0; st < pre; ++st) issue_w(st, st);
+    pdl_wait();
+    for (int st = 0; st < pre; ++st) issue_x(st, st);
+    __syncwarp();
+    bool ok = ZW(mbar_wait(&ctl.map_ready, 0, abort_flag, tmo, p.err), 7);
+    ok = __all_sync(0xFFFFFFFFu, ok);
+    int bst = pre, bs = 0, bph = 1;  // next stage, its slot, the slot's fill parity
+    int rf = 0;                       // next (column, tile, half) whose residual record is due
+    const int nf = 2 * T * nstg;
+    uint64_t idle_since = 0;
+    for (int idle = 0; ok && (bst < nstg || rf < nf);) {
+      bool progress = false;
+      const int rlim = min(nf, 2 * T * bst);
+      if (rf < rlim) {
+        const int f = rf + lane;
+        bool ready = false;
+        int e = -1, cpos = 0;
+        if (f < rlim) {
+          e = (&ctl.map[0][0][0])[f];
+          cpos = e >= 0 ? (&ctl.rpos[0][0][0])[f] : 0;
+          // the slot's previous record (cpos - kRS) has been issued, so the
+          // slot's phase is one of two and the parity test is exact
+          ready = e < 0 || cpos < kRS || mbar_test_wait(&ctl.r_empty[cpos % kRS], ((cpos / kRS) - 1) & 1);
+        }
+        const unsigned blocked = __ballot_sync(0xFFFFFFFFu, !ready);
+        const int n = blocked ? __ffs(blocked) - 1 : 32;  // the ready prefix, in ring order
+        if (lane < n && e >= 0) {
+          const int slot = cpos % kRS;
+          mbar_arrive_expect_tx(&ctl.r_full[slot], kRRecBytes);
+          bulk_g2s(rring + slot * kRRecBytes, (&ctl.rsrc[0][0])[f >> 1] + static_cast<int64_t>(e) * kRRecBytes,
+                   kRRecBytes, &ctl.r_full[slot]);
+        }
+        const int nrec = __popc(__ballot_sync(0xFFFFFFFFu, lane < n && e >= 0));
+        if (lane == 0 && nrec) ctl.r_issued = ctl.r_issued + nrec;
+        rf += n;
+        progress = n > 0;
+      }
+      if (bst < nstg) {
+        int go = 0;
+        if (lane == 0 && mbar_test_wait(&ctl.empty[bs], bph ^ 1)) go = 1;
+        if (__shfl_sync(0xFFFFFFFFu, go, 0)) {
+          issue_w(bst, bs);
+          issue_x(bst, bs);
+          ++bst;
+          if (++bs == S) bs = 0, bph ^= 1;
+          progress = true;
+        }
+      }
+      if (progress) {
+        idle = 0;
+        continue;
+      }
+      // back off (32 ns doubling to 512 ns): the polls share a scheduler with compute warps
+      __nanosleep(32u << min(idle >> 2, 4));
+      if ((++idle & 15) == 0) {  // bounded: give up after the timeout without progress
+        int give_up = 0;
+        if (lane == 0) {
+          const uint64_t now = globaltimer();
+          if (*abort_flag) {
+            give_up = 1;
+          } else if (idle == 16) {
+            idle_since = now;
+          } else if (now - idle_since > tmo) {
+            ZW(false, 7);
+            atomicOr(p.err, kDevErrTimeout);
+            *abort_flag = 1;
+            give_up = 1;
+          }
+        }
+        ok = !__shfl_sync(0xFFFFFFFFu, give_up, 0);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWEpi) {
+    // ---------------- epilogue: stream-K flags off the compute warps' path ----------------
+    pdl_wait();  // the flags and pieces in the workspace may still be in use by the preceding kernel
+    bool ok = true;
+    if (publishes) {  // release this CTA's piece once every compute warp has written its share
+      if (lane == 0) {
+        ok = ZW(mbar_wait_sleep(&ctl.piece_written, 0, abort_flag, tmo, p.err), 4);
+        if (ok) {
+          fence_acq_rel_gpu();
+          st_relaxed_gpu(p.tcount + c, 1);
+        }
+      }
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    }
+    if (finishes && ok) {
+      // the flags of the other pieces (lane j: CTA c + 1 + j), each cleared for
+      // the next launch once seen; then the compute warps read the pieces
+      for (int j0 = 0; ok && j0 < npc; j0 += 32) {
+        const int j = j0 + lane;
+        bool seen = true;
+        if (j < npc && ZOK(c + 1 + j < P, 4) && (seen = ZW(flag_wait(p.tcount + c + 1 + j, abort_flag, tmo, p.err), 5)))
+          p.tcount[c + 1 + j] = 0;
+        ok = __all_sync(0xFFFFFFFFu, seen);
+      }
+      if (ok && lane == 0) mbar_arrive(&ctl.pieces_in);
+    }
+  } else {
+    // ---------------- compute warps ----------------
+    const int q = warp / WPS, wq = warp % WPS;    // set (= tile of the tile-group), row block within the set
+    const int g = lane >> 2, t = lane & 3;         // MMA fragment coordinates
+    const int rw = 16 * MT * wq, half = rw >> 6;   // first row of this warp, its residual half
+    if (warp == 0) {
+      // Residual map of the CTA's columns (CSR entry per column, tile and
+      // half) and the records' ring positions.  The block lists are read
+      // before the dependency wait, like the weights.
+      int32_t* mp = &ctl.map[0][0][0];
+      for (int i = lane; i < nstg * T * 2; i += 32) mp[i] = -1;
+      __syncwarp();
+      for (int tg = t_first; tg <= t_last; ++tg) {
+        for (int qq = 0; qq < T; ++qq) {
+          const int tt = tg * T + qq;
+          if (tt >= p.tiles) break;
+          const ZMat& mt = p.mat[mat_of_tile(p, tt)];
+          if (mt.nnzb == 0) continue;
+          const int64_t br = 2 * static_cast<int64_t>(tt - mt.tile0);
+          const int a0 = max(0, min(mt.nnzb, mt.row_ptr[br]));
+          const int a1 = max(a0, min(mt.nnzb, mt.row_ptr[br + 1]));
+          const int a2 = max(a1, min(mt.nnzb, mt.row_ptr[br + 2]));
+          for (int e = a0 + lane; e < a2; e += 32) {
+            const int gg = mt.col_idx[e];
+            if (gg < 0 || gg >= G) continue;
+            const int cc = tg * G + gg;
+            if (cc >= col0 && cc < col1) {
+              ctl.map[cc - col0][qq][e >= a1 ? 1 : 0] = e;
+              ctl.rsrc[cc - col0][qq] = mt.rpk;
+            }
+          }
+        }
+      }
+      __syncwarp();
+      const int nf = nstg * T * 2;
+      const int chunk = (nf + 31) / 32, f0 = min(nf, lane * chunk), f1 = min(nf, f0 + chunk);
+      int cnt = 0;
+      for (int fx = f0; fx < f1; ++fx) cnt += mp[fx] >= 0;
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int pos = incl - cnt;
+      for (int fx = f0; fx < f1; ++fx)
+        if (mp[fx] >= 0) (&ctl.rpos[0][0][0])[fx] = pos++;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.map_ready);
+    }
+    bool ok = ZW(mbar_wait(&ctl.map_ready, 0, abort_flag, tmo, p.err), 0);
+    pdl_wait();  // X, Y and the workspace pieces may still be in use by the preceding kernel
+    // accumulators: [mt][nb] pairs {row r, tokens 8nb+2t, +1}, {row r+8, same tokens}
+    uint64_t acc[MT][NB][2];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) acc[mt][nb][0] = acc[mt][nb][1] = 0ull;
+
+    // The image of a stage's group, built by every compute warp: lane
+    // L = 32 warp + lane takes token m = L / 16 and its inputs 8k..8k+7,
+    // k = L % 16 (one 8-code word of the image); a token's 16 lanes share a
+    // half-warp.  Tokens M..TN-1 get zero codes, scales and offsets.
+    int b_i = 0, b_s = 0, b_ph = 0;  // next stage to build, its slot, the slot's fill parity
+    auto build_next = [&]() -> bool {
+      if (!ZW(mbar_wait(&ctl.xfull[b_s], b_ph, abort_flag, tmo, p.err), 10)) return false;
+      uint8_t* img = stage(b_s);
+      const uint8_t* raw = img + Geo::kOffRaw;
+      const int L = warp * 32 + lane;
+      if (L < TN * 16) {  // whole warps
+        const int m = L >> 4, k = L & 15;
+        const bool real = m < p.M;
+        const int gg = (col0 + b_i) % G;
+        uint32_t ev, od;
+        int sum;
+        float sx;
+        if (p.raw) {
+          uint4 w = make_uint4(0u, 0u, 0u, 0u);
+          if (real) w = *reinterpret_cast<const uint4*>(raw + m * 256 + k * 16);
+          const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+          float v[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (p.x_bf16) {
+              v[2 * i] = __uint_as_float(wv[i] << 16);
+              v[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
+            } else {
+              v[2 * i] = __half2float(__ushort_as_half(static_cast<unsigned short>(wv[i] & 0xFFFFu)));
+              v[2 * i + 1] = __half2float(__ushort_as_half(static_cast<unsigned short>(wv[i] >> 16)));
+            }
+          }
+          float amax = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+          for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+          const uint16_t sb = act_scale_bits(amax);
+          const float sf = __half2float(__ushort_as_half(sb));
+          float qf[8];
+          if (sf != 0.0f) {
+            quant8(v, sf, __frcp_rn(sf), qf);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) qf[i] = 0.0f;
+          }
+          ev = e4m3x2_of(qf[2], qf[0]) | (e4m3x2_of(qf[6], qf[4]) << 16);
+          od = e4m3x2_of(qf[3], qf[1]) | (e4m3x2_of(qf[7], qf[5]) << 16);
+          const float fs = ((qf[0] + qf[1]) + (qf[2] + qf[3])) + ((qf[4] + qf[5]) + (qf[6] + qf[7]));
+          sum = static_cast<int>(fs);
+          sx = 512.0f * sf;
+          // the quantized activations, as the quantizer writes them (once: the columns of tile-group 0)
+          if (p.xq_out && col0 + b_i < G && m < p.Mp) {
+            uint32_t pk = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) pk |= (static_cast<uint32_t>(static_cast<int>(qf[i])) & 0xFu) << (4 * i);
+            *reinterpret_cast<uint32_t*>(p.xq_out + (static_cast<int64_t>(gg) * p.Mp + m) * 64 + k * 4) = pk;
+            if (k == 0) p.xs_out[static_cast<int64_t>(gg) * p.Mp + m] = real ? sb : static_cast<uint16_t>(0);
+          }
+        } else {
+          const uint32_t wv = real ? *reinterpret_cast<const uint32_t*>(raw + m * 64 + k * 4) : 0u;
+          uint32_t lo, hi;
+          int4x8_to_e4m3(wv, lo, hi);
+          ev = prmt(lo, hi, 0x6420u);
+          od = prmt(lo, hi, 0x7531u);
+          sum = nibble_sum8(wv);
+          sx = real ? 512.0f * __half2float(__ushort_as_half(
+                                   *reinterpret_cast<const uint16_t*>(raw + Geo::kOffScales + m * 2)))
+                    : 0.0f;
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+        // codes 8k..8k+7 of token m: K-step k / 4, fragment lane 4 (m % 8) + k % 4 of block m / 8
+        *reinterpret_cast<uint2*>(img + ((((k >> 2) * NB + (m >> 3)) * 32 + 4 * (m & 7) + (k & 3)) * 8)) =
+            make_uint2(ev, od);
+        if (k == 0) {
+          float* sco = reinterpret_cast<float*>(img + TN * 128);  // {2^9 sx, 2^9 sx', c, c'} per token pair
+          sco[(m >> 1) * 4 + (m & 1)] = sx;
+          sco[(m >> 1) * 4 + 2 + (m & 1)] = static_cast<float>(sum) * (1.0f / 64.0f);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.built[b_s]);
+      ++b_i;
+      if (++b_s == S) b_s = 0, b_ph ^= 1;
+      return true;
+    };
+
+    // One group's product for this warp's rows (the same arithmetic as the
+    // warp-MMA form): codes (K-steps jstride apart, 16 bytes per row, first
+    // row row0), the image's fragments and scale pairs, row scales sc; into
+    // acc, or the test hook's dots.
+    auto group_product = [&](const uint8_t* codes, int jstride, int row0, const uint16_t* sc, const uint8_t* img,
+                             int tile, int gg, int e) {
+      const uint8_t* wr = codes + (row0 + g) * 16 + t * 4;
+      const float4* sg = reinterpret_cast<const float4*>(img + TN * 128) + t;  // token pairs 2t, 2t+1 of block nb
+      float s[MT][2];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        s[mt][0] = __half2float(__ushort_as_half(sc[row0 + 16 * mt + g]));
+        s[mt][1] = __half2float(__ushort_as_half(sc[row0 + 16 * mt + 8 + g]));
+      }
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        float d[MT][4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t a[MT][4];
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            const uint32_t w0 = *reinterpret_cast<const uint32_t*>(wr + j * jstride + mt * 256);        // row +0
+            const uint32_t w1 = *reinterpret_cast<const uint32_t*>(wr + j * jstride + mt * 256 + 128);  // row +8
+            unpack_u4(w0, a[mt][0], a[mt][2]);
+            unpack_u4(w1, a[mt][1], a[mt][3]);
+          }
+          const uint2 b = *reinterpret_cast<const uint2*>(img + ((j * NB + nb) * 32 + lane) * 8);
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            if (j == 0)
+              mma_e4m3_z(d[mt], a[mt], b.x, b.y);
+            else
+              mma_e4m3(d[mt], a[mt], b.x, b.y);
+          }
+        }
+        const uint64_t m1 = f2pack(-1.0f, -1.0f);
+        const float4 f = sg[4 * nb];  // 2^9 sx (tokens 8nb+2t, +1), c (same tokens)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          if constexpr (kDebug) {
+            const float ev[2][2] = {{d[mt][0] - f.z, d[mt][1] - f.w}, {d[mt][2] - f.z, d[mt][3] - f.w}};
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int cc = 0; cc < 2; ++cc) {
+                const int m = 8 * nb + 2 * t + cc, r = rw + 16 * mt + 8 * h + g;
+                if (m < p.M) {
+                  const int32_t dv = static_cast<int32_t>(ev[h][cc] * 512.0f);
+                  if (e < 0)
+                    p.dots_w[(static_cast<int64_t>(m) * (p.tiles * kTileN) + static_cast<int64_t>(tile) * kTileN + r) * G +
+                             gg] = dv;
+                  else
+                    p.dots_r[(static_cast<int64_t>(m) * p.mat[0].nnzb + e) * 64 + (r & 63)] = dv;
+                }
+              }
+          } else {
+            const uint64_t sx2 = f2pack(f.x, f.y), c2 = f2pack(f.z, f.w);
+            const uint64_t e0 = f2fma(c2, m1, f2pack(d[mt][0], d[mt][1]));  // row +0: exact 2^-9 D
+            const uint64_t e1 = f2fma(c2, m1, f2pack(d[mt][2], d[mt][3]));  // row +8
+            acc[mt][nb][0] = f2fma(sx2, f2mul(f2pack(s[mt][0], s[mt][0]), e0), acc[mt][nb][0]);
+            acc[mt][nb][1] = f2fma(sx2, f2mul(f2pack(s[mt][1], s[mt][1]), e1), acc[mt][nb][1]);
+          }
+        }
+      }
+    };
+    auto store_y = [&](const ZMat& mt, int64_t n, int m, float v) {
+      const int64_t o = static_cast<int64_t>(m) * mt.ldy + n;
+      if (p.y_f32)
+        st_global_f32(static_cast<float*>(mt.y) + o, v);
+      else
+        st_global_b16(static_cast<__nv_bfloat16*>(mt.y) + o, __bfloat16_as_ushort(__float2bfloat16_rn(v)));
+    };
+    // End of this CTA's share of tile-group tg: the set's tile is complete
+    // here (store Y), or is this CTA's piece (publish), or needs the later
+    // CTAs' pieces first (finish: added in CTA order).  No cross-warp step.
+    auto flush = [&](int tg) -> bool {
+      const int tile = tg * T + q;
+      const bool pub = publishes && tg == t_first;
+      const bool fin = finishes && tg == t_last;
+      const int64_t frag0 = static_cast<int64_t>((q * WPS + wq) * MT) * NB * 2 * 32 + lane;  // this lane's pairs
+      if (fin) {
+        if (!ZW(mbar_wait(&ctl.pieces_in, 0, abort_flag, tmo, p.err), 3)) return false;
+        for (int j = 0; j < npc; ++j) {  // CTA order
+          const uint64_t* pc = piece_of(c + 1 + j) + frag0;
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                acc[mt][nb][h] = f2add(acc[mt][nb][h], ld_global_cg_u64(pc + ((mt * NB + nb) * 2 + h) * 32));
+        }
+      }
+      if (pub) {
+        uint64_t* pc = piece_of(c) + frag0;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) st_global_cg_u64(pc + ((mt * NB + nb) * 2 + h) * 32, acc[mt][nb][h]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.piece_written);
+      } else if (tile < p.tiles) {
+        const ZMat& mt = p.mat[mat_of_tile(p, tile)];
+        const int64_t nbase = static_cast<int64_t>(tile - mt.tile0) * kTileN;
+#pragma unroll
+        for (int m2 = 0; m2 < MT; ++m2)
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int r = rw + 16 * m2 + 8 * h + g, m0 = 8 * nb + 2 * t;
+              float v0, v1;
+              f2unpack(acc[m2][nb][h], v0, v1);
+              if (m0 < p.M) store_y(mt, nbase + r, m0, v0);
+              if (m0 + 1 < p.M) store_y(mt, nbase + r, m0 + 1, v1);
+            }
+      }
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) acc[mt][nb][0] = acc[mt][nb][1] = 0ull;
+      return true;
+    };
+
+    // Stages in order: build the image `ahead` stages in advance (every warp
+    // its share), then wait for this stage's image and base records, run the
+    // set's tile, release the stage.  Builds ahead let the warps drift apart
+    // by that many stages (a residual block makes one set slower for a stage).
+    const int ahead = min(2, S - 1);
+    for (int i = 0; ok && i < min(ahead, nstg); ++i) ok = build_next();
+    int s = 0, ph = 0;
+    int tg = t_first, gg = col0 - t_first * G;
+    for (int i = 0; ok && i < nstg; ++i) {
+      if (b_i < nstg && !(ok = build_next())) break;
+      if (!(ok = ZW(mbar_wait(&ctl.built[s], ph, abort_flag, tmo, p.err), 11))) break;
+      if (!(ok = ZW(mbar_wait(&ctl.full[s], ph, abort_flag, tmo, p.err), 0))) break;
+      const uint8_t* sg = stage(s);
+      const int tile = tg * T + q;
+      if (tile < p.tiles) {
+        const uint8_t* rec = sg + Geo::kOffRec + q * kWRecBytes;
+        group_product(rec, 2048, rw, reinterpret_cast<const uint16_t*>(rec + kWRecScales), sg, tile, gg, -1);
+        const int e = ctl.map[i][q][half];
+        if (e >= 0) {  // the residual block of this warp's half
+          const int cpos = ctl.rpos[i][q][half], slot = cpos % kRS;
+          // Sets run a few stages apart, so this slot may still hold (or await) a record two laps
+          // older: its parity would alias.  Once record cpos is issued, every older record of the
+          // slot has been consumed and the newer one waits for this warp: the parity is exact.
+          if (!(ok = ZW(count_wait(&ctl.r_issued, cpos, abort_flag, tmo, p.err), 1))) break;
+          if (!(ok = ZW(mbar_wait(&ctl.r_full[slot], (cpos / kRS) & 1, abort_flag, tmo, p.err), 1))) break;
+          const uint8_t* rrec = rring + slot * kRRecBytes;
+          group_product(rrec, 1024, rw - 64 * half, reinterpret_cast<const uint16_t*>(rrec + kRRecScales), sg, tile,
+                        gg, e);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl.r_empty[slot]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.empty[s]);  // this warp is done with the stage
+      if (++s == S) s = 0, ph ^= 1;
+      if (++gg == G) {  // the tile-group's last group
+        if (!kDebug && !(ok = flush(tg))) break;
+        gg = 0;
+        ++tg;
+      }
+    }
+    if (ok && !kDebug && gg != 0) ok = flush(tg);  // a share ending inside a tile-group
+  }
+
+  // Every role is done.
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&ctl.exit_bar);
+  mbar_wait(&ctl.exit_bar, 0, abort_flag, tmo, p.err);
+  __syncthreads();
+  if (*abort_flag) {
+    // A wait gave up: copies may still be in flight; give them 200 us.
+    if (threadIdx.x == 0) {
+      const uint64_t t0 = globaltimer();
+      while (globaltimer() - t0 < 200000ull) {
+      }
+    }
+    __syncthreads();
+  }
+}
+
 // The activation images of one launch, written to the workspace for the GEMM
 // to bulk-copy: for group g, the MMA's B operand (the integer codes as E4M3
-// bytes in the 128-byte-swizzled, K-major tile, K permuted inside each 8-code
-// word like the weight unpack), 2^9 sx and the offset terms 2^-9 * 8 * sum_k qx.
-// From packed codes (xq, xs), or straight from X (kQuant: quantized here with
-// mq_quantize_act's rule and bits; xq / xs written too when asked).  One CTA of
-// 256 threads per group.
+// bytes, K permuted inside each 8-code word like the weight unpack), 2^9 sx
+// and the offset terms 2^-9 * 8 * sum_k qx.  From packed codes (xq, xs), or
+// straight from X (kQuant: quantized here with mq_quantize_act's rule and
+// bits; xq / xs written too when asked).  One CTA of 128 threads per (group,
+// 8-token block): thread L takes token 8 blockIdx.y + L / 16 and the group's
+// inputs 8k..8k+7, k = L % 16 (one 8-code word); a token's 16 threads share a
+// half-warp.  Tokens M..TN-1 get zero codes, scales and offsets.
 struct ImgParams {
   const uint8_t* xq;
   const uint16_t* xs;
@@ -1597,83 +2220,81 @@ struct ImgParams {
 // then the odd ones; then {2^9 sx, 2^9 sx', c, c'} per token pair); else the
 // tensor-memory form's swizzled tile (then 2^9 sx [TN], c [TN], padding).
 template <int TN, bool kQuant, bool kFrag>
-__global__ void __launch_bounds__(256) act_image_kernel(const ImgParams p) {
+__global__ void __launch_bounds__(128) act_image_kernel(const ImgParams p) {
   constexpr int kArec = kFrag ? TN * 136 : act_rec_bytes(TN);
   constexpr int NB = TN / 8;
-  // byte offset of codes 8w..8w+7 (word w of 16) of token m, and of its two scale values
-  auto word_off = [](int m, int w) {
-    return kFrag ? ((((w >> 2) * NB + (m >> 3)) * 32 + 4 * (m & 7) + (w & 3)) * 8) : act_word_offset(m, w);
-  };
-  auto sx_idx = [](int m) { return kFrag ? (m >> 1) * 4 + (m & 1) : m; };
-  auto c_idx = [](int m) { return kFrag ? (m >> 1) * 4 + 2 + (m & 1) : TN + m; };
   pdl_trigger();
   // the inputs are the preceding kernel's output, and the previous GEMM may
   // still be reading the images this overwrites
   pdl_wait();
   const int64_t g = blockIdx.x;
-  const int ct = threadIdx.x;
+  const int m = static_cast<int>(blockIdx.y) * 8 + static_cast<int>(threadIdx.x >> 4), k = threadIdx.x & 15;
+  const bool real = m < p.M;
   uint8_t* rec = p.act + g * kArec;
   float* sco = reinterpret_cast<float*>(rec + TN * 128);
-  if constexpr (!kQuant) {
-    // from packed codes: item = (token m, word t), 16 words per token
-    for (int idx = ct; idx < TN * 16; idx += 256) {
-      const int m = idx >> 4, t = idx & 15;
-      const uint32_t wv = m < p.Mp ? *reinterpret_cast<const uint32_t*>(p.xq + (g * p.Mp + m) * 64 + t * 4) : 0u;
-      uint32_t lo, hi;
-      int4x8_to_e4m3(wv, lo, hi);
-      *reinterpret_cast<uint2*>(rec + word_off(m, t)) = make_uint2(prmt(lo, hi, 0x6420u), prmt(lo, hi, 0x7531u));
-      int sum = nibble_sum8(wv);
+  uint32_t ev, od;
+  int sum;
+  float sx;
+  if constexpr (kQuant) {
+    uint32_t wv[4] = {0u, 0u, 0u, 0u};
+    if (real) {  // x is 8-byte aligned and ldx a multiple of 4
+      const uint2* src = reinterpret_cast<const uint2*>(p.x + static_cast<int64_t>(m) * p.ldx + g * kGroup + 8 * k);
+      const uint2 a = src[0], b = src[1];
+      wv[0] = a.x, wv[1] = a.y, wv[2] = b.x, wv[3] = b.y;
+    }
+    float v[8];
 #pragma unroll
-      for (int o = 1; o < 16; o <<= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-      if (t == 0) {
-        sco[sx_idx(m)] = m < p.Mp ? 512.0f * __half2float(__ushort_as_half(p.xs[g * p.Mp + m])) : 0.0f;
-        sco[c_idx(m)] = static_cast<float>(sum) * (1.0f / 64.0f);
+    for (int i = 0; i < 4; ++i) {
+      if (p.x_bf16) {
+        v[2 * i] = __uint_as_float(wv[i] << 16);
+        v[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
+      } else {
+        v[2 * i] = __half2float(__ushort_as_half(static_cast<unsigned short>(wv[i] & 0xFFFFu)));
+        v[2 * i + 1] = __half2float(__ushort_as_half(static_cast<unsigned short>(wv[i] >> 16)));
       }
     }
-  } else {
-    // from X: threads of one token: 16 (TN <= 16) or 8 (TN = 32), each on 128 / that inputs
-    // (whole 8-code words); threads past the tile's tokens have nothing to do
-    constexpr int kTpt = TN == 32 ? 8 : 16, kEpt = 128 / kTpt, kWpt = kEpt / 8;
-    static_assert(kWpt >= 1 && kTpt * TN <= 256, "quantizer thread mapping");
-    const int m = ct / kTpt, part = ct % kTpt;
-    if (m >= TN) return;
-    float v[kEpt];
     float amax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < kEpt; ++i) {
-      v[i] = m < p.M ? act_value(p.x, static_cast<int64_t>(m) * p.ldx + g * kGroup + part * kEpt + i, p.x_bf16) : 0.0f;
-      amax = fmaxf(amax, fabsf(v[i]));
-    }
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
 #pragma unroll
-    for (int o = 1; o < kTpt; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-    const uint16_t sb = m < p.M ? act_scale_bits(amax) : static_cast<uint16_t>(0);
+    for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const uint16_t sb = act_scale_bits(amax);
     const float sf = __half2float(__ushort_as_half(sb));
-    int sum = 0;
+    float qf[8];
+    if (sf != 0.0f) {
+      quant8(v, sf, __frcp_rn(sf), qf);
+    } else {
 #pragma unroll
-    for (int w = 0; w < kWpt; ++w) {
-      uint32_t ev = 0, od = 0, pk = 0;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int qv = act_code(v[w * 8 + e], sf);
-        sum += qv;
-        pk |= (static_cast<uint32_t>(qv) & 0xFu) << (4 * e);
-        const uint32_t byte = e4m3_of_code(qv);
-        if (e & 1)
-          od |= byte << (8 * (e >> 1));
-        else
-          ev |= byte << (8 * (e >> 1));
-      }
-      const int t = part * kWpt + w;  // word of the token's 16
-      *reinterpret_cast<uint2*>(rec + word_off(m, t)) = make_uint2(ev, od);
-      if (p.xq_out && m < p.Mp) *reinterpret_cast<uint32_t*>(p.xq_out + (g * p.Mp + m) * 64 + t * 4) = pk;
+      for (int i = 0; i < 8; ++i) qf[i] = 0.0f;
     }
+    ev = e4m3x2_of(qf[2], qf[0]) | (e4m3x2_of(qf[6], qf[4]) << 16);
+    od = e4m3x2_of(qf[3], qf[1]) | (e4m3x2_of(qf[7], qf[5]) << 16);
+    sum = static_cast<int>(((qf[0] + qf[1]) + (qf[2] + qf[3])) + ((qf[4] + qf[5]) + (qf[6] + qf[7])));
+    sx = 512.0f * sf;
+    if (p.xq_out && m < p.Mp) {
+      uint32_t pk = 0;
 #pragma unroll
-    for (int o = 1; o < kTpt; o <<= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-    if (part == 0) {
-      sco[sx_idx(m)] = 512.0f * sf;
-      sco[c_idx(m)] = static_cast<float>(sum) * (1.0f / 64.0f);
-      if (p.xs_out && m < p.Mp) p.xs_out[g * p.Mp + m] = sb;
+      for (int i = 0; i < 8; ++i) pk |= (static_cast<uint32_t>(static_cast<int>(qf[i])) & 0xFu) << (4 * i);
+      *reinterpret_cast<uint32_t*>(p.xq_out + (g * p.Mp + m) * 64 + k * 4) = pk;
+      if (k == 0) p.xs_out[g * p.Mp + m] = real ? sb : static_cast<uint16_t>(0);
     }
+  } else {
+    const uint32_t wv = real ? *reinterpret_cast<const uint32_t*>(p.xq + (g * p.Mp + m) * 64 + k * 4) : 0u;
+    uint32_t lo, hi;
+    int4x8_to_e4m3(wv, lo, hi);
+    ev = prmt(lo, hi, 0x6420u);
+    od = prmt(lo, hi, 0x7531u);
+    sum = nibble_sum8(wv);
+    sx = real ? 512.0f * __half2float(__ushort_as_half(p.xs[g * p.Mp + m])) : 0.0f;
+  }
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+  if (m >= TN) return;
+  const int off = kFrag ? ((((k >> 2) * NB + (m >> 3)) * 32 + 4 * (m & 7) + (k & 3)) * 8) : act_word_offset(m, k);
+  *reinterpret_cast<uint2*>(rec + off) = make_uint2(ev, od);
+  if (k == 0) {
+    sco[kFrag ? (m >> 1) * 4 + (m & 1) : m] = sx;
+    sco[kFrag ? (m >> 1) * 4 + 2 + (m & 1) : TN + m] = static_cast<float>(sum) * (1.0f / 64.0f);
   }
 }
 
@@ -1691,16 +2312,28 @@ int sm_count_current() {
 }
 
 struct ZPlan {
-  bool tc;  // the tensor-memory form (else warp-MMA)
+  bool tc;   // the tensor-memory form
+  bool col;  // the column form (else, without tc, the warp-MMA form)
   int tn, mld, ctas, nstages, stage_bytes, smem, arec;
-  int64_t units;
-  size_t o_act, o_part, bytes;  // workspace layout after the zeroed prefix
+  int64_t units;  // units, or columns in the column form
+  size_t o_act, o_part, o_q, o_s, bytes;  // workspace layout after the zeroed prefix
 };
 
-// The tensor-memory form when MQ_DECODE_VARIANT = "tc" (benchmarks and tests), else the warp-MMA form.
-bool use_tc_variant() {
+// The decode kernel's form: 4 warp-MMA (the default), or as MQ_DECODE_VARIANT
+// forces it (benchmarks and tests): 3 tensor-memory ("tc"), 5 column ("col").
+int decode_form() {
   const char* v = getenv("MQ_DECODE_VARIANT");
-  return v && strcmp(v, "tc") == 0;
+  if (v && strcmp(v, "tc") == 0) return 3;
+  if (v && strcmp(v, "col") == 0) return 5;
+  return 4;
+}
+
+constexpr int kMinCols = 2;  // columns per CTA at least (bounds the pieces a tile-group is cut into)
+
+// Static shared memory of the column form's control block (with its alignment slack).
+template <int TN>
+int c_ctl_bytes() {
+  return (static_cast<int>(sizeof(CCtl<ColGeo<TN>::kMaxCols, ColGeo<TN>::T>)) + 127) / 128 * 128;
 }
 
 // Plan for M tokens over `tiles` 128-row tiles of K inputs; false if the
@@ -1713,14 +2346,43 @@ int w_ctl_bytes() {
 
 bool zplan(int64_t M, int64_t tiles, int64_t K, ZPlan* out) {
   if (M < 1 || M > 32) return false;
-  ZPlan pl;
-  pl.tc = use_tc_variant();
+  ZPlan pl = {};
+  const int form = decode_form();
+  pl.tc = form == 3;
+  pl.col = form == 5;
   pl.tn = pl.tc ? (M <= 16 ? 16 : 32) : (M <= 8 ? 8 : M <= 16 ? 16 : 32);
   pl.mld = M <= 4 ? 4 : M <= 8 ? 8 : M <= 16 ? 16 : 32;
   const int64_t G = K / kGroup;
   pl.units = tiles * G;
   const int sms = sm_count_current();
   if (sms <= 0 || sms > kWsZeroBytes / 4) return false;
+  if (pl.col) {
+    // columns: (tile-group of T tiles, group); one stage per column
+    const int T = w_sets(pl.tn);
+    const int64_t ncol = (tiles + T - 1) / T * G;
+    pl.units = ncol;
+    pl.ctas = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms, ncol / kMinCols)));
+    if ((ncol + pl.ctas - 1) / pl.ctas > kMaxUnits / T || ncol >= (int64_t{1} << 31)) return false;
+    int ctl_bytes;
+    switch (pl.tn) {
+      case 8: pl.stage_bytes = ColGeo<8>::kStage, ctl_bytes = c_ctl_bytes<8>(); break;
+      case 16: pl.stage_bytes = ColGeo<16>::kStage, ctl_bytes = c_ctl_bytes<16>(); break;
+      default: pl.stage_bytes = ColGeo<32>::kStage, ctl_bytes = c_ctl_bytes<32>(); break;
+    }
+    const int fixed = 128 + kRS * kRRecBytes;  // alignment, residual ring
+    pl.nstages = std::min(kMaxStages, (kSmemLimit - ctl_bytes - fixed) / pl.stage_bytes);
+    if (pl.nstages < 2) return false;
+    pl.smem = pl.nstages * pl.stage_bytes + fixed;
+    // workspace: the zeroed prefix (flags [ctas]), the stream-K pieces, and
+    // the quantized activations for inputs the stages cannot copy directly
+    const size_t Mp = static_cast<size_t>((M + 7) / 8 * 8);
+    pl.o_part = kWsZeroBytes;
+    pl.o_q = pl.o_part + a256(static_cast<size_t>(pl.ctas) * T * pl.tn * kTileN * sizeof(float));
+    pl.o_s = pl.o_q + a256(static_cast<size_t>(G) * Mp * 64);
+    pl.bytes = pl.o_s + a256(static_cast<size_t>(G) * Mp * 2);
+    *out = pl;
+    return true;
+  }
   pl.ctas = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms, pl.units / kMinUnits)));
   if ((pl.units + pl.ctas - 1) / pl.ctas > kMaxUnits || pl.units >= (int64_t{1} << 31)) return false;
   int ctl_bytes, fixed;
@@ -1819,6 +2481,45 @@ mq_status wlaunch(const ZParams& zp, const ZPlan& pl, cudaStream_t stream) {
   return launch_status("zipper");
 }
 
+template <int TN, bool kDebug>
+mq_status claunch(const ZParams& zp, const ZPlan& pl, cudaStream_t stream) {
+  auto kern = zipper_col_kernel<TN, kDebug>;
+  static std::mutex mu;
+  static bool attr_set[64];  // per device, per instantiation
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return launch_status("zipper: device");
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (!attr_set[dev]) {
+      const int ctl_bytes = c_ctl_bytes<TN>();
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit - ctl_bytes) != cudaSuccess)
+        return launch_status("zipper: smem attribute");
+      attr_set[dev] = true;
+    }
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(pl.ctas), 1, 1);
+  cfg.blockDim = dim3(w_threads(TN), 1, 1);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, zp) != cudaSuccess) return launch_status("zipper launch");
+  return launch_status("zipper");
+}
+
+template <bool kDebug>
+mq_status cdispatch(const ZParams& zp, const ZPlan& pl, cudaStream_t stream) {
+  switch (pl.tn) {
+    case 8: return claunch<8, kDebug>(zp, pl, stream);
+    case 16: return claunch<16, kDebug>(zp, pl, stream);
+    default: return claunch<32, kDebug>(zp, pl, stream);
+  }
+}
+
 template <bool kDebug>
 mq_status wdispatch(const ZParams& zp, const ZPlan& pl, cudaStream_t stream) {
   switch (pl.tn) {
@@ -1831,8 +2532,8 @@ mq_status wdispatch(const ZParams& zp, const ZPlan& pl, cudaStream_t stream) {
 template <int TN, bool kQuant, bool kFrag>
 mq_status image_launch(const ImgParams& ip, int G, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(G), 1, 1);
-  cfg.blockDim = dim3(256, 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(G), TN / 8, 1);
+  cfg.blockDim = dim3(128, 1, 1);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1845,6 +2546,9 @@ mq_status image_launch(const ImgParams& ip, int G, cudaStream_t stream) {
 
 }  // namespace
 
+mq_status quantize_act_launch(const void* x, mq_dtype xt, int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
+                              uint16_t* xs, cudaStream_t stream);
+
 // Workspace bytes of the decode kernel for M tokens over `tiles` tiles of K
 // inputs on the current device, or 0 when it does not cover the shape.
 size_t zipper_workspace_bytes(int64_t M, int64_t tiles, int64_t K) {
@@ -1852,11 +2556,11 @@ size_t zipper_workspace_bytes(int64_t M, int64_t tiles, int64_t K) {
   return zplan(M, tiles, K, &pl) ? pl.bytes : 0;
 }
 
-// Plan summary for mq_gemm_plan: {form (3 tensor-memory, 4 warp-MMA), tokens per tile, CTAs, stages}.
+// Plan summary for mq_gemm_plan: {form (3 tensor-memory, 4 warp-MMA, 5 column), tokens per tile, CTAs, stages}.
 bool zipper_plan_info(int64_t M, int64_t tiles, int64_t K, int32_t* form, int32_t* tn, int32_t* ctas, int32_t* stages) {
   ZPlan pl;
   if (!zplan(M, tiles, K, &pl)) return false;
-  *form = pl.tc ? 3 : 4;
+  *form = pl.tc ? 3 : pl.col ? 5 : 4;
   *tn = pl.tn;
   *ctas = pl.ctas;
   *stages = pl.nstages;
@@ -1864,7 +2568,7 @@ bool zipper_plan_info(int64_t M, int64_t tiles, int64_t K, int32_t* form, int32_
 }
 
 // The kernel choice for (M, N, K) on the current device: {form (3: tensor
-// memory, 4: warp MMA), tokens per tile, 1, CTAs, stages} for the decode
+// memory, 4: warp MMA, 5: column), tokens per tile, 1, CTAs, stages} for the decode
 // kernel, else zeros (the general kernel runs).
 mq_status gemm_plan_info(int64_t M, int64_t N, int64_t K, int32_t* info) {
   for (int i = 0; i < 5; ++i) info[i] = 0;
@@ -1944,6 +2648,21 @@ mq_status zipper_launch(bool* handled, int nmat, const uint8_t* const* wpk, cons
   if (!zp.err) return set_error(MQ_ERR_CUDA, "zipper: device error word unavailable");
   const bool quant = x != nullptr;
   mq_status st;
+  if (pl.col) {
+    // X rows go straight into the stages when every row starts on a 16-byte
+    // boundary; otherwise the quantizer runs first and the stages take codes
+    zp.raw = quant && aligned(x, 16) && ldx % 8 == 0;
+    if (quant && !zp.raw) {
+      uint8_t* qb = xq_out ? xq_out : w + pl.o_q;
+      uint16_t* sbuf = xs_out ? xs_out : reinterpret_cast<uint16_t*>(w + pl.o_s);
+      if ((st = quantize_act_launch(x, xt, M, K, ldx, qb, sbuf, stream)) != MQ_OK) return st;
+      zp.xq = qb;
+      zp.xs = sbuf;
+      zp.xq_out = nullptr;
+      zp.xs_out = nullptr;
+    }
+    return dots_w ? cdispatch<true>(zp, pl, stream) : cdispatch<false>(zp, pl, stream);
+  }
   if (pl.tc)
     st = pl.tn == 16 ? (quant ? image_launch<16, true, false>(ip, zp.G, stream) : image_launch<16, false, false>(ip, zp.G, stream))
                      : (quant ? image_launch<32, true, false>(ip, zp.G, stream) : image_launch<32, false, false>(ip, zp.G, stream));

@@ -276,7 +276,7 @@ def gemm_plan(M: int, N: int, K: int) -> dict:
     info = (ctypes.c_int32 * 5)()
     _check(lib().mq_gemm_plan(M, N, K, ctypes.cast(info, ctypes.c_void_p)), "mq_gemm_plan")
     return {"decode": bool(info[0]),
-            "variant": {0: "general", 3: "tensor-memory", 4: "warp-mma"}[info[0]],
+            "variant": {0: "general", 3: "tensor-memory", 4: "warp-mma", 5: "column"}[info[0]],
             "tokens_per_tile": info[1], "cluster": info[2], "clusters": info[3], "stages": info[4]}
 
 

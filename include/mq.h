@@ -285,9 +285,11 @@ mq_status mq_debug_group_dots(const uint8_t* xq, const uint16_t* xs, int64_t M, 
  * for a problem of M tokens, N outputs and K inputs on the current device.
  *   info  host array of 5 int32, written:
  *         [0] the decode kernel (stream-K over every SM, up to 32 tokens):
- *             4 = its warp-MMA form (the default), 3 = its tensor-memory form
- *             (taken when the environment variable MQ_DECODE_VARIANT is
- *             "tc"); 0 = the general kernel;
+ *             4 = its warp-MMA form (the default; the fused call quantizes
+ *             in a short kernel of its own first), 5 = its column form (warp
+ *             MMA with the activation quantizer inside the GEMM) and 3 = its
+ *             tensor-memory form (taken when the environment variable
+ *             MQ_DECODE_VARIANT is "col" or "tc"); 0 = the general kernel;
  *         for the decode kernel, [1] tokens per tile (8, 16 or 32), [2] 1,
  *         [3] CTAs launched, [4] weight stages in shared memory; zeros for
  *         the general kernel.

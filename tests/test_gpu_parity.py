@@ -146,14 +146,16 @@ def test_decode_kernel_covers_decode_shapes(lin):
     assert not mq.gemm_plan(33, lin.N, lin.K)["decode"]
 
 
-@pytest.mark.parametrize("variant", ["warp", "tc"])
-@pytest.mark.parametrize("M,N,K,budget", [(9, 384, 1024, 0.3), (16, 512, 2048, 0.2), (24, 256, 768, 1.0)])
+@pytest.mark.parametrize("variant", ["col", "warp", "tc"])
+@pytest.mark.parametrize("M,N,K,budget", [(9, 384, 1024, 0.3), (16, 512, 2048, 0.2), (24, 256, 768, 1.0),
+                                          (3, 640, 384, 0.4)])
 def test_decode_variants_match_oracle(variant, M, N, K, budget, monkeypatch):
-    """Both variants of the decode kernel (forced through MQ_DECODE_VARIANT):
-    dots bit for bit, Y within the fp32 bound, on sizes either may serve."""
+    """Every form of the decode kernel (forced through MQ_DECODE_VARIANT):
+    dots bit for bit, Y within the fp32 bound, on sizes any may serve (640
+    rows: a ragged last tile-group of the column form)."""
     monkeypatch.setenv("MQ_DECODE_VARIANT", variant)
     plan = mq.gemm_plan(M, N, K)
-    assert plan["variant"] == {"warp": "warp-mma", "tc": "tensor-memory"}[variant]
+    assert plan["variant"] == {"col": "column", "warp": "warp-mma", "tc": "tensor-memory"}[variant]
     x, w, xcal = _case(M, N, K, budget, seed=M + N)
     pl = mq.prepare_linear(dev_half(w), dev_half(xcal), budget)
     xq, xs = mq.quantize_act(dev_half(x))
@@ -171,13 +173,14 @@ def test_decode_variants_match_oracle(variant, M, N, K, budget, monkeypatch):
     check_bf16(host_u16(y16), y, a)
 
 
-@pytest.mark.parametrize("M,variant", [(32, "warp"), (32, "tc"), (16, "tc"), (8, "warp"), (8, "tc"), (4, "warp"),
+@pytest.mark.parametrize("M,variant", [(32, "col"), (16, "col"), (8, "col"), (4, "col"), (1, "col"),
+                                       (32, "warp"), (32, "tc"), (16, "tc"), (8, "warp"), (8, "tc"), (4, "warp"),
                                        (1, "warp"), (1, "tc"), (33, None), (128, None)])
 def test_group_dots_extremes(M, variant, monkeypatch):
     """Adversarial codes: every product +49, every product -49, alternating
     cancellation; sums reach +-6272 per group, exactly.  Up to 32 tokens this
-    runs the decode kernel, in its warp-MMA form (mask-and-offset unpack to
-    E4M3, fp32 MMA accumulators) and its tensor-memory form; above 32 tokens
+    runs the decode kernel, in its column and warp-MMA forms (mask-and-offset
+    unpack to E4M3, fp32 MMA accumulators) and its tensor-memory form; above 32 tokens
     the general kernel (exact-integer E4M3 table)."""
     if variant:
         monkeypatch.setenv("MQ_DECODE_VARIANT", variant)
@@ -197,7 +200,7 @@ def test_group_dots_extremes(M, variant, monkeypatch):
     ref = O.group_dots(qx, p.qw)
     assert ref.max() == 6272 and ref.min() == -6272 and (ref == 0).any() == (M > 1)
     plan = mq.gemm_plan(M, N, K)
-    assert plan["variant"] == {"warp": "warp-mma", "tc": "tensor-memory", None: "general"}[variant]
+    assert plan["variant"] == {"col": "column", "warp": "warp-mma", "tc": "tensor-memory", None: "general"}[variant]
     assert np.array_equal(dw.cpu().numpy(), ref)
 
 
@@ -315,15 +318,77 @@ def test_fused_linear_matches_oracle(M, K, Ns, budget, x_dtype):
     assert mq.gemm_plan(M, sum(Ns), K)["decode"] == (M <= 32)
 
 
-@pytest.mark.parametrize("variant", ["warp", "tc"])
-def test_dense_residual_back_to_back(variant, monkeypatch):
+def _quantizer_corner_rows(M, K, dtype, seed):
+    """Activation rows (as fp16 / bf16 bits) that hit the quantizer's corners,
+    one kind per token: exact half-integer quotients v / s (round half to
+    even) with amax = 7 s, the same moved one ulp of the input format either
+    way, fp16-subnormal scales (codes clamp), all-zero groups, scales that
+    saturate at 65504 (bf16 only), random rows."""
+    rng = np.random.default_rng(seed)
+    out = np.zeros((M, K), np.uint16)
+    for m in range(M):
+        kind = m % 6
+        for g in range(K // 128):
+            s = np.float32(2.0 ** int(rng.integers(-6, 4)) * (1 + int(rng.integers(0, 8)) / 8))
+            if kind in (0, 1):
+                row = ((rng.integers(-7, 7, 128) + 0.5) * s).astype(np.float32)  # exact in both formats
+                bits = synth.to_bits(row, dtype)
+                if kind == 1:  # one ulp up or down in magnitude: no longer a tie
+                    bits = (bits.astype(np.int32) + rng.choice([-1, 1], 128)).astype(np.uint16)
+                bits[int(rng.integers(0, 128))] = synth.to_bits(np.array([7 * s], np.float32), dtype)[0]
+            elif kind == 2:
+                bits = synth.to_bits((rng.standard_normal(128) * 2.0 ** -19).astype(np.float32), dtype)
+            elif kind == 3:
+                bits = np.zeros(128, np.uint16)
+            elif kind == 4 and dtype == "bf16":
+                bits = synth.to_bits((rng.standard_normal(128) * 1e6).astype(np.float32), dtype)
+            else:
+                bits = synth.to_bits((rng.standard_normal(128) * 3.0).astype(np.float32), dtype)
+            out[m, 128 * g:128 * (g + 1)] = bits
+    return out
+
+
+@pytest.mark.parametrize("variant", ["col", "warp"])
+@pytest.mark.parametrize("M,x_dtype,pad", [(32, "f16", 0), (32, "bf16", 0), (6, "f16", 0), (12, "bf16", 4)])
+def test_fused_quantizer_corners(variant, M, x_dtype, pad, monkeypatch):
+    """The quantizer inside the fused call (the column form's stage build and
+    the image kernel, which round with a refined reciprocal rather than a
+    division) against the oracle bit for bit on corner rows, and Y within the
+    fp32 bound.  pad > 0 gives X a row stride that is not a multiple of 8
+    elements: the column form then runs the stand-alone quantizer first."""
+    monkeypatch.setenv("MQ_DECODE_VARIANT", variant)
+    K, N = 512, 256
+    isb = x_dtype == "bf16"
+    x = _quantizer_corner_rows(M, K, x_dtype, seed=M + pad)
+    xw = np.zeros((M, K + pad), np.uint16)
+    xw[:, :K] = x
+    xt = dev_act(xw, isb)[:, :K]
+    w = synth.weights(N, K, seed=5)
+    xcal = synth.calibration(K, seed=5, count=4, dtype=x_dtype)
+    pl = mq.prepare_linear(dev_half(w), dev_act(xcal, isb), 0.25)
+    Mp = mq.padded_tokens(M)
+    xq = torch.full((K // 128, Mp, 64), 0xAB, dtype=torch.uint8, device="cuda")
+    xs = torch.full((K // 128, Mp), float("nan"), dtype=torch.float16, device="cuda")
+    y32 = mq.fused_linear(xt, [pl], out_dtype=torch.float32, xq=xq, xs=xs)[0]
+    mq.check_device_error()
+    assert mq.gemm_plan(M, N, K)["variant"] == {"col": "column", "warp": "warp-mma"}[variant]
+    qx, sx = O.quantize_act(x, isb)
+    assert np.array_equal(logical_xq(xq, M), O.pack_nibbles(qx))
+    assert np.array_equal(logical_xs(xs, M), sx)
+    assert not host_u16(xs)[:, M:].any() and not xq_padding(xq, M).any()
+    y, a = O.linear(qx, sx, O.prepare(w, xcal, isb, 0.25))
+    check_close(y32.cpu().numpy(), y, a)
+
+
+@pytest.mark.parametrize("variant,M", [("col", 4), ("col", 32), ("warp", 4), ("tc", 32)])
+def test_dense_residual_back_to_back(variant, M, monkeypatch):
     """Every block residual (budget 1): each stage fills the residual ring a
     full lap, and with ~4 stages per CTA the compute sets drift apart.  Twelve
     calls back to back on one stream and workspace (each launch overlapping
     the previous one's tail) must all equal the oracle: a set must never take
     a ring slot's older record for its own."""
     monkeypatch.setenv("MQ_DECODE_VARIANT", variant)
-    M, N, K = 4 if variant == "warp" else 32, 8192, 4096
+    N, K = 8192, 4096
     x = synth.activations(M, K, seed=91, count=synth.n_outliers(K))
     w = synth.weights(N, K, seed=92)
     xcal = synth.calibration(K, seed=93, count=synth.n_outliers(K))
@@ -344,7 +409,7 @@ def test_dense_residual_back_to_back(variant, monkeypatch):
     yo, a = O.linear(qx, sx, p)
     for y in ys:
         check_close(y.cpu().numpy(), yo, a)
-    assert mq.gemm_plan(M, N, K)["variant"] == ("warp-mma" if variant == "warp" else "tensor-memory")
+    assert mq.gemm_plan(M, N, K)["variant"] == {"col": "column", "warp": "warp-mma", "tc": "tensor-memory"}[variant]
 
 
 # ----------------------------------------------------------------------------
@@ -377,7 +442,8 @@ def _sampled_parity(M, lin, budget, x_dtype, seed, conc=False, nsamp=384):
     check_bf16(host_u16(y16)[ms, ns], y, a)
 
 
-@pytest.mark.parametrize("name,M,variant", [("gate", 8, "warp"), ("gate", 16, "warp"), ("gate", 32, "tc"),
+@pytest.mark.parametrize("name,M,variant", [("gate", 8, "col"), ("gate", 32, "col"), ("down", 4, "col"),
+                                            ("gate", 8, "warp"), ("gate", 16, "warp"), ("gate", 32, "tc"),
                                             ("down", 4, "warp")])
 def test_full_size_whole_output(name, M, variant, monkeypatch):
     """One full-size Llama-3-8B linear through the fused call, every output
@@ -390,7 +456,7 @@ def test_full_size_whole_output(name, M, variant, monkeypatch):
     y32 = mq.fused_linear(xt, [pl], out_dtype=torch.float32)[0]
     y16 = mq.fused_linear(xt, [pl])[0]
     mq.check_device_error()
-    assert mq.gemm_plan(M, lin.N, lin.K)["variant"] == ("warp-mma" if variant == "warp" else "tensor-memory")
+    assert mq.gemm_plan(M, lin.N, lin.K)["variant"] == {"col": "column", "warp": "warp-mma", "tc": "tensor-memory"}[variant]
     qx, sx = O.quantize_act(x, False)
     y, a = O.linear(qx, sx, O.prepare(w, xcal, False, 0.10))
     check_close(y32.cpu().numpy(), y, a)
