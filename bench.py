@@ -267,6 +267,13 @@ def rate_microbenchmarks() -> dict:
         o = ctypes.c_double()
         rc = L.mqp_mma_sync(kind, 4000, ctypes.byref(o))
         out[name] = round(o.value / 1e12, 1) if rc == 0 else f"error {rc}"
+    # the decode kernel's group product at its occupancy (16 warps per SM, 32-token tiles): operands
+    # loaded from shared memory and unpacked every K-step, against the same MMAs fed from registers
+    L.mqp_mma_fed.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_double)]
+    for feed, name in ((0, "mma_sync_e4m3_decode_group_product_tflops"), (1, "mma_sync_e4m3_same_mmas_register_fed_tflops")):
+        o = ctypes.c_double()
+        rc = L.mqp_mma_fed(feed, 2000, ctypes.byref(o))
+        out[name] = round(o.value / 1e12, 1) if rc == 0 else f"error {rc}"
     return out
 
 

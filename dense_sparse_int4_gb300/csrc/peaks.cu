@@ -7,10 +7,14 @@
 //    shapes, whose int4 codes run as exact E4M3;
 //  * the legacy warp-level mma.sync rates for E4M3 (m16n8k32, fp32
 //    accumulators), s8 (m16n8k32) and s4 (m16n8k64, int32 accumulators): the
-//    integer A/B context next to the E4M3 path the decode kernel takes.
+//    integer A/B context next to the E4M3 path the decode kernel takes;
+//  * the E4M3 mma.sync rate at the decode kernel's occupancy and data flow
+//    (16 warps per SM, four accumulator chains per warp, 32-token tiles):
+//    operands loaded from shared memory and unpacked every K-step as the
+//    kernel does, against the same MMAs fed from registers.
 //
-// Every kernel keeps many independent accumulators per issuing thread, so it
-// measures issue throughput, not latency.  Waits are bounded.
+// The first two kernels keep many independent accumulators per issuing
+// thread, so they measure issue throughput, not latency.  Waits are bounded.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -136,6 +140,66 @@ __global__ void __launch_bounds__(512) mma_sync_rate(int iters, uint32_t magic, 
   if (x == magic) sink[0] = x;  // keeps the chains live; magic is never hit in practice
 }
 
+// The decode kernel's group product at 32 tokens (16 rows per warp, four
+// 8-token blocks one at a time, weights unpacked from INT4 every block),
+// repeated over two shared-memory units chosen pseudo-randomly per iteration
+// (nothing is loop-invariant).  kFeed 0: operands from shared memory; 1: the
+// same MMAs with register operands.
+__device__ __forceinline__ void unpack_u4p(uint32_t p, uint32_t& ev, uint32_t& od) {
+  const uint32_t u = p ^ 0x88888888u;
+  ev = u & 0x0F0F0F0Fu;
+  od = (u >> 4) & 0x0F0F0F0Fu;
+}
+__device__ __forceinline__ void mma_f32_e4m3(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1, bool zero) {
+  if (zero)
+    asm volatile("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                 "{%10, %10, %10, %10};"
+                 : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
+  else
+    asm volatile("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+constexpr int kFedUnit = 8448, kFedImg = 32 * 136, kFedSmem = 2 * kFedUnit + 2 * kFedImg;
+
+template <int kFeed>
+__global__ void __launch_bounds__(512, 1) mma_fed_rate(int iters, float* sink) {
+  extern __shared__ __align__(16) uint8_t fs[];
+  for (int i = threadIdx.x; i < kFedSmem / 4; i += blockDim.x)
+    reinterpret_cast<uint32_t*>(fs)[i] = (static_cast<uint32_t>(i) * 2654435761u) & 0x37373737u;  // finite E4M3
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const int q = warp >> 3, rw = 16 * (warp & 7);
+  float acc = 0.0f;
+  for (int it = 0; it < iters; ++it) {
+    const int sel = static_cast<int>((static_cast<uint32_t>(it) * 2654435761u) >> 31);
+    const uint8_t* wr = fs + (q ^ sel) * kFedUnit + (rw + g) * 16 + t * 4;
+    const uint8_t* img = fs + 2 * kFedUnit + (q ^ sel) * kFedImg;
+#pragma unroll
+    for (int nb = 0; nb < 4; ++nb) {
+      float d[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t a[4], b0, b1;
+        if (kFeed == 0) {
+          unpack_u4p(*reinterpret_cast<const uint32_t*>(wr + j * 2048), a[0], a[2]);
+          unpack_u4p(*reinterpret_cast<const uint32_t*>(wr + j * 2048 + 128), a[1], a[3]);
+          const uint2 b = *reinterpret_cast<const uint2*>(img + ((j * 4 + nb) * 32 + lane) * 8);
+          b0 = b.x, b1 = b.y;
+        } else {
+          a[0] = 0x30303030u ^ static_cast<uint32_t>(sel), a[1] = 0x31313131u, a[2] = 0x32323232u, a[3] = 0x33333333u;
+          b0 = 0x34343434u ^ static_cast<uint32_t>(nb), b1 = 0x35353535u ^ static_cast<uint32_t>(j);
+        }
+        mma_f32_e4m3(d, a, b0, b1, j == 0);
+      }
+      acc += d[0] + d[1] + d[2] + d[3];
+    }
+  }
+  if (acc == 1234.5f) sink[0] = acc;  // keeps the MMAs live
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -237,6 +301,30 @@ int mqp_mma_sync(int kind, int iters, double* ops) {
     const double per_mma = 2.0 * 16 * 8 * k;
     *ops = per_mma * kChains * static_cast<double>(iters) * (grid * threads / 32) / (ms * 1e-3);
   }
+  return rc;
+}
+
+// The decode kernel's E4M3 group product over all SMs, one CTA of 16 warps
+// each (feed 0: operands from shared memory, unpacked as the kernel does;
+// feed 1: the same MMAs from registers).  *ops = multiply-adds x 2 per second.
+int mqp_mma_fed(int feed, int iters, double* ops) {
+  const int sms = sm_count();
+  if (sms <= 0 || iters < 1 || !ops || feed < 0 || feed > 1) return 1;
+  if (cudaFuncSetAttribute(mma_fed_rate<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFedSmem) != cudaSuccess ||
+      cudaFuncSetAttribute(mma_fed_rate<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFedSmem) != cudaSuccess)
+    return 1;
+  float* sink = nullptr;
+  if (cudaMalloc(&sink, sizeof(float)) != cudaSuccess) return 1;
+  float ms = 0.f;
+  int rc = timed(
+      [&] {
+        if (feed == 0) mma_fed_rate<0><<<sms, 512, kFedSmem>>>(iters, sink);
+        if (feed == 1) mma_fed_rate<1><<<sms, 512, kFedSmem>>>(iters, sink);
+        return cudaGetLastError() == cudaSuccess;
+      },
+      &ms);
+  cudaFree(sink);
+  if (rc == 0) *ops = 2.0 * 16 * 8 * 32 * 16 * static_cast<double>(iters) * (16.0 * sms) / (ms * 1e-3);
   return rc;
 }
 
