@@ -57,7 +57,9 @@
 #include <algorithm>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 // Timeline probes for profiling builds: compiled out unless MQ_ZTRACE is
 // defined, in which case stamps go to a buffer the host sets: ZT(slot) the
@@ -131,6 +133,8 @@ struct ZParams {
   int64_t units;
   int y_f32;
   int raw;          // column form: the stages take X rows (else packed codes and scales)
+  int cluster;      // warp-MMA form: CTAs per cluster (one tile per cluster, pieces through DSMEM), or 0
+  int rx_off;       // its byte offset of the received pieces in dynamic shared memory
   int32_t* dots_w;  // test hook (one matrix): raw group dots instead of Y
   int32_t* dots_r;
   const uint8_t* act;  // workspace: [G] activation images (written by the image kernel)
@@ -211,6 +215,64 @@ __device__ __forceinline__ bool zcheck(bool ok, int bit, uint32_t* err) {
 #define ZOK(cond, site) true
 #define ZW(ok, site) (ok)
 #endif
+// --- thread-block clusters -----------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster, with release / acquire ordering.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// This CTA's shared-memory address `saddr` as seen in cluster peer `rank`.
+__device__ __forceinline__ uint32_t mapa_peer(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+// Bulk copy of this CTA's shared memory into a cluster peer's; completion is
+// counted in bytes on the peer's mbarrier.  Addresses 16-byte aligned, bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_s2peer(uint32_t dst_cluster, const void* src, uint32_t bytes,
+                                            uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_cluster),
+      "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
+      : "memory");
+}
+// This thread's bulk copies have read their sources.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// mbar_wait with cluster-scope acquire (for phases completed by cluster peers' copies).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                  uint64_t timeout_ns, uint32_t* err_word) {
+  uint64_t t0 = 0;
+  for (uint32_t n = 0;; ++n) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if ((n & 63u) == 63u) {
+      if (*abort_flag) return false;
+      const uint64_t now = globaltimer();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > timeout_ns) {
+        atomicOr(err_word, kDevErrTimeout);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ void named_bar(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -1063,7 +1125,17 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
     fence_mbar_init();
     if (lane == 0) ZC(11);
   }
-  __syncthreads();
+  // Cluster mode: one tile per cluster; its CTAs' pieces go into the head
+  // CTA's shared memory (rx) by bulk copy, counted on the head's pieces_in.
+  // (read from the parameters where used: kept out of the compute warps' registers)
+#define ZCK (kDebug ? 0 : p.cluster)
+#define ZRX reinterpret_cast<float*>(smem + p.rx_off)
+  if (ZCK > 0) {
+    cluster_sync_all();  // every peer's barriers are initialised before any copy targets them
+    if (finishes && threadIdx.x == 0) mbar_arrive_expect_tx(&ctl.pieces_in, static_cast<uint32_t>(npc) * piece_bytes);
+  } else {
+    __syncthreads();
+  }
   if (threadIdx.x == 0) ZC(12);
   pdl_trigger();
   auto stage = [&](int s) { return stages + static_cast<size_t>(s) * SB; };
@@ -1229,7 +1301,7 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
     // The slots stages nstg, nstg + 1, .. would take are free once the compute
     // warps are done with their last stages (at once if never filled): they
     // take the pieces of the tile this CTA finishes, handed over one by one.
-    if (ok && finishes && pieces_in_smem && lane == 0) {
+    if (ok && ZCK == 0 && finishes && pieces_in_smem && lane == 0) {
       for (int k = 0; k < need_slots; ++k) {
         const int v = nstg + k, slot = v % S;  // the slot's last fill was stage v - S; its phases are waited in order
         if (v >= S && !ZW(mbar_wait_sleep(&ctl.empty[slot], ((v / S) - 1) & 1, abort_flag, tmo, p.err), 7)) break;
@@ -1241,7 +1313,7 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
     // ---------------- epilogue: stream-K pieces off the compute warps' path ----------------
     pdl_wait();  // the flags and pieces in the workspace may still be in use by the preceding kernel
     bool ok = true;
-    if (publishes) {  // release this CTA's piece once every compute warp has written its share
+    if (publishes && ZCK == 0) {  // release this CTA's piece once every compute warp has written its share
       if (lane == 0) {
         ok = ZW(mbar_wait_sleep(&ctl.piece_written, 0, abort_flag, tmo, p.err), 4);
         if (ok) {
@@ -1252,7 +1324,7 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
       }
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
     }
-    if (finishes && ok) {
+    if (finishes && ok && ZCK == 0) {
       // the flags of the other pieces (lane j: CTA c + 1 + j), then the pieces
       // into the free slot; each flag is cleared for the next launch once seen
       for (int j0 = 0; ok && j0 < npc; j0 += 32) {
@@ -1444,7 +1516,9 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
       float* mine = red + q * (kRedTok * kRedLd);
       const int slot0 = nstg % S;  // the first slot handed over for pieces
       if (fin) {
-        if (!ZW(mbar_wait(&ctl.pieces_in, 0, abort_flag, tmo, p.err), 3)) return false;
+        const bool got = ZCK > 0 ? mbar_wait_cluster(&ctl.pieces_in, 0, abort_flag, tmo, p.err)
+                                : mbar_wait(&ctl.pieces_in, 0, abort_flag, tmo, p.err);
+        if (!ZW(got, 3)) return false;
         if (warp == 0 && lane == 0) ZC(92);
       }
 #pragma unroll
@@ -1473,7 +1547,10 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
           float v = ld_shared_f32(red + mr * kRedLd + r);
 #pragma unroll
           for (int qq = 1; qq < US; ++qq) v += ld_shared_f32(red + (qq * kRedTok + mr) * kRedLd + r);  // set order
-          if (fin && pieces_in_smem) {
+          if (fin && ZCK > 0) {
+            for (int j = 0; j < npc; ++j)  // cluster rank order
+              v += ld_shared_f32(ZRX + j * (piece_bytes / 4) + m * kTileN + r);
+          } else if (fin && pieces_in_smem) {
             // piece j sits at slot (nstg + j / per_slot) % S, (j % per_slot) pieces in: walked, not divided
             uint32_t off = static_cast<uint32_t>(slot0) * SB;
             for (int j = 0, in = 0, sl = slot0; j < npc; ++j) {  // CTA order
@@ -1491,7 +1568,9 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
 #pragma unroll 8
             for (int j = 0; j < npc; ++j) v += __ldcg(piece_of(c + 1 + j) + m * kTileN + r);  // CTA order
           }
-          if (pub) {
+          if (pub && ZCK > 0) {
+            st_shared_f32(ZRX + m * kTileN + r, v);
+          } else if (pub) {
             if (ZOK(c < P && m < TN, 9)) st_global_f32(piece + m * kTileN + r, v);
           } else if (ZOK(tile >= mt.tile0 && tile < mat_end_tile(p, tile) && m < p.M, 8)) {
             store_y(mt, nbase + r, m, v);
@@ -1500,6 +1579,20 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
         if (warp == kWCompute - WPS && lane == 0) ZC(172 + 4 * pass);
         if (pass + 1 < kRedPasses && !tile_sync()) return false;  // the buffers are free again
         if (warp == kWCompute - WPS && lane == 0) ZC(173 + 4 * pass);
+      }
+      if (pub && ZCK > 0) {
+        // the piece (this CTA's only tile) into the head CTA's shared memory, slot rank - 1
+        fence_proxy_async_smem();  // this thread's writes of the piece, before the bulk copy reads them
+        if (!tile_sync()) return false;
+        if (warp == 0 && lane == 0) {
+          const uint32_t rank = cluster_ctarank();
+          if (ZOK(rank >= 1 && static_cast<int>(rank) < ZCK, 10)) {
+            bulk_s2peer(mapa_peer(smem_u32(ZRX) + (rank - 1) * piece_bytes, 0), ZRX, piece_bytes,
+                        mapa_peer(smem_u32(&ctl.pieces_in), 0));
+            bulk_wait_read_all();  // the source stays valid until the copy has read it
+          }
+        }
+        return true;
       }
       if (pub) {
         __syncwarp();
@@ -1572,6 +1665,8 @@ __global__ void __launch_bounds__(w_threads(TN), 1) zipper_warp_kernel(const ZPa
     }
     __syncthreads();
   }
+#undef ZCK
+#undef ZRX
 }
 
 // ---------------------------------------------------------------------------
@@ -2317,6 +2412,8 @@ struct ZPlan {
   int tn, mld, ctas, nstages, stage_bytes, smem, arec;
   int64_t units;  // units, or columns in the column form
   size_t o_act, o_part, o_q, o_s, bytes;  // workspace layout after the zeroed prefix
+  int cluster = 0;  // warp-MMA form: CTAs per cluster (one tile per cluster), or 0
+  int rx_off = 0;   // its received pieces' offset in dynamic shared memory
 };
 
 // The decode kernel's form: 4 warp-MMA (the default), or as MQ_DECODE_VARIANT
@@ -2342,6 +2439,47 @@ int c_ctl_bytes() {
 template <int TN>
 int w_ctl_bytes() {
   return (static_cast<int>(sizeof(WCtl<kMaxUnits / w_sets(TN) + 1>)) + 127) / 128 * 128;
+}
+
+constexpr int kMaxClusterCtas = 8;           // portable cluster size
+constexpr int kClusterRxBytes = 48 * 1024;   // the head CTA's room for its peers' pieces
+
+// Clusters of k CTAs of the warp-MMA form (dynamic shared memory `smem`) that
+// the current device holds at once, or 0; asked once per (device, size).
+template <int TN>
+int w_max_clusters(int dev, int k, int smem) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int>, int> cache;
+  std::lock_guard<std::mutex> lk(mu);
+  const auto key = std::make_tuple(dev, k, smem);
+  const auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  auto kern = zipper_warp_kernel<TN, false>;
+  int n = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit - w_ctl_bytes<TN>()) ==
+      cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(k), 1, 1);
+    cfg.blockDim = dim3(w_threads(TN), 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(k);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();  // a refused query leaves no sticky error behind
+  cache[key] = n;
+  return n;
+}
+
+// Cluster mode is on unless MQ_DECODE_CLUSTER is "0" (benchmarks and tests).
+bool cluster_mode_allowed() {
+  const char* v = getenv("MQ_DECODE_CLUSTER");
+  return !(v && strcmp(v, "0") == 0);
 }
 
 bool zplan(int64_t M, int64_t tiles, int64_t K, ZPlan* out) {
@@ -2401,6 +2539,32 @@ bool zplan(int64_t M, int64_t tiles, int64_t K, ZPlan* out) {
   pl.nstages = std::min(kMaxStages, (kSmemLimit - ctl_bytes - fixed) / pl.stage_bytes);
   if (pl.nstages < 2) return false;
   pl.smem = pl.nstages * pl.stage_bytes + fixed;
+  // Cluster mode (warp-MMA form): when k CTAs per tile over all tiles use
+  // about as many SMs as stream-K would, each tile gets a cluster of k CTAs
+  // (the stream-K partition over tiles x k CTAs then cuts tiles only inside
+  // clusters) and the pieces travel by bulk copy into the head CTA's shared
+  // memory instead of through the workspace and flags.
+  if (!pl.tc && cluster_mode_allowed() && tiles > 0) {
+    const int64_t kk = std::min<int64_t>(
+        {kMaxClusterCtas, sms / tiles, G, kClusterRxBytes / (M * kTileN * 4) + 1});
+    if (kk >= 2 && tiles * kk * 10 >= static_cast<int64_t>(pl.ctas) * 9 && (G + kk - 1) / kk <= kMaxUnits) {
+      const int rx = static_cast<int>((kk - 1) * M * kTileN * 4 + 127) / 128 * 128;
+      const int ns = std::min(kMaxStages, (kSmemLimit - ctl_bytes - fixed - rx) / pl.stage_bytes);
+      const int smem = ns * pl.stage_bytes + fixed + rx;
+      int dev = 0;
+      const int fits = ns < 2 || cudaGetDevice(&dev) != cudaSuccess ? 0
+                       : pl.tn == 8                                  ? w_max_clusters<8>(dev, static_cast<int>(kk), smem)
+                       : pl.tn == 16                                 ? w_max_clusters<16>(dev, static_cast<int>(kk), smem)
+                                                                     : w_max_clusters<32>(dev, static_cast<int>(kk), smem);
+      if (fits >= tiles) {
+        pl.cluster = static_cast<int>(kk);
+        pl.ctas = static_cast<int>(tiles * kk);
+        pl.nstages = ns;
+        pl.smem = smem;
+        pl.rx_off = ns * pl.stage_bytes + (fixed - 128);  // after the stages, the ring and the tile partials
+      }
+    }
+  }
   // workspace: the zeroed prefix (tile counters [ctas]), the activation
   // images, the stream-K pieces
   pl.o_act = kWsZeroBytes;
@@ -2454,6 +2618,7 @@ mq_status zdispatch(const ZParams& zp, const ZPlan& pl, cudaStream_t stream) {
 template <int TN, bool kDebug>
 mq_status wlaunch(const ZParams& zp, const ZPlan& pl, cudaStream_t stream) {
   auto kern = zipper_warp_kernel<TN, kDebug>;
+  // (the debug form ignores cluster mode: the same partition, no exchange)
   static std::mutex mu;
   static bool attr_set[64];  // per device, per instantiation
   int dev = 0;
@@ -2472,11 +2637,18 @@ mq_status wlaunch(const ZParams& zp, const ZPlan& pl, cudaStream_t stream) {
   cfg.blockDim = dim3(w_threads(TN), 1, 1);
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (!kDebug && pl.cluster > 0) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(pl.cluster);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   if (cudaLaunchKernelEx(&cfg, kern, zp) != cudaSuccess) return launch_status("zipper launch");
   return launch_status("zipper");
 }
@@ -2556,23 +2728,26 @@ size_t zipper_workspace_bytes(int64_t M, int64_t tiles, int64_t K) {
   return zplan(M, tiles, K, &pl) ? pl.bytes : 0;
 }
 
-// Plan summary for mq_gemm_plan: {form (3 tensor-memory, 4 warp-MMA, 5 column), tokens per tile, CTAs, stages}.
-bool zipper_plan_info(int64_t M, int64_t tiles, int64_t K, int32_t* form, int32_t* tn, int32_t* ctas, int32_t* stages) {
+// Plan summary for mq_gemm_plan: {form (3 tensor-memory, 4 warp-MMA, 5 column), tokens per tile, CTAs, stages,
+// CTAs per cluster (1: no clusters)}.
+bool zipper_plan_info(int64_t M, int64_t tiles, int64_t K, int32_t* form, int32_t* tn, int32_t* ctas, int32_t* stages,
+                      int32_t* cluster) {
   ZPlan pl;
   if (!zplan(M, tiles, K, &pl)) return false;
   *form = pl.tc ? 3 : pl.col ? 5 : 4;
   *tn = pl.tn;
   *ctas = pl.ctas;
   *stages = pl.nstages;
+  *cluster = pl.cluster > 0 ? pl.cluster : 1;
   return true;
 }
 
 // The kernel choice for (M, N, K) on the current device: {form (3: tensor
-// memory, 4: warp MMA, 5: column), tokens per tile, 1, CTAs, stages} for the decode
+// memory, 4: warp MMA, 5: column), tokens per tile, CTAs per cluster, CTAs, stages} for the decode
 // kernel, else zeros (the general kernel runs).
 mq_status gemm_plan_info(int64_t M, int64_t N, int64_t K, int32_t* info) {
   for (int i = 0; i < 5; ++i) info[i] = 0;
-  if (zipper_plan_info(M, N / kTileN, K, &info[0], &info[1], &info[3], &info[4])) info[2] = 1;
+  zipper_plan_info(M, N / kTileN, K, &info[0], &info[1], &info[3], &info[4], &info[2]);
   return MQ_OK;
 }
 
@@ -2626,6 +2801,8 @@ mq_status zipper_launch(bool* handled, int nmat, const uint8_t* const* wpk, cons
   zp.stage_bytes = pl.stage_bytes;
   zp.units = pl.units;
   zp.y_f32 = yt == MQ_F32;
+  zp.cluster = pl.cluster;
+  zp.rx_off = pl.rx_off;
   zp.dots_w = dots_w;
   zp.dots_r = dots_r;
   uint8_t* w = static_cast<uint8_t*>(ws);

@@ -290,7 +290,10 @@ mq_status mq_debug_group_dots(const uint8_t* xq, const uint16_t* xs, int64_t M, 
  *             MMA with the activation quantizer inside the GEMM) and 3 = its
  *             tensor-memory form (taken when the environment variable
  *             MQ_DECODE_VARIANT is "col" or "tc"); 0 = the general kernel;
- *         for the decode kernel, [1] tokens per tile (8, 16 or 32), [2] 1,
+ *         for the decode kernel, [1] tokens per tile (8, 16 or 32), [2] CTAs
+ *         per thread-block cluster (1 without clusters; the warp-MMA form
+ *         gives each weight tile a cluster of this many CTAs when that uses
+ *         about as many SMs as stream-K, unless MQ_DECODE_CLUSTER is "0"),
  *         [3] CTAs launched, [4] weight stages in shared memory; zeros for
  *         the general kernel.
  * MQ_ERR_INVALID_ARG for bad sizes (the same rules as the GEMM) or NULL info;

@@ -380,6 +380,34 @@ def test_fused_quantizer_corners(variant, M, x_dtype, pad, monkeypatch):
     check_close(y32.cpu().numpy(), y, a)
 
 
+@pytest.mark.parametrize("M,N,K,budget", [(4, 4096, 4096, 0.10), (32, 4096, 4096, 0.10), (8, 1536, 4096, 0.3),
+                                          (16, 640, 1024, 1.0), (3, 2048, 512, 0.2)])
+def test_cluster_mode_matches_oracle(M, N, K, budget, monkeypatch):
+    """Small launches give each weight tile a thread-block cluster whose CTAs send their
+    stream-K pieces into the head CTA's shared memory: Y (fp32 and bf16) within the bound,
+    the same bits twice in a row, and the stream-K form (clusters off) within the bound too."""
+    x, w, xcal = _case(M, N, K, budget, seed=M + N + K)
+    pl = mq.prepare_linear(dev_half(w), dev_half(xcal), budget)
+    xq, xs = mq.quantize_act(dev_half(x))
+    plan = mq.gemm_plan(M, N, K)
+    assert plan["variant"] == "warp-mma" and plan["cluster"] >= 2, plan
+    assert plan["clusters"] == plan["cluster"] * (N // 128)
+    y32 = mq.gemm(xq, xs, M, pl, out_dtype=torch.float32)
+    y32b = mq.gemm(xq, xs, M, pl, out_dtype=torch.float32)
+    y16 = mq.gemm(xq, xs, M, pl, out_dtype=torch.bfloat16)
+    mq.check_device_error()
+    monkeypatch.setenv("MQ_DECODE_CLUSTER", "0")
+    assert mq.gemm_plan(M, N, K)["cluster"] == 1
+    y32s = mq.gemm(xq, xs, M, pl, out_dtype=torch.float32)
+    mq.check_device_error()
+    qx, sx = O.quantize_act(x, False)
+    y, a = O.linear(qx, sx, O.prepare(w, xcal, False, budget))
+    check_close(y32.cpu().numpy(), y, a)
+    check_bf16(host_u16(y16), y, a)
+    assert torch.equal(y32, y32b)
+    check_close(y32s.cpu().numpy(), y, a)
+
+
 @pytest.mark.parametrize("variant,M", [("col", 4), ("col", 32), ("warp", 4), ("tc", 32)])
 def test_dense_residual_back_to_back(variant, M, monkeypatch):
     """Every block residual (budget 1): each stage fills the residual ring a
