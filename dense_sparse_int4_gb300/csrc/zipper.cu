@@ -2547,7 +2547,7 @@ bool zplan(int64_t M, int64_t tiles, int64_t K, ZPlan* out) {
   if (!pl.tc && cluster_mode_allowed() && tiles > 0) {
     const int64_t kk = std::min<int64_t>(
         {kMaxClusterCtas, sms / tiles, G, kClusterRxBytes / (M * kTileN * 4) + 1});
-    if (kk >= 2 && tiles * kk * 10 >= static_cast<int64_t>(pl.ctas) * 9 && (G + kk - 1) / kk <= kMaxUnits) {
+    if (kk >= 2 && tiles * kk * 10 >= static_cast<int64_t>(pl.ctas) * 8 && (G + kk - 1) / kk <= kMaxUnits) {
       const int rx = static_cast<int>((kk - 1) * M * kTileN * 4 + 127) / 128 * 128;
       const int ns = std::min(kMaxStages, (kSmemLimit - ctl_bytes - fixed - rx) / pl.stage_bytes);
       const int smem = ns * pl.stage_bytes + fixed + rx;
