@@ -758,11 +758,13 @@ struct Plan {
   size_t ws_counters;  // bytes
 };
 
+// Token-tile width.  Above 32 tokens, 64: two converter groups share a CTA's
+// items (at 128 there is room for one), and the 2048-token prefill runs ~10 %
+// faster than with 128-token tiles.
 static int pick_tn(int64_t M) {
   if (M <= 16) return 16;
   if (M <= 32) return 32;
-  if (M <= 64) return 64;
-  return 128;
+  return 64;
 }
 
 static size_t a256(size_t b) { return (b + 255) / 256 * 256; }
@@ -901,8 +903,7 @@ mq_status gemm_launch(const uint8_t* xq, const uint16_t* xs, int64_t M, const ui
   switch (pl.tn) {
     case 16: return dbg ? launch_tn<16, true>(gp, pl, stream) : launch_tn<16, false>(gp, pl, stream);
     case 32: return dbg ? launch_tn<32, true>(gp, pl, stream) : launch_tn<32, false>(gp, pl, stream);
-    case 64: return dbg ? launch_tn<64, true>(gp, pl, stream) : launch_tn<64, false>(gp, pl, stream);
-    default: return dbg ? launch_tn<128, true>(gp, pl, stream) : launch_tn<128, false>(gp, pl, stream);
+    default: return dbg ? launch_tn<64, true>(gp, pl, stream) : launch_tn<64, false>(gp, pl, stream);
   }
 }
 
