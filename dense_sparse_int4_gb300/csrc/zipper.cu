@@ -2318,13 +2318,20 @@ template <int TN, bool kQuant, bool kFrag>
 __global__ void __launch_bounds__(128) act_image_kernel(const ImgParams p) {
   constexpr int kArec = kFrag ? TN * 136 : act_rec_bytes(TN);
   constexpr int NB = TN / 8;
-  pdl_trigger();
-  // the inputs are the preceding kernel's output, and the previous GEMM may
-  // still be reading the images this overwrites
-  pdl_wait();
   const int64_t g = blockIdx.x;
   const int m = static_cast<int>(blockIdx.y) * 8 + static_cast<int>(threadIdx.x >> 4), k = threadIdx.x & 15;
   const bool real = m < p.M;
+  pdl_trigger();
+  // This CTA usually starts while the preceding kernel still runs: bring its
+  // rows of X into L2 meanwhile (L2 is coherent with that kernel's writes, so
+  // a line fetched early still reads the final values), one request per
+  // 128-byte line.
+  if constexpr (kQuant)
+    if (real && (k & 7) == 0)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(p.x + static_cast<int64_t>(m) * p.ldx + g * kGroup + 8 * k));
+  // the inputs are the preceding kernel's output, and the previous GEMM may
+  // still be reading the images this overwrites
+  pdl_wait();
   uint8_t* rec = p.act + g * kArec;
   float* sco = reinterpret_cast<float*>(rec + TN * 128);
   uint32_t ev, od;
