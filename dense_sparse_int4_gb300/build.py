@@ -22,7 +22,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmq.so")
 PEAKS_LIB = os.path.join(BUILD, "libmq_peaks.so")
 PEAKS_SOURCE = "peaks.cu"
-SOURCES = ["abi.cu", "status.cu", "quantize.cu", "select.cu", "pack.cu", "gemm.cu", "zipper.cu", "noalloc.cu"]
+SOURCES = ["abi.cu", "status.cu", "quantize.cu", "select.cu", "pack.cu", "gemm.cu", "image_gemm.cu", "zipper.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -790,16 +790,23 @@ static Plan make_plan(int64_t M, int64_t N, int64_t K) {
 }
 
 size_t zipper_workspace_bytes(int64_t M, int64_t tiles, int64_t K);
+bool image_form_wanted(int64_t M);
+size_t image_workspace_bytes(int64_t M, int64_t N, int64_t K);
+mq_status image_gemm_launch(bool* handled, const uint8_t* xq, const uint16_t* xs, int64_t M, const uint8_t* wpk,
+                            int64_t N, int64_t K, const int32_t* row_ptr, const int32_t* col_idx, int64_t nnzb,
+                            const uint8_t* rpk, void* y, int64_t ldy, mq_dtype yt, int32_t* dots_w, int32_t* dots_r,
+                            void* ws, size_t ws_bytes, cudaStream_t stream);
 
-// Bytes of workspace of the general kernel alone.
+// Bytes of workspace of the general kernel: its pieces, or the image form's
+// operand images where that form serves M (image_gemm.cu).
 size_t general_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   const Plan pl = make_plan(M, N, K);
-  return pl.ws_partials + pl.ws_counters;
+  const size_t conv = pl.ws_partials + pl.ws_counters;
+  return image_form_wanted(M) ? std::max(conv, image_workspace_bytes(M, N, K)) : conv;
 }
 
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  const Plan pl = make_plan(M, N, K);
-  return std::max(pl.ws_partials + pl.ws_counters, zipper_workspace_bytes(M, N / kTileN, K));
+  return std::max(general_workspace_bytes(M, N, K), zipper_workspace_bytes(M, N / kTileN, K));
 }
 
 // Bytes of workspace the kernel that mq_w4a4_residual_gemm will run for
@@ -864,6 +871,12 @@ mq_status gemm_launch(const uint8_t* xq, const uint16_t* xs, int64_t M, const ui
                                        nullptr, MQ_F16, 0, nullptr, nullptr, M, K, dots_w, dots_r, ws, ws_bytes,
                                        stream);
     if (handled || zs != MQ_OK) return zs;
+  }
+  {
+    // Large batches: the image form, when the workspace holds its images.
+    const mq_status is = image_gemm_launch(&handled, xq, xs, M, wpk, N, K, row_ptr, col_idx, nnzb, rpk, y, ldy, yt,
+                                           dots_w, dots_r, ws, ws_bytes, stream);
+    if (handled || is != MQ_OK) return is;
   }
   const Plan pl = make_plan(M, N, K);
   if (pl.ctas > kWsZeroBytes / 4)

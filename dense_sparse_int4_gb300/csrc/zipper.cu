@@ -2752,9 +2752,16 @@ bool zipper_plan_info(int64_t M, int64_t tiles, int64_t K, int32_t* form, int32_
 // The kernel choice for (M, N, K) on the current device: {form (3: tensor
 // memory, 4: warp MMA, 5: column), tokens per tile, CTAs per cluster, CTAs, stages} for the decode
 // kernel, else zeros (the general kernel runs).
+bool image_form_wanted(int64_t M);
+void image_plan_info(int64_t M, int64_t N, int64_t K, int32_t* tn, int32_t* ctas);
+
 mq_status gemm_plan_info(int64_t M, int64_t N, int64_t K, int32_t* info) {
   for (int i = 0; i < 5; ++i) info[i] = 0;
   zipper_plan_info(M, N / kTileN, K, &info[0], &info[1], &info[3], &info[4], &info[2]);
+  if (info[0] == 0 && image_form_wanted(M)) {  // the general kernel's image form
+    info[0] = 6;
+    image_plan_info(M, N, K, &info[1], &info[3]);
+  }
   return MQ_OK;
 }
 

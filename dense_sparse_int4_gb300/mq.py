@@ -275,8 +275,8 @@ def gemm_plan(M: int, N: int, K: int) -> dict:
     """The kernel the GEMM entry points run for (M, N, K) on the current device."""
     info = (ctypes.c_int32 * 5)()
     _check(lib().mq_gemm_plan(M, N, K, ctypes.cast(info, ctypes.c_void_p)), "mq_gemm_plan")
-    return {"decode": bool(info[0]),
-            "variant": {0: "general", 3: "tensor-memory", 4: "warp-mma", 5: "column"}[info[0]],
+    return {"decode": info[0] in (3, 4, 5),
+            "variant": {0: "general", 3: "tensor-memory", 4: "warp-mma", 5: "column", 6: "image"}[info[0]],
             "tokens_per_tile": info[1], "cluster": info[2], "clusters": info[3], "stages": info[4]}
 
 

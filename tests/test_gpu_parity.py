@@ -175,14 +175,17 @@ def test_decode_variants_match_oracle(variant, M, N, K, budget, monkeypatch):
 
 @pytest.mark.parametrize("M,variant", [(32, "col"), (16, "col"), (8, "col"), (4, "col"), (1, "col"),
                                        (32, "warp"), (32, "tc"), (16, "tc"), (8, "warp"), (8, "tc"), (4, "warp"),
-                                       (1, "warp"), (1, "tc"), (33, None), (128, None)])
+                                       (1, "warp"), (1, "tc"), (33, None), (128, None), (33, "image"),
+                                       (300, "image")])
 def test_group_dots_extremes(M, variant, monkeypatch):
     """Adversarial codes: every product +49, every product -49, alternating
     cancellation; sums reach +-6272 per group, exactly.  Up to 32 tokens this
     runs the decode kernel, in its column and warp-MMA forms (mask-and-offset
     unpack to E4M3, fp32 MMA accumulators) and its tensor-memory form; above 32 tokens
     the general kernel (exact-integer E4M3 table)."""
-    if variant:
+    if variant == "image":
+        monkeypatch.setenv("MQ_GENERAL_FORM", "image")
+    elif variant:
         monkeypatch.setenv("MQ_DECODE_VARIANT", variant)
     N, K = 128, 256
     x = np.full((M, K), 7.0, np.float32)
@@ -200,7 +203,8 @@ def test_group_dots_extremes(M, variant, monkeypatch):
     ref = O.group_dots(qx, p.qw)
     assert ref.max() == 6272 and ref.min() == -6272 and (ref == 0).any() == (M > 1)
     plan = mq.gemm_plan(M, N, K)
-    assert plan["variant"] == {"col": "column", "warp": "warp-mma", "tc": "tensor-memory", None: "general"}[variant]
+    assert plan["variant"] == {"col": "column", "warp": "warp-mma", "tc": "tensor-memory", "image": "image",
+                               None: "general"}[variant]
     assert np.array_equal(dw.cpu().numpy(), ref)
 
 
@@ -246,10 +250,14 @@ def test_gemm_concentrated_block_row():
     check_close(y32.cpu().numpy(), y, a)
 
 
-def test_gemm_both_halves_and_empty_rows():
+@pytest.mark.parametrize("M,form", [(20, None), (140, "image"), (140, "conv")])
+def test_gemm_both_halves_and_empty_rows(M, form, monkeypatch):
     """Blocks in both 64-row halves of a tile at the same group, single halves,
-    and tiles with no residual at all."""
-    M, N, K = 20, 512, 1024
+    and tiles with no residual at all (decode kernel, and both forms of the
+    general kernel)."""
+    if form:
+        monkeypatch.setenv("MQ_GENERAL_FORM", form)
+    N, K = 512, 1024
     x, w, _ = _case(M, N, K, 0.0, seed=9)
     G = K // 128
     rows = {0: [0, 3, 7], 1: [3, 5], 2: [], 3: [1], 4: [], 5: [], 6: [0, 7], 7: [0, 1, 2, 3, 4, 5, 6, 7]}
@@ -268,6 +276,42 @@ def test_gemm_both_halves_and_empty_rows():
     y, a = O.linear(qx, sx, p)
     check_close(y32.cpu().numpy(), y, a)
     assert np.array_equal(dr.cpu().numpy(), O.residual_dots(qx, p.qr, ci))
+    assert np.array_equal(dw.cpu().numpy(), O.group_dots(qx, p.qw))
+    if form:
+        assert mq.gemm_plan(M, N, K)["variant"] == {"image": "image", "conv": "general"}[form]
+
+
+@pytest.mark.parametrize("form", ["image", "conv"])
+@pytest.mark.parametrize("M,N,K,budget,x_dtype", [(33, 256, 512, 1.0, "f16"), (130, 384, 1280, 0.2, "bf16"),
+                                                  (300, 256, 640, 0.3, "f16"), (257, 1024, 2048, 0.1, "bf16"),
+                                                  (512, 128, 128, 0.0, "f16"), (384, 640, 512, 0.5, "f16")])
+def test_general_forms_match_oracle(form, M, N, K, budget, x_dtype, monkeypatch):
+    """The general kernel's two forms, forced through MQ_GENERAL_FORM: the image
+    form (a pre-pass writes every operand's shared-memory image; both MMA
+    operands from shared memory) and the converter form.  Dots bit for bit, Y
+    within the fp32 bound and bf16 within 1 ulp; ragged token tails, odd group
+    counts, tiles cut across several CTAs (several rounds of pieces) and a
+    single-group K; a second call gives the same bits."""
+    monkeypatch.setenv("MQ_GENERAL_FORM", form)
+    assert mq.gemm_plan(M, N, K)["variant"] == {"image": "image", "conv": "general"}[form]
+    x, w, xcal = _case(M, N, K, budget, seed=M * 3 + N + K, x_dtype=x_dtype)
+    isb = x_dtype == "bf16"
+    pl = mq.prepare_linear(dev_half(w), dev_act(xcal, isb), budget)
+    xq, xs = mq.quantize_act(dev_act(x, isb))
+    dw, dr = mq.debug_group_dots(xq, xs, M, pl)
+    y32 = mq.gemm(xq, xs, M, pl, out_dtype=torch.float32)
+    y16 = mq.gemm(xq, xs, M, pl, out_dtype=torch.bfloat16)
+    y32b = mq.gemm(xq, xs, M, pl, out_dtype=torch.float32)
+    mq.check_device_error()
+    qx, sx = O.quantize_act(x, isb)
+    p = O.prepare(w, xcal, isb, budget)
+    assert np.array_equal(dw.cpu().numpy(), O.group_dots(qx, p.qw))
+    if p.ksel:
+        assert np.array_equal(dr.cpu().numpy(), O.residual_dots(qx, p.qr, p.col_idx))
+    y, a = O.linear(qx, sx, p)
+    check_close(y32.cpu().numpy(), y, a)
+    check_bf16(host_u16(y16), y, a)
+    assert torch.equal(y32, y32b)
 
 
 # ----------------------------------------------------------------------------
