@@ -18,26 +18,29 @@
 // tcgen05.mma with both operands in shared memory; the CUDA cores only apply
 // the per-group scales.
 //
-// Roles per CTA (one CTA per SM, persistent stream-K over (tile, group)
-// units; tiles are token-tile major, so that the CTAs running at one time
-// read the same few weight tiles and every image stays in L2):
+// A unit is two consecutive groups of one (weight tile, token tile) (one
+// group at the end of a tile of odd G): every role pays its waits, arrivals
+// and loop once per two groups.  Roles per CTA (one CTA per SM, persistent
+// stream-K over units; tiles are token-tile major, so that the CTAs running at
+// one time read the same few weight tiles and every image stays in L2):
 //   warps 0, 2 producers, alternating units: a stage is one unit's weight and
-//              activation images; the drain's scales go to a ring of their
-//              own; a unit with residual blocks also brings the blocks' images
-//              (top half at 0, bottom half at 8 KiB) into a slot of the
+//              activation images (64 KiB); the drain's scales go to a ring of
+//              their own; a group with residual blocks also brings the blocks'
+//              images (top half at 0, bottom half at 8 KiB) into a slot of the
 //              residual ring (each producer its own half of the slots).  The
-//              copies of a unit leave in one warp instruction.
+//              copies of a unit (up to 16) leave in one warp instruction.
 //   warp 1     builds the CTA's residual map, then one thread issues per unit
-//              4 MMAs (K = 32 each) into a TMEM accumulator, and, where the
-//              unit has residual blocks, 4 more from the residual slot into
-//              the next accumulator (M = 128: a half without a block gives
-//              rows nobody reads).
-//   warps 3-18 drain, 4 warps per TMEM lane quarter, TN/4 tokens each: load
-//              the item's dots, free the accumulator, then acc += sx * (s * D)
-//              in packed fp32 pairs; at tile ends store Y or a stream-K
-//              piece.  Tiles cut by a CTA range are finished by the CTA whose
-//              piece arrives last, summing the pieces in CTA order
-//              (deterministic; no floating-point atomics).
+//              4 MMAs (K = 32 each) per group into a TMEM accumulator of 256
+//              columns (the two groups side by side), and, where a group has
+//              residual blocks, 4 more from its residual slot into the next
+//              accumulator (M = 128: a half without a block gives rows nobody
+//              reads).
+//   warps 3-18 drain, 4 warps per TMEM lane quarter, TN/4 tokens each: load a
+//              group's dots (16 columns at a time), free the accumulator after
+//              the last load, acc += sx * (s * D) in packed fp32 pairs; at tile
+//              ends store Y or a stream-K piece.  Tiles cut by a CTA range are
+//              finished by the CTA whose piece arrives last, summing the pieces
+//              in CTA order (deterministic; no floating-point atomics).
 // Every wait is bounded (mbar_wait): a broken pipeline reports a timeout in
 // the device error word and the kernel returns.
 #include "mq_internal.cuh"
@@ -54,8 +57,8 @@ namespace mq {
 namespace {
 
 constexpr int kImgMaxDevices = 64;
-constexpr int kImgMinTokens = 256;       // the image form's default lower bound on M
-constexpr int kImgMaxUnitsPerCta = 1024;  // size of the CTA's residual map
+constexpr int kImgMinTokens = 128;       // the image form's default lower bound on M (measured crossover: 64 tokens run faster on the converter form, 128 on this one)
+constexpr int kImgMaxUnitsPerCta = 512;  // size of the CTA's residual map
 constexpr int kImgPlanCtasNoDevice = 152;
 constexpr int kImgMinUnitsPerCta = 4;
 constexpr int kWImg = 16384;  // image of one (weight tile, group): 128 rows x 128 bytes
@@ -65,23 +68,28 @@ constexpr int kWarpProd = 0, kWarpMma = 1, kWarpProd2 = 2, kWarpDrain0 = 3, kDra
 
 template <int TN>
 struct ICfg {
-  static constexpr int kA = kWImg;     // weight image of the unit
-  static constexpr int kB = TN * 128;  // activation image of the unit
-  static constexpr int kStageBytes = kA + kB;
-  static constexpr int kStages = TN <= 128 ? 4 : 3;
-  // residual images, 16 KiB each (top + bottom block); half the slots per producer
-  static constexpr int kRSlots = TN <= 128 ? 4 : 2;
-  static constexpr int kScSlots = TN <= 128 ? 16 : 12;
-  // scale slot: weight scales [128] fp16, residual scales [2][64] fp16, activation scales [TN] fp32
+  static constexpr int kUG = 2;         // groups per unit
+  static constexpr int kA = kWImg;      // weight image of a group
+  static constexpr int kB = TN * 128;   // activation image of a group
+  static constexpr int kGB = kA + kB;   // a group's part of a stage
+  static constexpr int kStageBytes = kUG * kGB;
+  static constexpr int kStages = 2;
+  // residual images of one group (top + bottom block, 16 KiB each); half the slots per producer
+  static constexpr int kRSlots = 4;
+  static constexpr int kScSlots = 8;
+  // scale slot, per group: weight scales [128] fp16, residual scales [2][64] fp16, activation scales [TN] fp32
   static constexpr int sWS = 0, sRS = 256, sSX = 512;
-  static constexpr int kScBytes = 512 + TN * 4;
-  static constexpr int kDSlots = 512 / TN;  // TMEM accumulators (all 512 columns)
-  static constexpr int kCols = TN / 4;      // tokens per drain thread
+  static constexpr int kScGroup = 512 + TN * 4;
+  static constexpr int kScBytes = kUG * kScGroup;
+  static constexpr int kDCols = kUG * TN;        // TMEM columns of one item (a unit's groups side by side)
+  static constexpr int kDSlots = 512 / kDCols;   // TMEM accumulators (all 512 columns)
+  static constexpr int kCols = TN / 4;           // tokens per drain thread
   static constexpr int kThreads = 32 * (kWarpDrain0 + kDrainWarps);
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kSmemBytes = kRingBytes + kRSlots * 2 * kRImg + kScSlots * kScBytes + 1024 /*align*/;
   static_assert(kSmemBytes + 12 * 1024 <= 227 * 1024, "shared memory budget");
-  static_assert(kCols % 32 == 0, "drain chunks");
+  static_assert(kCols == 32, "a drain thread loads a group's dots in one 32-column load");
+  static_assert(kDSlots >= 2, "two accumulators at least");
   // instruction descriptor: D f32, A/B E4M3, both K-major, N = TN, M = 128
   static constexpr uint32_t kIdesc =
       (1u << 4) | (static_cast<uint32_t>(TN >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
@@ -136,9 +144,11 @@ struct __align__(8) ICtl {
   uint64_t drain_bar;  // bounded barrier of the drain threads
   uint64_t red_bar;    // bulk loads of stream-K pieces
   uint64_t map_ready;  // residual map built
-  int32_t blk[NS][2];    // CSR entries of the stage's top / bottom residual block, or -1
-  int32_t sblk[NSC][2];  // the same, for the drain (lives as long as the scale slot)
-  int64_t deferred[2];   // cut tiles this CTA finishes (at most its first and last)
+  int32_t blk[NS][2][2];    // per group of the stage's unit: CSR entries of its top / bottom residual block, or -1
+  int32_t sblk[NSC][2][2];  // the same, for the drain (lives as long as the scale slot)
+  int32_t ng[NS];           // groups of the stage's unit (2, or 1 at the end of a tile of odd G)
+  int32_t sng[NSC];
+  int64_t deferred[2];      // cut tiles this CTA finishes (at most its first and last)
   uint32_t tmem_base;
   int abort_flag;
   int ndeferred;
@@ -238,12 +248,15 @@ __global__ void __launch_bounds__(256) image_prep_kernel(const PrepParams p) {
 template <int TN, bool kDebug>
 __global__ void __launch_bounds__(ICfg<TN>::kThreads, 1) image_gemm_kernel(const ImgParams p) {
   using C = ICfg<TN>;
-  constexpr int NS = C::kStages, NR = C::kRSlots, NSC = C::kScSlots, ND = C::kDSlots;
+  constexpr int NS = C::kStages, NR = C::kRSlots, NSC = C::kScSlots, ND = C::kDSlots, UG = C::kUG;
+  constexpr int NRP = NR / 2;  // residual slots per producer
   extern __shared__ uint8_t smem_raw[];
   __shared__ ICtl<NS, NR, NSC, ND> ctl;
-  __shared__ int32_t res_map[2][kImgMaxUnitsPerCta];  // per local unit: CSR entry of the top / bottom block, or -1
-  __shared__ int16_t res_ord[kImgMaxUnitsPerCta];     // its position among the units with residual blocks of the
-                                                       // same parity (the same producer)
+  // per local unit and group: CSR entry of the top / bottom block, or -1
+  __shared__ int32_t res_map[UG][2][kImgMaxUnitsPerCta];
+  // per local unit and group with residual blocks: its position among those of units of the same parity
+  // (the same producer), which picks its slot of the residual ring
+  __shared__ int16_t res_ord[UG][kImgMaxUnitsPerCta];
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* rring = smem + C::kRingBytes;
@@ -252,7 +265,7 @@ __global__ void __launch_bounds__(ICfg<TN>::kThreads, 1) image_gemm_kernel(const
   const int64_t U = p.units, P = p.ctas, c = blockIdx.x;
   const int64_t u0 = c * U / P, u1 = (c + 1) * U / P;
   const int nunits = static_cast<int>(u1 - u0);
-  const int G = p.G;
+  const int G = p.G, UPT = (G + UG - 1) / UG;  // groups, units per tile
   volatile int* abort_flag = &ctl.abort_flag;
   const uint64_t tmo = p.timeout_ns;
 
@@ -289,9 +302,8 @@ __global__ void __launch_bounds__(ICfg<TN>::kThreads, 1) image_gemm_kernel(const
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
 
-  // unit -> tile (token-tile major) and group; tile -> weight tile t, token tile mt
-  auto unit_tile = [&](int64_t u) { return u / G; };
-  auto unit_g = [&](int64_t u) { return static_cast<int>(u % G); };
+  // unit -> tile (token-tile major) and unit of the tile; tile -> weight tile t, token tile mt
+  auto unit_tile = [&](int64_t u) { return u / UPT; };
   auto tile_t = [&](int64_t tile) { return static_cast<int>(tile % p.tiles_n); };
   auto tile_mt = [&](int64_t tile) { return static_cast<int>(tile / p.tiles_n); };
   auto owner = [&](int64_t u) { return ((u + 1) * P - 1) / U; };  // the CTA whose range holds unit u
@@ -300,18 +312,17 @@ __global__ void __launch_bounds__(ICfg<TN>::kThreads, 1) image_gemm_kernel(const
   // and two roles would pay it every unit).
   struct Pos {
     int64_t tile;
-    int g, t, mt;
+    int j, t, mt;  // unit of the tile (groups UG*j, UG*j + 1), weight tile, token tile
   };
-  const Pos pos0 = {unit_tile(u0), unit_g(u0), tile_t(unit_tile(u0)), tile_mt(unit_tile(u0))};
+  const Pos pos0 = {unit_tile(u0), static_cast<int>(u0 % UPT), tile_t(unit_tile(u0)), tile_mt(unit_tile(u0))};
   auto advance = [&](Pos& q) {
-    if (++q.g == G) {
-      q.g = 0;
+    if (++q.j == UPT) {
+      q.j = 0;
       ++q.tile;
       if (++q.t == p.tiles_n) q.t = 0, ++q.mt;
     }
   };
 
-  constexpr int NRP = NR / 2;  // residual slots per producer
   if (warp == kWarpProd || warp == kWarpProd2) {
     const int pw = warp == kWarpProd ? 0 : 1;  // this producer fills units pw, pw + 2, ...
     pdl_wait();  // the images are the pre-pass's output
@@ -319,39 +330,49 @@ __global__ void __launch_bounds__(ICfg<TN>::kThreads, 1) image_gemm_kernel(const
     bool ok = mbar_wait(&ctl.map_ready, 0, &never0, tmo, p.err);
     Pos q = pos0;
     if (pw) advance(q);
+    // lane L: group gq = L / 8 of the unit, copy kind k = L % 8 (0 weight image, 1 activation image,
+    // 2 weight scales, 3 activation scales, 4 / 5 top / bottom residual scales, 6 / 7 their images)
+    const int gq = (lane >> 3) & 1, kind = lane & 7, hh = kind & 1;
     for (int i = pw; ok && i < nunits; i += 2, advance(q), advance(q)) {
       const int st = i % NS, sc = i % NSC;
-      const int g = q.g, t = q.t, m0 = q.mt * TN;
-      const int e0 = res_map[0][i], e1 = res_map[1][i];
-      const int nres = (e0 >= 0) + (e1 >= 0);
-      const int ri = nres ? res_ord[i] : 0, rs = pw * NRP + ri % NRP;
+      const int g0 = UG * q.j, t = q.t, m0 = q.mt * TN;
+      const int ng = min(UG, G - g0);
+      // this lane's group: residual entries, slot, and whether it has blocks
+      const bool mine = lane < 8 * ng;
+      const int ea = mine ? res_map[gq][0][i] : -1, eb = mine ? res_map[gq][1][i] : -1;
+      const bool has = ea >= 0 || eb >= 0;
+      const int ro = has ? res_ord[gq][i] : 0, rs = pw * NRP + ro % NRP;
       int wait_ok = 1;
-      if (lane == 0) {
-        if (i >= NS) wait_ok = mbar_wait(&ctl.empty[st], ((i / NS) & 1) ^ 1, abort_flag, tmo, p.err);
-        if (wait_ok && i >= NSC) wait_ok = mbar_wait(&ctl.sc_empty[sc], ((i / NSC) & 1) ^ 1, abort_flag, tmo, p.err);
-        if (wait_ok && nres && ri >= NRP)
-          wait_ok = mbar_wait(&ctl.r_empty[rs], ((ri / NRP) & 1) ^ 1, abort_flag, tmo, p.err);
-        if (wait_ok) {
-          ctl.blk[st][0] = ctl.sblk[sc][0] = e0;
-          ctl.blk[st][1] = ctl.sblk[sc][1] = e1;
-          mbar_arrive_expect_tx(&ctl.full[st], C::kA + C::kB);
-          mbar_arrive_expect_tx(&ctl.sc_full[sc], 256 + TN * 4 + nres * 128);
-          if (nres) mbar_arrive_expect_tx(&ctl.r_full[rs], nres * kRImg);
-        }
+      if (kind == 0 && lane < 8 * ng) {  // lanes 0 and 8: the stage, the scale slot, this group's residual slot
+        if (lane == 0 && i >= NS) wait_ok = mbar_wait(&ctl.empty[st], ((i / NS) & 1) ^ 1, abort_flag, tmo, p.err);
+        if (lane == 0 && wait_ok && i >= NSC)
+          wait_ok = mbar_wait(&ctl.sc_empty[sc], ((i / NSC) & 1) ^ 1, abort_flag, tmo, p.err);
+        if (wait_ok && has && ro >= NRP)
+          wait_ok = mbar_wait(&ctl.r_empty[rs], ((ro / NRP) & 1) ^ 1, abort_flag, tmo, p.err);
       }
-      ok = __shfl_sync(0xFFFFFFFFu, wait_ok, 0);
+      ok = __all_sync(0xFFFFFFFFu, wait_ok);
       if (!ok) break;
-      uint8_t* sb = smem + st * C::kStageBytes;
-      uint8_t* scb = scring + sc * C::kScBytes;
+      if (kind == 0 && has) mbar_arrive_expect_tx(&ctl.r_full[rs], ((ea >= 0) + (eb >= 0)) * kRImg);
+      const int nsr = __popc(__ballot_sync(0xFFFFFFFFu, (kind == 4 || kind == 5) && (hh ? eb : ea) >= 0));
+      __syncwarp();
+      if (lane == 0) {  // one thread writes what the consumers read after this arrival
+#pragma unroll
+        for (int g2 = 0; g2 < UG; ++g2)
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) ctl.blk[st][g2][h2] = ctl.sblk[sc][g2][h2] = g2 < ng ? res_map[g2][h2][i] : -1;
+        ctl.ng[st] = ctl.sng[sc] = ng;
+        mbar_arrive_expect_tx(&ctl.full[st], ng * C::kGB);
+        mbar_arrive_expect_tx(&ctl.sc_full[sc], ng * (256 + TN * 4) + nsr * 128);
+      }
+      __syncwarp();
+      // The unit's copies, one per lane, leave in one warp instruction (a bulk
+      // copy costs its issuing instruction a fixed time); selects, not a
+      // switch: divergent lanes would resolve an indirect branch one after another.
+      uint8_t* sb = smem + st * C::kStageBytes + gq * C::kGB;
+      uint8_t* scb = scring + sc * C::kScBytes + gq * C::kScGroup;
+      const int g = g0 + gq;
       const int64_t wrec = static_cast<int64_t>(t) * G + g;
-      // The unit's copies, one per lane, leave in one warp instruction: a bulk
-      // copy costs its issuing instruction a fixed time, so lanes that issued
-      // theirs one after another (divergent branches) would pace the stream.
-      // lane: 0 weight image, 1 activation image, 2 weight scales, 3 activation
-      // scales, 4 / 5 residual scales and 6 / 7 residual images of the top /
-      // bottom block.  Selects, not a switch: divergent lanes would resolve an
-      // indirect branch one after another.
-      const int e = (lane & 1) ? e1 : e0;
+      const int e = hh ? eb : ea;
       const int64_t ee = e >= 0 ? e : 0;
       const uint8_t* s_a = p.wimg + wrec * kWImg;
       const uint8_t* s_b = p.ximg + (static_cast<int64_t>(g) * p.Mt + m0) * 128;
@@ -359,31 +380,30 @@ __global__ void __launch_bounds__(ICfg<TN>::kThreads, 1) image_gemm_kernel(const
       const uint8_t* s_sx = reinterpret_cast<const uint8_t*>(p.sxf + static_cast<int64_t>(g) * p.Mt + m0);
       const uint8_t* s_rs = p.rpk + ee * kRRecBytes + kRRecScales;
       const uint8_t* s_ri = p.rimg + ee * kRImg;
-      const uint8_t* src = lane == 0 ? s_a : lane == 1 ? s_b : lane == 2 ? s_ws : lane == 3 ? s_sx : lane < 6 ? s_rs : s_ri;
-      uint8_t* dst = lane == 0   ? sb
-                     : lane == 1 ? sb + C::kA
-                     : lane == 2 ? scb + C::sWS
-                     : lane == 3 ? scb + C::sSX
-                     : lane < 6  ? scb + C::sRS + (lane - 4) * 128
-                                 : rring + rs * 2 * kRImg + (lane - 6) * kRImg;
-      const uint32_t bytes = lane == 0   ? static_cast<uint32_t>(C::kA)
-                             : lane == 1 ? static_cast<uint32_t>(C::kB)
-                             : lane == 2 ? 256u
-                             : lane == 3 ? static_cast<uint32_t>(TN * 4)
-                             : lane < 6  ? 128u
+      const uint8_t* src = kind == 0 ? s_a : kind == 1 ? s_b : kind == 2 ? s_ws : kind == 3 ? s_sx : kind < 6 ? s_rs : s_ri;
+      uint8_t* dst = kind == 0   ? sb
+                     : kind == 1 ? sb + C::kA
+                     : kind == 2 ? scb + C::sWS
+                     : kind == 3 ? scb + C::sSX
+                     : kind < 6  ? scb + C::sRS + hh * 128
+                                 : rring + rs * 2 * kRImg + hh * kRImg;
+      const uint32_t bytes = kind == 0   ? static_cast<uint32_t>(C::kA)
+                             : kind == 1 ? static_cast<uint32_t>(C::kB)
+                             : kind == 2 ? 256u
+                             : kind == 3 ? static_cast<uint32_t>(TN * 4)
+                             : kind < 6  ? 128u
                                          : static_cast<uint32_t>(kRImg);
-      uint64_t* bar = lane < 2 ? &ctl.full[st] : lane < 6 ? &ctl.sc_full[sc] : &ctl.r_full[rs];
-      if (lane < 4 || (lane < 8 && e >= 0)) bulk_g2s(dst, src, bytes, bar);
+      uint64_t* bar = kind < 2 ? &ctl.full[st] : kind < 6 ? &ctl.sc_full[sc] : &ctl.r_full[rs];
+      if (mine && (kind < 4 || e >= 0)) bulk_g2s(dst, src, bytes, bar);
       __syncwarp();
     }
     // Every copy issued here is waited on by a consumer before the CTA ends;
     // after an abort, the end of the kernel gives copies in flight time to land.
   } else if (warp == kWarpMma) {
     // residual map of this CTA's units, from the block-list rows of its tiles
-    for (int i = lane; i < nunits; i += 32) {
-      res_map[0][i] = -1;
-      res_map[1][i] = -1;
-    }
+    for (int i = lane; i < nunits; i += 32)
+#pragma unroll
+      for (int gq = 0; gq < UG; ++gq) res_map[gq][0][i] = res_map[gq][1][i] = -1;
     __syncwarp();
     if (p.nnzb > 0 && nunits > 0) {
       for (int64_t tile = unit_tile(u0); tile <= unit_tile(u1 - 1); ++tile) {
@@ -395,19 +415,21 @@ __global__ void __launch_bounds__(ICfg<TN>::kThreads, 1) image_gemm_kernel(const
           const int e1 = max(e0, min(p.nnzb, p.row_ptr[br + 1]));
           for (int e = e0 + lane; e < e1; e += 32) {
             const int g = p.col_idx[e];
-            const int64_t lu = tile * G + g - u0;
-            if (g >= 0 && g < G && lu >= 0 && lu < nunits) res_map[half][lu] = e;
+            const int64_t lu = tile * UPT + g / UG - u0;
+            if (g >= 0 && g < G && lu >= 0 && lu < nunits) res_map[g % UG][half][lu] = e;
           }
         }
       }
     }
     __syncwarp();
-    {  // ordinal of each unit with residual blocks among those of its parity
-       // (lane l scans a contiguous chunk of an even number of units)
-      const int chunk = ((nunits + 63) / 64) * 2;
+    {  // ordinal of each group with residual blocks among those of units of its parity, in
+       // (unit, group) order (lane l scans a contiguous chunk of units)
+      const int chunk = (nunits + 31) / 32;
       const int l0 = min(nunits, lane * chunk), l1 = min(nunits, l0 + chunk);
       int cnt[2] = {0, 0};
-      for (int lu = l0; lu < l1; ++lu) cnt[lu & 1] += (res_map[0][lu] >= 0 || res_map[1][lu] >= 0);
+      for (int lu = l0; lu < l1; ++lu)
+#pragma unroll
+        for (int gq = 0; gq < UG; ++gq) cnt[lu & 1] += (res_map[gq][0][lu] >= 0 || res_map[gq][1][lu] >= 0);
       int pos[2];
 #pragma unroll
       for (int par = 0; par < 2; ++par) {
@@ -420,7 +442,9 @@ __global__ void __launch_bounds__(ICfg<TN>::kThreads, 1) image_gemm_kernel(const
         pos[par] = incl - cnt[par];
       }
       for (int lu = l0; lu < l1; ++lu)
-        if (res_map[0][lu] >= 0 || res_map[1][lu] >= 0) res_ord[lu] = static_cast<int16_t>(pos[lu & 1]++);
+#pragma unroll
+        for (int gq = 0; gq < UG; ++gq)
+          if (res_map[gq][0][lu] >= 0 || res_map[gq][1][lu] >= 0) res_ord[gq][lu] = static_cast<int16_t>(pos[lu & 1]++);
     }
     __syncwarp();
     mbar_arrive(&ctl.map_ready);
@@ -430,24 +454,34 @@ __global__ void __launch_bounds__(ICfg<TN>::kThreads, 1) image_gemm_kernel(const
       for (int i = 0; i < nunits && ok; ++i) {
         const int st = i % NS;
         if (!mbar_wait(&ctl.full[st], (i / NS) & 1, abort_flag, tmo, p.err)) break;
-        const bool has_r = ctl.blk[st][0] >= 0 || ctl.blk[st][1] >= 0;
-        const uint32_t a_base = smem_u32(smem + st * C::kStageBytes), b_base = a_base + C::kA;
-        for (int k = 0; k < 1 + has_r; ++k, ++item) {
+        const int ng = ctl.ng[st];
+        bool hr[UG];
+#pragma unroll
+        for (int gq = 0; gq < UG; ++gq) hr[gq] = gq < ng && (ctl.blk[st][gq][0] >= 0 || ctl.blk[st][gq][1] >= 0);
+        const bool any_r = hr[0] || hr[1];
+        const uint32_t s_base = smem_u32(smem + st * C::kStageBytes);
+        for (int k = 0; k < 1 + any_r; ++k, ++item) {
           const int d = item % ND;
           if (!mbar_wait(&ctl.d_empty[d], ((item / ND) & 1) ^ 1, abort_flag, tmo, p.err)) { ok = false; break; }
-          uint32_t a = a_base;
-          int rs = 0;
-          if (k == 1) {  // the residual slot of this unit's producer
-            const int ri = res_ord[i];
-            rs = (i & 1) * NRP + ri % NRP;
-            if (!mbar_wait(&ctl.r_full[rs], (ri / NRP) & 1, abort_flag, tmo, p.err)) { ok = false; break; }
-            a = smem_u32(rring + rs * 2 * kRImg);
-          }
-          tc_fence_after();
-          const uint32_t d_col = tmem + d * TN;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) img_mma(d_col, img_desc(a + 32 * j), img_desc(b_base + 32 * j), C::kIdesc, j > 0);
-          if (k == 1) tc_commit(&ctl.r_empty[rs]);
+          for (int gq = 0; gq < UG; ++gq) {
+            if (gq >= ng || (k == 1 && !hr[gq])) continue;
+            const uint32_t b = s_base + gq * C::kGB + C::kA;
+            uint32_t a = s_base + gq * C::kGB;
+            int rs = 0;
+            if (k == 1) {  // the residual slot of this group (its unit's producer's half of the ring)
+              const int ro = res_ord[gq][i];
+              rs = (i & 1) * NRP + ro % NRP;
+              if (!mbar_wait(&ctl.r_full[rs], (ro / NRP) & 1, abort_flag, tmo, p.err)) { ok = false; break; }
+              a = smem_u32(rring + rs * 2 * kRImg);
+            }
+            tc_fence_after();
+            const uint32_t d_col = tmem + d * C::kDCols + gq * TN;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) img_mma(d_col, img_desc(a + 32 * j), img_desc(b + 32 * j), C::kIdesc, j > 0);
+            if (k == 1) tc_commit(&ctl.r_empty[rs]);
+          }
+          if (!ok) break;
           tc_commit(&ctl.d_full[d]);
         }
         if (ok) tc_commit(&ctl.empty[st]);
@@ -501,67 +535,93 @@ __global__ void __launch_bounds__(ICfg<TN>::kThreads, 1) image_gemm_kernel(const
     Pos q = pos0;
     for (int i = 0; i < nunits && ok; ++i, advance(q)) {
       const int64_t tile = q.tile;
-      const int g = q.g;
+      const int g0 = UG * q.j;
       const int n = q.t * kTileN + r, m0 = q.mt * TN;
       const int sc = i % NSC;
       if (!mbar_wait(&ctl.sc_full[sc], (i / NSC) & 1, abort_flag, tmo, p.err)) { ok = false; break; }
       const uint8_t* scb = scring + sc * C::kScBytes;
-      const int e_top = ctl.sblk[sc][0], e_bot = ctl.sblk[sc][1];
-      const int e_mine = half ? e_bot : e_top;
-      const int nitems = 1 + (e_top >= 0 || e_bot >= 0);
-      const uint64_t* sxp = reinterpret_cast<const uint64_t*>(scb + C::sSX) + c0 / 2;
-      for (int k = 0; k < nitems; ++k, ++item) {
+      const int ng = ctl.sng[sc];
+      int e_mine[UG];
+      bool any_r = false;
+#pragma unroll
+      for (int gq = 0; gq < UG; ++gq) {
+        e_mine[gq] = gq < ng ? ctl.sblk[sc][gq][half] : -1;
+        any_r = any_r || (gq < ng && (ctl.sblk[sc][gq][0] >= 0 || ctl.sblk[sc][gq][1] >= 0));
+      }
+      for (int k = 0; k < 1 + any_r; ++k, ++item) {
         const int d = item % ND;
         if (!mbar_wait(&ctl.d_full[d], (item / ND) & 1, abort_flag, tmo, p.err)) { ok = false; break; }
         tc_fence_after();
-        if (k == 0 || e_mine >= 0) {  // warp-uniform: a warp's 32 rows sit in one half
-          const uint16_t sbits = k == 0 ? reinterpret_cast<const uint16_t*>(scb + C::sWS)[r]
-                                        : reinterpret_cast<const uint16_t*>(scb + C::sRS)[half * 64 + (r & 63)];
-          const float s = __half2float(__ushort_as_half(sbits));
-          const uint64_t s2 = p2(s, s);
 #pragma unroll
-          for (int ch = 0; ch < C::kCols / 32; ++ch) {
+        for (int gq = 0; gq < UG; ++gq) {
+          const bool active = gq < ng && (k == 0 || e_mine[gq] >= 0);  // warp-uniform: a warp's rows sit in one half
+          const uint8_t* scg = scb + gq * C::kScGroup;
+          if constexpr (kDebug) {
             uint32_t dv[32];
-            tmem_ld32(tmem + lane_base + d * TN + c0 + 32 * ch, dv);
-            tc_wait_ld();
-            if (ch == C::kCols / 32 - 1) {  // every dot of the item is in registers: free the accumulator
+            if (active) {
+              tmem_ld32(tmem + lane_base + d * C::kDCols + gq * TN + c0, dv);
+              tc_wait_ld();
+            }
+            if (gq == UG - 1) {  // every dot of the item this warp reads is in registers: free the accumulator
               tc_fence_before();
               __syncwarp();
               if (lane == 0) mbar_arrive(&ctl.d_empty[d]);
             }
-            if constexpr (kDebug) {
+            if (!active) continue;
+            const int g = g0 + gq;
 #pragma unroll
-              for (int q = 0; q < 32; ++q) {
-                const int m = m0 + c0 + 32 * ch + q;
-                if (m < p.M) {
-                  const int32_t v = static_cast<int32_t>(__uint_as_float(dv[q]));
-                  if (k == 0)
-                    p.dots_w[(static_cast<int64_t>(m) * p.N + n) * G + g] = v;
-                  else
-                    p.dots_r[(static_cast<int64_t>(m) * p.nnzb + e_mine) * 64 + (r & 63)] = v;
-                }
+            for (int q2 = 0; q2 < 32; ++q2) {
+              const int m = m0 + c0 + q2;
+              if (m < p.M) {
+                const int32_t v = static_cast<int32_t>(__uint_as_float(dv[q2]));
+                if (k == 0)
+                  p.dots_w[(static_cast<int64_t>(m) * p.N + n) * G + g] = v;
+                else
+                  p.dots_r[(static_cast<int64_t>(m) * p.nnzb + e_mine[gq]) * 64 + (r & 63)] = v;
               }
-            } else {
+            }
+          } else {
+            // 16 columns at a time: fewer live registers than one 32-column load (measured faster)
+            const uint32_t sxa = smem_u32(scg + C::sSX) + c0 * 4;
+            uint64_t s2 = 0;
+            if (active) {
+              const uint16_t sbits = k == 0 ? reinterpret_cast<const uint16_t*>(scg + C::sWS)[r]
+                                            : reinterpret_cast<const uint16_t*>(scg + C::sRS)[half * 64 + (r & 63)];
+              const float s = __half2float(__ushort_as_half(sbits));
+              s2 = p2(s, s);
+            }
 #pragma unroll
-              for (int q = 0; q < 16; ++q) {
-                const int jp = 16 * ch + q;
-                const uint64_t t2 = mul2(p2(__uint_as_float(dv[2 * q]), __uint_as_float(dv[2 * q + 1])), s2);
-                acc[jp] = fma2(sxp[jp], t2, acc[jp]);
+            for (int hx = 0; hx < 2; ++hx) {
+              uint32_t dv[16];
+              if (active) {
+                tmem_ld16(tmem + lane_base + d * C::kDCols + gq * TN + c0 + 16 * hx, dv);
+                tc_wait_ld();
+              }
+              if (gq == UG - 1 && hx == 1) {  // every dot of the item this warp reads is in registers
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl.d_empty[d]);
+              }
+              if (!active) continue;
+#pragma unroll
+              for (int j2 = 0; j2 < 4; ++j2) {
+                uint64_t sx0, sx1;  // activation scales of token pairs 8 hx + 2 j2, + 1 of this thread's columns
+                asm volatile("ld.shared.v2.u64 {%0, %1}, [%2];" : "=l"(sx0), "=l"(sx1) : "r"(sxa + 64 * hx + 16 * j2));
+                const uint64_t t0 = mul2(p2(__uint_as_float(dv[4 * j2]), __uint_as_float(dv[4 * j2 + 1])), s2);
+                const uint64_t t1 = mul2(p2(__uint_as_float(dv[4 * j2 + 2]), __uint_as_float(dv[4 * j2 + 3])), s2);
+                acc[8 * hx + 2 * j2] = fma2(sx0, t0, acc[8 * hx + 2 * j2]);
+                acc[8 * hx + 2 * j2 + 1] = fma2(sx1, t1, acc[8 * hx + 2 * j2 + 1]);
               }
             }
           }
-        } else {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&ctl.d_empty[d]);
         }
       }
       if (!ok) break;
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.sc_empty[sc]);  // scales read: the slot may be refilled
       // ---- tile end: store Y, or hand a stream-K piece to the workspace ----
-      if (!kDebug && (g == G - 1 || i == nunits - 1)) {
-        const int64_t tu0 = tile * G, tu1 = tu0 + G;  // the tile's units
+      if (!kDebug && (q.j == UPT - 1 || i == nunits - 1)) {
+        const int64_t tu0 = tile * UPT, tu1 = tu0 + UPT;  // the tile's units
         if (tu0 >= u0 && tu1 <= u1) {
           store_tile(m0, n);
         } else {
@@ -569,10 +629,10 @@ __global__ void __launch_bounds__(ICfg<TN>::kThreads, 1) image_gemm_kernel(const
           // that brings the count to the number of pieces finishes the tile
           // after its own range (no stall here).
           const int slot = (tile == pos0.tile) ? 0 : 1;
-          uint4* mine = reinterpret_cast<uint4*>(p.partials + ((c * 2 + slot) * kTileN + r) * TN + c0);
+          uint4* part = reinterpret_cast<uint4*>(p.partials + ((c * 2 + slot) * kTileN + r) * TN + c0);
 #pragma unroll
           for (int q4 = 0; q4 < NP / 2; ++q4)
-            mine[q4] = make_uint4(static_cast<uint32_t>(acc[2 * q4]), static_cast<uint32_t>(acc[2 * q4] >> 32),
+            part[q4] = make_uint4(static_cast<uint32_t>(acc[2 * q4]), static_cast<uint32_t>(acc[2 * q4] >> 32),
                                   static_cast<uint32_t>(acc[2 * q4 + 1]), static_cast<uint32_t>(acc[2 * q4 + 1] >> 32));
           __threadfence();
           if (!drain_sync()) { ok = false; break; }
@@ -596,7 +656,7 @@ __global__ void __launch_bounds__(ICfg<TN>::kThreads, 1) image_gemm_kernel(const
       int nred = 0;
       for (int di = 0; di < nd && ok; ++di) {
         const int64_t tile = ctl.deferred[di];
-        const int64_t tu0 = tile * G, tu1 = tu0 + G;
+        const int64_t tu0 = tile * UPT, tu1 = tu0 + UPT;
         const int64_t cf = owner(tu0), cl = owner(tu1 - 1);
         const int m0 = tile_mt(tile) * TN, n = tile_t(tile) * kTileN + r;
 #pragma unroll
@@ -692,7 +752,7 @@ IPlan iplan(int64_t M, int64_t N, int64_t K, int64_t nnzb) {
   pl.tiles_n = static_cast<int>(N / kTileN);
   pl.G = static_cast<int>(K / kGroup);
   pl.Mt = pl.tiles_m * pl.tn;
-  pl.units = static_cast<int64_t>(pl.tiles_m) * pl.tiles_n * pl.G;
+  pl.units = static_cast<int64_t>(pl.tiles_m) * pl.tiles_n * ((pl.G + 1) / 2);  // units of two groups
   const int sms = img_sms();
   int64_t ctas = std::min<int64_t>(sms > 0 ? sms : kImgPlanCtasNoDevice,
                                    std::max<int64_t>(1, pl.units / kImgMinUnitsPerCta));

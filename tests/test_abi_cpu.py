@@ -55,9 +55,9 @@ def test_workspace_sizes(L):
     ws32 = L.mq_gemm_workspace_bytes(32, 4096, 4096)
     assert ws32 >= 64 * 2 * 128 * 32 * 4 + 32 * 4  # at least 64 CTAs (4+ units of 2 groups each)
     assert L.mq_gemm_workspace_bytes(2048, 14336, 4096) >= 152 * 2 * 128 * 64 * 4  # 64-token tiles above 32 tokens
-    # from 256 tokens: the image form's operand images (E4M3 weights, the densest residual, activations)
+    # from 128 tokens: the image form's operand images (E4M3 weights, the densest residual, activations)
     assert L.mq_gemm_workspace_bytes(2048, 14336, 4096) >= 2 * 14336 * 4096 + 2048 * 4096
-    assert L.mq_gemm_workspace_bytes(255, 14336, 4096) < 14336 * 4096
+    assert L.mq_gemm_workspace_bytes(127, 14336, 4096) < 14336 * 4096
     assert L.mq_gemm_workspace_bytes(4, 512, 512) > 0
     assert L.mq_gemm_workspace_bytes(4, 100, 4096) == 0  # invalid N
 
