@@ -57,7 +57,9 @@ namespace mq {
 namespace {
 
 constexpr int kImgMaxDevices = 64;
-constexpr int kImgMinTokens = 128;       // the image form's default lower bound on M (measured crossover: 64 tokens run faster on the converter form, 128 on this one)
+// the image form's default lower bound on M (measured: 64 tokens run faster on the
+// converter form, 128 on this one)
+constexpr int kImgMinTokens = 128;
 constexpr int kImgMaxUnitsPerCta = 512;  // size of the CTA's residual map
 constexpr int kImgPlanCtasNoDevice = 152;
 constexpr int kImgMinUnitsPerCta = 4;

@@ -176,15 +176,16 @@ def test_decode_variants_match_oracle(variant, M, N, K, budget, monkeypatch):
 @pytest.mark.parametrize("M,variant", [(32, "col"), (16, "col"), (8, "col"), (4, "col"), (1, "col"),
                                        (32, "warp"), (32, "tc"), (16, "tc"), (8, "warp"), (8, "tc"), (4, "warp"),
                                        (1, "warp"), (1, "tc"), (33, None), (128, None), (33, "image"),
-                                       (300, "image")])
+                                       (300, "image"), (300, "conv")])
 def test_group_dots_extremes(M, variant, monkeypatch):
     """Adversarial codes: every product +49, every product -49, alternating
     cancellation; sums reach +-6272 per group, exactly.  Up to 32 tokens this
     runs the decode kernel, in its column and warp-MMA forms (mask-and-offset
     unpack to E4M3, fp32 MMA accumulators) and its tensor-memory form; above 32 tokens
-    the general kernel (exact-integer E4M3 table)."""
-    if variant == "image":
-        monkeypatch.setenv("MQ_GENERAL_FORM", "image")
+    the general kernel (exact-integer E4M3 table), in its converter form and its
+    image form (the default from 128 tokens)."""
+    if variant in ("image", "conv"):
+        monkeypatch.setenv("MQ_GENERAL_FORM", variant)
     elif variant:
         monkeypatch.setenv("MQ_DECODE_VARIANT", variant)
     N, K = 128, 256
@@ -204,7 +205,7 @@ def test_group_dots_extremes(M, variant, monkeypatch):
     assert ref.max() == 6272 and ref.min() == -6272 and (ref == 0).any() == (M > 1)
     plan = mq.gemm_plan(M, N, K)
     assert plan["variant"] == {"col": "column", "warp": "warp-mma", "tc": "tensor-memory", "image": "image",
-                               None: "general"}[variant]
+                               "conv": "general", None: "image" if M >= 128 else "general"}[variant]
     assert np.array_equal(dw.cpu().numpy(), ref)
 
 
