@@ -339,34 +339,20 @@ __global__ void __launch_bounds__(ICfg<TN>::kThreads, 1) image_gemm_kernel(const
       const int st = i % NS, sc = i % NSC;
       const int g0 = UG * q.j, t = q.t, m0 = q.mt * TN;
       const int ng = min(UG, G - g0);
-      // this lane's group: residual entries, slot, and whether it has blocks
+      // Everything about the unit's copies is worked out before the waits: a
+      // stage is refilled only after its previous unit's MMAs, so the time
+      // from that release to the copies' issue is on the critical path.
+      // This lane's group: residual entries, slot, and whether it has blocks.
       const bool mine = lane < 8 * ng;
       const int ea = mine ? res_map[gq][0][i] : -1, eb = mine ? res_map[gq][1][i] : -1;
       const bool has = ea >= 0 || eb >= 0;
       const int ro = has ? res_ord[gq][i] : 0, rs = pw * NRP + ro % NRP;
-      int wait_ok = 1;
-      if (kind == 0 && lane < 8 * ng) {  // lanes 0 and 8: the stage, the scale slot, this group's residual slot
-        if (lane == 0 && i >= NS) wait_ok = mbar_wait(&ctl.empty[st], ((i / NS) & 1) ^ 1, abort_flag, tmo, p.err);
-        if (lane == 0 && wait_ok && i >= NSC)
-          wait_ok = mbar_wait(&ctl.sc_empty[sc], ((i / NSC) & 1) ^ 1, abort_flag, tmo, p.err);
-        if (wait_ok && has && ro >= NRP)
-          wait_ok = mbar_wait(&ctl.r_empty[rs], ((ro / NRP) & 1) ^ 1, abort_flag, tmo, p.err);
-      }
-      ok = __all_sync(0xFFFFFFFFu, wait_ok);
-      if (!ok) break;
-      if (kind == 0 && has) mbar_arrive_expect_tx(&ctl.r_full[rs], ((ea >= 0) + (eb >= 0)) * kRImg);
       const int nsr = __popc(__ballot_sync(0xFFFFFFFFu, (kind == 4 || kind == 5) && (hh ? eb : ea) >= 0));
-      __syncwarp();
-      if (lane == 0) {  // one thread writes what the consumers read after this arrival
+      int blk0[UG][2];  // lane 0: what the consumers read after its arrival
 #pragma unroll
-        for (int g2 = 0; g2 < UG; ++g2)
+      for (int g2 = 0; g2 < UG; ++g2)
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) ctl.blk[st][g2][h2] = ctl.sblk[sc][g2][h2] = g2 < ng ? res_map[g2][h2][i] : -1;
-        ctl.ng[st] = ctl.sng[sc] = ng;
-        mbar_arrive_expect_tx(&ctl.full[st], ng * C::kGB);
-        mbar_arrive_expect_tx(&ctl.sc_full[sc], ng * (256 + TN * 4) + nsr * 128);
-      }
-      __syncwarp();
+        for (int h2 = 0; h2 < 2; ++h2) blk0[g2][h2] = (lane == 0 && g2 < ng) ? res_map[g2][h2][i] : -1;
       // The unit's copies, one per lane, leave in one warp instruction (a bulk
       // copy costs its issuing instruction a fixed time); selects, not a
       // switch: divergent lanes would resolve an indirect branch one after another.
@@ -396,7 +382,29 @@ __global__ void __launch_bounds__(ICfg<TN>::kThreads, 1) image_gemm_kernel(const
                              : kind < 6  ? 128u
                                          : static_cast<uint32_t>(kRImg);
       uint64_t* bar = kind < 2 ? &ctl.full[st] : kind < 6 ? &ctl.sc_full[sc] : &ctl.r_full[rs];
-      if (mine && (kind < 4 || e >= 0)) bulk_g2s(dst, src, bytes, bar);
+      const bool issue = mine && (kind < 4 || e >= 0);
+      int wait_ok = 1;
+      if (kind == 0 && lane < 8 * ng) {  // lanes 0 and 8: the stage, the scale slot, this group's residual slot
+        if (lane == 0 && i >= NS) wait_ok = mbar_wait(&ctl.empty[st], ((i / NS) & 1) ^ 1, abort_flag, tmo, p.err);
+        if (lane == 0 && wait_ok && i >= NSC)
+          wait_ok = mbar_wait(&ctl.sc_empty[sc], ((i / NSC) & 1) ^ 1, abort_flag, tmo, p.err);
+        if (wait_ok && has && ro >= NRP)
+          wait_ok = mbar_wait(&ctl.r_empty[rs], ((ro / NRP) & 1) ^ 1, abort_flag, tmo, p.err);
+      }
+      ok = __all_sync(0xFFFFFFFFu, wait_ok);
+      if (!ok) break;
+      if (kind == 0 && has) mbar_arrive_expect_tx(&ctl.r_full[rs], ((ea >= 0) + (eb >= 0)) * kRImg);
+      if (lane == 0) {  // one thread writes what the consumers read after this arrival
+#pragma unroll
+        for (int g2 = 0; g2 < UG; ++g2)
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) ctl.blk[st][g2][h2] = ctl.sblk[sc][g2][h2] = blk0[g2][h2];
+        ctl.ng[st] = ctl.sng[sc] = ng;
+        mbar_arrive_expect_tx(&ctl.full[st], ng * C::kGB);
+        mbar_arrive_expect_tx(&ctl.sc_full[sc], ng * (256 + TN * 4) + nsr * 128);
+      }
+      __syncwarp();
+      if (issue) bulk_g2s(dst, src, bytes, bar);
       __syncwarp();
     }
     // Every copy issued here is waited on by a consumer before the CTA ends;
