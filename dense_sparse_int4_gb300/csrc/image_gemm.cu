@@ -107,7 +107,7 @@ struct PrepParams {
   uint8_t* ximg;        // [G][Mt][128]
   float* sxf;           // [G][Mt]
   int M, Mp, Mt, G;
-  int64_t n_w, n_r, n_x, n_s;  // threads' items per part
+  int64_t n_w, n_r, n_x, n_s;  // weight, residual and activation images; activation scales
 };
 
 struct ImgParams {
@@ -188,62 +188,62 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
   return r;
 }
 
-// 16 bytes of packed codes (32 inputs of row r, K-step j) -> their 32 E4M3
-// bytes as chunks 2j, 2j+1 of the row's 128-byte line in a 128B-swizzled
-// K-major image (8-row atoms of 1024 bytes, chunk c of row r at c ^ (r & 7)).
-// A null source writes zero codes.
-__device__ __forceinline__ void code_line(const uint8_t* src, uint8_t* img, int r, int j) {
-  uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-  if (src) {
-    const uint4 pk = __ldg(reinterpret_cast<const uint4*>(src));
-    int4x8_to_e4m3(pk.x, lo.x, lo.y);
-    int4x8_to_e4m3(pk.y, lo.z, lo.w);
-    int4x8_to_e4m3(pk.z, hi.x, hi.y);
-    int4x8_to_e4m3(pk.w, hi.z, hi.w);
+// One image of `rows` rows (128, or 64 for a residual block): the packed
+// codes of row r, K-step j (16 bytes) at src + r*rs + j*js (a null source
+// gives zero codes, rows at or past `valid` too) -> the 128B-swizzled K-major
+// E4M3 image, row r at r*128, K-step j in chunks 2j (its codes 0..15) and
+// 2j+1 (16..31), chunk c stored at c ^ (r & 7).  The block reads the codes
+// into shared memory with 16-byte loads along the source's contiguous
+// dimension, then writes the image in address order (one 16-byte chunk per
+// thread and step): both sides coalesced.
+__device__ __forceinline__ void image_tile(uint8_t (*sm)[64], const uint8_t* src, int64_t rs, int64_t js, int rows,
+                                           int valid, uint8_t* img) {
+  for (int it = threadIdx.x; it < rows * 4; it += blockDim.x) {
+    // along r when rows are 16 bytes apart (records), else along j (activations)
+    const int r = rs == 16 ? it % rows : it >> 2, j = rs == 16 ? it / rows : it & 3;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (src && r < valid) v = __ldg(reinterpret_cast<const uint4*>(src + r * rs + j * js));
+    *reinterpret_cast<uint4*>(&sm[r][16 * j]) = v;
   }
-  uint8_t* row = img + (r >> 3) * 1024 + (r & 7) * 128;
-  *reinterpret_cast<uint4*>(row + (((2 * j) ^ (r & 7)) * 16)) = lo;
-  *reinterpret_cast<uint4*>(row + (((2 * j + 1) ^ (r & 7)) * 16)) = hi;
+  __syncthreads();
+  for (int o = threadIdx.x; o < rows * 8; o += blockDim.x) {
+    const int r = o >> 3, x = (o & 7) ^ (r & 7);  // chunk x of row r's codes: K-step x / 2, half x % 2
+    const uint2 pk = *reinterpret_cast<const uint2*>(&sm[r][8 * x]);
+    uint4 e;
+    int4x8_to_e4m3(pk.x, e.x, e.y);
+    int4x8_to_e4m3(pk.y, e.z, e.w);
+    *reinterpret_cast<uint4*>(img + 16 * o) = e;
+  }
+  __syncthreads();
 }
 
-// The pre-pass: every thread item is one code line (or one scale).
+// The pre-pass: one block per image (a base record, a residual block, or 128
+// token rows of one group's activations), then the activation scales.
 __global__ void __launch_bounds__(256) image_prep_kernel(const PrepParams p) {
+  __shared__ __align__(16) uint8_t sm[128][64];
   // The images overwrite the workspace a preceding GEMM may still read, and
   // the activations may be the preceding kernel's output.
   pdl_wait();
   pdl_trigger();
-  const int64_t total = p.n_w + p.n_r + p.n_x + p.n_s;
-  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; idx < total;
-       idx += static_cast<int64_t>(gridDim.x) * 256) {
-    int64_t k = idx;
-    if (k < p.n_w) {  // base record rec: row r, K-step j at j*2048 + r*16
-      const int64_t rec = k >> 9;
-      const int w = static_cast<int>(k & 511), j = w >> 7, r = w & 127;
-      code_line(p.wpk + rec * kWRecBytes + j * 2048 + r * 16, p.wimg + rec * kWImg, r, j);
-      continue;
+  const int64_t mtiles = p.Mt / 128;
+  const int64_t n_w = p.n_w, n_r = p.n_r, n_x = static_cast<int64_t>(p.G) * mtiles;
+  for (int64_t b = blockIdx.x; b < n_w + n_r + n_x; b += gridDim.x) {
+    if (b < n_w) {
+      image_tile(sm, p.wpk + b * kWRecBytes, 16, 2048, 128, 128, p.wimg + b * kWImg);
+    } else if (b < n_w + n_r) {
+      const int64_t e = b - n_w;
+      image_tile(sm, p.rpk + e * kRRecBytes, 16, 1024, 64, 64, p.rimg + e * kRImg);
+    } else {
+      const int64_t x = b - n_w - n_r, g = x / mtiles;
+      const int m0 = static_cast<int>(x - g * mtiles) * 128;
+      image_tile(sm, p.xq + (g * p.Mp + m0) * 64, 64, 16, 128, p.M - m0, p.ximg + (g * p.Mt + m0) * 128);
     }
-    k -= p.n_w;
-    if (k < p.n_r) {  // residual record e: row r, K-step j at j*1024 + r*16
-      const int64_t e = k >> 8;
-      const int w = static_cast<int>(k & 255), j = w >> 6, r = w & 63;
-      code_line(p.rpk + e * kRRecBytes + j * 1024 + r * 16, p.rimg + e * kRImg, r, j);
-      continue;
-    }
-    k -= p.n_r;
-    if (k < p.n_x) {  // activations: group g, token m, K-step j
-      const int j = static_cast<int>(k & 3);
-      const int64_t gm = k >> 2;
-      const int64_t g = gm / p.Mt;
-      const int m = static_cast<int>(gm - g * p.Mt);
-      code_line(m < p.M ? p.xq + (g * p.Mp + m) * 64 + j * 16 : nullptr, p.ximg + g * p.Mt * 128, m, j);
-      continue;
-    }
-    k -= p.n_x;
-    {  // activation scales as fp32, zero past M
-      const int64_t g = k / p.Mt;
-      const int m = static_cast<int>(k - g * p.Mt);
-      p.sxf[k] = m < p.M ? __half2float(__ushort_as_half(p.xs[g * p.Mp + m])) : 0.0f;
-    }
+  }
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (int64_t k = tid; k < p.n_s; k += static_cast<int64_t>(gridDim.x) * blockDim.x) {  // scales as fp32, zero past M
+    const int64_t g = k / p.Mt;
+    const int m = static_cast<int>(k - g * p.Mt);
+    p.sxf[k] = m < p.M ? __half2float(__ushort_as_half(p.xs[g * p.Mp + m])) : 0.0f;
   }
 }
 
@@ -858,14 +858,15 @@ mq_status image_gemm_launch(bool* handled, const uint8_t* xq, const uint16_t* xs
   pp.Mp = Mp;
   pp.Mt = pl.Mt;
   pp.G = pl.G;
-  pp.n_w = static_cast<int64_t>(pl.tiles_n) * pl.G * 512;
-  pp.n_r = nnzb * 256;
-  pp.n_x = static_cast<int64_t>(pl.G) * pl.Mt * 4;
+  pp.n_w = static_cast<int64_t>(pl.tiles_n) * pl.G;  // weight images
+  pp.n_r = nnzb;                                      // residual images
+  pp.n_x = static_cast<int64_t>(pl.G) * pl.Mt / 128;  // activation images of 128 token rows
   pp.n_s = static_cast<int64_t>(pl.G) * pl.Mt;
   {
-    const int64_t total = pp.n_w + pp.n_r + pp.n_x + pp.n_s;
+    const int64_t images = pp.n_w + pp.n_r + pp.n_x;
     const int sms = img_sms();
-    const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256, (sms > 0 ? sms : 152) * 16));
+    // one block per image, at most one wave (8 blocks of 256 threads per SM)
+    const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(images, (sms > 0 ? sms : 152) * 8));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
     cfg.blockDim = dim3(256, 1, 1);
