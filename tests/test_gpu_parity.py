@@ -425,6 +425,26 @@ def test_fused_quantizer_corners(variant, M, x_dtype, pad, monkeypatch):
     check_close(y32.cpu().numpy(), y, a)
 
 
+@pytest.mark.parametrize("M,K,x_dtype,pad", [(12, 512, "f16", 0), (12, 512, "bf16", 0), (37, 2304, "f16", 4),
+                                             (300, 640, "bf16", 4)])
+def test_quantize_act_corners(M, K, x_dtype, pad):
+    """The stand-alone quantizer (a half-warp per token and group, rounding with
+    a refined reciprocal instead of a division) against the oracle bit for bit
+    on the corner rows: exact ties, ties moved one ulp, subnormal and saturating
+    scales, zero groups; 18 groups (a block whose second half-warps have no
+    group), padding tokens, and a row stride of K + 4 elements."""
+    isb = x_dtype == "bf16"
+    x = _quantizer_corner_rows(M, K, x_dtype, seed=3 * M + pad)
+    xw = np.zeros((M, K + pad), np.uint16)
+    xw[:, :K] = x
+    xq, xs = mq.quantize_act(dev_act(xw, isb)[:, :K])
+    mq.check_device_error()
+    qx, sx = O.quantize_act(x, isb)
+    assert np.array_equal(logical_xq(xq, M), O.pack_nibbles(qx))
+    assert np.array_equal(logical_xs(xs, M), sx)
+    assert not host_u16(xs)[:, M:].any() and not xq_padding(xq, M).any()
+
+
 @pytest.mark.parametrize("M,N,K,budget", [(4, 4096, 4096, 0.10), (32, 4096, 4096, 0.10), (8, 1536, 4096, 0.3),
                                           (16, 640, 1024, 1.0), (3, 2048, 512, 0.2)])
 def test_cluster_mode_matches_oracle(M, N, K, budget, monkeypatch):
