@@ -73,11 +73,16 @@ struct ICfg {
   static constexpr int kUG = 2;         // groups per unit
   static constexpr int kA = kWImg;      // weight image of a group
   static constexpr int kB = TN * 128;   // activation image of a group
-  static constexpr int kGB = kA + kB;   // a group's part of a stage
-  static constexpr int kStageBytes = kUG * kGB;
-  static constexpr int kStages = 2;
-  // residual images of one group (top + bottom block, 16 KiB each); half the slots per producer
-  static constexpr int kRSlots = 4;
+  // One ring of 16 KiB slots holds every image a unit needs, in order: the
+  // weight and activation images of each group, then the residual image (top
+  // block, bottom block) of each group that has one.  A unit takes 2 slots per
+  // group and 1 per group with residual blocks, so the ring keeps three units
+  // without residual in flight, and residual blocks take room only where the
+  // block list has them.
+  static constexpr int kSlot = 16384;
+  static_assert(kA == kSlot && kB == kSlot && 2 * kRImg == kSlot, "one image per slot");
+  static constexpr int kSlots = 12;
+  static constexpr int kUnitBars = 8;   // full / done barriers, by unit (more than the units in flight)
   static constexpr int kScSlots = 8;
   // scale slot, per group: weight scales [128] fp16, residual scales [2][64] fp16, activation scales [TN] fp32
   static constexpr int sWS = 0, sRS = 256, sSX = 512;
@@ -87,8 +92,8 @@ struct ICfg {
   static constexpr int kDSlots = 512 / kDCols;   // TMEM accumulators (all 512 columns)
   static constexpr int kCols = TN / 4;           // tokens per drain thread
   static constexpr int kThreads = 32 * (kWarpDrain0 + kDrainWarps);
-  static constexpr int kRingBytes = kStages * kStageBytes;
-  static constexpr int kSmemBytes = kRingBytes + kRSlots * 2 * kRImg + kScSlots * kScBytes + 1024 /*align*/;
+  static constexpr int kRingBytes = kSlots * kSlot;
+  static constexpr int kSmemBytes = kRingBytes + kScSlots * kScBytes + 1024 /*align*/;
   static_assert(kSmemBytes + 12 * 1024 <= 227 * 1024, "shared memory budget");
   static_assert(kCols == 32, "a drain thread loads a group's dots in one 32-column load");
   static_assert(kDSlots >= 2, "two accumulators at least");
@@ -133,22 +138,20 @@ struct ImgParams {
   uint32_t* err;
 };
 
-template <int NS, int NR, int NSC, int ND>
+template <int NU, int NSC, int ND>
 struct __align__(8) ICtl {
-  uint64_t full[NS];
-  uint64_t empty[NS];
+  uint64_t full[NU];  // unit i (by i % NU): its images have landed
+  uint64_t done[NU];  // unit i: its MMAs have completed (its slots are free)
   uint64_t sc_full[NSC];
   uint64_t sc_empty[NSC];
-  uint64_t r_full[NR];
-  uint64_t r_empty[NR];
   uint64_t d_full[ND];
   uint64_t d_empty[ND];
   uint64_t drain_bar;  // bounded barrier of the drain threads
   uint64_t red_bar;    // bulk loads of stream-K pieces
   uint64_t map_ready;  // residual map built
-  int32_t blk[NS][2][2];    // per group of the stage's unit: CSR entries of its top / bottom residual block, or -1
+  int32_t blk[NU][2][2];    // per group of unit i: CSR entries of its top / bottom residual block, or -1
   int32_t sblk[NSC][2][2];  // the same, for the drain (lives as long as the scale slot)
-  int32_t ng[NS];           // groups of the stage's unit (2, or 1 at the end of a tile of odd G)
+  int32_t ng[NU];           // groups of unit i (2, or 1 at the end of a tile of odd G)
   int32_t sng[NSC];
   int64_t deferred[2];      // cut tiles this CTA finishes (at most its first and last)
   uint32_t tmem_base;
@@ -250,19 +253,17 @@ __global__ void __launch_bounds__(256) image_prep_kernel(const PrepParams p) {
 template <int TN, bool kDebug>
 __global__ void __launch_bounds__(ICfg<TN>::kThreads, 1) image_gemm_kernel(const ImgParams p) {
   using C = ICfg<TN>;
-  constexpr int NS = C::kStages, NR = C::kRSlots, NSC = C::kScSlots, ND = C::kDSlots, UG = C::kUG;
-  constexpr int NRP = NR / 2;  // residual slots per producer
+  constexpr int NSL = C::kSlots, NU = C::kUnitBars, NSC = C::kScSlots, ND = C::kDSlots, UG = C::kUG;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ ICtl<NS, NR, NSC, ND> ctl;
+  __shared__ ICtl<NU, NSC, ND> ctl;
   // per local unit and group: CSR entry of the top / bottom block, or -1
   __shared__ int32_t res_map[UG][2][kImgMaxUnitsPerCta];
-  // per local unit and group with residual blocks: its position among those of units of the same parity
-  // (the same producer), which picks its slot of the residual ring
-  __shared__ int16_t res_ord[UG][kImgMaxUnitsPerCta];
+  // per local unit: its first slot, counted over the CTA's units (slot ubase[i] % NSL of the ring)
+  __shared__ int32_t ubase[kImgMaxUnitsPerCta + 1];
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* rring = smem + C::kRingBytes;
-  uint8_t* scring = rring + NR * 2 * kRImg;
+  uint8_t* scring = smem + C::kRingBytes;
+  auto slot = [&](int64_t k) { return smem + static_cast<int>(k % NSL) * C::kSlot; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t U = p.units, P = p.ctas, c = blockIdx.x;
   const int64_t u0 = c * U / P, u1 = (c + 1) * U / P;
@@ -272,17 +273,13 @@ __global__ void __launch_bounds__(ICfg<TN>::kThreads, 1) image_gemm_kernel(const
   const uint64_t tmo = p.timeout_ns;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
+    for (int s = 0; s < NU; ++s) {
       mbar_init(&ctl.full[s], 1);
-      mbar_init(&ctl.empty[s], 1);  // the MMA commit
+      mbar_init(&ctl.done[s], 1);  // the MMA commit
     }
     for (int s = 0; s < NSC; ++s) {
       mbar_init(&ctl.sc_full[s], 1);
       mbar_init(&ctl.sc_empty[s], kDrainWarps);
-    }
-    for (int s = 0; s < NR; ++s) {
-      mbar_init(&ctl.r_full[s], 1);
-      mbar_init(&ctl.r_empty[s], 1);  // the MMA commit
     }
     for (int s = 0; s < ND; ++s) {
       mbar_init(&ctl.d_full[s], 1);
@@ -336,31 +333,30 @@ __global__ void __launch_bounds__(ICfg<TN>::kThreads, 1) image_gemm_kernel(const
     // 2 weight scales, 3 activation scales, 4 / 5 top / bottom residual scales, 6 / 7 their images)
     const int gq = (lane >> 3) & 1, kind = lane & 7, hh = kind & 1;
     for (int i = pw; ok && i < nunits; i += 2, advance(q), advance(q)) {
-      const int st = i % NS, sc = i % NSC;
+      const int ub = i % NU, sc = i % NSC;
       const int g0 = UG * q.j, t = q.t, m0 = q.mt * TN;
       const int ng = min(UG, G - g0);
+      const int base = ubase[i], nsl = ubase[i + 1] - base;  // the unit's slots: [base, base + nsl) of the ring
       // Everything about the unit's copies is worked out before the waits: a
-      // stage is refilled only after its previous unit's MMAs, so the time
-      // from that release to the copies' issue is on the critical path.
-      // This lane's group: residual entries, slot, and whether it has blocks.
-      const bool mine = lane < 8 * ng;
-      const int ea = mine ? res_map[gq][0][i] : -1, eb = mine ? res_map[gq][1][i] : -1;
-      const bool has = ea >= 0 || eb >= 0;
-      const int ro = has ? res_ord[gq][i] : 0, rs = pw * NRP + ro % NRP;
-      const int nsr = __popc(__ballot_sync(0xFFFFFFFFu, (kind == 4 || kind == 5) && (hh ? eb : ea) >= 0));
-      int blk0[UG][2];  // lane 0: what the consumers read after its arrival
+      // slot is refilled only after the MMAs that read it, so the time from
+      // that release to the copies' issue is on the critical path.
+      int e4[UG][2];  // residual entries of both groups (-1: none)
 #pragma unroll
       for (int g2 = 0; g2 < UG; ++g2)
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) blk0[g2][h2] = (lane == 0 && g2 < ng) ? res_map[g2][h2][i] : -1;
+        for (int h2 = 0; h2 < 2; ++h2) e4[g2][h2] = g2 < ng ? res_map[g2][h2][i] : -1;
+      const bool hr0 = e4[0][0] >= 0 || e4[0][1] >= 0;
+      const int nblk = (e4[0][0] >= 0) + (e4[0][1] >= 0) + (e4[1][0] >= 0) + (e4[1][1] >= 0);
+      // this lane's copy
+      const bool mine = lane < 8 * ng;
+      const int e = mine ? (gq ? e4[1][hh] : e4[0][hh]) : -1;
+      const int nsr = __popc(__ballot_sync(0xFFFFFFFFu, (kind == 4 || kind == 5) && e >= 0));
       // The unit's copies, one per lane, leave in one warp instruction (a bulk
       // copy costs its issuing instruction a fixed time); selects, not a
       // switch: divergent lanes would resolve an indirect branch one after another.
-      uint8_t* sb = smem + st * C::kStageBytes + gq * C::kGB;
       uint8_t* scb = scring + sc * C::kScBytes + gq * C::kScGroup;
       const int g = g0 + gq;
       const int64_t wrec = static_cast<int64_t>(t) * G + g;
-      const int e = hh ? eb : ea;
       const int64_t ee = e >= 0 ? e : 0;
       const uint8_t* s_a = p.wimg + wrec * kWImg;
       const uint8_t* s_b = p.ximg + (static_cast<int64_t>(g) * p.Mt + m0) * 128;
@@ -369,38 +365,42 @@ __global__ void __launch_bounds__(ICfg<TN>::kThreads, 1) image_gemm_kernel(const
       const uint8_t* s_rs = p.rpk + ee * kRRecBytes + kRRecScales;
       const uint8_t* s_ri = p.rimg + ee * kRImg;
       const uint8_t* src = kind == 0 ? s_a : kind == 1 ? s_b : kind == 2 ? s_ws : kind == 3 ? s_sx : kind < 6 ? s_rs : s_ri;
-      uint8_t* dst = kind == 0   ? sb
-                     : kind == 1 ? sb + C::kA
+      // slots of the unit: weight, activation image per group, then one residual image per group with blocks
+      const int ks = kind < 2 ? 2 * gq + kind : 2 * ng + (gq && hr0 ? 1 : 0);
+      uint8_t* dst = kind < 2    ? slot(base + ks)
                      : kind == 2 ? scb + C::sWS
                      : kind == 3 ? scb + C::sSX
                      : kind < 6  ? scb + C::sRS + hh * 128
-                                 : rring + rs * 2 * kRImg + hh * kRImg;
-      const uint32_t bytes = kind == 0   ? static_cast<uint32_t>(C::kA)
-                             : kind == 1 ? static_cast<uint32_t>(C::kB)
+                                 : slot(base + ks) + hh * kRImg;
+      const uint32_t bytes = kind < 2    ? static_cast<uint32_t>(C::kSlot)
                              : kind == 2 ? 256u
                              : kind == 3 ? static_cast<uint32_t>(TN * 4)
                              : kind < 6  ? 128u
                                          : static_cast<uint32_t>(kRImg);
-      uint64_t* bar = kind < 2 ? &ctl.full[st] : kind < 6 ? &ctl.sc_full[sc] : &ctl.r_full[rs];
+      uint64_t* bar = (kind < 2 || kind >= 6) ? &ctl.full[ub] : &ctl.sc_full[sc];
       const bool issue = mine && (kind < 4 || e >= 0);
       int wait_ok = 1;
-      if (kind == 0 && lane < 8 * ng) {  // lanes 0 and 8: the stage, the scale slot, this group's residual slot
-        if (lane == 0 && i >= NS) wait_ok = mbar_wait(&ctl.empty[st], ((i / NS) & 1) ^ 1, abort_flag, tmo, p.err);
-        if (lane == 0 && wait_ok && i >= NSC)
-          wait_ok = mbar_wait(&ctl.sc_empty[sc], ((i / NSC) & 1) ^ 1, abort_flag, tmo, p.err);
-        if (wait_ok && has && ro >= NRP)
-          wait_ok = mbar_wait(&ctl.r_empty[rs], ((ro / NRP) & 1) ^ 1, abort_flag, tmo, p.err);
+      if (lane == 0) {
+        // The ring's slots are released in unit order (one MMA thread commits
+        // them), so the slots are free once the unit that last held the
+        // unit's last slot is done.
+        const int prev = base + nsl - 1 - NSL;
+        if (prev >= 0) {
+          int o = i - 1;
+          while (o > 0 && ubase[o] > prev) --o;
+          wait_ok = mbar_wait(&ctl.done[o % NU], (o / NU) & 1, abort_flag, tmo, p.err);
+        }
+        if (wait_ok && i >= NSC) wait_ok = mbar_wait(&ctl.sc_empty[sc], ((i / NSC) & 1) ^ 1, abort_flag, tmo, p.err);
       }
-      ok = __all_sync(0xFFFFFFFFu, wait_ok);
+      ok = __shfl_sync(0xFFFFFFFFu, wait_ok, 0);
       if (!ok) break;
-      if (kind == 0 && has) mbar_arrive_expect_tx(&ctl.r_full[rs], ((ea >= 0) + (eb >= 0)) * kRImg);
-      if (lane == 0) {  // one thread writes what the consumers read after this arrival
+      if (lane == 0) {  // one thread writes what the consumers read after its arrivals
 #pragma unroll
         for (int g2 = 0; g2 < UG; ++g2)
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) ctl.blk[st][g2][h2] = ctl.sblk[sc][g2][h2] = blk0[g2][h2];
-        ctl.ng[st] = ctl.sng[sc] = ng;
-        mbar_arrive_expect_tx(&ctl.full[st], ng * C::kGB);
+          for (int h2 = 0; h2 < 2; ++h2) ctl.blk[ub][g2][h2] = ctl.sblk[sc][g2][h2] = e4[g2][h2];
+        ctl.ng[ub] = ctl.sng[sc] = ng;
+        mbar_arrive_expect_tx(&ctl.full[ub], ng * 2 * C::kSlot + nblk * kRImg);
         mbar_arrive_expect_tx(&ctl.sc_full[sc], ng * (256 + TN * 4) + nsr * 128);
       }
       __syncwarp();
@@ -432,29 +432,32 @@ __global__ void __launch_bounds__(ICfg<TN>::kThreads, 1) image_gemm_kernel(const
       }
     }
     __syncwarp();
-    {  // ordinal of each group with residual blocks among those of units of its parity, in
-       // (unit, group) order (lane l scans a contiguous chunk of units)
+    {  // each unit's first slot: 2 slots per group and 1 per group with residual blocks, summed in
+       // unit order (lane l scans a contiguous chunk of units)
       const int chunk = (nunits + 31) / 32;
       const int l0 = min(nunits, lane * chunk), l1 = min(nunits, l0 + chunk);
-      int cnt[2] = {0, 0};
-      for (int lu = l0; lu < l1; ++lu)
+      auto nsl = [&](int lu) {
+        const int j = static_cast<int>((u0 + lu) % UPT);
+        const int ng = min(UG, G - UG * j);
+        int n = 2 * ng;
 #pragma unroll
-        for (int gq = 0; gq < UG; ++gq) cnt[lu & 1] += (res_map[gq][0][lu] >= 0 || res_map[gq][1][lu] >= 0);
-      int pos[2];
+        for (int gq = 0; gq < UG; ++gq) n += (res_map[gq][0][lu] >= 0 || res_map[gq][1][lu] >= 0);
+        return n;
+      };
+      int cnt = 0;
+      for (int lu = l0; lu < l1; ++lu) cnt += nsl(lu);
+      int incl = cnt;
 #pragma unroll
-      for (int par = 0; par < 2; ++par) {
-        int incl = cnt[par];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-          if (lane >= o) incl += v;
-        }
-        pos[par] = incl - cnt[par];
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
       }
-      for (int lu = l0; lu < l1; ++lu)
-#pragma unroll
-        for (int gq = 0; gq < UG; ++gq)
-          if (res_map[gq][0][lu] >= 0 || res_map[gq][1][lu] >= 0) res_ord[gq][lu] = static_cast<int16_t>(pos[lu & 1]++);
+      int pos = incl - cnt;
+      for (int lu = l0; lu < l1; ++lu) {
+        ubase[lu] = pos;
+        pos += nsl(lu);
+      }
+      if (lane == 31) ubase[nunits] = incl;
     }
     __syncwarp();
     mbar_arrive(&ctl.map_ready);
@@ -462,39 +465,31 @@ __global__ void __launch_bounds__(ICfg<TN>::kThreads, 1) image_gemm_kernel(const
       int item = 0;
       bool ok = true;
       for (int i = 0; i < nunits && ok; ++i) {
-        const int st = i % NS;
-        if (!mbar_wait(&ctl.full[st], (i / NS) & 1, abort_flag, tmo, p.err)) break;
-        const int ng = ctl.ng[st];
+        const int ub = i % NU;
+        if (!mbar_wait(&ctl.full[ub], (i / NU) & 1, abort_flag, tmo, p.err)) break;
+        const int ng = ctl.ng[ub];
         bool hr[UG];
 #pragma unroll
-        for (int gq = 0; gq < UG; ++gq) hr[gq] = gq < ng && (ctl.blk[st][gq][0] >= 0 || ctl.blk[st][gq][1] >= 0);
+        for (int gq = 0; gq < UG; ++gq) hr[gq] = gq < ng && (ctl.blk[ub][gq][0] >= 0 || ctl.blk[ub][gq][1] >= 0);
         const bool any_r = hr[0] || hr[1];
-        const uint32_t s_base = smem_u32(smem + st * C::kStageBytes);
+        const int base = ubase[i];
         for (int k = 0; k < 1 + any_r; ++k, ++item) {
           const int d = item % ND;
           if (!mbar_wait(&ctl.d_empty[d], ((item / ND) & 1) ^ 1, abort_flag, tmo, p.err)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll
           for (int gq = 0; gq < UG; ++gq) {
             if (gq >= ng || (k == 1 && !hr[gq])) continue;
-            const uint32_t b = s_base + gq * C::kGB + C::kA;
-            uint32_t a = s_base + gq * C::kGB;
-            int rs = 0;
-            if (k == 1) {  // the residual slot of this group (its unit's producer's half of the ring)
-              const int ro = res_ord[gq][i];
-              rs = (i & 1) * NRP + ro % NRP;
-              if (!mbar_wait(&ctl.r_full[rs], (ro / NRP) & 1, abort_flag, tmo, p.err)) { ok = false; break; }
-              a = smem_u32(rring + rs * 2 * kRImg);
-            }
-            tc_fence_after();
+            const uint32_t b = smem_u32(slot(base + 2 * gq + 1));
+            // the weight image, or the group's residual image (after the unit's weight and activation images)
+            const uint32_t a = smem_u32(slot(k == 0 ? base + 2 * gq : base + 2 * ng + (gq && hr[0] ? 1 : 0)));
             const uint32_t d_col = tmem + d * C::kDCols + gq * TN;
 #pragma unroll
             for (int j = 0; j < 4; ++j) img_mma(d_col, img_desc(a + 32 * j), img_desc(b + 32 * j), C::kIdesc, j > 0);
-            if (k == 1) tc_commit(&ctl.r_empty[rs]);
           }
-          if (!ok) break;
           tc_commit(&ctl.d_full[d]);
         }
-        if (ok) tc_commit(&ctl.empty[st]);
+        if (ok) tc_commit(&ctl.done[ub]);  // the unit's slots are free once its MMAs complete
       }
       // the issued MMAs finish before TMEM can be released
       if (item > 0) {
