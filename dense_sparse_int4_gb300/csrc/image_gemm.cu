@@ -23,18 +23,20 @@
 // and loop once per two groups.  Roles per CTA (one CTA per SM, persistent
 // stream-K over units; tiles are token-tile major, so that the CTAs running at
 // one time read the same few weight tiles and every image stays in L2):
-//   warps 0, 2 producers, alternating units: a stage is one unit's weight and
-//              activation images (64 KiB); the drain's scales go to a ring of
-//              their own; a group with residual blocks also brings the blocks'
-//              images (top half at 0, bottom half at 8 KiB) into a slot of the
-//              residual ring (each producer its own half of the slots).  The
-//              copies of a unit (up to 16) leave in one warp instruction.
-//   warp 1     builds the CTA's residual map, then one thread issues per unit
-//              4 MMAs (K = 32 each) per group into a TMEM accumulator of 256
-//              columns (the two groups side by side), and, where a group has
-//              residual blocks, 4 more from its residual slot into the next
-//              accumulator (M = 128: a half without a block gives rows nobody
-//              reads).
+//   warps 0, 2 producers, alternating units: one ring of 16 KiB slots takes
+//              each unit's images in order (weight and activation image per
+//              group, then one residual image (top block at 0, bottom block at
+//              8 KiB) per group that has blocks); the drain's scales go to a
+//              ring of their own.  Slots are released in unit order, so a
+//              unit's slots are free once the unit that last held its last
+//              slot is done.  The copies of a unit (up to 16) leave in one warp
+//              instruction, their addresses worked out before the waits.
+//   warp 1     builds the CTA's residual map and each unit's first slot,
+//              then one thread issues per unit 4 MMAs (K = 32 each) per group
+//              into a TMEM accumulator of 256 columns (the two groups side by
+//              side), and, where a group has residual blocks, 4 more from its
+//              residual image into the next accumulator (M = 128: a half
+//              without a block gives rows nobody reads).
 //   warps 3-18 drain, 4 warps per TMEM lane quarter, TN/4 tokens each: load a
 //              group's dots (16 columns at a time), free the accumulator after
 //              the last load, acc += sx * (s * D) in packed fp32 pairs; at tile
