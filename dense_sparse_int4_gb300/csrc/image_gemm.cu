@@ -37,8 +37,9 @@
 //              side), and, where a group has residual blocks, 4 more from its
 //              residual image into the next accumulator (M = 128: a half
 //              without a block gives rows nobody reads).
-//   warps 3-18 drain, 4 warps per TMEM lane quarter, TN/4 tokens each: load a
-//              group's dots (16 columns at a time), free the accumulator after
+//   warps 3-10 drain, 2 warps per TMEM lane quarter, TN/2 tokens each (11
+//              warps leave a thread 168 registers): load a group's dots (32
+//              columns at a time), free the accumulator after
 //              the last load, acc += sx * (s * D) in packed fp32 pairs; at tile
 //              ends store Y or a stream-K piece.  Tiles cut by a CTA range are
 //              finished by the CTA whose piece arrives last, summing the pieces
@@ -67,8 +68,8 @@ constexpr int kImgPlanCtasNoDevice = 152;
 constexpr int kImgMinUnitsPerCta = 4;
 constexpr int kWImg = 16384;  // image of one (weight tile, group): 128 rows x 128 bytes
 constexpr int kRImg = 8192;   // image of one residual block: 64 rows x 128 bytes
-// warps 0 and 2 producers (alternating units), 1 block list + MMA, 3-18 drain
-constexpr int kWarpProd = 0, kWarpMma = 1, kWarpProd2 = 2, kWarpDrain0 = 3, kDrainWarps = 16;
+// warps 0 and 2 producers (alternating units), 1 block list + MMA, 3-10 drain
+constexpr int kWarpProd = 0, kWarpMma = 1, kWarpProd2 = 2, kWarpDrain0 = 3, kDrainWarps = 8;
 
 template <int TN>
 struct ICfg {
@@ -92,12 +93,12 @@ struct ICfg {
   static constexpr int kScBytes = kUG * kScGroup;
   static constexpr int kDCols = kUG * TN;        // TMEM columns of one item (a unit's groups side by side)
   static constexpr int kDSlots = 512 / kDCols;   // TMEM accumulators (all 512 columns)
-  static constexpr int kCols = TN / 4;           // tokens per drain thread
+  static constexpr int kCols = TN * 4 / kDrainWarps;  // tokens per drain thread (4 lane quarters)
   static constexpr int kThreads = 32 * (kWarpDrain0 + kDrainWarps);
   static constexpr int kRingBytes = kSlots * kSlot;
   static constexpr int kSmemBytes = kRingBytes + kScSlots * kScBytes + 1024 /*align*/;
   static_assert(kSmemBytes + 12 * 1024 <= 227 * 1024, "shared memory budget");
-  static_assert(kCols == 32, "a drain thread loads a group's dots in one 32-column load");
+  static_assert(kCols % 32 == 0, "a drain thread loads its dots in 32-column chunks");
   static_assert(kDSlots >= 2, "two accumulators at least");
   // instruction descriptor: D f32, A/B E4M3, both K-major, N = TN, M = 128
   static constexpr uint32_t kIdesc =
@@ -505,7 +506,7 @@ __global__ void __launch_bounds__(ICfg<TN>::kThreads, 1) image_gemm_kernel(const
     pdl_wait();  // Y and the workspace pieces may still be in use by the preceding kernel
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;              // weight row (TMEM lane)
-    const int sub = (warp - kWarpDrain0) >> 2;      // token quarter of the tile
+    const int sub = (warp - kWarpDrain0) >> 2;      // token slice of the tile (kCols tokens)
     const int c0 = sub * C::kCols;                  // first token column of this thread
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const int half = r >> 6;
@@ -564,12 +565,14 @@ __global__ void __launch_bounds__(ICfg<TN>::kThreads, 1) image_gemm_kernel(const
           const bool active = gq < ng && (k == 0 || e_mine[gq] >= 0);  // warp-uniform: a warp's rows sit in one half
           const uint8_t* scg = scb + gq * C::kScGroup;
           if constexpr (kDebug) {
+#pragma unroll
+           for (int dc = 0; dc < C::kCols / 32; ++dc) {
             uint32_t dv[32];
             if (active) {
-              tmem_ld32(tmem + lane_base + d * C::kDCols + gq * TN + c0, dv);
+              tmem_ld32(tmem + lane_base + d * C::kDCols + gq * TN + c0 + 32 * dc, dv);
               tc_wait_ld();
             }
-            if (gq == UG - 1) {  // every dot of the item this warp reads is in registers: free the accumulator
+            if (gq == UG - 1 && dc == C::kCols / 32 - 1) {  // every dot of the item this warp reads is in registers
               tc_fence_before();
               __syncwarp();
               if (lane == 0) mbar_arrive(&ctl.d_empty[d]);
@@ -578,7 +581,7 @@ __global__ void __launch_bounds__(ICfg<TN>::kThreads, 1) image_gemm_kernel(const
             const int g = g0 + gq;
 #pragma unroll
             for (int q2 = 0; q2 < 32; ++q2) {
-              const int m = m0 + c0 + q2;
+              const int m = m0 + c0 + 32 * dc + q2;
               if (m < p.M) {
                 const int32_t v = static_cast<int32_t>(__uint_as_float(dv[q2]));
                 if (k == 0)
@@ -587,8 +590,10 @@ __global__ void __launch_bounds__(ICfg<TN>::kThreads, 1) image_gemm_kernel(const
                   p.dots_r[(static_cast<int64_t>(m) * p.nnzb + e_mine[gq]) * 64 + (r & 63)] = v;
               }
             }
+           }
           } else {
-            // 16 columns at a time: fewer live registers than one 32-column load (measured faster)
+            // 32 columns at a time (with 18 warps' 96 registers a thread, 16 at a time measured faster;
+            // with 11 warps and 168, 32)
             const uint32_t sxa = smem_u32(scg + C::sSX) + c0 * 4;
             uint64_t s2 = 0;
             if (active) {
@@ -598,26 +603,26 @@ __global__ void __launch_bounds__(ICfg<TN>::kThreads, 1) image_gemm_kernel(const
               s2 = p2(s, s);
             }
 #pragma unroll
-            for (int hx = 0; hx < 2; ++hx) {
-              uint32_t dv[16];
+            for (int hx = 0; hx < C::kCols / 32; ++hx) {
+              uint32_t dv[32];
               if (active) {
-                tmem_ld16(tmem + lane_base + d * C::kDCols + gq * TN + c0 + 16 * hx, dv);
+                tmem_ld32(tmem + lane_base + d * C::kDCols + gq * TN + c0 + 32 * hx, dv);
                 tc_wait_ld();
               }
-              if (gq == UG - 1 && hx == 1) {  // every dot of the item this warp reads is in registers
+              if (gq == UG - 1 && hx == C::kCols / 32 - 1) {  // every dot of the item this warp reads is in registers
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl.d_empty[d]);
               }
               if (!active) continue;
 #pragma unroll
-              for (int j2 = 0; j2 < 4; ++j2) {
-                uint64_t sx0, sx1;  // activation scales of token pairs 8 hx + 2 j2, + 1 of this thread's columns
-                asm volatile("ld.shared.v2.u64 {%0, %1}, [%2];" : "=l"(sx0), "=l"(sx1) : "r"(sxa + 64 * hx + 16 * j2));
+              for (int j2 = 0; j2 < 8; ++j2) {
+                uint64_t sx0, sx1;  // activation scales of token pairs 16 hx + 2 j2, + 1 of this thread's columns
+                asm volatile("ld.shared.v2.u64 {%0, %1}, [%2];" : "=l"(sx0), "=l"(sx1) : "r"(sxa + 128 * hx + 16 * j2));
                 const uint64_t t0 = mul2(p2(__uint_as_float(dv[4 * j2]), __uint_as_float(dv[4 * j2 + 1])), s2);
                 const uint64_t t1 = mul2(p2(__uint_as_float(dv[4 * j2 + 2]), __uint_as_float(dv[4 * j2 + 3])), s2);
-                acc[8 * hx + 2 * j2] = fma2(sx0, t0, acc[8 * hx + 2 * j2]);
-                acc[8 * hx + 2 * j2 + 1] = fma2(sx1, t1, acc[8 * hx + 2 * j2 + 1]);
+                acc[16 * hx + 2 * j2] = fma2(sx0, t0, acc[16 * hx + 2 * j2]);
+                acc[16 * hx + 2 * j2 + 1] = fma2(sx1, t1, acc[16 * hx + 2 * j2 + 1]);
               }
             }
           }
