@@ -45,7 +45,7 @@ def _noalloc(L, xq, xs, M, pl, out):
 
 
 @pytest.mark.parametrize("M,N,K,budget", [(4, 512, 512, 0.10), (32, 4096, 4096, 0.10), (17, 1024, 2048, 0.30),
-                                          (40, 512, 1024, 0.20), (64, 1024, 512, 0.10)])
+                                          (40, 512, 1024, 0.20), (64, 1024, 512, 0.10), (160, 512, 640, 0.20)])
 def test_noalloc_matches_oracle_twice(lib, M, N, K, budget):
     from dense_sparse_int4_gb300 import mq, synth
     from tests.gpu_helpers import check_close, dev_half
@@ -58,6 +58,8 @@ def test_noalloc_matches_oracle_twice(lib, M, N, K, budget):
     qx, sx = O.quantize_act(x, False)
     y, a = O.linear(qx, sx, O.prepare(w, xcal, False, budget))
     assert mq.gemm_plan(M, N, K)["decode"] == (M <= 32)
+    # 160 tokens: the image form, whose operand images fit the fixed scratch at this size
+    assert (mq.gemm_plan(M, N, K)["variant"] == "image") == (M >= 128)
     assert int(lib.mq_gemm_workspace_bytes(M, N, K)) > 0
     for _ in range(2):
         out = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
