@@ -159,7 +159,13 @@ mq_status mq_pack_weights(const uint16_t* w, int64_t N, int64_t K, const int32_t
 /* Metodologia 3).                                                           */
 /* ------------------------------------------------------------------------ */
 
-/* Bytes of device workspace mq_w4a4_residual_gemm needs for (M, N, K). */
+/* Bytes of device workspace mq_w4a4_residual_gemm needs for (M, N, K).
+ * From 128 tokens this includes the general kernel's image form: its
+ * operand images (N*K bytes of E4M3 weights, residual images sized for the
+ * densest block list, N*K bytes, and 128 bytes per padded token and
+ * 128-input group), so the size does not depend on the block list.  A
+ * caller that gives the GEMM less (mq_w4a4_residual_gemm_noalloc, whose
+ * scratch is fixed) gets the converter form where the images do not fit. */
 size_t mq_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /* Zero a GEMM workspace before its first use (and after an MQ_ERR_TIMEOUT);
@@ -289,13 +295,21 @@ mq_status mq_debug_group_dots(const uint8_t* xq, const uint16_t* xs, int64_t M, 
  *             in a short kernel of its own first), 5 = its column form (warp
  *             MMA with the activation quantizer inside the GEMM) and 3 = its
  *             tensor-memory form (taken when the environment variable
- *             MQ_DECODE_VARIANT is "col" or "tc"); 0 = the general kernel;
+ *             MQ_DECODE_VARIANT is "col" or "tc"); 0 = the general kernel
+ *             in its converter form (33 to 127 tokens, or any M > 32 when
+ *             the environment variable MQ_GENERAL_FORM is "conv"); 6 = the
+ *             general kernel in its image form (a pre-pass writes the E4M3
+ *             operand images, the GEMM runs both MMA operands from shared
+ *             memory: from 128 tokens, or any M > 32 when MQ_GENERAL_FORM
+ *             is "image"; it needs the workspace mq_gemm_workspace_bytes
+ *             gives);
  *         for the decode kernel, [1] tokens per tile (8, 16 or 32), [2] CTAs
  *         per thread-block cluster (1 without clusters; the warp-MMA form
  *         gives each weight tile a cluster of this many CTAs when that uses
  *         about as many SMs as stream-K, unless MQ_DECODE_CLUSTER is "0"),
- *         [3] CTAs launched, [4] weight stages in shared memory; zeros for
- *         the general kernel.
+ *         [3] CTAs launched, [4] weight stages in shared memory; for the
+ *         image form [1] tokens per tile (128) and [3] CTAs launched, the
+ *         rest zero; zeros for the converter form.
  * MQ_ERR_INVALID_ARG for bad sizes (the same rules as the GEMM) or NULL info;
  * MQ_ERR_UNSUPPORTED_DEVICE if the current device is not compute capability 10.3.
  * Launches nothing.
