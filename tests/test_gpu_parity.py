@@ -326,6 +326,9 @@ def test_general_forms_match_oracle(form, M, N, K, budget, x_dtype, monkeypatch)
     (17, 2048, [512, 512], 0.50, "f16"),
     (32, 4096, [4096, 1024, 1024], 0.10, "f16"),  # q, k, v of the Llama-3-8B-shaped layer
     (40, 512, [256, 384], 0.10, "f16"),  # above 32 tokens: the quantizer, then the general kernel
+    # from 128 tokens: the image form, whose pre-pass quantizes X (and reports xq / xs) itself
+    (130, 640, [256, 384, 128], 0.20, "bf16"),
+    (300, 1024, [512], 0.10, "f16"),
 ])
 def test_fused_linear_matches_oracle(M, K, Ns, budget, x_dtype):
     """mq_w4a4_residual_linear: the quantized activations it reports are bit
@@ -417,6 +420,36 @@ def test_fused_quantizer_corners(variant, M, x_dtype, pad, monkeypatch):
     y32 = mq.fused_linear(xt, [pl], out_dtype=torch.float32, xq=xq, xs=xs)[0]
     mq.check_device_error()
     assert mq.gemm_plan(M, N, K)["variant"] == {"col": "column", "warp": "warp-mma"}[variant]
+    qx, sx = O.quantize_act(x, isb)
+    assert np.array_equal(logical_xq(xq, M), O.pack_nibbles(qx))
+    assert np.array_equal(logical_xs(xs, M), sx)
+    assert not host_u16(xs)[:, M:].any() and not xq_padding(xq, M).any()
+    y, a = O.linear(qx, sx, O.prepare(w, xcal, isb, 0.25))
+    check_close(y32.cpu().numpy(), y, a)
+
+
+@pytest.mark.parametrize("M,x_dtype,pad", [(160, "f16", 0), (160, "bf16", 4), (300, "f16", 4)])
+def test_image_prepass_quantizer_corners(M, x_dtype, pad):
+    """From 128 tokens the fused call's image pre-pass quantizes X itself (half
+    a warp per token and group): the xq / xs it reports against the oracle
+    bit for bit on the corner rows (ties, ties moved one ulp, subnormal and
+    saturating scales, zero groups; a row stride of K + pad), padding tokens
+    zero, and Y within the fp32 bound (the activation image carries the same codes)."""
+    K, N = 640, 256
+    isb = x_dtype == "bf16"
+    x = _quantizer_corner_rows(M, K, x_dtype, seed=M + 7 * pad)
+    xw = np.zeros((M, K + pad), np.uint16)
+    xw[:, :K] = x
+    xt = dev_act(xw, isb)[:, :K]
+    w = synth.weights(N, K, seed=9)
+    xcal = synth.calibration(K, seed=9, count=4, dtype=x_dtype)
+    pl = mq.prepare_linear(dev_half(w), dev_act(xcal, isb), 0.25)
+    assert mq.gemm_plan(M, N, K)["variant"] == "image"
+    Mp = mq.padded_tokens(M)
+    xq = torch.full((K // 128, Mp, 64), 0xAB, dtype=torch.uint8, device="cuda")
+    xs = torch.full((K // 128, Mp), float("nan"), dtype=torch.float16, device="cuda")
+    y32 = mq.fused_linear(xt, [pl], out_dtype=torch.float32, xq=xq, xs=xs)[0]
+    mq.check_device_error()
     qx, sx = O.quantize_act(x, isb)
     assert np.array_equal(logical_xq(xq, M), O.pack_nibbles(qx))
     assert np.array_equal(logical_xs(xs, M), sx)
