@@ -25,12 +25,6 @@ mq_status gemm_launch(const uint8_t* xq, const uint16_t* xs, int64_t M, const ui
                       int64_t ldy, mq_dtype yt, int32_t* dots_w, int32_t* dots_r, void* ws, size_t ws_bytes,
                       cudaStream_t stream);
 size_t general_workspace_bytes(int64_t M, int64_t N, int64_t K);
-bool image_form_fits(int64_t M, int64_t N, int64_t K, int64_t nnzb, const void* ws, size_t ws_bytes);
-mq_status image_gemm_launch(bool* handled, const uint8_t* xq, const uint16_t* xs, int64_t M, const uint8_t* wpk,
-                            int64_t N, int64_t K, const int32_t* row_ptr, const int32_t* col_idx, int64_t nnzb,
-                            const uint8_t* rpk, void* y, int64_t ldy, mq_dtype yt, int32_t* dots_w, int32_t* dots_r,
-                            void* ws, size_t ws_bytes, cudaStream_t stream, const void* x, mq_dtype xt,
-                            int64_t ldx, uint8_t* xq_out, uint16_t* xs_out);
 size_t zipper_workspace_bytes(int64_t M, int64_t tiles, int64_t K);
 mq_status zipper_launch(bool* handled, int nmat, const uint8_t* const* wpk, const int64_t* N,
                         const int32_t* const* row_ptr, const int32_t* const* col_idx, const int64_t* nnzb,
@@ -345,26 +339,6 @@ mq_status mq_w4a4_residual_linear(const void* x, mq_dtype xt, int64_t M, int64_t
     const mq_status zs = zipper_launch(&handled, nmat, wpk, N, rp, ci, nz, rpk, y, ldy, yt, nullptr, nullptr, x, xt,
                                        ldx, xq, xs, M, K, nullptr, nullptr, ws, ws_bytes, st);
     if (zs != MQ_OK || handled) return zs;
-  }
-  // From 128 tokens, when the image form serves every matrix: its pre-pass
-  // quantizes X into the activation image itself (the first matrix's also
-  // writes xq / xs when the caller wants them), so no quantizer launch and no
-  // round trip of the packed activations through HBM.
-  if (gen > 0) {
-    bool all = true;
-    for (int i = 0; i < nmat && all; ++i) all = image_form_fits(M, N[i], K, nz[i], ws, gen);
-    if (all) {
-      for (int i = 0; i < nmat; ++i) {
-        bool h = false;
-        if (mq_status s = image_gemm_launch(&h, nullptr, nullptr, M, wpk[i], N[i], K, rp[i], ci[i], nz[i], rpk[i], y[i],
-                                            ldy[i], yt, nullptr, nullptr, ws, gen, st, x, xt, ldx,
-                                            i == 0 ? xq : nullptr, i == 0 ? xs : nullptr);
-            s != MQ_OK)
-          return s;
-        if (!h) return set_error(MQ_ERR_CUDA, "linear: image form declined a planned launch");
-      }
-      return MQ_OK;
-    }
   }
   // the quantizer, then each matrix's GEMM
   const size_t Mp = static_cast<size_t>((M + 7) / 8 * 8), G = static_cast<size_t>(K / kGroup);

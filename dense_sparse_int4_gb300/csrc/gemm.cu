@@ -795,8 +795,7 @@ size_t image_workspace_bytes(int64_t M, int64_t N, int64_t K);
 mq_status image_gemm_launch(bool* handled, const uint8_t* xq, const uint16_t* xs, int64_t M, const uint8_t* wpk,
                             int64_t N, int64_t K, const int32_t* row_ptr, const int32_t* col_idx, int64_t nnzb,
                             const uint8_t* rpk, void* y, int64_t ldy, mq_dtype yt, int32_t* dots_w, int32_t* dots_r,
-                            void* ws, size_t ws_bytes, cudaStream_t stream, const void* x, mq_dtype xt,
-                            int64_t ldx, uint8_t* xq_out, uint16_t* xs_out);
+                            void* ws, size_t ws_bytes, cudaStream_t stream);
 
 // Bytes of workspace of the general kernel: its pieces, or the image form's
 // operand images where that form serves M (image_gemm.cu).
@@ -876,7 +875,7 @@ mq_status gemm_launch(const uint8_t* xq, const uint16_t* xs, int64_t M, const ui
   {
     // Large batches: the image form, when the workspace holds its images.
     const mq_status is = image_gemm_launch(&handled, xq, xs, M, wpk, N, K, row_ptr, col_idx, nnzb, rpk, y, ldy, yt,
-                                           dots_w, dots_r, ws, ws_bytes, stream, nullptr, MQ_F16, 0, nullptr, nullptr);
+                                           dots_w, dots_r, ws, ws_bytes, stream);
     if (handled || is != MQ_OK) return is;
   }
   const Plan pl = make_plan(M, N, K);

@@ -114,14 +114,6 @@ struct PrepParams {
   uint8_t* rimg;        // [nnzb][8192]
   uint8_t* ximg;        // [G][Mt][128]
   float* sxf;           // [G][Mt]
-  // X rows (fp16 or bf16 bits, row stride ldx) when the activations are
-  // quantized here rather than read from xq / xs; then the quantizer's
-  // outputs xq_out / xs_out are written too, where not null
-  const uint16_t* x;
-  int64_t ldx;
-  int x_bf16;
-  uint8_t* xq_out;
-  uint16_t* xs_out;
   int M, Mp, Mt, G;
   int64_t n_w, n_r, n_x, n_s;  // weight, residual and activation images; activation scales
 };
@@ -231,83 +223,6 @@ __device__ __forceinline__ void image_tile(uint8_t (*sm)[64], const uint8_t* src
   __syncthreads();
 }
 
-// The activation quantizer's rules (per token and 128-input group:
-// s = fp16_RNE(amax / 7) saturated to 65504, q = clamp(RNE(x / s), -7, 7)),
-// with the rounding of the stand-alone quantizer: rint of the refined
-// quotient q0 + (x - q0 s) r, q0 = x r, r = 1/s rounded, which is the exact
-// round-half-even for inputs and scales of 11 significant bits or fewer.
-__device__ __forceinline__ uint16_t img_scale_bits(float amax) {
-  uint16_t b = __half_as_ushort(__float2half_rn(__fdiv_rn(amax, 7.0f)));
-  if ((b & 0x7FFFu) == 0x7C00u) b = (b & 0x8000u) | 0x7BFFu;  // saturate
-  return b;
-}
-__device__ __forceinline__ int img_code(float v, float s, float r) {
-  const float q0 = v * r;
-  const float q1 = fmaf(fmaf(q0, -s, v), r, q0);
-  return static_cast<int>(fminf(fmaxf(rintf(q1), -7.0f), 7.0f));
-}
-__device__ __forceinline__ uint32_t e4m3x2(float hi, float lo) {  // two small integers, exact in E4M3
-  unsigned short r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-// The activation image of 128 token rows (m0 ..) of group g, quantized from X:
-// half a warp per token (lane k of the half: inputs 8k .. 8k+7, two 8-byte
-// loads), 16 tokens per pass.  Input i of a row sits at chunk i / 16, byte
-// i % 16 of its 128-byte line (chunk c stored at c ^ (row & 7)), as the image
-// of the packed codes has it.  Rows past M get zero codes and a zero scale.
-__device__ __forceinline__ void image_tile_from_x(const PrepParams& p, int64_t g, int m0) {
-  const int k = threadIdx.x & 15;
-  const unsigned half_mask = 0xFFFFu << (threadIdx.x & 16);
-  uint8_t* img = p.ximg + (g * p.Mt + m0) * 128;
-  for (int r = threadIdx.x >> 4; r < 128; r += blockDim.x >> 4) {
-    const int m = m0 + r;
-    float v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = 0.0f;
-    if (m < p.M) {
-      const uint16_t* src = p.x + m * p.ldx + g * kGroup + 8 * k;
-      const uint2 a = *reinterpret_cast<const uint2*>(src), b = *reinterpret_cast<const uint2*>(src + 4);
-      const uint32_t w[4] = {a.x, a.y, b.x, b.y};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint16_t lo = static_cast<uint16_t>(w[i] & 0xFFFFu), hi = static_cast<uint16_t>(w[i] >> 16);
-        v[2 * i] = p.x_bf16 ? __uint_as_float(static_cast<uint32_t>(lo) << 16) : __half2float(__ushort_as_half(lo));
-        v[2 * i + 1] = p.x_bf16 ? __uint_as_float(static_cast<uint32_t>(hi) << 16) : __half2float(__ushort_as_half(hi));
-      }
-    }
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(half_mask, amax, o));
-    const uint16_t sb = m < p.M ? img_scale_bits(amax) : static_cast<uint16_t>(0);
-    const float s = __half2float(__ushort_as_half(sb));
-    int q[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = 0;
-    if (s != 0.0f) {
-      const float rc = __frcp_rn(s);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) q[i] = img_code(v[i], s, rc);
-    }
-    const uint32_t lo = e4m3x2(static_cast<float>(q[1]), static_cast<float>(q[0])) |
-                        (e4m3x2(static_cast<float>(q[3]), static_cast<float>(q[2])) << 16);
-    const uint32_t hi = e4m3x2(static_cast<float>(q[5]), static_cast<float>(q[4])) |
-                        (e4m3x2(static_cast<float>(q[7]), static_cast<float>(q[6])) << 16);
-    *reinterpret_cast<uint2*>(img + r * 128 + (((k >> 1) ^ (r & 7)) * 16) + 8 * (k & 1)) = make_uint2(lo, hi);
-    if (k == 0) p.sxf[g * p.Mt + m] = s;
-    if (p.xq_out && m < p.Mp) {  // the quantizer's outputs: packed codes (even input in the low nibble), scales
-      uint32_t pk = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) pk |= (static_cast<uint32_t>(q[i]) & 0xFu) << (4 * i);
-      *reinterpret_cast<uint32_t*>(p.xq_out + (g * p.Mp + m) * 64 + 4 * k) = pk;
-      if (k == 0) p.xs_out[g * p.Mp + m] = sb;
-    }
-  }
-}
-
 // The pre-pass: one block per image (a base record, a residual block, or 128
 // token rows of one group's activations), then the activation scales.
 __global__ void __launch_bounds__(256) image_prep_kernel(const PrepParams p) {
@@ -327,10 +242,7 @@ __global__ void __launch_bounds__(256) image_prep_kernel(const PrepParams p) {
     } else {
       const int64_t x = b - n_w - n_r, g = x / mtiles;
       const int m0 = static_cast<int>(x - g * mtiles) * 128;
-      if (p.x)
-        image_tile_from_x(p, g, m0);
-      else
-        image_tile(sm, p.xq + (g * p.Mp + m0) * 64, 64, 16, 128, p.M - m0, p.ximg + (g * p.Mt + m0) * 128);
+      image_tile(sm, p.xq + (g * p.Mp + m0) * 64, 64, 16, 128, p.M - m0, p.ximg + (g * p.Mt + m0) * 128);
     }
   }
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -923,24 +835,15 @@ void image_plan_info(int64_t M, int64_t N, int64_t K, int32_t* tn, int32_t* ctas
 // The pre-pass and the GEMM, when the image form is wanted for M and the
 // workspace holds its images (`handled` false otherwise: the caller runs the
 // general kernel).
-// Whether the image form serves (M, N, K, nnzb) with this workspace.
-bool image_form_fits(int64_t M, int64_t N, int64_t K, int64_t nnzb, const void* ws, size_t ws_bytes) {
-  if (!image_form_wanted(M)) return false;
-  const IPlan pl = iplan(M, N, K, nnzb);
-  return ws != nullptr && ws_bytes >= pl.bytes && aligned(ws, 256) && pl.ctas <= kWsZeroBytes / 4;
-}
-
-// x (fp16 / bf16, row stride ldx) non-null: the pre-pass quantizes X itself
-// (xq, xs unused) and writes the quantizer's outputs to xq_out / xs_out where
-// given; else it reads the packed activations xq, xs.
 mq_status image_gemm_launch(bool* handled, const uint8_t* xq, const uint16_t* xs, int64_t M, const uint8_t* wpk,
                             int64_t N, int64_t K, const int32_t* row_ptr, const int32_t* col_idx, int64_t nnzb,
                             const uint8_t* rpk, void* y, int64_t ldy, mq_dtype yt, int32_t* dots_w, int32_t* dots_r,
-                            void* ws, size_t ws_bytes, cudaStream_t stream, const void* x, mq_dtype xt,
-                            int64_t ldx, uint8_t* xq_out, uint16_t* xs_out) {
+                            void* ws, size_t ws_bytes, cudaStream_t stream) {
   *handled = false;
-  if (!image_form_fits(M, N, K, nnzb, ws, ws_bytes)) return MQ_OK;
+  if (!image_form_wanted(M)) return MQ_OK;
   const IPlan pl = iplan(M, N, K, nnzb);
+  if (ws == nullptr || ws_bytes < pl.bytes || !aligned(ws, 256)) return MQ_OK;
+  if (pl.ctas > kWsZeroBytes / 4) return MQ_OK;
   *handled = true;
   uint8_t* base = static_cast<uint8_t*>(ws);
   const int Mp = static_cast<int>((M + 7) / 8 * 8);
@@ -949,11 +852,6 @@ mq_status image_gemm_launch(bool* handled, const uint8_t* xq, const uint16_t* xs
   pp.rpk = rpk;
   pp.xq = xq;
   pp.xs = xs;
-  pp.x = static_cast<const uint16_t*>(x);
-  pp.ldx = ldx;
-  pp.x_bf16 = xt == MQ_BF16;
-  pp.xq_out = x ? xq_out : nullptr;
-  pp.xs_out = x ? xs_out : nullptr;
   pp.wimg = base + pl.off_w;
   pp.rimg = base + pl.off_r;
   pp.ximg = base + pl.off_x;
@@ -965,7 +863,7 @@ mq_status image_gemm_launch(bool* handled, const uint8_t* xq, const uint16_t* xs
   pp.n_w = static_cast<int64_t>(pl.tiles_n) * pl.G;  // weight images
   pp.n_r = nnzb;                                      // residual images
   pp.n_x = static_cast<int64_t>(pl.G) * pl.Mt / 128;  // activation images of 128 token rows
-  pp.n_s = x ? 0 : static_cast<int64_t>(pl.G) * pl.Mt;  // (from X, the activation blocks write the scales)
+  pp.n_s = static_cast<int64_t>(pl.G) * pl.Mt;
   {
     const int64_t images = pp.n_w + pp.n_r + pp.n_x;
     const int sms = img_sms();

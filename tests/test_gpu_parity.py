@@ -326,7 +326,7 @@ def test_general_forms_match_oracle(form, M, N, K, budget, x_dtype, monkeypatch)
     (17, 2048, [512, 512], 0.50, "f16"),
     (32, 4096, [4096, 1024, 1024], 0.10, "f16"),  # q, k, v of the Llama-3-8B-shaped layer
     (40, 512, [256, 384], 0.10, "f16"),  # above 32 tokens: the quantizer, then the general kernel
-    # from 128 tokens: the image form, whose pre-pass quantizes X (and reports xq / xs) itself
+    # from 128 tokens: the quantizer, then the image form
     (130, 640, [256, 384, 128], 0.20, "bf16"),
     (300, 1024, [512], 0.10, "f16"),
 ])
@@ -430,10 +430,10 @@ def test_fused_quantizer_corners(variant, M, x_dtype, pad, monkeypatch):
 
 @pytest.mark.parametrize("M,x_dtype,pad", [(160, "f16", 0), (160, "bf16", 4), (300, "f16", 4)])
 def test_image_prepass_quantizer_corners(M, x_dtype, pad):
-    """From 128 tokens the fused call's image pre-pass quantizes X itself (half
-    a warp per token and group): the xq / xs it reports against the oracle
-    bit for bit on the corner rows (ties, ties moved one ulp, subnormal and
-    saturating scales, zero groups; a row stride of K + pad), padding tokens
+    """From 128 tokens the fused call quantizes X, then its image pre-pass turns
+    the codes into the activation image: the xq / xs it reports against the
+    oracle bit for bit on the corner rows (ties, ties moved one ulp, subnormal
+    and saturating scales, zero groups; a row stride of K + pad), padding tokens
     zero, and Y within the fp32 bound (the activation image carries the same codes)."""
     K, N = 640, 256
     isb = x_dtype == "bf16"
