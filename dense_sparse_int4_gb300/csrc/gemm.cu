@@ -769,7 +769,9 @@ static int pick_tn(int64_t M) {
 
 static size_t a256(size_t b) { return (b + 255) / 256 * 256; }
 
-// The plan depends only on (M, N, K): the workspace size must not depend on the device.
+// The plan depends on (M, N, K) and the current device's SM count (the
+// persistent grid; 152 when no device is current), so a workspace sized on a
+// device serves that device.
 static Plan make_plan(int64_t M, int64_t N, int64_t K) {
   Plan pl;
   pl.tn = pick_tn(M);

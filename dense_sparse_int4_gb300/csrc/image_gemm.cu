@@ -756,7 +756,8 @@ int image_form_mode() {
 // do not fit the 96 registers 18 warps leave a thread.
 int pick_img_tn(int64_t) { return 128; }
 
-// The plan's sizes depend only on (M, N, K, nnzb), not on the device.
+// The plan depends on (M, N, K, nnzb) and the current device's SM count (the
+// persistent grid and its stream-K pieces; 152 when no device is current).
 IPlan iplan(int64_t M, int64_t N, int64_t K, int64_t nnzb) {
   IPlan pl;
   pl.tn = pick_img_tn(M);

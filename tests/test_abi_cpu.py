@@ -58,6 +58,13 @@ def test_workspace_sizes(L):
     # from 128 tokens: the image form's operand images (E4M3 weights, the densest residual, activations)
     assert L.mq_gemm_workspace_bytes(2048, 14336, 4096) >= 2 * 14336 * 4096 + 2048 * 4096
     assert L.mq_gemm_workspace_bytes(127, 14336, 4096) < 14336 * 4096
+    # ... exactly: the counter prefix, 152 CTAs' two stream-K pieces of 128 x 128 fp32, the weight images
+    # (16 KiB per tile and group), the densest residual's images (8 KiB per block), the activation images
+    # (128 bytes per token and group, tokens padded to 128) and their fp32 scales
+    M, N, K = 2048, 14336, 4096
+    G, Mt = K // 128, (M + 127) // 128 * 128
+    want = 16384 + 152 * 2 * 128 * 128 * 4 + (N // 128) * G * 16384 + (N // 64) * G * 8192 + G * Mt * 128 + G * Mt * 4
+    assert L.mq_gemm_workspace_bytes(M, N, K) == want
     assert L.mq_gemm_workspace_bytes(4, 512, 512) > 0
     assert L.mq_gemm_workspace_bytes(4, 100, 4096) == 0  # invalid N
 
